@@ -1,0 +1,433 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle of the single-GPU MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  It is built and called by tests/, by
+ * __graft_entry__.smoke() and by the cpu_baseline / reference leg of bench.py.
+ * The CUDA library never links, includes or calls anything here, and this file
+ * includes nothing from the CUDA side: the two share no code.
+ *
+ * What it computes is the layer's mathematical definition, written as naive loops
+ * in double precision:
+ *
+ *   route       top-k selection on the fp32 router logits, the gate weights, the
+ *               per-expert histogram, capacity dropping "only on overflow" in token
+ *               order, the exclusive scan of kept counts into segment offsets, and
+ *               the padding-free token buffer's side arrays (token ids, slot ids,
+ *               destination rows).  X-MoE verdict page (arXiv 2508.13337):
+ *               "key machinery" (padding-free token buffer with token ids, expert
+ *               ids, per-expert counts and combine weights), referee minor comment
+ *               on section 4.1.1 Listing 1 (max_token_count = floor(c*S*K/E)) and
+ *               major comment on section 5.6 (drops only on capacity).
+ *               Primus MoE blog, Figure 7 dataflow: "the router scores each token
+ *               and picks its top-k experts", "a permutation gathers tokens into
+ *               expert order".
+ *   ffn         SwiGLU expert FFN with three matrices (gate, up: d x f; down: f x d).
+ *               Primus MoE blog, Figure 7 dataflow (FC1 gate/up, SwiGLU, FC2 down);
+ *               DeepSeek-V3 memory-model page, "key machinery" (three matrices per
+ *               expert).
+ *   combine     unpermute-and-scale: y[t] = sum over kept slots of w * yp[row].
+ *               Primus MoE blog, Figure 7 dataflow, last step.
+ *   backward    dispatch(dy) -> FC2 data-grad, FC1 data-grad -> combine/reduce,
+ *               plus the two variable-K weight gradients.  Primus MoE blog,
+ *               MegaMoE section ("dispatch/combine duality") and the JAX grouped
+ *               GEMM paragraph (two backward grouped GEMMs incl. variable-K).
+ *
+ * Rounding points: when `rnd` is non-zero every tensor that the GPU path stores in
+ * bf16 (a, b, h, yp, y, dyp, da, db, dxp, dx) is rounded to bf16 (round to nearest,
+ * ties to even, straight from the double value) at the point where it is stored.
+ * With `rnd` = 0 everything stays in double, which is what the finite-difference
+ * and autograd pins use.  Weight gradients are accumulated in double; the caller
+ * rounds them once.
+ *
+ * Readings where the pages are silent (each listed in the design notes too):
+ *   - selection compares the fp32 logits with IEEE '>' (so +0 == -0), ties go to the
+ *     lower expert id, NaN ranks below -inf and is counted in the return value;
+ *   - softmax gate: w_j = exp(l_j - m) / sum_{i in top-k} exp(l_i - m), m = max
+ *     selected logit (= softmax over E renormalised over the top-k);
+ *     sigmoid gate: w_j = scale * sigma(l_j) / sum_{i in top-k} sigma(l_i);
+ *   - weights are computed over all k selected slots before any capacity drop and
+ *     are not renormalised after drops;
+ *   - assignments to an expert are ranked by ascending token index; the first `cap`
+ *     are kept (cap = 0: unlimited);
+ *   - unselected logits get a zero gradient (selection is piecewise constant).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define GATE_SOFTMAX 0
+#define GATE_SIGMOID 1
+
+/* bf16 round-to-nearest-even of a double, from the format's definition: 8
+ * significant bits (1 implicit + 7 stored), the fp32 exponent range, subnormal
+ * spacing 2^-133, overflow to infinity past the largest finite value. */
+double orc_bf16(double x)
+{
+    if (isnan(x) || isinf(x) || x == 0.0)
+        return x;
+    int e;
+    frexp(x, &e);                 /* x = m * 2^e with 0.5 <= |m| < 1 */
+    int ulp_exp = e - 8;          /* spacing of 8-significant-bit numbers near x */
+    if (ulp_exp < -133)
+        ulp_exp = -133;
+    double q = nearbyint(ldexp(x, -ulp_exp));   /* default mode: ties to even */
+    double r = ldexp(q, ulp_exp);
+    if (fabs(r) >= ldexp(1.0, 128))
+        return copysign(INFINITY, x);
+    return r;
+}
+
+static inline double rb(double x, int rnd) { return rnd ? orc_bf16(x) : x; }
+
+void orc_round_bf16_array(double *a, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        a[i] = orc_bf16(a[i]);
+}
+
+/* Does (la, ea) rank before (lb, eb)?  Larger logit first, lower id on ties, NaN last. */
+static int ranks_before(float la, int ea, float lb, int eb)
+{
+    int na = isnan(la), nb = isnan(lb);
+    if (na || nb) {
+        if (na && nb)
+            return ea < eb;
+        return nb;            /* a non-NaN logit beats a NaN one */
+    }
+    if (la > lb)
+        return 1;
+    if (la < lb)
+        return 0;
+    return ea < eb;           /* equal (including +0 vs -0): lower expert id first */
+}
+
+/*
+ * Route T tokens over E experts, k per token.
+ *   logits    [T,E] fp32 (read only)
+ *   topk_idx  [T,k] expert of slot j, in rank order
+ *   topk_w    [T,k] gate weight of slot j
+ *   counts    [E]   assignments routed to e
+ *   kept      [E]   min(counts, cap)
+ *   offsets   [E+1] exclusive scan of kept (offsets[E] = rows kept)
+ *   dest_row  [T,k] row of slot (t,j) in the expert-ordered buffer, or -1 if dropped
+ *   src_tok   [T*k] token of row p (rows >= offsets[E] are set to -1)
+ *   src_slot  [T*k] t*k+j of row p (-1 past the end)
+ *   drop_mask [T,k] 1 if the slot was dropped by the capacity limit
+ * Returns the number of NaN logits seen.
+ */
+int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
+                  const float *logits, int32_t *topk_idx, double *topk_w,
+                  int32_t *counts, int32_t *kept, int32_t *offsets, int32_t *dest_row,
+                  int32_t *src_tok, int32_t *src_slot, uint8_t *drop_mask)
+{
+    int64_t nan_seen = 0;
+    int *order = (int *)malloc(sizeof(int) * (size_t)E);
+    int32_t *rank = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T * k));
+
+    /* 1. selection: order experts by (logit desc, id asc), take the first k */
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        for (int e = 0; e < E; ++e) {
+            if (isnan(l[e]))
+                ++nan_seen;
+            order[e] = e;
+        }
+        /* insertion sort: plain and obviously stable w.r.t. the key */
+        for (int i = 1; i < E; ++i) {
+            int cur = order[i], j = i - 1;
+            while (j >= 0 && ranks_before(l[cur], cur, l[order[j]], order[j])) {
+                order[j + 1] = order[j];
+                --j;
+            }
+            order[j + 1] = cur;
+        }
+        for (int j = 0; j < k; ++j)
+            topk_idx[t * k + j] = order[j];
+
+        /* 2. gate weights over the selected k */
+        double sel[64];
+        for (int j = 0; j < k; ++j)
+            sel[j] = (double)l[order[j]];
+        if (gate == GATE_SOFTMAX) {
+            double m = sel[0];
+            for (int j = 1; j < k; ++j)
+                if (sel[j] > m)
+                    m = sel[j];
+            double z = 0.0;
+            for (int j = 0; j < k; ++j)
+                z += exp(sel[j] - m);
+            for (int j = 0; j < k; ++j)
+                topk_w[t * k + j] = exp(sel[j] - m) / z;
+        } else {
+            double z = 0.0;
+            for (int j = 0; j < k; ++j)
+                z += 1.0 / (1.0 + exp(-sel[j]));
+            for (int j = 0; j < k; ++j)
+                topk_w[t * k + j] = scale * (1.0 / (1.0 + exp(-sel[j]))) / z;
+        }
+    }
+
+    /* 3. histogram and rank of each assignment among its expert's, by ascending t */
+    for (int e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int e = topk_idx[t * k + j];
+            rank[t * k + j] = counts[e];
+            counts[e] += 1;
+        }
+
+    /* 4. capacity (drop only on overflow) and exclusive scan of the kept counts */
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int64_t c = counts[e];
+        kept[e] = (int32_t)((cap > 0 && c > cap) ? cap : c);
+        offsets[e + 1] = offsets[e] + kept[e];
+    }
+
+    /* 5. destination rows and the inverse maps */
+    for (int64_t p = 0; p < T * k; ++p) {
+        src_tok[p] = -1;
+        src_slot[p] = -1;
+    }
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            int64_t s = t * k + j;
+            int e = topk_idx[s];
+            if (cap > 0 && rank[s] >= cap) {
+                dest_row[s] = -1;
+                drop_mask[s] = 1;
+            } else {
+                int32_t p = offsets[e] + rank[s];
+                dest_row[s] = p;
+                drop_mask[s] = 0;
+                src_tok[p] = (int32_t)t;
+                src_slot[p] = (int32_t)s;
+            }
+        }
+    free(order);
+    free(rank);
+    return nan_seen;
+}
+
+/* xp[p] = x[src_tok[p]] for p < n_rows  (a pure copy) */
+void orc_permute(int64_t n_rows, int d, const int32_t *src_tok, const double *x, double *xp)
+{
+    for (int64_t p = 0; p < n_rows; ++p)
+        memcpy(xp + p * d, x + (int64_t)src_tok[p] * d, sizeof(double) * (size_t)d);
+}
+
+/*
+ * SwiGLU expert FFN on n rows that all belong to one expert.
+ *   xr [n,d], W1e [2f,d] (rows 0..f-1 gate, f..2f-1 up), W2e [d,f]
+ *   ab [n,2f] = [a | b] with a = xr W_gate^T, b = xr W_up^T
+ *   h  [n,f]  = silu(a) * b,  silu(a) = a / (1 + exp(-a))
+ *   yp [n,d]  = h W2e^T
+ */
+void orc_ffn_fwd_rows(int64_t n, int d, int f, const double *xr, const double *W1e,
+                      const double *W2e, int rnd, double *ab, double *h, double *yp)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const double *x = xr + r * d;
+        double *abr = ab + r * 2 * f;
+        double *hr = h + r * f;
+        for (int c = 0; c < 2 * f; ++c) {
+            const double *w = W1e + (int64_t)c * d;
+            double s = 0.0;
+            for (int i = 0; i < d; ++i)
+                s += x[i] * w[i];
+            abr[c] = rb(s, rnd);
+        }
+        for (int c = 0; c < f; ++c) {
+            double a = abr[c], b = abr[f + c];
+            hr[c] = rb(a / (1.0 + exp(-a)) * b, rnd);
+        }
+        for (int i = 0; i < d; ++i) {
+            const double *w = W2e + (int64_t)i * f;
+            double s = 0.0;
+            for (int c = 0; c < f; ++c)
+                s += hr[c] * w[c];
+            yp[r * d + i] = rb(s, rnd);
+        }
+    }
+}
+
+/*
+ * Backward of the SwiGLU FFN on n rows of one expert (data gradients only).
+ *   dyp [n,d] upstream gradient of yp;  ab [n,2f] saved pre-activations
+ *   dh  = dyp W2e                              (not stored: stays fp32 on the GPU)
+ *   da  = dh * b * silu'(a),  silu'(a) = s (1 + a (1 - s)),  s = sigma(a)
+ *   db  = dh * silu(a)
+ *   dab [n,2f] = [da | db];   dxr [n,d] = dab W1e
+ */
+void orc_ffn_bwd_rows(int64_t n, int d, int f, const double *dyp, const double *ab,
+                      const double *W1e, const double *W2e, int rnd, double *dab, double *dxr)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const double *g = dyp + r * d;
+        const double *abr = ab + r * 2 * f;
+        double *dr = dab + r * 2 * f;
+        for (int c = 0; c < f; ++c) {
+            double dh = 0.0;
+            for (int i = 0; i < d; ++i)
+                dh += g[i] * W2e[(int64_t)i * f + c];
+            double a = abr[c], b = abr[f + c];
+            double s = 1.0 / (1.0 + exp(-a));
+            double silu = a * s;
+            double dsilu = s * (1.0 + a * (1.0 - s));
+            dr[c] = rb(dh * b * dsilu, rnd);
+            dr[f + c] = rb(dh * silu, rnd);
+        }
+        for (int i = 0; i < d; ++i) {
+            double s = 0.0;
+            for (int c = 0; c < 2 * f; ++c)
+                s += dr[c] * W1e[(int64_t)c * d + i];
+            dxr[r * d + i] = rb(s, rnd);
+        }
+    }
+}
+
+/*
+ * Weight gradients of one expert, summed over its n rows (the variable-K GEMMs):
+ *   dW2e[i][c] += sum_r dyp[r][i] * h[r][c]        [d,f]
+ *   dW1e[c][i] += sum_r dab[r][c] * xr[r][i]       [2f,d]
+ * Accumulated in double; the caller rounds once.
+ */
+void orc_ffn_wgrad_rows(int64_t n, int d, int f, const double *xr, const double *h,
+                        const double *dyp, const double *dab, double *dW1e, double *dW2e)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < d; ++i)
+        for (int c = 0; c < f; ++c) {
+            double s = 0.0;
+            for (int64_t r = 0; r < n; ++r)
+                s += dyp[r * d + i] * h[r * f + c];
+            dW2e[(int64_t)i * f + c] += s;
+        }
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < 2 * f; ++c)
+        for (int i = 0; i < d; ++i) {
+            double s = 0.0;
+            for (int64_t r = 0; r < n; ++r)
+                s += dab[r * 2 * f + c] * xr[r * d + i];
+            dW1e[(int64_t)c * d + i] += s;
+        }
+}
+
+/*
+ * Combine (unpermute and scale): for each token t in `toks` (or all T if toks is
+ * NULL), y[t] = sum over slots j = 0..k-1 with dest_row >= 0 of w[t,j] * yp[dest_row]
+ * (+ ys[t] if ys is not NULL).  A fully dropped token gives 0 (+ ys).
+ * `yp_row_of` maps a destination row to the row index inside yp (NULL = identity),
+ * which lets the caller pass only the rows it evaluated.
+ */
+void orc_combine(int64_t n_tok, const int64_t *toks, int k, int d, const int32_t *dest_row,
+                 const double *topk_w, const double *yp, const int64_t *yp_row_of,
+                 const double *ys, int rnd, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t q = 0; q < n_tok; ++q) {
+        int64_t t = toks ? toks[q] : q;
+        for (int i = 0; i < d; ++i) {
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t p = dest_row[t * k + j];
+                if (p < 0)
+                    continue;
+                int64_t rr = yp_row_of ? yp_row_of[p] : p;
+                s += topk_w[t * k + j] * yp[rr * d + i];
+            }
+            if (ys)
+                s += ys[q * d + i];
+            y[q * d + i] = rb(s, rnd);
+        }
+    }
+}
+
+/*
+ * Backward of combine and of the gate, per token t in `toks` (all if NULL):
+ *   dyp[row] = w[t,j] * dy[t]                      for kept slots
+ *   dw[t,j]  = <dy[t], yp[row]>                    (0 for a dropped slot)
+ *   softmax gate: dl_j = w_j (dw_j - sum_i w_i dw_i)
+ *   sigmoid gate: S = sum_i s_i, ds_j = scale (dw_j / S - sum_i s_i dw_i / S^2),
+ *                 dl_j = ds_j s_j (1 - s_j)
+ *   dlogits[t, e] = dl_j for e = topk_idx[t,j], 0 for unselected experts.
+ * dy is indexed by q (the position in toks), yp through yp_row_of as in orc_combine,
+ * and dyp is written at yp_row_of[row].
+ */
+void orc_combine_bwd(int64_t n_tok, const int64_t *toks, int E, int k, int d, int gate,
+                     double scale, const float *logits, const int32_t *topk_idx,
+                     const double *topk_w, const int32_t *dest_row, const double *dy,
+                     const double *yp, const int64_t *yp_row_of, int rnd, double *dyp,
+                     double *dlogits)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t q = 0; q < n_tok; ++q) {
+        int64_t t = toks ? toks[q] : q;
+        const double *g = dy + q * d;
+        double dw[64], s[64];
+        for (int j = 0; j < k; ++j) {
+            int32_t p = dest_row[t * k + j];
+            double w = topk_w[t * k + j];
+            dw[j] = 0.0;
+            if (p < 0)
+                continue;
+            int64_t rr = yp_row_of ? yp_row_of[p] : p;
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) {
+                acc += g[i] * yp[rr * d + i];
+                dyp[rr * d + i] = rb(w * g[i], rnd);
+            }
+            dw[j] = acc;
+        }
+        double *dl = dlogits + q * E;
+        for (int e = 0; e < E; ++e)
+            dl[e] = 0.0;
+        if (gate == GATE_SOFTMAX) {
+            double sw = 0.0;
+            for (int j = 0; j < k; ++j)
+                sw += topk_w[t * k + j] * dw[j];
+            for (int j = 0; j < k; ++j)
+                dl[topk_idx[t * k + j]] = topk_w[t * k + j] * (dw[j] - sw);
+        } else {
+            double S = 0.0, sd = 0.0;
+            for (int j = 0; j < k; ++j) {
+                double l = (double)logits[t * E + topk_idx[t * k + j]];
+                s[j] = 1.0 / (1.0 + exp(-l));
+                S += s[j];
+                sd += s[j] * dw[j];
+            }
+            for (int j = 0; j < k; ++j) {
+                double ds = scale * (dw[j] / S - sd / (S * S));
+                dl[topk_idx[t * k + j]] = ds * s[j] * (1.0 - s[j]);
+            }
+        }
+    }
+}
+
+/* dx[t] = sum over kept slots of dxp[dest_row] (+ dxs[t]); same indexing as orc_combine. */
+void orc_unpermute_reduce(int64_t n_tok, const int64_t *toks, int k, int d,
+                          const int32_t *dest_row, const double *dxp, const int64_t *row_of,
+                          const double *dxs, int rnd, double *dx)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t q = 0; q < n_tok; ++q) {
+        int64_t t = toks ? toks[q] : q;
+        for (int i = 0; i < d; ++i) {
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t p = dest_row[t * k + j];
+                if (p < 0)
+                    continue;
+                int64_t rr = row_of ? row_of[p] : p;
+                s += dxp[rr * d + i];
+            }
+            if (dxs)
+                s += dxs[q * d + i];
+            dx[q * d + i] = rb(s, rnd);
+        }
+    }
+}
