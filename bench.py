@@ -1,0 +1,448 @@
+"""Benchmark of the single-GPU MoE layer (forward + backward) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one forward + backward of the MoE layer over one batch of T tokens:
+route -> permute -> grouped FC1/SwiGLU/FC2 -> (shared expert) -> combine, then
+combine/gate backward -> FC2 data-grad + SwiGLU backward -> FC2 weight-grad ->
+FC1 data-grad -> FC1 weight-grad -> un-permute reduce.  The default workload is the
+Mixtral-style layer (T=4096, d=4096, E=8, top-2, f=14336) on synthetic seeded
+inputs.  The metric is tokens/s of the whole step; the dominant kernel (the tcgen05
+grouped GEMM, six launches per step) is also reported against the measured bf16
+tensor peak.
+
+With N > 1 (torchrun) every rank runs an independent replica of the layer (the path
+does not shard: replicas only); the reported value is the sum over ranks, the time
+the max over ranks.
+
+--impl reference times the CPU oracle (the plain double-precision C reference of the
+layer) on the host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gemm_flops(c, rows_kept: int) -> float:
+    """Algorithmic flops of the six grouped-GEMM launches: 18*d*f per kept row, plus the
+    shared expert's 18*d*fs per token."""
+    return 18.0 * c.d * c.f * rows_kept + (18.0 * c.d * c.fs * c.T if c.fs else 0.0)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- dist
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- oracle timing
+class OracleTimer:
+    """The CPU oracle's full forward + backward (routing, expert FFN with both weight
+    gradients, combine, all in float64) on the first t tokens of the workload, with the
+    workload's d, f, E, k, gate and capacity rule.  Inputs come from the host generators
+    and are built once."""
+
+    def __init__(self, c):
+        import oracle
+        from workloads import WEIGHT_STD, gen_bf16, gen_logits, weight_shapes
+
+        oracle.build()
+        self.c = c
+        self.threads = os.cpu_count() or 1
+        try:
+            self.threads = len(os.sched_getaffinity(0))
+        except AttributeError:
+            pass
+        self.logits = gen_logits(c)
+        self.x = gen_bf16(c, "x", (c.T, c.d))
+        self.dy = gen_bf16(c, "dy", (c.T, c.d))
+        self.W = {n: oracle.layer._f64(gen_bf16(c, n, shape, WEIGHT_STD))
+                  for n, shape in weight_shapes(c).items()}
+
+    def run(self, t: int) -> float:
+        import oracle
+        c = self.c
+        sub = c.replace(T=t)
+        inp = {"logits": self.logits[:t], "x": self.x[:t], "dy": self.dy[:t]}
+        inp.update(self.W)
+        t0 = time.perf_counter()
+        fo = oracle.layer_fwd(sub, inp)
+        oracle.layer_bwd(sub, inp, fo)
+        return time.perf_counter() - t0
+
+    def calibrate(self, budget_s: float) -> int:
+        """Largest token count whose run takes about budget_s seconds."""
+        probe = 2
+        dt = self.run(probe)
+        return int(min(self.c.T, max(probe, probe * budget_s / max(dt, 1e-3))))
+
+
+# --------------------------------------------------------------------------- ours
+def bench_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import token_dispatch_expert_gb300 as tde
+    from workloads import CONFIGS, gen_inputs_device
+
+    c = CONFIGS[args.config]
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    tde.lib()
+    cfg = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity)
+    g = gen_inputs_device(c, dev, seed=rank)
+    R = c.T * c.k
+    ws_b, ctx_b = tde.moe_workspace_size(cfg)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
+    ctx = torch.empty(ctx_b, dtype=torch.uint8, device=dev)
+    tde.moe_ws_init(ws)
+    v = tde.ctx_views(cfg, ctx)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    y = torch.empty((c.T, c.d), **bf)
+    dyp = torch.empty((R, c.d), **bf)
+    dab = torch.empty((R, 2 * c.f), **bf)
+    dxp = torch.empty((R, c.d), **bf)
+    dx = torch.empty((c.T, c.d), **bf)
+    dW1 = torch.empty_like(g["W1"])
+    dW2 = torch.empty_like(g["W2"])
+    dl = torch.empty((c.T, c.E), dtype=torch.float32, device=dev)
+    shared = None
+    if c.fs:
+        # the shared expert as a one-group grouped FFN over all T tokens
+        s_cfg = tde.make_config(c.T, c.d, 1, 1, c.fs)
+        s_off = torch.tensor([0, c.T], dtype=torch.int32, device=dev)
+        shared = dict(cfg=s_cfg, off=s_off, ab=torch.empty((c.T, 2 * c.fs), **bf),
+                      h=torch.empty((c.T, c.fs), **bf), ys=torch.empty((c.T, c.d), **bf),
+                      dab=torch.empty((c.T, 2 * c.fs), **bf), dx=torch.empty((c.T, c.d), **bf),
+                      dW1=torch.empty_like(g["W1s"]), dW2=torch.empty_like(g["W2s"]))
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def step(record):
+        # forward
+        tde.moe_route(cfg, g["logits"], v["topk_idx"], v["topk_w"], v["counts"], v["kept"],
+                      v["offsets"], v["dest_row"], v["src_tok"], v["src_slot"], v["drop_mask"],
+                      ws)
+        tde.moe_permute(cfg, g["x"], v["src_tok"], v["offsets"], v["xp"], ws)
+        if record:
+            ev[0].record(stream)
+        tde.moe_grouped_ffn(cfg, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"], v["h"],
+                            v["yp"], ws)
+        if shared:
+            tde.moe_grouped_ffn(shared["cfg"], g["x"], shared["off"], g["W1s"], g["W2s"],
+                                shared["ab"], shared["h"], shared["ys"], ws)
+        if record:
+            ev[1].record(stream)
+        tde.moe_combine(cfg, v["yp"], v["dest_row"], v["topk_w"],
+                        shared["ys"] if shared else None, y, ws)
+        # backward
+        tde.moe_combine_bwd(cfg, g["dy"], v["yp"], g["logits"], v["topk_idx"], v["topk_w"],
+                            v["dest_row"], dyp, dl, ws)
+        if record:
+            ev[2].record(stream)
+        tde.moe_grouped_ffn_bwd(cfg, dyp, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"],
+                                v["h"], dab, dxp, dW1, dW2, ws)
+        if shared:
+            tde.moe_grouped_ffn_bwd(shared["cfg"], g["dy"], g["x"], shared["off"], g["W1s"],
+                                    g["W2s"], shared["ab"], shared["h"], shared["dab"],
+                                    shared["dx"], shared["dW1"], shared["dW2"], ws)
+        if record:
+            ev[3].record(stream)
+        tde.moe_unpermute_reduce(cfg, dxp, v["dest_row"], shared["dx"] if shared else None,
+                                 dx, ws)
+
+    launches_per_step = 3 + 1 + 2 + 1 + 1 + 4 + 1 + (6 if shared else 0)
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    st, fl = tde.moe_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {tde.moe_status_string(st)} {fl:#x}")
+    rows_kept = int(v["offsets"][-1].item())
+
+    clocks = ClockSampler(local)
+    gemm_ms = 0.0
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    per_step_gemm = []
+    for i in range(args.steps):
+        step(True)
+        # the events are read back after the loop (no host sync inside it)
+        per_step_gemm.append(ev[:4])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    for e0, e1, e2, e3 in per_step_gemm:
+        gemm_ms += e0.elapsed_time(e1) + e2.elapsed_time(e3)
+    st, fl = tde.moe_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {tde.moe_status_string(st)} {fl:#x}")
+
+    total_ms_max = max_over_ranks(world, total_ms)
+    ms_per_step = total_ms_max / args.steps
+    tokens_total = sum_over_ranks(world, float(c.T * args.steps))
+    value = tokens_total / (total_ms_max / 1e3)
+
+    # end to end through the public whole-layer API, host buffers in pinned memory
+    layer = tde.MoELayer(cfg, device=dev)
+    h_logits = g["logits"].cpu().pin_memory()
+    h_x = g["x"].cpu().pin_memory()
+    h_dy = g["dy"].cpu().pin_memory()
+    d_logits = torch.empty_like(g["logits"]); d_x = torch.empty_like(g["x"])
+    d_dy = torch.empty_like(g["dy"])
+    h_y = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
+    h_dx = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
+    h_dl = torch.empty((c.T, c.E), dtype=torch.float32).pin_memory()
+    outs = {"dx": dx, "dW1": dW1, "dW2": dW2, "dlogits": dl}
+    if shared:
+        outs["dW1s"] = shared["dW1"]; outs["dW2s"] = shared["dW2"]
+
+    def e2e_step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        d_dy.copy_(h_dy, non_blocking=True)
+        yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"), y=y)
+        layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
+                       out=outs)
+        h_y.copy_(yy, non_blocking=True)
+        h_dx.copy_(outs["dx"], non_blocking=True)
+        h_dl.copy_(outs["dlogits"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    e2e_value = tokens_total / (e2e_ms / 1e3)
+    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
+    d2h = h_y.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
+
+    peaks, peak_src = load_peaks()
+    flops = gemm_flops(c, rows_kept)
+    gemm_launches = 6 * (2 if shared else 1)
+    gemm_s_per_step = gemm_ms / args.steps / 1e3
+    achieved = flops / gemm_s_per_step / 1e12
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": "MoE layer fwd+bwd tokens/s on 1 GB300",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens/logits, N(0,0.02) bf16 weights)",
+        "config": {"workload": f"{c.name}: T={c.T} d={c.d} E={c.E} top-{c.k} "
+                               f"{c.gate} f={c.f}" + (f" shared fs={c.fs}" if c.fs else "")
+                               + (f" capacity {c.capacity}" if c.capacity else ""),
+                   "tokens_per_step": c.T, "rows_kept": rows_kept,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: each step streams >10 GB of weights/grads (> 129 MB L2)"},
+        "roofline": {"kernel": "grouped_gemm (tcgen05; FC1, FC2, 2 dgrad, 2 wgrad per step)",
+                     "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                     "traffic": None,
+                     "gemm_ms_per_step": round(gemm_ms / args.steps, 4),
+                     "gemm_share_of_step": round(gemm_ms / total_ms, 4)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ot = OracleTimer(c)
+        t = ot.calibrate(args.cpu_seconds)
+        dt = ot.run(t)
+        rate = t / dt
+        line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": ot.threads,
+                                "kind": "oracle",
+                                "sample": f"full fwd+bwd of the first {t} tokens of the "
+                                          f"workload ({dt:.1f} s, float64 C oracle, OpenMP)"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def bench_reference(args, world, rank, local):
+    """The CPU oracle timed on the host cores (rank 0 only)."""
+    from workloads import CONFIGS
+    if rank != 0:
+        return None
+    c = CONFIGS[args.config]
+    ot = OracleTimer(c)
+    # size each step so that warm-up + steps end within a few minutes
+    budget = max(2.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    t = ot.calibrate(budget)
+    for _ in range(args.warmup):
+        ot.run(t)
+    times = [ot.run(t) for _ in range(args.steps)]
+    sec_per_token = sorted(times)[len(times) // 2] / t
+    value = 1.0 / sec_per_token
+    thr = ot.threads
+    return {
+        "impl": "reference",
+        "metric": "MoE layer fwd+bwd tokens/s on 1 GB300",
+        "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec_per_token * c.T * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{c.name}: T={c.T} d={c.d} E={c.E} top-{c.k} f={c.f}",
+                   "tokens_per_step": c.T},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr,
+                         "kind": "oracle",
+                         "sample": f"each step: full fwd+bwd of the first {t} tokens"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = bench_reference(args, world, rank, local)
+    else:
+        line = bench_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -314,14 +314,21 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     row_of = np.full(cfg.T * k, -1, np.int64)
     row_of[rows] = np.arange(len(rows))
     n = len(rows)
-    ab = np.empty((n, 2 * f)); yp = np.empty((n, d)); h = np.empty((n, f))
+    yp = np.empty((n, d)); dxp = np.empty((n, d))
     xp = src.rows("x", r["src_tok"][rows])
+    # dyp rows straight from their definition w * dy[t] (the same values combine_bwd writes)
+    slots = r["src_slot"][rows]
+    dyp = src.rows("dy", slots // k) * r["topk_w"].reshape(-1)[slots][:, None]
+    if rnd:
+        dyp = bf16(dyp)
     off = r["offsets"]
     eid = np.searchsorted(off, rows, side="right") - 1   # expert of each row
-    for e in np.unique(eid):
+    for e in np.unique(eid):           # each expert's weights are fetched once
         sel = np.nonzero(eid == e)[0]
-        ab[sel], h[sel], yp[sel] = ffn_fwd_rows(xp[sel], src.expert("W1", int(e)),
-                                                src.expert("W2", int(e)), rnd)
+        W1e, W2e = src.expert("W1", int(e)), src.expert("W2", int(e))
+        ab, _, yp[sel] = ffn_fwd_rows(xp[sel], W1e, W2e, rnd)
+        _, dxp[sel] = ffn_bwd_rows(dyp[sel], ab, W1e, W2e, rnd)
+        del W1e, W2e
     out = {"route": r, "tokens": toks}
     ys = dxs = None
     x_t = src.rows("x", toks)
@@ -329,16 +336,10 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     if cfg.fs:
         W1s, W2s = src.whole("W1s"), src.whole("W2s")
         ab_s, h_s, ys = ffn_fwd_rows(x_t, W1s, W2s, rnd)
-    out["y"] = combine(cfg, dest, r["topk_w"], yp, ys, toks=toks, yp_row_of=row_of, rnd=rnd)
-    dyp, dl = combine_bwd(cfg, src.logits, r, dy_t, yp, toks=toks, yp_row_of=row_of, rnd=rnd)
-    out["dlogits"] = dl
-    dxp = np.empty((n, d))
-    for e in np.unique(eid):
-        sel = np.nonzero(eid == e)[0]
-        _, dxp[sel] = ffn_bwd_rows(dyp[sel], ab[sel], src.expert("W1", int(e)),
-                                   src.expert("W2", int(e)), rnd)
-    if cfg.fs:
         _, dxs = ffn_bwd_rows(dy_t, ab_s, W1s, W2s, rnd)
+    out["y"] = combine(cfg, dest, r["topk_w"], yp, ys, toks=toks, yp_row_of=row_of, rnd=rnd)
+    _, dl = combine_bwd(cfg, src.logits, r, dy_t, yp, toks=toks, yp_row_of=row_of, rnd=rnd)
+    out["dlogits"] = dl
     out["dx"] = unpermute_reduce(cfg, dest, dxp, dxs, toks=toks, row_of=row_of, rnd=rnd)
 
     # weight-gradient entries of whole experts (every row of the expert contributes)

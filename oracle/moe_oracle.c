@@ -270,23 +270,36 @@ void orc_ffn_bwd_rows(int64_t n, int d, int f, const double *dyp, const double *
         const double *g = dyp + r * d;
         const double *abr = ab + r * 2 * f;
         double *dr = dab + r * 2 * f;
+        double *dx = dxr + r * d;
+        double *dh = (double *)calloc((size_t)f, sizeof(double));
+        /* dh[c] = sum_i g[i] W2e[i][c], summed over ascending i */
+        for (int i = 0; i < d; ++i) {
+            const double gi = g[i];
+            const double *w = W2e + (int64_t)i * f;
+            for (int c = 0; c < f; ++c)
+                dh[c] += gi * w[c];
+        }
         for (int c = 0; c < f; ++c) {
-            double dh = 0.0;
-            for (int i = 0; i < d; ++i)
-                dh += g[i] * W2e[(int64_t)i * f + c];
             double a = abr[c], b = abr[f + c];
             double s = 1.0 / (1.0 + exp(-a));
             double silu = a * s;
             double dsilu = s * (1.0 + a * (1.0 - s));
-            dr[c] = rb(dh * b * dsilu, rnd);
-            dr[f + c] = rb(dh * silu, rnd);
+            dr[c] = rb(dh[c] * b * dsilu, rnd);
+            dr[f + c] = rb(dh[c] * silu, rnd);
         }
-        for (int i = 0; i < d; ++i) {
-            double s = 0.0;
-            for (int c = 0; c < 2 * f; ++c)
-                s += dr[c] * W1e[(int64_t)c * d + i];
-            dxr[r * d + i] = rb(s, rnd);
+        /* dx[i] = sum_c dab[c] W1e[c][i], summed over ascending c */
+        for (int i = 0; i < d; ++i)
+            dx[i] = 0.0;
+        for (int c = 0; c < 2 * f; ++c) {
+            const double dc = dr[c];
+            const double *w = W1e + (int64_t)c * d;
+            for (int i = 0; i < d; ++i)
+                dx[i] += dc * w[i];
         }
+        if (rnd)
+            for (int i = 0; i < d; ++i)
+                dx[i] = orc_bf16(dx[i]);
+        free(dh);
     }
 }
 

@@ -1,0 +1,106 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point that
+include/moe.h declares, and its host-only logic (capacity, sizes, validation, status
+names) behaves as documented.  CPU only: nothing here launches a kernel."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import token_dispatch_expert_gb300 as tde
+from workloads import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    tde.build()
+    return tde.lib()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_binding_names_match_the_header():
+    for n in declared_symbols():
+        assert hasattr(tde, n), n
+
+
+def cfg_of(c):
+    return tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity)
+
+
+def test_capacity_from_factor(L):
+    assert tde.moe_capacity_from_factor(16384, 6, 64, 1.25) == 1920
+    assert tde.moe_capacity_from_factor(256, 2, 8, 0.5) == 32
+    assert tde.moe_capacity_from_factor(5, 2, 4, 0.8) == 2
+    assert tde.moe_capacity_from_factor(100, 2, 8, 0.0) == 0
+    assert tde.moe_capacity_from_factor(0, 2, 8, 1.0) == -1
+    for c in CONFIGS.values():
+        if c.cap_factor:
+            assert tde.moe_capacity_from_factor(c.T, c.k, c.E, c.cap_factor) == c.capacity
+
+
+def test_workspace_and_ctx_layout(L):
+    for c in CONFIGS.values():
+        cfg = cfg_of(c)
+        ws, ctx = tde.moe_workspace_size(cfg)
+        off = tde.moe_ctx_offsets(cfg)
+        assert all(o % 256 == 0 for o in off)
+        assert off == sorted(off)
+        R = c.T * c.k
+        # the saved activations alone: xp, ab, h, yp
+        assert ctx >= R * (c.d + 2 * c.f + c.f + c.d) * 2
+        assert ws >= 256
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(k=9, E=16), 2),          # k > 8 unsupported
+    (dict(E=300, k=2), 2),         # E > 256
+    (dict(d=100), 2),              # d % 64
+    (dict(ffn=96), 2),             # f % 64
+    (dict(k=5, E=4), 1),           # k > E invalid
+    (dict(T=0), 1),
+    (dict(gate=7), 1),
+    (dict(capacity=-1), 1),
+])
+def test_invalid_configs_rejected_before_launch(L, bad, status):
+    base = dict(T=64, d=128, E=8, k=2, ffn=128, ffn_shared=0, gate=0, route_scale=1.0,
+                capacity=0)
+    base.update(bad)
+    cfg = tde.MoEConfigC(**base)
+    ws, ctx = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(ws), ctypes.byref(ctx)) == status
+    # a device call with the bad config returns the same status with nothing enqueued
+    assert L.moe_permute(ctypes.byref(cfg), 16, 16, 16, 16, 16, None) == status
+
+
+def test_null_and_misaligned_pointers_rejected(L):
+    cfg = cfg_of(CONFIGS["tiny"])
+    assert L.moe_permute(ctypes.byref(cfg), None, 16, 16, 16, 16, None) == 1
+    assert L.moe_permute(ctypes.byref(cfg), 8, 16, 16, 16, 16, None) == 1   # not 16B aligned
+    assert L.moe_route(ctypes.byref(cfg), *([None] * 11), None) == 1
+    assert L.moe_layer_fwd(ctypes.byref(cfg), *([None] * 9), None) == 1
+    # the shared expert's weights are required when ffn_shared > 0
+    c = CONFIGS["dsv3"]
+    cfg = cfg_of(c)
+    assert L.moe_layer_fwd(ctypes.byref(cfg), 16, 16, 16, 16, None, None, 16, 16, 16,
+                           None) == 1
+
+
+def test_status_strings(L):
+    for s, name in tde.STATUS.items():
+        assert tde.moe_status_string(s) == name
+    assert tde.moe_status_string(99) == "MOE_ERR_UNKNOWN"

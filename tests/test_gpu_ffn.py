@@ -1,0 +1,110 @@
+"""GPU parity of the grouped SwiGLU FFN (the tcgen05 grouped GEMMs) against the oracle's
+per-expert rows: FC1 + SwiGLU epilogue, FC2, FC2 data-gradient + SwiGLU backward,
+FC1 data-gradient and the two variable-K weight gradients.  Shapes span several M, N
+and K tiles with ragged segment ends, an empty expert, N tails narrower than a tile,
+and buffer rows past offsets[E] poisoned with NaN (they must not leak into anything)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import token_dispatch_expert_gb300 as tde
+from gpu_util import assert_close, cfg_c, dev, f64, new_ws
+from workloads import CONFIGS, MoEConfig, gen_bf16, gen_inputs_host, gen_logits, gen_rows_bf16
+
+pytestmark = pytest.mark.gpu
+
+NAN_BF16 = np.uint16(0x7FC0)
+
+CASES = {
+    "tiny": CONFIGS["tiny"],
+    "ragged": MoEConfig("ragged", T=512, d=256, E=4, k=2, f=384, zipf_s=1.2),
+    "tails_empty": MoEConfig("tails_empty", T=700, d=320, E=5, k=2, f=192, cap_factor=0.9,
+                             zipf_s=1.0),
+    "single": MoEConfig("single", T=300, d=128, E=1, k=1, f=256),
+    "deepK": MoEConfig("deepK", T=256, d=1024, E=3, k=1, f=640),
+}
+
+
+def setup(c):
+    inp = gen_inputs_host(c)
+    logits = gen_logits(c)
+    if c.name == "tails_empty":
+        logits[:, 4] = -1e30            # expert 4 never selected: an empty segment
+    o = oracle.route(c, logits)
+    n = int(o["offsets"][-1])
+    R = c.T * c.k
+    xp = np.full((R, c.d), NAN_BF16, np.uint16)
+    xp[:n] = inp["x"][o["src_tok"][:n]]
+    return inp, o, n, xp
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_grouped_ffn_fwd(name):
+    c = CASES[name]
+    inp, o, n, xp = setup(c)
+    R = c.T * c.k
+    cfg = cfg_c(c)
+    ws = new_ws(cfg)
+    ab = torch.empty((R, 2 * c.f), dtype=torch.bfloat16, device="cuda")
+    h = torch.empty((R, c.f), dtype=torch.bfloat16, device="cuda")
+    yp = torch.empty((R, c.d), dtype=torch.bfloat16, device="cuda")
+    tde.moe_grouped_ffn(cfg, dev(xp), dev(o["offsets"]), dev(inp["W1"]), dev(inp["W2"]), ab, h,
+                        yp, ws)
+    off = o["offsets"]
+    r_ab = np.empty((n, 2 * c.f)); r_h = np.empty((n, c.f)); r_yp = np.empty((n, c.d))
+    for e in range(c.E):
+        s, t = int(off[e]), int(off[e + 1])
+        r_ab[s:t], r_h[s:t], r_yp[s:t] = oracle.ffn_fwd_rows(xp[s:t], inp["W1"][e], inp["W2"][e])
+    assert_close("ab", f64(ab)[:n], r_ab)
+    assert_close("h", f64(h)[:n], r_h)
+    assert_close("yp", f64(yp)[:n], r_yp)
+    assert tde.moe_status(ws) == (0, 0)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_grouped_ffn_bwd(name):
+    c = CASES[name]
+    inp, o, n, xp = setup(c)
+    R = c.T * c.k
+    off = o["offsets"]
+    # the backward's saved inputs come from the oracle's forward (rounded to bf16)
+    ab = np.empty((n, 2 * c.f)); h = np.empty((n, c.f))
+    for e in range(c.E):
+        s, t = int(off[e]), int(off[e + 1])
+        ab[s:t], h[s:t], _ = oracle.ffn_fwd_rows(xp[s:t], inp["W1"][e], inp["W2"][e])
+    dyp = gen_rows_bf16("dyp", R, c.d)
+    dyp[n:] = NAN_BF16
+
+    def bits(a, rows, cols):
+        t = torch.full((rows, cols), float("nan"), dtype=torch.bfloat16)
+        t[:n] = torch.from_numpy(a).to(torch.bfloat16)   # exact: a holds bf16 values
+        return t.cuda()
+
+    cfg = cfg_c(c)
+    ws = new_ws(cfg)
+    dab = torch.empty((R, 2 * c.f), dtype=torch.bfloat16, device="cuda")
+    dxp = torch.empty((R, c.d), dtype=torch.bfloat16, device="cuda")
+    dW1 = torch.full((c.E, 2 * c.f, c.d), 7.0, dtype=torch.bfloat16, device="cuda")
+    dW2 = torch.full((c.E, c.d, c.f), 7.0, dtype=torch.bfloat16, device="cuda")
+    tde.moe_grouped_ffn_bwd(cfg, dev(dyp), dev(xp), dev(off), dev(inp["W1"]), dev(inp["W2"]),
+                            bits(ab, R, 2 * c.f), bits(h, R, c.f), dab, dxp, dW1, dW2, ws)
+    r_dab = np.empty((n, 2 * c.f)); r_dxp = np.empty((n, c.d))
+    r_dW1 = np.zeros((c.E, 2 * c.f, c.d)); r_dW2 = np.zeros((c.E, c.d, c.f))
+    for e in range(c.E):
+        s, t = int(off[e]), int(off[e + 1])
+        r_dab[s:t], r_dxp[s:t] = oracle.ffn_bwd_rows(dyp[s:t], ab[s:t], inp["W1"][e],
+                                                     inp["W2"][e])
+        r_dW1[e], r_dW2[e] = oracle.layer.ffn_wgrad_rows(
+            oracle.layer._f64(xp[s:t]), h[s:t], oracle.layer._f64(dyp[s:t]), r_dab[s:t], c.d, c.f)
+    assert_close("dab", f64(dab)[:n], r_dab)
+    assert_close("dxp", f64(dxp)[:n], r_dxp)
+    g1, g2 = f64(dW1), f64(dW2)
+    for e in range(c.E):
+        if off[e + 1] == off[e]:
+            assert (g1[e] == 0).all() and (g2[e] == 0).all(), "empty expert must get zero dW"
+            continue
+        assert_close(f"dW1[{e}]", g1[e], oracle.bf16(r_dW1[e]))
+        assert_close(f"dW2[{e}]", g2[e], oracle.bf16(r_dW2[e]))
+    assert tde.moe_status(ws) == (0, 0)

@@ -1,0 +1,605 @@
+// grouped_gemm.cu -- the expert FFN's grouped GEMMs on the 5th-generation tensor cores.
+//
+// "MoE Training Optimization with Primus": Figure 7 (FC1 gate/up and FC2 down grouped
+// GEMMs with SwiGLU between them), the MegaMoE section (backward = FC2 data-gradient,
+// FC1 data-gradient, plus two variable-K weight-gradient GEMMs) and the JAX section
+// (one launch over the ragged, variable-M per-expert groups of a sorted-by-expert
+// layout).  X-MoE verdict page, key machinery: the groups are the padding-free
+// buffer's expert segments -- no segment is padded; a tile that crosses a segment's
+// end masks its stores, and a K-block that crosses it is zero-filled in shared memory.
+//
+// One persistent kernel per mode, one CTA per SM, 192 threads:
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage ring
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M128 x N256 x K16, bf16 in,
+//               fp32 accumulate in TMEM); tcgen05.commit frees a smem stage / hands an
+//               accumulator to the epilogue
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp its 32-lane quarter),
+//               fused SwiGLU / SwiGLU-backward, bf16 rounding, masked 16-byte stores
+// Two 256-column fp32 accumulators in TMEM (512 columns) let the epilogue of one tile
+// overlap the mainloop of the next.  The tile list is built on the device from the
+// segment offsets (no host synchronisation): tiles are ordered expert-major, then
+// N-tile, then M-tile, so CTAs running at the same time share one weight tile (read
+// from HBM once, the rest from L2).  Every wait on an mbarrier is bounded; a wait that
+// gives up sets MOE_DEVERR_TIMEOUT in the error word and the CTA drains and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int CHUNK_BYTES = 64 * BK * 2;     // one 64-element x 64-row MN-major box: 8 KB
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int MAX_G = 256;
+constexpr long long WAIT_BUDGET = 4000000000LL;   // clock cycles (about 2 s)
+
+struct Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int bad;
+  int pad;
+  int gstart[MAX_G + 2];
+  int tprefix[MAX_G + 2];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Ctl);
+
+struct KParams {
+  int G;
+  long long uniform_rows;
+  long long rows_cap;
+  int d, f;
+  int wg_M, wg_N;
+  int num_n_tiles;
+  int wg_m_tiles;
+  int num_kb;          // K blocks of the fixed-K modes
+  int n_out;           // valid output columns of the accumulator's N axis
+  const int32_t* offsets;
+  __nv_bfloat16* out0;
+  __nv_bfloat16* out1;
+  const __nv_bfloat16* aux;
+  int* err;
+};
+
+template <int MODE>
+struct ModeTraits {
+  static constexpr bool A_MN = (MODE == GEMM_WGRAD);
+  static constexpr bool B_MN = (MODE == GEMM_DGRAD2_SWIGLU || MODE == GEMM_DGRAD1 ||
+                                MODE == GEMM_WGRAD);
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Tile -> (group, m-tile, n-tile) and the K extent.
+template <int MODE>
+__device__ __forceinline__ void map_tile(const Ctl* ctl, const KParams& p, int tile, int& g,
+                                         int& mt, int& nt) {
+  if (MODE == GEMM_WGRAD) {
+    const int per = p.wg_m_tiles * p.num_n_tiles;
+    g = tile / per;
+    const int r = tile - g * per;
+    nt = r / p.wg_m_tiles;
+    mt = r - nt * p.wg_m_tiles;
+  } else {
+    int lo = 0, hi = p.G;   // tprefix[0] = 0 <= tile < tprefix[G]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ctl->tprefix[mid] <= tile) lo = mid;
+      else hi = mid;
+    }
+    g = lo;
+    const int local = tile - ctl->tprefix[g];
+    const int mtg = ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], BM);
+    nt = local / mtg;
+    mt = local - nt * mtg;
+  }
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  volatile int* abort_flag = &ctl->abort;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->tfull[b]), 1);
+      mbar_init(smem_u32(&ctl->tempty[b]), 4);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    fence_mbar_init();
+    ctl->abort = 0;
+    ctl->bad = 0;
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (p.uniform_rows > 0) {
+    if (threadIdx.x == 0) {
+      ctl->gstart[0] = 0;
+      ctl->gstart[1] = static_cast<int>(p.uniform_rows);
+    }
+  } else {
+    for (int g = threadIdx.x; g <= p.G; g += NUM_THREADS) ctl->gstart[g] = p.offsets[g];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // validate the offsets and build the tile prefix (warp scan over the groups)
+    const int per = ceil_div(p.G, 32);
+    int local = 0, bad = 0;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < p.G) {
+        const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
+        if (b < a || a < 0 || b > p.rows_cap) bad = 1;
+        int tiles = (MODE == GEMM_WGRAD) ? p.wg_m_tiles * p.num_n_tiles
+                                         : ceil_div(b - a, BM) * p.num_n_tiles;
+        if (b < a) tiles = 0;
+        local += tiles;
+      }
+    }
+    const int incl = warp_incl_scan(local);
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < p.G) {
+        ctl->tprefix[g] = run;
+        const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
+        int tiles = (MODE == GEMM_WGRAD) ? p.wg_m_tiles * p.num_n_tiles
+                                         : ceil_div(b - a, BM) * p.num_n_tiles;
+        if (b < a) tiles = 0;
+        run += tiles;
+      }
+    }
+    if (lane == 31) ctl->tprefix[p.G] = incl;
+    if (ctl->gstart[0] != 0) bad = 1;
+    bad = __any_sync(FULL_MASK, bad);
+    if (lane == 0 && bad) {
+      ctl->bad = 1;
+      if (blockIdx.x == 0) flag_error(p.err, MOE_DEVERR_BAD_OFFSETS);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = ctl->bad ? 0 : ctl->tprefix[p.G];
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int issued_ph[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued_ph[i] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int g, mt, nt;
+        map_tile<MODE>(ctl, p, tile, g, mt, nt);
+        const int seg0 = ctl->gstart[g];
+        const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(ctl->gstart[g + 1] - seg0, BK) : p.num_kb;
+        const int arow = seg0 + mt * BM;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err,
+                                 WAIT_BUDGET)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (MODE == GEMM_FC1_SWIGLU) {
+            tma_load_2d(sa, &tmA, fb, k0, arow);
+            const int wrow = g * 2 * p.f + nt * (BN / 2);
+            tma_load_2d(sb, &tmB, fb, k0, wrow);                      // gate rows
+            tma_load_2d(sb + B_BYTES / 2, &tmB, fb, k0, wrow + p.f);  // up rows
+          } else if (MODE == GEMM_FC2) {
+            tma_load_2d(sa, &tmA, fb, k0, arow);
+            tma_load_2d(sb, &tmB, fb, k0, g * p.d + nt * BN);
+          } else if (MODE == GEMM_DGRAD2_SWIGLU || MODE == GEMM_DGRAD1) {
+            tma_load_2d(sa, &tmA, fb, k0, arow);
+            const int krow = (MODE == GEMM_DGRAD2_SWIGLU ? g * p.d : g * 2 * p.f) + k0;
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * CHUNK_BYTES, &tmB, fb, nt * BN + 64 * j, krow);
+          } else {   // WGRAD
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d(sa + j * CHUNK_BYTES, &tmA, fb, mt * BM + 64 * j, seg0 + k0);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * CHUNK_BYTES, &tmB, fb, nt * BN + 64 * j, seg0 + k0);
+          }
+          issued_ph[s] = static_cast<int>(ph);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) for the copies still in flight into this CTA's smem
+        for (int i = 0; i < STAGES; ++i)
+          if (issued_ph[i] >= 0) {
+            const uint32_t fb = smem_u32(&ctl->full[i]);
+            long long t0 = clock64();
+            while (!mbar_try_wait(fb, static_cast<uint32_t>(issued_ph[i])) &&
+                   clock64() - t0 < WAIT_BUDGET / 4) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t IDESC =
+        make_idesc_bf16(BM, BN, ModeTraits<MODE>::A_MN ? 1 : 0, ModeTraits<MODE>::B_MN ? 1 : 0);
+    int s = 0;
+    uint32_t ph = 0;
+    int it = 0;
+    bool ok = true, issued_any = false;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      int g, mt, nt;
+      map_tile<MODE>(ctl, p, tile, g, mt, nt);
+      const int seg0 = ctl->gstart[g];
+      const int seg_rows = ctl->gstart[g + 1] - seg0;
+      const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
+      const int buf = it & 1;
+      const uint32_t tph = (it >> 1) & 1;
+      if (!mbar_wait_bounded(smem_u32(&ctl->tempty[buf]), tph ^ 1u, abort_flag, p.err,
+                             WAIT_BUDGET)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, WAIT_BUDGET)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_base + s * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        if (MODE == GEMM_WGRAD) {
+          const int valid = seg_rows - kb * BK;   // K rows of this block inside the segment
+          if (valid < BK) {
+            // rows past the segment end belong to the next expert (or are unwritten
+            // buffer rows): zero them in both operands so they add nothing
+            for (int idx = lane; idx < (BM / 64 + BN / 64) * 64 * 8; idx += 32) {
+              const int chunk = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
+              if (r >= valid) {
+                const uint32_t base = chunk < BM / 64 ? sa + chunk * CHUNK_BYTES
+                                                      : sb + (chunk - BM / 64) * CHUNK_BYTES;
+                st_shared_zero16(base + r * 128 + c * 16);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            uint64_t adesc, bdesc;
+            if (ModeTraits<MODE>::A_MN) adesc = make_smem_desc(sa + kk * 2048, CHUNK_BYTES, 1024);
+            else adesc = make_smem_desc(sa + kk * 32, 16, 1024);
+            if (ModeTraits<MODE>::B_MN) bdesc = make_smem_desc(sb + kk * 2048, CHUNK_BYTES, 1024);
+            else bdesc = make_smem_desc(sb + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&ctl->empty[s]));   // stage is free once these MMAs finish
+        }
+        issued_any = true;
+        __syncwarp();
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (nkb > 0) tc_commit(smem_u32(&ctl->tfull[buf]));
+        else mbar_arrive(smem_u32(&ctl->tfull[buf]));
+      }
+      __syncwarp();
+    }
+    if (!ok && issued_any && lane == 0) {
+      // drain the MMAs in flight before TMEM is released
+      tc_commit(smem_u32(&ctl->drain));
+      long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < WAIT_BUDGET / 4) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      int g, mt, nt;
+      map_tile<MODE>(ctl, p, tile, g, mt, nt);
+      const int seg0 = ctl->gstart[g];
+      const int seg_end = ctl->gstart[g + 1];
+      const int buf = it & 1;
+      const uint32_t tph = (it >> 1) & 1;
+      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[buf]), tph, abort_flag, p.err, WAIT_BUDGET))
+        break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN);
+      if (MODE == GEMM_FC1_SWIGLU) {
+        const long long prow = static_cast<long long>(seg0) + mt * BM + r_in_tile;
+        const bool valid = prow < seg_end;
+        const int f = p.f;
+#pragma unroll 1
+        for (int c = 0; c < (BN / 2) / 32; ++c) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr + c * 32, ra);
+          tmem_ld32(taddr + BN / 2 + c * 32, rb);
+          tmem_ld_wait();
+          const int n0 = nt * (BN / 2) + c * 32;
+          if (valid && n0 < f) {
+            uint4* ab_a = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
+            uint4* ab_b = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
+            uint4* hp = reinterpret_cast<uint4*>(p.out1 + prow * f + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float a[8], b[8], h[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                // round a, b to bf16 first: h is computed from the stored values
+                a[e] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(ra[v * 8 + e])));
+                b[e] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(rb[v * 8 + e])));
+                h[e] = silu_f(a[e]) * b[e];
+              }
+              ab_a[v] = pack8(a);
+              ab_b[v] = pack8(b);
+              hp[v] = pack8(h);
+            }
+          }
+        }
+      } else if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
+        const long long prow = static_cast<long long>(seg0) + mt * BM + r_in_tile;
+        const bool valid = prow < seg_end;
+        const int n_out = p.n_out;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t ra[32];
+          tmem_ld32(taddr + c * 32, ra);
+          tmem_ld_wait();
+          const int n0 = nt * BN + c * 32;
+          if (valid && n0 < n_out) {
+            uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * n_out + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ra[v * 8 + e]);
+              o[v] = pack8(x);
+            }
+          }
+        }
+      } else if (MODE == GEMM_DGRAD2_SWIGLU) {
+        const long long prow = static_cast<long long>(seg0) + mt * BM + r_in_tile;
+        const bool valid = prow < seg_end;
+        const int f = p.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t ra[32];
+          tmem_ld32(taddr + c * 32, ra);
+          tmem_ld_wait();
+          const int n0 = nt * BN + c * 32;
+          if (valid && n0 < f) {
+            const uint4* sa_ = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + n0);
+            const uint4* sb_ = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + f + n0);
+            uint4* da_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
+            uint4* db_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float a[8], b[8], da[8], db[8];
+              unpack8(__ldg(sa_ + v), a);
+              unpack8(__ldg(sb_ + v), b);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float dh = __uint_as_float(ra[v * 8 + e]);
+                const float sg = 1.0f / (1.0f + expf(-a[e]));
+                const float silu = a[e] * sg;
+                const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
+                da[e] = dh * b[e] * dsilu;
+                db[e] = dh * silu;
+              }
+              da_[v] = pack8(da);
+              db_[v] = pack8(db);
+            }
+          }
+        }
+      } else {   // WGRAD: dW[g][m][n]
+        const int m = mt * BM + r_in_tile;
+        const bool valid = m < p.wg_M;
+        const bool empty_seg = (seg_end - seg0) <= 0;
+        __nv_bfloat16* outg = p.out0 + static_cast<long long>(g) * p.wg_M * p.wg_N;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t ra[32];
+          if (!empty_seg) {
+            tmem_ld32(taddr + c * 32, ra);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ra[e] = 0u;
+          }
+          const int n0 = nt * BN + c * 32;
+          if (valid && n0 < p.wg_N) {
+            uint4* o = reinterpret_cast<uint4*>(outg + static_cast<long long>(m) * p.wg_N + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ra[v * 8 + e]);
+              o[v] = pack8(x);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[buf]));
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle,
+// box = 64 columns (128 bytes) x box_rows rows, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp,
+                        cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  kern<<<sms, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
+  if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
+  KParams kp{};
+  kp.G = a.uniform_rows > 0 ? 1 : a.G;
+  kp.uniform_rows = a.uniform_rows;
+  kp.rows_cap = a.rows_cap;
+  kp.d = a.d;
+  kp.f = a.f;
+  kp.wg_M = a.wg_M;
+  kp.wg_N = a.wg_N;
+  kp.offsets = a.offsets;
+  kp.out0 = static_cast<__nv_bfloat16*>(a.out0);
+  kp.out1 = static_cast<__nv_bfloat16*>(a.out1);
+  kp.aux = static_cast<const __nv_bfloat16*>(a.aux);
+  kp.err = a.err;
+  const uint64_t G = static_cast<uint64_t>(kp.G);
+  const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
+  const uint64_t d = static_cast<uint64_t>(a.d), f = static_cast<uint64_t>(a.f);
+  CUtensorMap ta, tb;
+  bool ok = true;
+  switch (a.mode) {
+    case GEMM_FC1_SWIGLU:
+      kp.num_n_tiles = (a.f + BN / 2 - 1) / (BN / 2);
+      kp.num_kb = a.d / BK;
+      kp.n_out = a.f;
+      ok = make_map(&ta, a.A, d, rows, BM) && make_map(&tb, a.B, d, G * 2 * f, BN / 2);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_mode<GEMM_FC1_SWIGLU>(ta, tb, kp, st);
+    case GEMM_FC2:
+      kp.num_n_tiles = (a.d + BN - 1) / BN;
+      kp.num_kb = a.f / BK;
+      kp.n_out = a.d;
+      ok = make_map(&ta, a.A, f, rows, BM) && make_map(&tb, a.B, f, G * d, BN);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_mode<GEMM_FC2>(ta, tb, kp, st);
+    case GEMM_DGRAD2_SWIGLU:
+      kp.num_n_tiles = (a.f + BN - 1) / BN;
+      kp.num_kb = a.d / BK;
+      kp.n_out = a.f;
+      ok = make_map(&ta, a.A, d, rows, BM) && make_map(&tb, a.B, f, G * d, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_mode<GEMM_DGRAD2_SWIGLU>(ta, tb, kp, st);
+    case GEMM_DGRAD1:
+      kp.num_n_tiles = (a.d + BN - 1) / BN;
+      kp.num_kb = 2 * a.f / BK;
+      kp.n_out = a.d;
+      ok = make_map(&ta, a.A, 2 * f, rows, BM) && make_map(&tb, a.B, d, G * 2 * f, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_mode<GEMM_DGRAD1>(ta, tb, kp, st);
+    case GEMM_WGRAD:
+      kp.num_n_tiles = (a.wg_N + BN - 1) / BN;
+      kp.wg_m_tiles = (a.wg_M + BM - 1) / BM;
+      kp.n_out = a.wg_N;
+      ok = make_map(&ta, a.A, static_cast<uint64_t>(a.wg_M), rows, 64) &&
+           make_map(&tb, a.B, static_cast<uint64_t>(a.wg_N), rows, 64);
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_mode<GEMM_WGRAD>(ta, tb, kp, st);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,75 @@
+// internal.h -- launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Number of 32-token chunks the routing histogram is built from.
+inline int64_t route_chunks(int64_t T) { return (T + 31) / 32; }
+
+// Scratch bytes the routing step needs inside ws (after the 256-byte header).
+inline size_t route_scratch_bytes(int64_t T, int E) {
+  return static_cast<size_t>(route_chunks(T)) * static_cast<size_t>(E) * sizeof(int32_t);
+}
+
+constexpr size_t WS_HEADER_BYTES = 256;
+
+cudaError_t launch_route(const float* logits, int64_t T, int E, int k, int gate, float scale,
+                         int capacity, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                         int32_t* kept, int32_t* offsets, int32_t* dest_row, int32_t* src_tok,
+                         int32_t* src_slot, uint8_t* drop_mask, int32_t* chunk_scratch,
+                         int* err, cudaStream_t st);
+
+cudaError_t launch_permute(const void* x, const int32_t* src_tok, const int32_t* offsets,
+                           int E, int64_t T, int64_t rows_cap, int d, void* xp, int* err,
+                           cudaStream_t st);
+
+// y[t] = sum_j w[t,j] * rows[dest_row[t,j]] (+ add[t]); w == nullptr means weight 1.
+cudaError_t launch_combine(const void* rows, const int32_t* dest_row, const float* w,
+                           const void* add, int64_t T, int k, int d, int64_t rows_cap, void* y,
+                           int* err, cudaStream_t st);
+
+cudaError_t launch_combine_bwd(const void* dy, const void* yp, const float* logits,
+                               const int32_t* topk_idx, const float* topk_w,
+                               const int32_t* dest_row, int64_t T, int E, int k, int d,
+                               int gate, float scale, int64_t rows_cap, void* dyp,
+                               float* dlogits, int* err, cudaStream_t st);
+
+// ----------------------------------------------------------------- grouped GEMM
+enum GemmMode : int {
+  GEMM_FC1_SWIGLU = 0,  // [a|b] = A W1^T, h = silu(a) b          A K-major, B K-major
+  GEMM_FC2 = 1,         // out = A W2^T                           A K-major, B K-major
+  GEMM_DGRAD2_SWIGLU = 2,  // dh = A W2; da, db from ab           A K-major, B MN-major
+  GEMM_DGRAD1 = 3,      // out = A W1                             A K-major, B MN-major
+  GEMM_WGRAD = 4,       // dW[g] = A_g^T B_g (K = rows of g)      A MN-major, B MN-major
+};
+
+struct GroupedGemmArgs {
+  int mode;
+  // groups: offsets[G+1] on the device, or a single group of `uniform_rows` rows
+  const int32_t* offsets;
+  int G;
+  int64_t uniform_rows;  // > 0: one group of this many rows, offsets ignored
+  int64_t rows_cap;      // capacity (rows) of the row-indexed buffers
+  int d;                 // model width of this expert set
+  int f;                 // SwiGLU width of this expert set
+  // operands (bf16)
+  const void* A;   // FC1: xp [rows,d]  FC2: h [rows,f]  DGRAD2: dyp [rows,d]
+                   // DGRAD1: dab [rows,2f]   WGRAD: [rows, M]
+  const void* B;   // FC1: W1 [G,2f,d]  FC2: W2 [G,d,f]  DGRAD2: W2  DGRAD1: W1
+                   // WGRAD: [rows, N]
+  int wg_M;        // WGRAD: M (= d for dW2, 2f for dW1)
+  int wg_N;        // WGRAD: N (= f for dW2, d for dW1)
+  // outputs
+  void* out0;      // FC1: ab  FC2: yp  DGRAD2: dab  DGRAD1: dxp  WGRAD: dW [G, M, N]
+  void* out1;      // FC1: h
+  const void* aux; // DGRAD2: ab (saved FC1 output)
+  int* err;
+};
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st);
+
+}  // namespace moe

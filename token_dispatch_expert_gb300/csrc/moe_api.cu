@@ -1,0 +1,412 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: host-side validation, the layout of
+// the caller-owned workspace and forward context, and the order in which the layer's
+// kernels are enqueued.  Nothing here allocates device memory or waits for the device
+// (except moe_status).
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t ALIGN = 256;
+
+size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+moe_status_t validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T <= 0 || c->E <= 0 || c->k <= 0 || c->k > c->E || c->d <= 0 || c->ffn <= 0 ||
+      c->ffn_shared < 0 || c->capacity < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->gate != MOE_GATE_SOFTMAX_TOPK && c->gate != MOE_GATE_SIGMOID_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
+  if (c->E > 256 || c->k > 8) return MOE_ERR_UNSUPPORTED;
+  if (c->d % 64 || c->ffn % 64 || c->ffn_shared % 64) return MOE_ERR_UNSUPPORTED;
+  if (c->T * static_cast<int64_t>(c->k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  // 2f rows x d of one expert must be addressable with int32 tile coordinates
+  if (static_cast<int64_t>(c->E) * 2 * c->ffn >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(c->E) * c->d >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// every pointer must be non-null and 16-byte aligned
+template <typename... P>
+bool ptrs_ok(P... ps) {
+  const void* arr[] = {static_cast<const void*>(ps)...};
+  for (const void* p : arr)
+    if (!p || !aligned16(p)) return false;
+  return true;
+}
+
+struct CtxLayout {
+  size_t off[MOE_CTX_NFIELDS];
+  size_t total;
+};
+
+CtxLayout ctx_layout(const moe_config_t* c) {
+  const size_t T = static_cast<size_t>(c->T), k = c->k, E = c->E, d = c->d, f = c->ffn,
+               fs = c->ffn_shared;
+  const size_t R = T * k;
+  size_t sz[MOE_CTX_NFIELDS];
+  sz[MOE_CTX_TOPK_IDX] = R * 4;
+  sz[MOE_CTX_TOPK_W] = R * 4;
+  sz[MOE_CTX_COUNTS] = E * 4;
+  sz[MOE_CTX_KEPT] = E * 4;
+  sz[MOE_CTX_OFFSETS] = (E + 1) * 4;
+  sz[MOE_CTX_DEST_ROW] = R * 4;
+  sz[MOE_CTX_SRC_TOK] = R * 4;
+  sz[MOE_CTX_SRC_SLOT] = R * 4;
+  sz[MOE_CTX_DROP_MASK] = R;
+  sz[MOE_CTX_XP] = R * d * 2;
+  sz[MOE_CTX_AB] = R * 2 * f * 2;
+  sz[MOE_CTX_H] = R * f * 2;
+  sz[MOE_CTX_YP] = R * d * 2;
+  sz[MOE_CTX_AB_S] = T * 2 * fs * 2;
+  sz[MOE_CTX_H_S] = T * fs * 2;
+  sz[MOE_CTX_YS] = fs ? T * d * 2 : 0;
+  CtxLayout L;
+  size_t o = 0;
+  for (int i = 0; i < MOE_CTX_NFIELDS; ++i) {
+    L.off[i] = o;
+    o += align_up(sz[i]);
+  }
+  L.total = o;
+  return L;
+}
+
+struct WsLayout {
+  size_t route, dyp, dab, dxp, dab_s, dx_s, total;
+};
+
+WsLayout ws_layout(const moe_config_t* c) {
+  const size_t T = static_cast<size_t>(c->T), k = c->k, d = c->d, f = c->ffn,
+               fs = c->ffn_shared;
+  const size_t R = T * k;
+  WsLayout L;
+  size_t o = WS_HEADER_BYTES;
+  L.route = o; o += align_up(route_scratch_bytes(c->T, c->E));
+  L.dyp = o;   o += align_up(R * d * 2);
+  L.dab = o;   o += align_up(R * 2 * f * 2);
+  L.dxp = o;   o += align_up(R * d * 2);
+  L.dab_s = o; o += align_up(T * 2 * fs * 2);
+  L.dx_s = o;  o += align_up(fs ? T * d * 2 : 0);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+template <typename T>
+const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                        \
+  do {                                                       \
+    cudaError_t e_ = (expr);                                 \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;              \
+  } while (0)
+
+GroupedGemmArgs gemm_args(int mode, const moe_config_t* c, const int32_t* offsets,
+                          int64_t uniform_rows, int d, int f, const void* A, const void* B,
+                          void* out0, void* out1, const void* aux, int* err) {
+  GroupedGemmArgs a{};
+  a.mode = mode;
+  a.offsets = offsets;
+  a.G = uniform_rows > 0 ? 1 : c->E;
+  a.uniform_rows = uniform_rows;
+  a.rows_cap = uniform_rows > 0 ? uniform_rows : c->T * c->k;
+  a.d = d;
+  a.f = f;
+  a.A = A;
+  a.B = B;
+  a.out0 = out0;
+  a.out1 = out1;
+  a.aux = aux;
+  a.err = err;
+  return a;
+}
+
+moe_status_t ffn_fwd(const moe_config_t* c, const void* xp, const int32_t* offsets,
+                     int64_t uniform_rows, int f, const void* W1, const void* W2, void* ab,
+                     void* h, void* yp, int* err, cudaStream_t st) {
+  GroupedGemmArgs a1 = gemm_args(GEMM_FC1_SWIGLU, c, offsets, uniform_rows, c->d, f, xp, W1, ab,
+                                 h, nullptr, err);
+  MOE_TRY(launch_grouped_gemm(a1, st));
+  GroupedGemmArgs a2 =
+      gemm_args(GEMM_FC2, c, offsets, uniform_rows, c->d, f, h, W2, yp, nullptr, nullptr, err);
+  MOE_TRY(launch_grouped_gemm(a2, st));
+  return MOE_OK;
+}
+
+moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
+                     const int32_t* offsets, int64_t uniform_rows, int f, const void* W1,
+                     const void* W2, const void* ab, const void* h, void* dab, void* dxp,
+                     void* dW1, void* dW2, int* err, cudaStream_t st) {
+  GroupedGemmArgs g2 = gemm_args(GEMM_DGRAD2_SWIGLU, c, offsets, uniform_rows, c->d, f, dyp, W2,
+                                 dab, nullptr, ab, err);
+  MOE_TRY(launch_grouped_gemm(g2, st));
+  GroupedGemmArgs w2 = gemm_args(GEMM_WGRAD, c, offsets, uniform_rows, c->d, f, dyp, h, dW2,
+                                 nullptr, nullptr, err);
+  w2.wg_M = c->d;
+  w2.wg_N = f;
+  MOE_TRY(launch_grouped_gemm(w2, st));
+  GroupedGemmArgs g1 = gemm_args(GEMM_DGRAD1, c, offsets, uniform_rows, c->d, f, dab, W1, dxp,
+                                 nullptr, nullptr, err);
+  MOE_TRY(launch_grouped_gemm(g1, st));
+  GroupedGemmArgs w1 = gemm_args(GEMM_WGRAD, c, offsets, uniform_rows, c->d, f, dab, xp, dW1,
+                                 nullptr, nullptr, err);
+  w1.wg_M = 2 * f;
+  w1.wg_N = c->d;
+  MOE_TRY(launch_grouped_gemm(w1, st));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_capacity_from_factor(int64_t T, int32_t k, int32_t E, double c) {
+  if (T <= 0 || k <= 0 || E <= 0) return -1;
+  if (!(c > 0.0)) return 0;
+  const long double v = static_cast<long double>(c) * static_cast<long double>(T) *
+                        static_cast<long double>(k) / static_cast<long double>(E);
+  // absorb binary representation error of c (e.g. 1.25 is exact, 0.1 is not)
+  const long double fl = std::floor(v + 1e-9L);
+  if (fl > 2147483647.0L) return 2147483647;
+  return static_cast<int32_t>(fl);
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_t* ctx_bytes) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (ws_bytes) *ws_bytes = ws_layout(cfg).total;
+  if (ctx_bytes) *ctx_bytes = ctx_layout(cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_ctx_offsets(const moe_config_t* cfg, size_t* offsets) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  CtxLayout L = ctx_layout(cfg);
+  for (int i = 0; i < MOE_CTX_NFIELDS; ++i) offsets[i] = L.off[i];
+  return MOE_OK;
+}
+
+moe_status_t moe_ws_init(void* ws, void* stream) {
+  if (!ptrs_ok(ws)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* topk_idx,
+                       float* topk_w, int32_t* counts, int32_t* kept, int32_t* offsets,
+                       int32_t* dest_row, int32_t* src_tok, int32_t* src_slot,
+                       uint8_t* drop_mask, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(logits, topk_idx, topk_w, counts, kept, offsets, dest_row, src_tok, src_slot,
+               drop_mask, ws))
+    return MOE_ERR_INVALID_ARG;
+  WsLayout W = ws_layout(cfg);
+  return cuda_status(launch_route(logits, cfg->T, cfg->E, cfg->k, cfg->gate, cfg->route_scale,
+                                  cfg->capacity, topk_idx, topk_w, counts, kept, offsets,
+                                  dest_row, src_tok, src_slot, drop_mask,
+                                  at<int32_t>(ws, W.route), static_cast<int*>(ws),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* src_tok,
+                         const int32_t* offsets, void* xp, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(x, src_tok, offsets, xp, ws)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_permute(x, src_tok, offsets, cfg->E, cfg->T, cfg->T * cfg->k, cfg->d,
+                                    xp, static_cast<int*>(ws),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* xp, const int32_t* offsets,
+                             const void* W1, const void* W2, void* ab, void* h, void* yp,
+                             void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(xp, offsets, W1, W2, ab, h, yp, ws)) return MOE_ERR_INVALID_ARG;
+  return ffn_fwd(cfg, xp, offsets, 0, cfg->ffn, W1, W2, ab, h, yp, static_cast<int*>(ws),
+                 static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* yp, const int32_t* dest_row,
+                         const float* topk_w, const void* ys_or_null, void* y, void* ws,
+                         void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(yp, dest_row, topk_w, y, ws)) return MOE_ERR_INVALID_ARG;
+  if (ys_or_null && !aligned16(ys_or_null)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(yp, dest_row, topk_w, ys_or_null, cfg->T, cfg->k, cfg->d,
+                                    cfg->T * cfg->k, y, static_cast<int*>(ws),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine_bwd(const moe_config_t* cfg, const void* dy, const void* yp,
+                             const float* logits, const int32_t* topk_idx, const float* topk_w,
+                             const int32_t* dest_row, void* dyp, float* dlogits, void* ws,
+                             void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(dy, yp, logits, topk_idx, topk_w, dest_row, dyp, dlogits, ws))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_bwd(dy, yp, logits, topk_idx, topk_w, dest_row, cfg->T,
+                                        cfg->E, cfg->k, cfg->d, cfg->gate, cfg->route_scale,
+                                        cfg->T * cfg->k, dyp, dlogits, static_cast<int*>(ws),
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_ffn_bwd(const moe_config_t* cfg, const void* dyp, const void* xp,
+                                 const int32_t* offsets, const void* W1, const void* W2,
+                                 const void* ab, const void* h, void* dab, void* dxp, void* dW1,
+                                 void* dW2, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(dyp, xp, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2, ws))
+    return MOE_ERR_INVALID_ARG;
+  return ffn_bwd(cfg, dyp, xp, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
+                 static_cast<int*>(ws), static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_unpermute_reduce(const moe_config_t* cfg, const void* dxp,
+                                  const int32_t* dest_row, const void* dxs_or_null, void* dx,
+                                  void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(dxp, dest_row, dx, ws)) return MOE_ERR_INVALID_ARG;
+  if (dxs_or_null && !aligned16(dxs_or_null)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(dxp, dest_row, nullptr, dxs_or_null, cfg->T, cfg->k, cfg->d,
+                                    cfg->T * cfg->k, dx, static_cast<int*>(ws),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_fwd(const moe_config_t* cfg, const float* logits, const void* x,
+                           const void* W1, const void* W2, const void* W1s, const void* W2s,
+                           void* y, void* ctx, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(logits, x, W1, W2, y, ctx, ws)) return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared && !ptrs_ok(W1s, W2s)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  CtxLayout C = ctx_layout(cfg);
+  WsLayout W = ws_layout(cfg);
+  int32_t* offsets = at<int32_t>(ctx, C.off[MOE_CTX_OFFSETS]);
+  MOE_TRY(launch_route(logits, cfg->T, cfg->E, cfg->k, cfg->gate, cfg->route_scale,
+                       cfg->capacity, at<int32_t>(ctx, C.off[MOE_CTX_TOPK_IDX]),
+                       at<float>(ctx, C.off[MOE_CTX_TOPK_W]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_COUNTS]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_KEPT]), offsets,
+                       at<int32_t>(ctx, C.off[MOE_CTX_DEST_ROW]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_SRC_TOK]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_SRC_SLOT]),
+                       at<uint8_t>(ctx, C.off[MOE_CTX_DROP_MASK]), at<int32_t>(ws, W.route), err,
+                       st));
+  void* xp = at<uint8_t>(ctx, C.off[MOE_CTX_XP]);
+  MOE_TRY(launch_permute(x, at<int32_t>(ctx, C.off[MOE_CTX_SRC_TOK]), offsets, cfg->E, cfg->T,
+                         cfg->T * cfg->k, cfg->d, xp, err, st));
+  void* yp = at<uint8_t>(ctx, C.off[MOE_CTX_YP]);
+  s = ffn_fwd(cfg, xp, offsets, 0, cfg->ffn, W1, W2, at<uint8_t>(ctx, C.off[MOE_CTX_AB]),
+              at<uint8_t>(ctx, C.off[MOE_CTX_H]), yp, err, st);
+  if (s != MOE_OK) return s;
+  const void* ys = nullptr;
+  if (cfg->ffn_shared) {
+    void* ysw = at<uint8_t>(ctx, C.off[MOE_CTX_YS]);
+    s = ffn_fwd(cfg, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s,
+                at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]), at<uint8_t>(ctx, C.off[MOE_CTX_H_S]), ysw,
+                err, st);
+    if (s != MOE_OK) return s;
+    ys = ysw;
+  }
+  MOE_TRY(launch_combine(yp, at<int32_t>(ctx, C.off[MOE_CTX_DEST_ROW]),
+                         at<float>(ctx, C.off[MOE_CTX_TOPK_W]), ys, cfg->T, cfg->k, cfg->d,
+                         cfg->T * cfg->k, y, err, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float* logits,
+                           const void* x, const void* dy, const void* W1, const void* W2,
+                           const void* W1s, const void* W2s, void* dx, void* dW1, void* dW2,
+                           void* dW1s, void* dW2s, float* dlogits, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(ctx, logits, x, dy, W1, W2, dx, dW1, dW2, dlogits, ws)) return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared && !ptrs_ok(W1s, W2s, dW1s, dW2s)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  CtxLayout C = ctx_layout(cfg);
+  WsLayout W = ws_layout(cfg);
+  const int32_t* offsets = at<int32_t>(ctx, C.off[MOE_CTX_OFFSETS]);
+  const int32_t* dest_row = at<int32_t>(ctx, C.off[MOE_CTX_DEST_ROW]);
+  void* dyp = at<uint8_t>(ws, W.dyp);
+  void* dab = at<uint8_t>(ws, W.dab);
+  void* dxp = at<uint8_t>(ws, W.dxp);
+  MOE_TRY(launch_combine_bwd(dy, at<uint8_t>(ctx, C.off[MOE_CTX_YP]), logits,
+                             at<int32_t>(ctx, C.off[MOE_CTX_TOPK_IDX]),
+                             at<float>(ctx, C.off[MOE_CTX_TOPK_W]), dest_row, cfg->T, cfg->E,
+                             cfg->k, cfg->d, cfg->gate, cfg->route_scale, cfg->T * cfg->k, dyp,
+                             dlogits, err, st));
+  s = ffn_bwd(cfg, dyp, at<uint8_t>(ctx, C.off[MOE_CTX_XP]), offsets, 0, cfg->ffn, W1, W2,
+              at<uint8_t>(ctx, C.off[MOE_CTX_AB]), at<uint8_t>(ctx, C.off[MOE_CTX_H]), dab, dxp,
+              dW1, dW2, err, st);
+  if (s != MOE_OK) return s;
+  const void* dxs = nullptr;
+  if (cfg->ffn_shared) {
+    void* dxsw = at<uint8_t>(ws, W.dx_s);
+    s = ffn_bwd(cfg, dy, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s,
+                at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]), at<uint8_t>(ctx, C.off[MOE_CTX_H_S]),
+                at<uint8_t>(ws, W.dab_s), dxsw, dW1s, dW2s, err, st);
+    if (s != MOE_OK) return s;
+    dxs = dxsw;
+  }
+  MOE_TRY(launch_combine(dxp, dest_row, nullptr, dxs, cfg->T, cfg->k, cfg->d, cfg->T * cfg->k,
+                         dx, err, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_status(void* ws, void* stream, int32_t* flags) {
+  if (!ptrs_ok(ws)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h) {
+    if (cudaMemsetAsync(ws, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (flags) *flags = h;
+  if (h & MOE_DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  return h ? MOE_ERR_DEVICE_FLAG : MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_FLAG: return "MOE_ERR_DEVICE_FLAG";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+}  // extern "C"
