@@ -51,7 +51,7 @@ def gemm_flops(c, rows_kept: int) -> float:
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 50 ms) while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -66,7 +66,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -188,9 +188,9 @@ def bench_ours(args, world, rank, local):
     import torch
 
     import token_dispatch_expert_gb300 as tde
-    from workloads import CONFIGS, gen_inputs_device
+    from workloads import CONFIGS, PROFILE_CONFIGS, gen_inputs_device
 
-    c = CONFIGS[args.config]
+    c = CONFIGS.get(args.config) or PROFILE_CONFIGS[args.config]
     torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
@@ -298,46 +298,49 @@ def bench_ours(args, world, rank, local):
     tokens_total = sum_over_ranks(world, float(c.T * args.steps))
     value = tokens_total / (total_ms_max / 1e3)
 
-    # end to end through the public whole-layer API, host buffers in pinned memory
-    layer = tde.MoELayer(cfg, device=dev)
-    h_logits = g["logits"].cpu().pin_memory()
-    h_x = g["x"].cpu().pin_memory()
-    h_dy = g["dy"].cpu().pin_memory()
-    d_logits = torch.empty_like(g["logits"]); d_x = torch.empty_like(g["x"])
-    d_dy = torch.empty_like(g["dy"])
-    h_y = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
-    h_dx = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
-    h_dl = torch.empty((c.T, c.E), dtype=torch.float32).pin_memory()
-    outs = {"dx": dx, "dW1": dW1, "dW2": dW2, "dlogits": dl}
-    if shared:
-        outs["dW1s"] = shared["dW1"]; outs["dW2s"] = shared["dW2"]
+    e2e_value = None
+    h2d = d2h = 0
+    if not args.no_e2e:
+        # end to end through the public whole-layer API, host buffers in pinned memory
+        layer = tde.MoELayer(cfg, device=dev)
+        h_logits = g["logits"].cpu().pin_memory()
+        h_x = g["x"].cpu().pin_memory()
+        h_dy = g["dy"].cpu().pin_memory()
+        d_logits = torch.empty_like(g["logits"]); d_x = torch.empty_like(g["x"])
+        d_dy = torch.empty_like(g["dy"])
+        h_y = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
+        h_dx = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
+        h_dl = torch.empty((c.T, c.E), dtype=torch.float32).pin_memory()
+        outs = {"dx": dx, "dW1": dW1, "dW2": dW2, "dlogits": dl}
+        if shared:
+            outs["dW1s"] = shared["dW1"]; outs["dW2s"] = shared["dW2"]
 
-    def e2e_step():
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        d_dy.copy_(h_dy, non_blocking=True)
-        yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"), y=y)
-        layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
-                       out=outs)
-        h_y.copy_(yy, non_blocking=True)
-        h_dx.copy_(outs["dx"], non_blocking=True)
-        h_dl.copy_(outs["dlogits"], non_blocking=True)
+        def e2e_step():
+            d_logits.copy_(h_logits, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+            d_dy.copy_(h_dy, non_blocking=True)
+            yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"), y=y)
+            layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
+                           out=outs)
+            h_y.copy_(yy, non_blocking=True)
+            h_dx.copy_(outs["dx"], non_blocking=True)
+            h_dl.copy_(outs["dlogits"], non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
-    e2e_value = tokens_total / (e2e_ms / 1e3)
-    h2d = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
-    d2h = h_y.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+        e2e_value = tokens_total / (e2e_ms / 1e3)
+        h2d = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
+        d2h = h_y.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
 
     peaks, peak_src = load_peaks()
     flops = gemm_flops(c, rows_kept)
@@ -371,8 +374,9 @@ def bench_ours(args, world, rank, local):
                      "traffic": None,
                      "gemm_ms_per_step": round(gemm_ms / args.steps, 4),
                      "gemm_share_of_step": round(gemm_ms / total_ms, 4)},
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_value is None else {
+            "value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -428,12 +432,13 @@ def bench_reference(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="mixtral")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -83,6 +83,14 @@ CONFIGS = {
 }
 
 
+# Smaller shapes with the same per-expert GEMM shapes, for profiler captures that must
+# stay within a few GB of device memory: Mixtral's expert (d=4096, f=14336, ~1024 rows
+# per expert) with 2 experts and top-1.
+PROFILE_CONFIGS = {
+    "mixtral_e2": MoEConfig("mixtral_e2", T=2048, d=4096, E=2, k=1, f=14336),
+}
+
+
 def _seed(seed: int, cfg_name: str, tensor: str) -> int:
     return (seed * 1_000_003 + zlib.crc32(f"{cfg_name}/{tensor}".encode())) & 0x7FFFFFFF
 
