@@ -47,7 +47,8 @@
  *     non-zero) multiples of 64.  Anything else returns MOE_ERR_UNSUPPORTED.
  *   - Thread safety: calls on different streams with disjoint buffers may run
  *     concurrently; the library keeps no mutable state of its own between calls
- *     (the error word lives in the caller's `ws`).
+ *     (the error word lives in the caller's `ws`) -- except the fixed scratch behind
+ *     moe_route_noalloc, whose own comment says how it is shared.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -147,6 +148,40 @@ moe_status_t moe_route(const moe_config_t *cfg, const float *logits, int32_t *to
                        float *topk_w, int32_t *counts, int32_t *kept, int32_t *offsets,
                        int32_t *dest_row, int32_t *src_tok, int32_t *src_slot,
                        uint8_t *drop_mask, void *ws, void *stream);
+
+/* Size of the fixed device scratch behind moe_route_noalloc (per GPU). */
+#define MOE_NOALLOC_ROUTE_SCRATCH_BYTES (1u << 20)
+
+/*
+ * moe_route_noalloc -- the routing step (same outputs, same kernels as moe_route) for
+ * callers that cannot allocate device memory, so cannot provide `ws`.  There is no
+ * counterpart of this entry point in the paper; it exists for deployment reasons.
+ *
+ * Who needs it: a plugin running inside a host framework that owns all device memory
+ * through its own pool and does not allow other code to call cudaMalloc, or a
+ * latency-critical caller that cannot accept the device-wide synchronisation that
+ * cudaMalloc / cudaFree may cause.  This call allocates nothing: the routing histogram
+ * lives in a fixed __device__ array of MOE_NOALLOC_ROUTE_SCRATCH_BYTES compiled into
+ * the library, which every GPU that loads the library holds until the process exits.
+ *
+ *   Arguments as for moe_route, except that `ws` is replaced by dev_flags_or_null: an
+ *   optional device int32 that receives the MOE_DEVERR_* bits (NaN logits); with NULL
+ *   those flags are dropped.
+ *   Limit: ceil(T/32) * E * 4 bytes must fit in MOE_NOALLOC_ROUTE_SCRATCH_BYTES (for
+ *   example T = 32768 with E = 256); larger shapes return MOE_ERR_UNSUPPORTED with
+ *   nothing enqueued.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any
+ *   stream capture.
+ *   Sharing: every call on a device uses the same array and leaves its contents behind
+ *   (the kernels overwrite every entry they read, so nothing has to be cleared between
+ *   calls); calls whose execution overlaps on the GPU -- e.g. on two streams without an
+ *   ordering between them -- race on it and must be serialised by the caller.
+ */
+moe_status_t moe_route_noalloc(const moe_config_t *cfg, const float *logits, int32_t *topk_idx,
+                               float *topk_w, int32_t *counts, int32_t *kept, int32_t *offsets,
+                               int32_t *dest_row, int32_t *src_tok, int32_t *src_slot,
+                               uint8_t *drop_mask, int32_t *dev_flags_or_null, void *stream);
 
 /*
  * F3: permute-gather into expert order (Primus MoE blog, Figure 7: "a permutation

@@ -19,7 +19,7 @@ from ._build import LIB_PATH, build  # noqa: F401
 __all__ = [
     "MoEConfigC", "MoEError", "make_config", "lib",
     "moe_capacity_from_factor", "moe_workspace_size", "moe_ctx_offsets", "moe_ws_init",
-    "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_combine_bwd",
+    "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_combine_bwd",
     "moe_grouped_ffn_bwd", "moe_unpermute_reduce", "moe_layer_fwd", "moe_layer_bwd",
     "moe_status", "moe_status_string", "ctx_views", "MoELayer", "CTX_FIELDS",
 ]
@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
             "moe_ctx_offsets": ([cfgp, ctypes.POINTER(ctypes.c_size_t)], I32),
             "moe_ws_init": ([P, P], I32),
             "moe_route": ([cfgp] + [P] * 12, I32),
+            "moe_route_noalloc": ([cfgp] + [P] * 12, I32),
             "moe_permute": ([cfgp] + [P] * 6, I32),
             "moe_grouped_ffn": ([cfgp] + [P] * 9, I32),
             "moe_combine": ([cfgp] + [P] * 7, I32),
@@ -150,6 +151,16 @@ def moe_route(cfg, logits, topk_idx, topk_w, counts, kept, offsets, dest_row, sr
     _check(lib().moe_route(_cfg(cfg), _p(logits), _p(topk_idx), _p(topk_w), _p(counts), _p(kept),
                            _p(offsets), _p(dest_row), _p(src_tok), _p(src_slot), _p(drop_mask),
                            _p(ws), _s(stream)), "moe_route")
+
+
+def moe_route_noalloc(cfg, logits, topk_idx, topk_w, counts, kept, offsets, dest_row, src_tok,
+                      src_slot, drop_mask, dev_flags=None, stream=None):
+    """moe_route without a workspace, for callers that cannot allocate device memory
+    (see include/moe.h); dev_flags is an optional device int32 for the error bits."""
+    _check(lib().moe_route_noalloc(_cfg(cfg), _p(logits), _p(topk_idx), _p(topk_w), _p(counts),
+                                   _p(kept), _p(offsets), _p(dest_row), _p(src_tok),
+                                   _p(src_slot), _p(drop_mask), _p(dev_flags), _s(stream)),
+           "moe_route_noalloc")
 
 
 def moe_permute(cfg, x, src_tok, offsets, xp, ws, stream=None):

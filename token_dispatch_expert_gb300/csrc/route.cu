@@ -21,6 +21,8 @@
 //      scan of kept gives the segment offsets.
 //   3. route_assign: one thread per (t, j): rank = chunk base + rank in chunk; kept
 //      slots get dest_row = offsets[e] + rank and fill the inverse maps.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -260,4 +262,70 @@ cudaError_t launch_route(const float* logits, int64_t T, int E, int k, int gate,
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------
+// moe_route_noalloc: the routing step for callers that cannot allocate device memory.
+//
+// Some callers cannot hand us a workspace: a plugin living inside a host framework that
+// owns every byte of device memory through its own pool (and forbids cudaMalloc from
+// anyone else), or a latency-critical caller that cannot risk the implicit device-wide
+// synchronisation a cudaMalloc/cudaFree may bring.  For them this entry point keeps the
+// routing histogram's scratch in a fixed array compiled into the library instead of in
+// the caller's `ws`.  The caller still passes every input and output.
+//
+// The array below is MOE_NOALLOC_ROUTE_SCRATCH_BYTES (1 MiB) per GPU; every GPU that loads
+// the library holds it until the process exits.  All calls share it and it keeps the last
+// call's contents (the kernels overwrite every entry they read, so nothing needs
+// clearing); calls whose execution overlaps on the GPU therefore race on it.
+namespace {
+
+__device__ __align__(256) int32_t g_noalloc_route_scratch[MOE_NOALLOC_ROUTE_SCRATCH_BYTES /
+                                                          sizeof(int32_t)];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_noalloc_once[kMaxDevices];
+int32_t* g_noalloc_ptr[kMaxDevices];
+cudaError_t g_noalloc_err[kMaxDevices];
+
+// The host-side name of a __device__ array is only a stand-in, not a device address:
+// look the real address up once per device, with that device current.
+cudaError_t noalloc_scratch(int dev, int32_t** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_noalloc_once[dev], [dev] {
+    void* p = nullptr;
+    g_noalloc_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_route_scratch);
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  });
+  *out = g_noalloc_ptr[dev];
+  return g_noalloc_err[dev];
+}
+
+}  // namespace
 }  // namespace moe
+
+extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* logits,
+                                          int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                          int32_t* kept, int32_t* offsets, int32_t* dest_row,
+                                          int32_t* src_tok, int32_t* src_slot,
+                                          uint8_t* drop_mask, int32_t* dev_flags_or_null,
+                                          void* stream) {
+  size_t ws_bytes = 0;
+  const moe_status_t s = moe_workspace_size(cfg, &ws_bytes, nullptr);   // validates cfg
+  if (s != MOE_OK) return s;
+  const void* ptrs[] = {logits, topk_idx, topk_w, counts, kept, offsets, dest_row, src_tok,
+                        src_slot, drop_mask};
+  for (const void* p : ptrs)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return MOE_ERR_INVALID_ARG;
+  if (dev_flags_or_null && (reinterpret_cast<uintptr_t>(dev_flags_or_null) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  if (moe::route_scratch_bytes(cfg->T, cfg->E) > MOE_NOALLOC_ROUTE_SCRATCH_BYTES)
+    return MOE_ERR_UNSUPPORTED;   // the fixed scratch is too small for this T x E
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t* scratch = nullptr;
+  if (moe::noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) return MOE_ERR_CUDA;
+  const cudaError_t e = moe::launch_route(
+      logits, cfg->T, cfg->E, cfg->k, cfg->gate, cfg->route_scale, cfg->capacity, topk_idx,
+      topk_w, counts, kept, offsets, dest_row, src_tok, src_slot, drop_mask, scratch,
+      dev_flags_or_null, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
