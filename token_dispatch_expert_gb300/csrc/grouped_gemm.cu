@@ -8,19 +8,23 @@
 // buffer's expert segments -- no segment is padded; a tile that crosses a segment's
 // end masks its stores, and a K-block that crosses it is zero-filled in shared memory.
 //
-// One persistent kernel per mode, one CTA per SM, 192 threads:
-//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a 4-stage ring
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M128 x N256 x K16, bf16 in,
-//               fp32 accumulate in TMEM); tcgen05.commit frees a smem stage / hands an
-//               accumulator to the epilogue
+// One persistent kernel per mode, 192 threads per CTA, one CTA per SM:
+//   warp 0      TMA producer: 128B-swizzled tiles of A and B into a shared-memory ring
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 in, fp32 accumulate in
+//               TMEM); tcgen05.commit frees a stage / hands an accumulator to the epilogue
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp its 32-lane quarter),
 //               fused SwiGLU / SwiGLU-backward, bf16 rounding, masked 16-byte stores
-// Two 256-column fp32 accumulators in TMEM (512 columns) let the epilogue of one tile
-// overlap the mainloop of the next.  The tile list is built on the device from the
-// segment offsets (no host synchronisation): tiles are ordered expert-major, then
-// N-tile, then M-tile, so CTAs running at the same time share one weight tile (read
-// from HBM once, the rest from L2).  Every wait on an mbarrier is bounded; a wait that
-// gives up sets MOE_DEVERR_TIMEOUT in the error word and the CTA drains and exits.
+// Long segments run on CTA pairs (a cluster of 2 SMs): a 256 x 256 output tile, each CTA
+// holding 128 rows of A and 128 rows of B in a 6-stage ring, the leader issuing
+// M256 x N256 x K16 pair MMAs -- half the shared-memory traffic per SM of a one-CTA
+// 128 x 256 tile.  Short segments (fine-grained experts) use one CTA with M128 x N256
+// MMAs and a 4-stage ring.  Two 256-column fp32 accumulators in TMEM (512 columns) let
+// the epilogue of one tile overlap the mainloop of the next.  The tile list is built on
+// the device from the segment offsets (no host synchronisation): tiles are ordered
+// expert-major, then N-tile, then M-tile, so CTAs running at the same time share one
+// weight tile (read from HBM once, the rest from L2).  Every wait on an mbarrier is
+// bounded; a wait that gives up sets MOE_DEVERR_TIMEOUT in the error word and the CTA
+// drains and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,19 +36,37 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// One tile is TILE_M x 256 of the output.  PAIR = 1: one CTA, M128 x N256 MMAs, A 128 rows
+// and B 256 rows per CTA.  PAIR = 2: a CTA pair (cluster of 2) shares a 256 x 256 tile:
+// each CTA holds 128 rows of A and 128 rows (N) of B, the leader issues M256 x N256 x K16
+// pair MMAs that read both CTAs' shared memory, and each CTA's TMEM receives its own 128
+// output rows.  The pair halves the shared-memory bytes each SM writes and reads per MMA.
+template <int PAIR>
+struct Geo {
+  static constexpr int BK = 64;
+  static constexpr int TILE_M = 128 * PAIR;
+  static constexpr int BN = 256;
+  static constexpr int BN_CTA = BN / PAIR;
+  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+};
+
+constexpr int BK = 64;
+constexpr int BN = 256;
 constexpr int CHUNK_BYTES = 64 * BK * 2;     // one 64-element x 64-row MN-major box: 8 KB
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_G = 256;
+constexpr int MAX_STAGES = 6;
 constexpr long long WAIT_BUDGET = 4000000000LL;   // clock cycles (about 2 s)
 
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t tailb[MAX_STAGES];
+  uint64_t tailpeer[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -56,7 +78,10 @@ struct Ctl {
   int tprefix[MAX_G + 2];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Ctl);
+template <int PAIR>
+constexpr size_t smem_bytes() {
+  return 1024 + Geo<PAIR>::STAGES * Geo<PAIR>::STAGE_BYTES + sizeof(Ctl);
+}
 
 struct KParams {
   int G;
@@ -84,8 +109,8 @@ struct ModeTraits {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Tile -> (group, m-tile, n-tile) and the K extent.
-template <int MODE>
+// Tile -> (group, m-tile, n-tile).
+template <int MODE, int PAIR>
 __device__ __forceinline__ void map_tile(const Ctl* ctl, const KParams& p, int tile, int& g,
                                          int& mt, int& nt) {
   if (MODE == GEMM_WGRAD) {
@@ -103,7 +128,7 @@ __device__ __forceinline__ void map_tile(const Ctl* ctl, const KParams& p, int t
     }
     g = lo;
     const int local = tile - ctl->tprefix[g];
-    const int mtg = ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], BM);
+    const int mtg = ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], Geo<PAIR>::TILE_M);
     nt = local / mtg;
     mt = local - nt * mtg;
   }
@@ -115,27 +140,83 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
 
-template <int MODE>
+// Every lane of the warp waits; the result is made warp-uniform so that a timeout seen by
+// one lane sends the whole warp down the same path (later warp-collective ops stay legal).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          int* err, long long budget) {
+  return __all_sync(FULL_MASK, mbar_wait_bounded(bar, parity, abort, err, budget));
+}
+
+// Issue this CTA's share of the copies of one K block into stage (sa, sb).
+template <int MODE, int PAIR>
+__device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                            const KParams& p, uint32_t sa, uint32_t sb,
+                                            uint32_t bar, bool pair_form, int rank, int g,
+                                            int mt, int nt, int seg0, int kb) {
+  using GE = Geo<PAIR>;
+  auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+    if (pair_form) tma_load_2d_pair(dst, m, bar, x, y);
+    else tma_load_2d(dst, m, bar, x, y);
+  };
+  const int k0 = kb * BK;
+  const int arow = seg0 + mt * GE::TILE_M + 128 * rank;
+  if (MODE == GEMM_FC1_SWIGLU) {
+    load(sa, tmA, k0, arow);
+    const int wrow = g * 2 * p.f + nt * (BN / 2);
+    if (PAIR == 1) {
+      load(sb, tmB, k0, wrow);                        // gate rows -> accumulator cols 0..127
+      load(sb + GE::B_BYTES / 2, tmB, k0, wrow + p.f);  // up rows -> cols 128..255
+    } else {
+      load(sb, tmB, k0, wrow + rank * p.f);           // CTA 0: gate half, CTA 1: up half
+    }
+  } else if (MODE == GEMM_FC2) {
+    load(sa, tmA, k0, arow);
+    load(sb, tmB, k0, g * p.d + nt * BN + rank * GE::BN_CTA);
+  } else if (MODE == GEMM_DGRAD2_SWIGLU || MODE == GEMM_DGRAD1) {
+    load(sa, tmA, k0, arow);
+    const int krow = (MODE == GEMM_DGRAD2_SWIGLU ? g * p.d : g * 2 * p.f) + k0;
+#pragma unroll
+    for (int j = 0; j < GE::BN_CTA / 64; ++j)
+      load(sb + j * CHUNK_BYTES, tmB, nt * BN + rank * GE::BN_CTA + 64 * j, krow);
+  } else {   // WGRAD: K rows run along the expert's segment
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      load(sa + j * CHUNK_BYTES, tmA, mt * GE::TILE_M + rank * 128 + 64 * j, seg0 + k0);
+#pragma unroll
+    for (int j = 0; j < GE::BN_CTA / 64; ++j)
+      load(sb + j * CHUNK_BYTES, tmB, nt * BN + rank * GE::BN_CTA + 64 * j, seg0 + k0);
+  }
+}
+
+template <int MODE, int PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using GE = Geo<PAIR>;
+  constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * GE::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   volatile int* abort_flag = &ctl->abort;
+  const int rank = PAIR == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / PAIR;
+  const int num_units = gridDim.x / PAIR;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->full[s]), 1);   // the leader's arrive (+ both CTAs' bytes)
       mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->tailb[s]), 1);
+      mbar_init(smem_u32(&ctl->tailpeer[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
-      mbar_init(smem_u32(&ctl->tempty[b]), 4);
+      mbar_init(smem_u32(&ctl->tempty[b]), 4 * PAIR);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     fence_mbar_init();
@@ -165,7 +246,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
         if (b < a || a < 0 || b > p.rows_cap) bad = 1;
         int tiles = (MODE == GEMM_WGRAD) ? p.wg_m_tiles * p.num_n_tiles
-                                         : ceil_div(b - a, BM) * p.num_n_tiles;
+                                         : ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
         if (b < a) tiles = 0;
         local += tiles;
       }
@@ -178,7 +259,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         ctl->tprefix[g] = run;
         const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
         int tiles = (MODE == GEMM_WGRAD) ? p.wg_m_tiles * p.num_n_tiles
-                                         : ceil_div(b - a, BM) * p.num_n_tiles;
+                                         : ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
         if (b < a) tiles = 0;
         run += tiles;
       }
@@ -192,183 +273,199 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR == 2) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR == 2) cluster_sync_all();   // barriers of both CTAs initialised before any remote use
+  else __syncthreads();
   tc_fence_after();
 
   const int total = ctl->bad ? 0 : ctl->tprefix[p.G];
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      int issued_ph[STAGES];
-      for (int i = 0; i < STAGES; ++i) issued_ph[i] = -1;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        int g, mt, nt;
-        map_tile<MODE>(ctl, p, tile, g, mt, nt);
-        const int seg0 = ctl->gstart[g];
-        const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(ctl->gstart[g + 1] - seg0, BK) : p.num_kb;
-        const int arow = seg0 + mt * BM;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err,
-                                 WAIT_BUDGET)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sa = smem_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const int k0 = kb * BK;
-          if (MODE == GEMM_FC1_SWIGLU) {
-            tma_load_2d(sa, &tmA, fb, k0, arow);
-            const int wrow = g * 2 * p.f + nt * (BN / 2);
-            tma_load_2d(sb, &tmB, fb, k0, wrow);                      // gate rows
-            tma_load_2d(sb + B_BYTES / 2, &tmB, fb, k0, wrow + p.f);  // up rows
-          } else if (MODE == GEMM_FC2) {
-            tma_load_2d(sa, &tmA, fb, k0, arow);
-            tma_load_2d(sb, &tmB, fb, k0, g * p.d + nt * BN);
-          } else if (MODE == GEMM_DGRAD2_SWIGLU || MODE == GEMM_DGRAD1) {
-            tma_load_2d(sa, &tmA, fb, k0, arow);
-            const int krow = (MODE == GEMM_DGRAD2_SWIGLU ? g * p.d : g * 2 * p.f) + k0;
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sb + j * CHUNK_BYTES, &tmB, fb, nt * BN + 64 * j, krow);
-          } else {   // WGRAD
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d(sa + j * CHUNK_BYTES, &tmA, fb, mt * BM + 64 * j, seg0 + k0);
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sb + j * CHUNK_BYTES, &tmB, fb, nt * BN + 64 * j, seg0 + k0);
-          }
-          issued_ph[s] = static_cast<int>(ph);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        // drain: wait (bounded) for the copies still in flight into this CTA's smem
-        for (int i = 0; i < STAGES; ++i)
-          if (issued_ph[i] >= 0) {
-            const uint32_t fb = smem_u32(&ctl->full[i]);
-            long long t0 = clock64();
-            while (!mbar_try_wait(fb, static_cast<uint32_t>(issued_ph[i])) &&
-                   clock64() - t0 < WAIT_BUDGET / 4) {
-            }
-          }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t IDESC =
-        make_idesc_bf16(BM, BN, ModeTraits<MODE>::A_MN ? 1 : 0, ModeTraits<MODE>::B_MN ? 1 : 0);
+    // ------------------------------------------------------------ TMA producer (whole warp)
     int s = 0;
-    uint32_t ph = 0;
-    int it = 0;
-    bool ok = true, issued_any = false;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+    uint32_t ph = 0, tail_ph = 0, peer_ph = 0;
+    bool ok = true;
+    for (int tile = unit; tile < total && ok; tile += num_units) {
       int g, mt, nt;
-      map_tile<MODE>(ctl, p, tile, g, mt, nt);
+      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
       const int seg0 = ctl->gstart[g];
       const int seg_rows = ctl->gstart[g + 1] - seg0;
       const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
-      const int buf = it & 1;
-      const uint32_t tph = (it >> 1) & 1;
-      if (!mbar_wait_bounded(smem_u32(&ctl->tempty[buf]), tph ^ 1u, abort_flag, p.err,
-                             WAIT_BUDGET)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, WAIT_BUDGET)) {
+        if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, WAIT_BUDGET)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t sa = smem_base + s * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-        if (MODE == GEMM_WGRAD) {
-          const int valid = seg_rows - kb * BK;   // K rows of this block inside the segment
-          if (valid < BK) {
-            // rows past the segment end belong to the next expert (or are unwritten
-            // buffer rows): zero them in both operands so they add nothing
-            for (int idx = lane; idx < (BM / 64 + BN / 64) * 64 * 8; idx += 32) {
-              const int chunk = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
-              if (r >= valid) {
-                const uint32_t base = chunk < BM / 64 ? sa + chunk * CHUNK_BYTES
-                                                      : sb + (chunk - BM / 64) * CHUNK_BYTES;
-                st_shared_zero16(base + r * 128 + c * 16);
-              }
+        const uint32_t sa = smem_base + s * GE::STAGE_BYTES;
+        const uint32_t sb = sa + GE::A_BYTES;
+        const uint32_t full_local = smem_u32(&ctl->full[s]);
+        const uint32_t full_leader = PAIR == 2 ? mapa_shared(full_local, 0) : full_local;
+        const int valid = seg_rows - kb * BK;
+        if (MODE != GEMM_WGRAD || valid >= BK) {
+          // the leader's single arrive announces both CTAs' bytes; the peer's copies count
+          // down the leader's barrier directly (its stage is free, so the leader's barrier
+          // for this stage has already completed its previous phase)
+          if (lane == 0) {
+            if (leader) mbar_arrive_expect_tx(full_local, PAIR * GE::STAGE_BYTES);
+            issue_loads<MODE, PAIR>(&tmA, &tmB, p, sa, sb, full_leader, PAIR == 2, rank, g, mt,
+                                    nt, seg0, kb);
+          }
+        } else {
+          // K block crossing the segment end: land it on a CTA-local barrier, zero the rows
+          // past the end (the next expert's rows, or unwritten buffer rows) in both
+          // operands, then release the stage to the MMA issuer (after the peer has too).
+          const uint32_t tb = smem_u32(&ctl->tailb[s]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(tb, GE::STAGE_BYTES);
+            issue_loads<MODE, PAIR>(&tmA, &tmB, p, sa, sb, tb, false, rank, g, mt, nt, seg0, kb);
+          }
+          if (!warp_wait(tb, (tail_ph >> s) & 1u, abort_flag, p.err, WAIT_BUDGET)) {
+            ok = false;
+            break;
+          }
+          tail_ph ^= 1u << s;
+          constexpr int CHUNKS = 2 + GE::BN_CTA / 64;   // 64 x 64 boxes in A and B
+          for (int idx = lane; idx < CHUNKS * 64 * 8; idx += 32) {
+            const int chunk = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
+            if (r >= valid) {
+              const uint32_t base = chunk < 2 ? sa + chunk * CHUNK_BYTES
+                                              : sb + (chunk - 2) * CHUNK_BYTES;
+              st_shared_zero16(base + r * 128 + c * 16);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t tp = smem_u32(&ctl->tailpeer[s]);
+          if (PAIR == 2 && !leader) {
+            if (lane == 0) mbar_arrive_cluster_release(mapa_shared(tp, 0));
+          } else {
+            if (PAIR == 2) {
+              if (!warp_wait(tp, (peer_ph >> s) & 1u, abort_flag, p.err, WAIT_BUDGET)) {
+                ok = false;
+                break;
+              }
+              peer_ph ^= 1u << s;
+            }
+            if (lane == 0) mbar_arrive(full_local);
           }
         }
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            uint64_t adesc, bdesc;
-            if (ModeTraits<MODE>::A_MN) adesc = make_smem_desc(sa + kk * 2048, CHUNK_BYTES, 1024);
-            else adesc = make_smem_desc(sa + kk * 32, 16, 1024);
-            if (ModeTraits<MODE>::B_MN) bdesc = make_smem_desc(sb + kk * 2048, CHUNK_BYTES, 1024);
-            else bdesc = make_smem_desc(sb + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&ctl->empty[s]));   // stage is free once these MMAs finish
-        }
-        issued_any = true;
-        __syncwarp();
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
       }
-      if (!ok) break;
-      if (lane == 0) {
-        if (nkb > 0) tc_commit(smem_u32(&ctl->tfull[buf]));
-        else mbar_arrive(smem_u32(&ctl->tfull[buf]));
+    }
+    // wait until every stage is free again: all commits aimed at this CTA have landed
+    for (int i = 0; i < STAGES && ok; ++i) {
+      if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, WAIT_BUDGET / 4))
+        break;
+      if (++s == STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (leader) {
+      constexpr uint32_t IDESC = make_idesc_bf16(GE::TILE_M, BN, ModeTraits<MODE>::A_MN ? 1 : 0,
+                                                 ModeTraits<MODE>::B_MN ? 1 : 0);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true, issued_any = false;
+      for (int tile = unit; tile < total && ok; tile += num_units, ++it) {
+        int g, mt, nt;
+        map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
+        const int seg_rows = ctl->gstart[g + 1] - ctl->gstart[g];
+        const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
+        const int buf = it & 1;
+        const uint32_t tph = (it >> 1) & 1;
+        if (!warp_wait(smem_u32(&ctl->tempty[buf]), tph ^ 1u, abort_flag, p.err, WAIT_BUDGET)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, WAIT_BUDGET)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * GE::STAGE_BYTES;
+          const uint32_t sb = sa + GE::A_BYTES;
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              uint64_t adesc, bdesc;
+              if (ModeTraits<MODE>::A_MN) adesc = make_smem_desc(sa + kk * 2048, CHUNK_BYTES, 1024);
+              else adesc = make_smem_desc(sa + kk * 32, 16, 1024);
+              if (ModeTraits<MODE>::B_MN) bdesc = make_smem_desc(sb + kk * 2048, CHUNK_BYTES, 1024);
+              else bdesc = make_smem_desc(sb + kk * 32, 16, 1024);
+              if (PAIR == 2) tc_mma_bf16_pair(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
+              else tc_mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
+            // the stage is free (in both CTAs) once these MMAs have read it
+            if (PAIR == 2) tc_commit_pair_mc(smem_u32(&ctl->empty[s]), 0x3);
+            else tc_commit(smem_u32(&ctl->empty[s]));
+          }
+          issued_any = true;
+          __syncwarp();
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t tf = smem_u32(&ctl->tfull[buf]);
+          if (nkb > 0) {
+            if (PAIR == 2) tc_commit_pair_mc(tf, 0x3);
+            else tc_commit(tf);
+          } else {   // an empty segment: nothing to accumulate, hand the buffer over
+            mbar_arrive(tf);
+            if (PAIR == 2) mbar_arrive_remote(mapa_shared(tf, 1));
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok && issued_any && lane == 0) {
+        // drain the MMAs in flight before TMEM is released
+        if (PAIR == 2) tc_commit_pair(smem_u32(&ctl->drain));
+        else tc_commit(smem_u32(&ctl->drain));
+        long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < WAIT_BUDGET / 4) {
+        }
       }
       __syncwarp();
     }
-    if (!ok && issued_any && lane == 0) {
-      // drain the MMAs in flight before TMEM is released
-      tc_commit(smem_u32(&ctl->drain));
-      long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < WAIT_BUDGET / 4) {
-      }
-    }
-    __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int r_in_tile = q * 32 + lane;
+    const int r_in_tile = rank * 128 + q * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = unit; tile < total; tile += num_units, ++it) {
       int g, mt, nt;
-      map_tile<MODE>(ctl, p, tile, g, mt, nt);
+      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
       const int seg0 = ctl->gstart[g];
       const int seg_end = ctl->gstart[g + 1];
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
-      if (!mbar_wait_bounded(smem_u32(&ctl->tfull[buf]), tph, abort_flag, p.err, WAIT_BUDGET))
-        break;
+      if (!warp_wait(smem_u32(&ctl->tfull[buf]), tph, abort_flag, p.err, WAIT_BUDGET)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
       if (MODE == GEMM_FC1_SWIGLU) {
-        const long long prow = static_cast<long long>(seg0) + mt * BM + r_in_tile;
+        const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
         const bool valid = prow < seg_end;
         const int f = p.f;
 #pragma unroll 1
@@ -399,7 +496,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       } else if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
-        const long long prow = static_cast<long long>(seg0) + mt * BM + r_in_tile;
+        const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
         const bool valid = prow < seg_end;
         const int n_out = p.n_out;
 #pragma unroll 1
@@ -420,7 +517,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       } else if (MODE == GEMM_DGRAD2_SWIGLU) {
-        const long long prow = static_cast<long long>(seg0) + mt * BM + r_in_tile;
+        const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
         const bool valid = prow < seg_end;
         const int f = p.f;
 #pragma unroll 1
@@ -454,7 +551,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       } else {   // WGRAD: dW[g][m][n]
-        const int m = mt * BM + r_in_tile;
+        const int m = mt * GE::TILE_M + r_in_tile;
         const bool valid = m < p.wg_M;
         const bool empty_seg = (seg_end - seg0) <= 0;
         __nv_bfloat16* outg = p.out0 + static_cast<long long>(g) * p.wg_M * p.wg_N;
@@ -483,15 +580,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[buf]));
+      if (lane == 0) {
+        const uint32_t te = smem_u32(&ctl->tempty[buf]);
+        if (PAIR == 2) mbar_arrive_remote(mapa_shared(te, 0));   // the leader's barrier
+        else mbar_arrive(te);
+      }
     }
   }
 
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
-  __syncthreads();
+  if (PAIR == 2) cluster_sync_all();   // no CTA leaves while its peer may still signal it
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) {
+    if (PAIR == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -524,18 +629,45 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, int PAIR>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp,
                         cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<MODE>;
+  auto kern = grouped_gemm_kernel<MODE, PAIR>;
+  constexpr size_t SMEM = smem_bytes<PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
+                                       static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  kern<<<sms, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, kp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = st;
+  if (PAIR == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent: as many CTA pairs as can be resident at once
+    int clusters = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+      clusters = sms / 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  } else {
+    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+  }
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, kp);
+}
+
+template <int MODE>
+cudaError_t launch_pick(bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
+                        const KParams& kp, cudaStream_t st) {
+  return pair ? launch_mode<MODE, 2>(ta, tb, kp, st) : launch_mode<MODE, 1>(ta, tb, kp, st);
 }
 
 }  // namespace
@@ -558,6 +690,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
   const uint64_t G = static_cast<uint64_t>(kp.G);
   const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
   const uint64_t d = static_cast<uint64_t>(a.d), f = static_cast<uint64_t>(a.f);
+  // The CTA pair's 256-row tile pays off when the segments are long; with short segments
+  // (e.g. many fine-grained experts) half of a 256-row tile would be masked, so the
+  // single-CTA 128-row tile is used.  The weight-gradient modes tile the fixed weight
+  // shape and always use the pair.
+  const double rows_per_group = static_cast<double>(a.rows_cap) / static_cast<double>(kp.G);
+  const bool pair_rows = rows_per_group >= 192.0;
+  const bool pair = a.mode == GEMM_WGRAD ? true : pair_rows;
+  const uint32_t b_rows = pair ? BN / 2 : BN;   // B rows (N) held by one CTA
   CUtensorMap ta, tb;
   bool ok = true;
   switch (a.mode) {
@@ -565,38 +705,38 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
       kp.num_n_tiles = (a.f + BN / 2 - 1) / (BN / 2);
       kp.num_kb = a.d / BK;
       kp.n_out = a.f;
-      ok = make_map(&ta, a.A, d, rows, BM) && make_map(&tb, a.B, d, G * 2 * f, BN / 2);
+      ok = make_map(&ta, a.A, d, rows, 128) && make_map(&tb, a.B, d, G * 2 * f, BN / 2);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_mode<GEMM_FC1_SWIGLU>(ta, tb, kp, st);
+      return launch_pick<GEMM_FC1_SWIGLU>(pair, ta, tb, kp, st);
     case GEMM_FC2:
       kp.num_n_tiles = (a.d + BN - 1) / BN;
       kp.num_kb = a.f / BK;
       kp.n_out = a.d;
-      ok = make_map(&ta, a.A, f, rows, BM) && make_map(&tb, a.B, f, G * d, BN);
+      ok = make_map(&ta, a.A, f, rows, 128) && make_map(&tb, a.B, f, G * d, b_rows);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_mode<GEMM_FC2>(ta, tb, kp, st);
+      return launch_pick<GEMM_FC2>(pair, ta, tb, kp, st);
     case GEMM_DGRAD2_SWIGLU:
       kp.num_n_tiles = (a.f + BN - 1) / BN;
       kp.num_kb = a.d / BK;
       kp.n_out = a.f;
-      ok = make_map(&ta, a.A, d, rows, BM) && make_map(&tb, a.B, f, G * d, 64);
+      ok = make_map(&ta, a.A, d, rows, 128) && make_map(&tb, a.B, f, G * d, 64);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_mode<GEMM_DGRAD2_SWIGLU>(ta, tb, kp, st);
+      return launch_pick<GEMM_DGRAD2_SWIGLU>(pair, ta, tb, kp, st);
     case GEMM_DGRAD1:
       kp.num_n_tiles = (a.d + BN - 1) / BN;
       kp.num_kb = 2 * a.f / BK;
       kp.n_out = a.d;
-      ok = make_map(&ta, a.A, 2 * f, rows, BM) && make_map(&tb, a.B, d, G * 2 * f, 64);
+      ok = make_map(&ta, a.A, 2 * f, rows, 128) && make_map(&tb, a.B, d, G * 2 * f, 64);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_mode<GEMM_DGRAD1>(ta, tb, kp, st);
+      return launch_pick<GEMM_DGRAD1>(pair, ta, tb, kp, st);
     case GEMM_WGRAD:
       kp.num_n_tiles = (a.wg_N + BN - 1) / BN;
-      kp.wg_m_tiles = (a.wg_M + BM - 1) / BM;
+      kp.wg_m_tiles = (a.wg_M + 256 - 1) / 256;
       kp.n_out = a.wg_N;
       ok = make_map(&ta, a.A, static_cast<uint64_t>(a.wg_M), rows, 64) &&
            make_map(&tb, a.B, static_cast<uint64_t>(a.wg_N), rows, 64);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_mode<GEMM_WGRAD>(ta, tb, kp, st);
+      return launch_mode<GEMM_WGRAD, 2>(ta, tb, kp, st);
     default:
       return cudaErrorInvalidValue;
   }
