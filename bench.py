@@ -176,10 +176,14 @@ class OracleTimer:
         return time.perf_counter() - t0
 
     def calibrate(self, budget_s: float) -> int:
-        """Largest token count whose run takes about budget_s seconds."""
-        probe = 2
-        dt = self.run(probe)
-        return int(min(self.c.T, max(probe, probe * budget_s / max(dt, 1e-3))))
+        """Token count whose run takes about budget_s seconds: fit time = a + b*t from two
+        probes (the weight-gradient buffers give the oracle a cost independent of t)."""
+        t1, t2 = 2, 6
+        d1, d2 = self.run(t1), self.run(t2)
+        b = max((d2 - d1) / (t2 - t1), 1e-6)
+        a = max(d1 - b * t1, 0.0)
+        t = int((budget_s - a) / b) if budget_s > a else t2
+        return int(min(self.c.T, max(t2, t)))
 
 
 # --------------------------------------------------------------------------- ours
@@ -224,44 +228,47 @@ def bench_ours(args, world, rank, local):
                       dab=torch.empty((c.T, 2 * c.fs), **bf), dx=torch.empty((c.T, c.d), **bf),
                       dW1=torch.empty_like(g["W1s"]), dW2=torch.empty_like(g["W2s"]))
     stream = torch.cuda.current_stream(dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    PHASES = ["route", "permute", "ffn_fwd", "combine", "combine_bwd", "ffn_bwd",
+              "unpermute_reduce"]
 
-    def step(record):
-        # forward
+    def step(ev):
+        # ev: len(PHASES) + 1 events recorded at the phase boundaries (or None)
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
         tde.moe_route(cfg, g["logits"], v["topk_idx"], v["topk_w"], v["counts"], v["kept"],
                       v["offsets"], v["dest_row"], v["src_tok"], v["src_slot"], v["drop_mask"],
                       ws)
+        mark(1)
         tde.moe_permute(cfg, g["x"], v["src_tok"], v["offsets"], v["xp"], ws)
-        if record:
-            ev[0].record(stream)
+        mark(2)
         tde.moe_grouped_ffn(cfg, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"], v["h"],
                             v["yp"], ws)
         if shared:
             tde.moe_grouped_ffn(shared["cfg"], g["x"], shared["off"], g["W1s"], g["W2s"],
                                 shared["ab"], shared["h"], shared["ys"], ws)
-        if record:
-            ev[1].record(stream)
+        mark(3)
         tde.moe_combine(cfg, v["yp"], v["dest_row"], v["topk_w"],
                         shared["ys"] if shared else None, y, ws)
-        # backward
+        mark(4)
         tde.moe_combine_bwd(cfg, g["dy"], v["yp"], g["logits"], v["topk_idx"], v["topk_w"],
                             v["dest_row"], dyp, dl, ws)
-        if record:
-            ev[2].record(stream)
+        mark(5)
         tde.moe_grouped_ffn_bwd(cfg, dyp, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"],
                                 v["h"], dab, dxp, dW1, dW2, ws)
         if shared:
             tde.moe_grouped_ffn_bwd(shared["cfg"], g["dy"], g["x"], shared["off"], g["W1s"],
                                     g["W2s"], shared["ab"], shared["h"], shared["dab"],
                                     shared["dx"], shared["dW1"], shared["dW2"], ws)
-        if record:
-            ev[3].record(stream)
+        mark(6)
         tde.moe_unpermute_reduce(cfg, dxp, v["dest_row"], shared["dx"] if shared else None,
                                  dx, ws)
+        mark(7)
 
     launches_per_step = 3 + 1 + 2 + 1 + 1 + 4 + 1 + (6 if shared else 0)
     for _ in range(args.warmup):
-        step(False)
+        step(None)
     torch.cuda.synchronize()
     st, fl = tde.moe_status(ws)
     if st != 0:
@@ -269,26 +276,27 @@ def bench_ours(args, world, rank, local):
     rows_kept = int(v["offsets"][-1].item())
 
     clocks = ClockSampler(local)
-    gemm_ms = 0.0
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    per_step_gemm = []
+    step_events = []
     for i in range(args.steps):
-        step(True)
-        # the events are read back after the loop (no host sync inside it)
-        per_step_gemm.append(ev[:4])
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)]
+        step(ev)   # events are read back after the loop (no host sync inside it)
+        step_events.append(ev)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    for e0, e1, e2, e3 in per_step_gemm:
-        gemm_ms += e0.elapsed_time(e1) + e2.elapsed_time(e3)
+    phase_ms = {ph: 0.0 for ph in PHASES}
+    for ev in step_events:
+        for i, ph in enumerate(PHASES):
+            phase_ms[ph] += ev[i].elapsed_time(ev[i + 1]) / args.steps
+    gemm_ms = (phase_ms["ffn_fwd"] + phase_ms["ffn_bwd"]) * args.steps
     st, fl = tde.moe_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timing: {tde.moe_status_string(st)} {fl:#x}")
@@ -344,10 +352,25 @@ def bench_ours(args, world, rank, local):
 
     peaks, peak_src = load_peaks()
     flops = gemm_flops(c, rows_kept)
-    gemm_launches = 6 * (2 if shared else 1)
     gemm_s_per_step = gemm_ms / args.steps / 1e3
     achieved = flops / gemm_s_per_step / 1e12
     peak = float(peaks["bf16_tflops"])
+    # algorithmic bytes of the HBM-bound steps (each source row read once, each
+    # destination row written once, index arrays counted)
+    T_, d_, k_, E_ = c.T, c.d, c.k, c.E
+    Rk = rows_kept
+    mem_bytes = {
+        "permute": (T_ + Rk) * d_ * 2 + Rk * 4,
+        "combine": (Rk + T_ + (T_ if c.fs else 0)) * d_ * 2 + T_ * k_ * 8,
+        "combine_bwd": (T_ + 2 * Rk) * d_ * 2 + T_ * E_ * 4 + T_ * k_ * 12,
+        "unpermute_reduce": (Rk + T_ + (T_ if c.fs else 0)) * d_ * 2 + T_ * k_ * 4,
+    }
+    hbm = float(peaks["hbm_gbs"])
+    mem = {}
+    for ph, b in mem_bytes.items():
+        gbs = b / (phase_ms[ph] * 1e-3) / 1e9
+        mem[ph] = {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
+                   "us": round(phase_ms[ph] * 1e3, 2), "bytes": b}
     line = {
         "metric": "MoE layer fwd+bwd tokens/s on 1 GB300",
         "value": round(value, 1),
@@ -377,6 +400,10 @@ def bench_ours(args, world, rank, local):
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h},
+        "permute_gbs": mem["permute"]["GB/s"],
+        "memory_kernels": dict(mem, hbm_peak_gbs=hbm,
+                               note=f"hbm_gbs of {peak_src}; CUDA events per phase, live"),
+        "phase_ms": {k2: round(v2, 4) for k2, v2 in phase_ms.items()},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }

@@ -7,10 +7,12 @@
 // dispatch/combine duality.  X-MoE verdict page, key machinery: the padding-free token
 // buffer these kernels fill and drain.
 //
-// One warp per destination row (permute) or per token (combine, its backward and the
-// reduce), 16-byte vector loads/stores (8 bf16), several rows' loads in flight per
-// lane, fp32 accumulation in slot order j = 0..k-1.  Every output element is written by
-// exactly one thread, so results are deterministic.
+// Permute walks its output as a flat array of 16-byte vectors (8 bf16), several per
+// thread.  Combine, its backward and the reduce run one warp per token and walk the row
+// in batches whose loads are all issued before any is used, so each lane keeps 8-16
+// independent 16-byte loads in flight whatever k is; the backward's dot products are
+// warp reductions.  Combine accumulates in fp32 in slot order j = 0..k-1.  Every output
+// element is written by exactly one thread: results are deterministic.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,192 +20,240 @@ namespace moe {
 namespace {
 
 constexpr int THREADS = 256;
+constexpr int VPT = 4;   // 16-byte vectors per thread in the flat kernels
 
-int grid_for(int64_t warps_needed) {
+int sm_count() {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t max_blocks = static_cast<int64_t>(sms) * 8;   // 64 warps per SM
-  const int64_t need = (warps_needed + (THREADS / 32) - 1) / (THREADS / 32);
-  return static_cast<int>(need < max_blocks ? (need > 0 ? need : 1) : max_blocks);
+  return sms;
 }
 
-// xp[p] = x[src_tok[p]] for p < offsets[E]
+// persistent grid over `items` work items of THREADS * VPT vectors each
+int grid_flat(int64_t vectors) {
+  const int64_t per_block = static_cast<int64_t>(THREADS) * VPT;
+  const int64_t need = (vectors + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+// xp[p] = x[src_tok[p]] for p < offsets[E].  The output is walked as a flat array of
+// 16-byte vectors; each thread moves VPT vectors that are THREADS apart, so a warp's
+// accesses are contiguous and every thread has VPT loads in flight.
 __global__ void __launch_bounds__(THREADS)
 permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
                const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap, int nvec,
                uint4* __restrict__ xp, int* err) {
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
-  const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
   int64_t n_rows = offsets[E];
   if (n_rows < 0 || n_rows > rows_cap) {
-    if (gw == 0 && lane == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
     n_rows = n_rows < 0 ? 0 : rows_cap;
   }
-  for (int64_t p = gw; p < n_rows; p += nw) {
-    const int t = src_tok[p];
-    if (t < 0 || t >= T) {
-      if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
-      continue;
+  const int64_t total = n_rows * nvec;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * THREADS * VPT;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * THREADS * VPT + threadIdx.x;
+       base < total; base += step) {
+    uint4 v[VPT];
+    int64_t dst[VPT];
+#pragma unroll
+    for (int u = 0; u < VPT; ++u) {
+      const int64_t idx = base + static_cast<int64_t>(u) * THREADS;
+      dst[u] = -1;
+      if (idx < total) {
+        const int64_t p = idx / nvec;
+        const int c = static_cast<int>(idx - p * nvec);
+        const int t = __ldg(src_tok + p);
+        if (t < 0 || t >= T) {
+          flag_error(err, MOE_DEVERR_BAD_INDEX);
+        } else {
+          v[u] = __ldg(x + static_cast<int64_t>(t) * nvec + c);
+          dst[u] = idx;
+        }
+      }
     }
-    const uint4* src = x + static_cast<int64_t>(t) * nvec;
-    uint4* dst = xp + p * nvec;
-    int i = lane;
-    for (; i + 96 < nvec; i += 128) {
-      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                  d = __ldg(src + i + 96);
-      dst[i] = a; dst[i + 32] = b; dst[i + 64] = c; dst[i + 96] = d;
-    }
-    for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+#pragma unroll
+    for (int u = 0; u < VPT; ++u)
+      if (dst[u] >= 0) xp[dst[u]] = v[u];
   }
 }
 
-// y[t] = sum_j w[t,j] rows[dest_row[t,j]] (+ add[t]); w == nullptr -> weight 1
+// Slot indices and weights of token t, one lane per slot, broadcast to the warp.
+template <int KMAX>
+__device__ __forceinline__ void load_slots(const int32_t* __restrict__ dest_row,
+                                           const float* __restrict__ w, int64_t t, int k,
+                                           int64_t rows_cap, int* err, int64_t* p, float* wt) {
+  const int lane = threadIdx.x & 31;
+  int my_p = -1;
+  float my_w = 1.0f;
+  if (lane < k) {
+    my_p = __ldg(dest_row + t * k + lane);
+    if (w) my_w = __ldg(w + t * k + lane);
+    if (my_p >= rows_cap || my_p < -1) {
+      flag_error(err, MOE_DEVERR_BAD_INDEX);
+      my_p = -1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    p[j] = __shfl_sync(FULL_MASK, my_p, j);
+    wt[j] = __shfl_sync(FULL_MASK, my_w, j);
+    if (j >= k) p[j] = -1;
+  }
+}
+
+// y[t] = sum_j w[t,j] rows[dest_row[t,j]] (+ add[t]); w == nullptr -> weight 1.
+// One warp per token; the row is walked in batches of B vectors per lane whose KMAX * B
+// loads are all issued before any is used (about 16 independent 16-byte loads in flight
+// per lane, whatever k is).
+template <int KMAX>
 __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ dest_row,
                const float* __restrict__ w, const uint4* __restrict__ add, int64_t T, int k,
                int nvec, int64_t rows_cap, uint4* __restrict__ y, int* err) {
+  constexpr int B = 16 / KMAX;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
   for (int64_t t = gw; t < T; t += nw) {
-    int my_p = -1;
-    float my_w = 1.0f;
-    if (lane < k) {
-      my_p = dest_row[t * k + lane];
-      if (w) my_w = w[t * k + lane];
-      if (my_p >= rows_cap || my_p < -1) {
-        flag_error(err, MOE_DEVERR_BAD_INDEX);
-        my_p = -1;
-      }
-    }
-    int64_t p[8];
-    float wt[8];
+    int64_t p[KMAX];
+    float wt[KMAX];
+    load_slots<KMAX>(dest_row, w, t, k, rows_cap, err, p, wt);
+    for (int c0 = lane; c0 < nvec; c0 += 32 * B) {
+      uint4 v[B][KMAX];
+      uint4 a[B];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      p[j] = __shfl_sync(FULL_MASK, my_p, j);
-      wt[j] = __shfl_sync(FULL_MASK, my_w, j);
-      if (j >= k) p[j] = -1;
-    }
-    for (int i = lane; i < nvec; i += 32) {
-      uint4 v[8];
+      for (int b = 0; b < B; ++b) {
+        const int c = c0 + 32 * b;
+        if (c < nvec) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (p[j] >= 0) v[j] = __ldg(rows + p[j] * nvec + i);
-      float acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (p[j] >= 0) {
-          float f[8];
-          unpack8(v[j], f);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] = fmaf(wt[j], f[q], acc[q]);
+          for (int j = 0; j < KMAX; ++j)
+            if (p[j] >= 0) v[b][j] = __ldg(rows + p[j] * nvec + c);
+          if (add) a[b] = __ldg(add + t * nvec + c);
         }
-      if (add) {
-        float f[8];
-        unpack8(__ldg(add + t * nvec + i), f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] += f[q];
       }
-      y[t * nvec + i] = pack8(acc);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int c = c0 + 32 * b;
+        if (c >= nvec) continue;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (p[j] >= 0) {
+            float f[8];
+            unpack8(v[b][j], f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(wt[j], f[q], acc[q]);
+          }
+        if (add) {
+          float f[8];
+          unpack8(a[b], f);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        }
+        y[t * nvec + c] = pack8(acc);
+      }
     }
   }
 }
 
-// dyp[p_j] = w_j dy[t]; dw_j = <dy[t], yp[p_j]>; dlogits from dw (softmax or sigmoid gate)
+// One warp per token: dyp[p_j] = w_j dy[t]; dw_j = <dy[t], yp[p_j]> (warp reduction);
+// dlogits from dw for the softmax or the sigmoid gate.  Batches of B vectors per lane with
+// all (1 + KMAX) * B loads issued first.
+template <int KMAX>
 __global__ void __launch_bounds__(THREADS)
 combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
                    const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ dest_row,
                    int64_t T, int E, int k, int nvec, int gate, float scale, int64_t rows_cap,
                    uint4* __restrict__ dyp, float* __restrict__ dlogits, int* err) {
+  constexpr int B = KMAX >= 8 ? 1 : 16 / (KMAX + 2);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
   for (int64_t t = gw; t < T; t += nw) {
-    int my_p = -1, my_e = -1;
-    float my_w = 0.0f;
+    int64_t p[KMAX];
+    float wt[KMAX];
+    load_slots<KMAX>(dest_row, topk_w, t, k, rows_cap, err, p, wt);
+    int my_e = -1;
     if (lane < k) {
-      my_p = dest_row[t * k + lane];
-      my_w = topk_w[t * k + lane];
-      my_e = topk_idx[t * k + lane];
-      if (my_p >= rows_cap || my_p < -1) {
-        flag_error(err, MOE_DEVERR_BAD_INDEX);
-        my_p = -1;
-      }
+      my_e = __ldg(topk_idx + t * k + lane);
       if (my_e < 0 || my_e >= E) {
         flag_error(err, MOE_DEVERR_BAD_INDEX);
         my_e = -1;
       }
     }
-    int64_t p[8];
-    float wt[8];
-    int se[8];
+    int se[KMAX];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      p[j] = __shfl_sync(FULL_MASK, my_p, j);
-      wt[j] = __shfl_sync(FULL_MASK, my_w, j);
-      se[j] = __shfl_sync(FULL_MASK, my_e, j);
-      if (j >= k) p[j] = -1;
-    }
-    float dot[8];
+    for (int j = 0; j < KMAX; ++j) se[j] = __shfl_sync(FULL_MASK, my_e, j);
+    float dot[KMAX];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) dot[j] = 0.0f;
-    for (int i = lane; i < nvec; i += 32) {
-      float g[8];
-      unpack8(__ldg(dy + t * nvec + i), g);
-      uint4 v[8];
+    for (int j = 0; j < KMAX; ++j) dot[j] = 0.0f;
+    for (int c0 = lane; c0 < nvec; c0 += 32 * B) {
+      uint4 g[B];
+      uint4 v[B][KMAX];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (p[j] >= 0) v[j] = __ldg(yp + p[j] * nvec + i);
+      for (int b = 0; b < B; ++b) {
+        const int c = c0 + 32 * b;
+        if (c < nvec) {
+          g[b] = __ldg(dy + t * nvec + c);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (p[j] >= 0) {
-          float f[8], o[8];
-          unpack8(v[j], f);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            dot[j] = fmaf(g[q], f[q], dot[j]);
-            o[q] = wt[j] * g[q];
-          }
-          dyp[p[j] * nvec + i] = pack8(o);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) dot[j] = warp_sum(dot[j]);
-
-    float dl[8];
-    if (gate == MOE_GATE_SOFTMAX_TOPK) {
-      float sw = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < k) sw += wt[j] * dot[j];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) dl[j] = wt[j] * (dot[j] - sw);
-    } else {
-      float s[8], S = 0.0f, sd = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        s[j] = 0.0f;
-        if (j < k && se[j] >= 0) {
-          s[j] = 1.0f / (1.0f + expf(-logits[t * E + se[j]]));
-          S += s[j];
-          sd += s[j] * dot[j];
+          for (int j = 0; j < KMAX; ++j)
+            if (p[j] >= 0) v[b][j] = __ldg(yp + p[j] * nvec + c);
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int b = 0; b < B; ++b) {
+        const int c = c0 + 32 * b;
+        if (c >= nvec) continue;
+        float gf[8];
+        unpack8(g[b], gf);
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (p[j] >= 0) {
+            float f[8], o[8];
+            unpack8(v[b][j], f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              dot[j] = fmaf(gf[q], f[q], dot[j]);
+              o[q] = wt[j] * gf[q];
+            }
+            dyp[p[j] * nvec + c] = pack8(o);
+          }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) dot[j] = warp_sum(dot[j]);
+    float dl[KMAX];
+    if (gate == MOE_GATE_SOFTMAX_TOPK) {
+      float sw = 0.0f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) sw += wt[j] * dot[j];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) dl[j] = wt[j] * (dot[j] - sw);
+    } else {
+      float sg[KMAX], S = 0.0f, sd = 0.0f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        sg[j] = 0.0f;
+        if (j < k && se[j] >= 0) {
+          sg[j] = 1.0f / (1.0f + expf(-__ldg(logits + t * E + se[j])));
+          S += sg[j];
+          sd += sg[j] * dot[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
         const float ds = scale * (dot[j] / S - sd / (S * S));
-        dl[j] = ds * s[j] * (1.0f - s[j]);
+        dl[j] = ds * sg[j] * (1.0f - sg[j]);
       }
     }
     for (int e = lane; e < E; e += 32) {
       float val = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < KMAX; ++j)
         if (j < k && se[j] == e) val = dl[j];
       dlogits[t * E + e] = val;
     }
@@ -215,18 +265,30 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
 cudaError_t launch_permute(const void* x, const int32_t* src_tok, const int32_t* offsets, int E,
                            int64_t T, int64_t rows_cap, int d, void* xp, int* err,
                            cudaStream_t st) {
-  permute_kernel<<<grid_for(rows_cap), THREADS, 0, st>>>(
+  permute_kernel<<<grid_flat(rows_cap * (d / 8)), THREADS, 0, st>>>(
       static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d / 8,
       static_cast<uint4*>(xp), err);
   return cudaGetLastError();
 }
 
+int grid_warps(int64_t warps) {
+  const int64_t need = (warps + THREADS / 32 - 1) / (THREADS / 32);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
 cudaError_t launch_combine(const void* rows, const int32_t* dest_row, const float* w,
                            const void* add, int64_t T, int k, int d, int64_t rows_cap, void* y,
                            int* err, cudaStream_t st) {
-  combine_kernel<<<grid_for(T), THREADS, 0, st>>>(
-      static_cast<const uint4*>(rows), dest_row, w, static_cast<const uint4*>(add), T, k, d / 8,
-      rows_cap, static_cast<uint4*>(y), err);
+  const int grid = grid_warps(T);
+#define MOE_COMBINE(KM)                                                                       \
+  combine_kernel<KM><<<grid, THREADS, 0, st>>>(static_cast<const uint4*>(rows), dest_row, w,    \
+                                               static_cast<const uint4*>(add), T, k, d / 8,     \
+                                               rows_cap, static_cast<uint4*>(y), err)
+  if (k <= 2) MOE_COMBINE(2);
+  else if (k <= 4) MOE_COMBINE(4);
+  else MOE_COMBINE(8);
+#undef MOE_COMBINE
   return cudaGetLastError();
 }
 
@@ -235,9 +297,15 @@ cudaError_t launch_combine_bwd(const void* dy, const void* yp, const float* logi
                                const int32_t* dest_row, int64_t T, int E, int k, int d,
                                int gate, float scale, int64_t rows_cap, void* dyp,
                                float* dlogits, int* err, cudaStream_t st) {
-  combine_bwd_kernel<<<grid_for(T), THREADS, 0, st>>>(
-      static_cast<const uint4*>(dy), static_cast<const uint4*>(yp), logits, topk_idx, topk_w,
-      dest_row, T, E, k, d / 8, gate, scale, rows_cap, static_cast<uint4*>(dyp), dlogits, err);
+  const int grid = grid_warps(T);
+#define MOE_COMBINE_BWD(KM)                                                                   \
+  combine_bwd_kernel<KM><<<grid, THREADS, 0, st>>>(                                            \
+      static_cast<const uint4*>(dy), static_cast<const uint4*>(yp), logits, topk_idx, topk_w,  \
+      dest_row, T, E, k, d / 8, gate, scale, rows_cap, static_cast<uint4*>(dyp), dlogits, err)
+  if (k <= 2) MOE_COMBINE_BWD(2);
+  else if (k <= 4) MOE_COMBINE_BWD(4);
+  else MOE_COMBINE_BWD(8);
+#undef MOE_COMBINE_BWD
   return cudaGetLastError();
 }
 

@@ -41,7 +41,7 @@ namespace {
 // each CTA holds 128 rows of A and 128 rows (N) of B, the leader issues M256 x N256 x K16
 // pair MMAs that read both CTAs' shared memory, and each CTA's TMEM receives its own 128
 // output rows.  The pair halves the shared-memory bytes each SM writes and reads per MMA.
-template <int PAIR>
+template <int MODE, int PAIR>
 struct Geo {
   static constexpr int BK = 64;
   static constexpr int TILE_M = 128 * PAIR;
@@ -50,13 +50,17 @@ struct Geo {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+  // the weight-gradient epilogue stores through shared memory with TMA: each epilogue
+  // warp double-buffers a 32-row x 64-column bf16 box (4 KB)
+  static constexpr bool TMA_STORE = MODE == GEMM_WGRAD;
+  static constexpr int STAGING_BYTES = TMA_STORE ? 4 * 2 * 4096 : 0;
+  static constexpr int STAGES = PAIR == 2 ? (TMA_STORE ? 5 : 6) : 4;
 };
 
 constexpr int BK = 64;
 constexpr int BN = 256;
 constexpr int CHUNK_BYTES = 64 * BK * 2;     // one 64-element x 64-row MN-major box: 8 KB
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;   // producer, MMA, 4 epilogue warps, tail fixer
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_G = 256;
 constexpr int MAX_STAGES = 6;
@@ -78,9 +82,10 @@ struct Ctl {
   int tprefix[MAX_G + 2];
 };
 
-template <int PAIR>
+template <int MODE, int PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 + Geo<PAIR>::STAGES * Geo<PAIR>::STAGE_BYTES + sizeof(Ctl);
+  using GE = Geo<MODE, PAIR>;
+  return 1024 + GE::STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES + sizeof(Ctl);
 }
 
 struct KParams {
@@ -128,7 +133,7 @@ __device__ __forceinline__ void map_tile(const Ctl* ctl, const KParams& p, int t
     }
     g = lo;
     const int local = tile - ctl->tprefix[g];
-    const int mtg = ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], Geo<PAIR>::TILE_M);
+    const int mtg = ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], Geo<MODE, PAIR>::TILE_M);
     nt = local / mtg;
     mt = local - nt * mtg;
   }
@@ -153,7 +158,7 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
                                             const KParams& p, uint32_t sa, uint32_t sb,
                                             uint32_t bar, bool pair_form, int rank, int g,
                                             int mt, int nt, int seg0, int kb) {
-  using GE = Geo<PAIR>;
+  using GE = Geo<MODE, PAIR>;
   auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
     if (pair_form) tma_load_2d_pair(dst, m, bar, x, y);
     else tma_load_2d(dst, m, bar, x, y);
@@ -191,13 +196,15 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
 template <int MODE, int PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using GE = Geo<PAIR>;
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const KParams p) {
+  using GE = Geo<MODE, PAIR>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * GE::STAGE_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES);
+  const uint32_t staging_base = smem_u32(smem + STAGES * GE::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   volatile int* abort_flag = &ctl->abort;
@@ -226,6 +233,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (GE::TMA_STORE) tma_prefetch_desc(&tmC);
   }
   if (p.uniform_rows > 0) {
     if (threadIdx.x == 0) {
@@ -292,7 +300,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (whole warp)
     int s = 0;
-    uint32_t ph = 0, tail_ph = 0, peer_ph = 0;
+    uint32_t ph = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += num_units) {
       int g, mt, nt;
@@ -320,42 +328,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                     nt, seg0, kb);
           }
         } else {
-          // K block crossing the segment end: land it on a CTA-local barrier, zero the rows
-          // past the end (the next expert's rows, or unwritten buffer rows) in both
-          // operands, then release the stage to the MMA issuer (after the peer has too).
-          const uint32_t tb = smem_u32(&ctl->tailb[s]);
+          // K block crossing the segment end: land it on a CTA-local barrier; the tail
+          // fixer warp zeroes the rows past the end and releases the stage
           if (lane == 0) {
-            mbar_arrive_expect_tx(tb, GE::STAGE_BYTES);
-            issue_loads<MODE, PAIR>(&tmA, &tmB, p, sa, sb, tb, false, rank, g, mt, nt, seg0, kb);
-          }
-          if (!warp_wait(tb, (tail_ph >> s) & 1u, abort_flag, p.err, WAIT_BUDGET)) {
-            ok = false;
-            break;
-          }
-          tail_ph ^= 1u << s;
-          constexpr int CHUNKS = 2 + GE::BN_CTA / 64;   // 64 x 64 boxes in A and B
-          for (int idx = lane; idx < CHUNKS * 64 * 8; idx += 32) {
-            const int chunk = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
-            if (r >= valid) {
-              const uint32_t base = chunk < 2 ? sa + chunk * CHUNK_BYTES
-                                              : sb + (chunk - 2) * CHUNK_BYTES;
-              st_shared_zero16(base + r * 128 + c * 16);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          const uint32_t tp = smem_u32(&ctl->tailpeer[s]);
-          if (PAIR == 2 && !leader) {
-            if (lane == 0) mbar_arrive_cluster_release(mapa_shared(tp, 0));
-          } else {
-            if (PAIR == 2) {
-              if (!warp_wait(tp, (peer_ph >> s) & 1u, abort_flag, p.err, WAIT_BUDGET)) {
-                ok = false;
-                break;
-              }
-              peer_ph ^= 1u << s;
-            }
-            if (lane == 0) mbar_arrive(full_local);
+            mbar_arrive_expect_tx(smem_u32(&ctl->tailb[s]), GE::STAGE_BYTES);
+            issue_loads<MODE, PAIR>(&tmA, &tmB, p, sa, sb, smem_u32(&ctl->tailb[s]), false, rank,
+                                    g, mt, nt, seg0, kb);
           }
         }
         if (++s == STAGES) {
@@ -448,9 +426,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp <= 5) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    int store_buf = 0;                      // staging buffer of the TMA-store epilogue
     const int r_in_tile = rank * 128 + q * 32 + lane;
     int it = 0;
     for (int tile = unit; tile < total; tile += num_units, ++it) {
@@ -550,31 +529,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
           }
         }
-      } else {   // WGRAD: dW[g][m][n]
-        const int m = mt * GE::TILE_M + r_in_tile;
-        const bool valid = m < p.wg_M;
+      } else {   // WGRAD: dW[g][m][n], written as 32 x 64 boxes through shared memory
+        const int m_base = mt * GE::TILE_M + rank * 128 + q * 32;   // this warp's 32 rows
+        const bool rows_ok = m_base < p.wg_M;
         const bool empty_seg = (seg_end - seg0) <= 0;
-        __nv_bfloat16* outg = p.out0 + static_cast<long long>(g) * p.wg_M * p.wg_N;
+        const uint32_t stage0 = staging_base + static_cast<uint32_t>((warp - 2) * 8192);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t ra[32];
+        for (int box = 0; box < BN / 64; ++box) {
+          uint32_t ra[32], rb[32];
           if (!empty_seg) {
-            tmem_ld32(taddr + c * 32, ra);
+            tmem_ld32(taddr + box * 64, ra);
+            tmem_ld32(taddr + box * 64 + 32, rb);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ra[e] = 0u;
+            for (int e = 0; e < 32; ++e) ra[e] = rb[e] = 0u;
           }
-          const int n0 = nt * BN + c * 32;
-          if (valid && n0 < p.wg_N) {
-            uint4* o = reinterpret_cast<uint4*>(outg + static_cast<long long>(m) * p.wg_N + n0);
+          const int n0 = nt * BN + box * 64;
+          if (rows_ok && n0 < p.wg_N) {
+            const uint32_t buf_addr = stage0 + static_cast<uint32_t>(store_buf * 4096);
+            // the box written two stores ago must have been read out of this buffer
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            // row `lane` of the box: 128 bytes = 8 chunks of 16 bytes, 128B-swizzled
+            const uint32_t row_addr = buf_addr + lane * 128;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t* src = c < 4 ? &ra[c * 8] : &rb[(c - 4) * 8];
               float x[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ra[v * 8 + e]);
-              o[v] = pack8(x);
+              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(src[e]);
+              const uint4 v = pack8(x);
+              const uint32_t dst = row_addr + ((c ^ (lane & 7)) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x),
+                           "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmC, buf_addr, n0, m_base, g);
+              bulk_commit_group();
+            }
+            store_buf ^= 1;
           }
         }
       }
@@ -585,6 +582,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (PAIR == 2) mbar_arrive_remote(mapa_shared(te, 0));   // the leader's barrier
         else mbar_arrive(te);
       }
+    }
+    if (GE::TMA_STORE && lane == 0) bulk_wait_group_all();   // stores done before exit
+  } else if (MODE == GEMM_WGRAD) {
+    // ------------------------------------------------------------ tail fixer (warp 6)
+    // Walks the same tiles as the producer; for each K block that crosses its segment's
+    // end: waits for that block's copies, zeroes the rows past the end in both operands
+    // and releases the stage to the MMA issuer (in a pair, after the peer CTA has too).
+    int s = 0;
+    uint32_t tail_ph = 0, peer_ph = 0;
+    for (int tile = unit; tile < total; tile += num_units) {
+      int g, mt, nt;
+      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
+      const int seg_rows = ctl->gstart[g + 1] - ctl->gstart[g];
+      const int nkb = ceil_div(seg_rows, BK);
+      const int valid = seg_rows - (nkb - 1) * BK;
+      if (nkb > 0 && valid < BK) {
+        const int st = (s + nkb - 1) % STAGES;
+        const uint32_t tb = smem_u32(&ctl->tailb[st]);
+        if (!warp_wait(tb, (tail_ph >> st) & 1u, abort_flag, p.err, WAIT_BUDGET)) break;
+        tail_ph ^= 1u << st;
+        const uint32_t sa = smem_base + st * GE::STAGE_BYTES;
+        const uint32_t sb = sa + GE::A_BYTES;
+        constexpr int CHUNKS = 2 + GE::BN_CTA / 64;   // 64 x 64 boxes in A and B
+        for (int idx = lane; idx < CHUNKS * 64 * 8; idx += 32) {
+          const int chunk = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
+          if (r >= valid) {
+            const uint32_t base = chunk < 2 ? sa + chunk * CHUNK_BYTES
+                                            : sb + (chunk - 2) * CHUNK_BYTES;
+            st_shared_zero16(base + r * 128 + c * 16);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const uint32_t tp = smem_u32(&ctl->tailpeer[st]);
+        if (PAIR == 2 && !leader) {
+          if (lane == 0) mbar_arrive_cluster_release(mapa_shared(tp, 0));
+        } else {
+          if (PAIR == 2) {
+            if (!warp_wait(tp, (peer_ph >> st) & 1u, abort_flag, p.err, WAIT_BUDGET)) break;
+            peer_ph ^= 1u << st;
+          }
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->full[st]));
+        }
+      }
+      s = (s + nkb) % STAGES;
     }
   }
 
@@ -629,11 +671,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map over dW viewed as [groups][rows][cols], 128-byte swizzle, box =
+// 64 columns x 32 rows x 1 group: a store never crosses into the next group's rows.
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t groups) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, groups};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MODE, int PAIR>
-cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp,
-                        cudaStream_t st) {
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        const KParams& kp, cudaStream_t st) {
   auto kern = grouped_gemm_kernel<MODE, PAIR>;
-  constexpr size_t SMEM = smem_bytes<PAIR>();
+  constexpr size_t SMEM = smem_bytes<MODE, PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
@@ -661,13 +718,15 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KPar
   } else {
     cfg.gridDim = dim3(static_cast<unsigned>(sms));
   }
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, kp);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp);
 }
 
 template <int MODE>
 cudaError_t launch_pick(bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
                         const KParams& kp, cudaStream_t st) {
-  return pair ? launch_mode<MODE, 2>(ta, tb, kp, st) : launch_mode<MODE, 1>(ta, tb, kp, st);
+  // the output map is used by the weight-gradient mode only; the others pass tb through
+  return pair ? launch_mode<MODE, 2>(ta, tb, tb, kp, st)
+              : launch_mode<MODE, 1>(ta, tb, tb, kp, st);
 }
 
 }  // namespace
@@ -733,10 +792,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
       kp.num_n_tiles = (a.wg_N + BN - 1) / BN;
       kp.wg_m_tiles = (a.wg_M + 256 - 1) / 256;
       kp.n_out = a.wg_N;
-      ok = make_map(&ta, a.A, static_cast<uint64_t>(a.wg_M), rows, 64) &&
-           make_map(&tb, a.B, static_cast<uint64_t>(a.wg_N), rows, 64);
-      if (!ok) return cudaErrorInvalidValue;
-      return launch_mode<GEMM_WGRAD, 2>(ta, tb, kp, st);
+      {
+        CUtensorMap tc;
+        ok = make_map(&ta, a.A, static_cast<uint64_t>(a.wg_M), rows, 64) &&
+             make_map(&tb, a.B, static_cast<uint64_t>(a.wg_N), rows, 64) &&
+             make_map_3d(&tc, a.out0, static_cast<uint64_t>(a.wg_N),
+                         static_cast<uint64_t>(a.wg_M), G);
+        if (!ok) return cudaErrorInvalidValue;
+        return launch_mode<GEMM_WGRAD, 2>(ta, tb, tc, kp, st);
+      }
     default:
       return cudaErrorInvalidValue;
   }
