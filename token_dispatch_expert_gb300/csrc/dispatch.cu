@@ -7,11 +7,10 @@
 // dispatch/combine duality.  X-MoE verdict page, key machinery: the padding-free token
 // buffer these kernels fill and drain.
 //
-// Permute walks its output as a flat array of 16-byte vectors (8 bf16), several per
-// thread.  Combine, its backward and the reduce run one warp per token and walk the row
-// in batches whose loads are all issued before any is used, so each lane keeps 8-16
-// independent 16-byte loads in flight whatever k is; the backward's dot products are
-// warp reductions.  Combine accumulates in fp32 in slot order j = 0..k-1.  Every output
+// Permute runs one warp per destination row, combine, its backward and the reduce one
+// warp per token; each walks its rows in batches of 16-byte vectors (8 bf16) whose loads
+// are all issued before any is used, so each lane keeps 12-18 independent loads in
+// flight whatever k is; the backward's dot products are warp reductions.  Combine accumulates in fp32 in slot order j = 0..k-1.  Every output
 // element is written by exactly one thread: results are deterministic.
 #include "common.cuh"
 #include "internal.h"
@@ -20,7 +19,6 @@ namespace moe {
 namespace {
 
 constexpr int THREADS = 256;
-constexpr int VPT = 4;   // 16-byte vectors per thread in the flat kernels
 
 int sm_count() {
   int dev = 0, sms = 148;
@@ -29,51 +27,45 @@ int sm_count() {
   return sms;
 }
 
-// persistent grid over `items` work items of THREADS * VPT vectors each
-int grid_flat(int64_t vectors) {
-  const int64_t per_block = static_cast<int64_t>(THREADS) * VPT;
-  const int64_t need = (vectors + per_block - 1) / per_block;
+// persistent grid of warps (8 CTAs of 8 warps per SM at most)
+int grid_warps(int64_t warps) {
+  const int64_t need = (warps + THREADS / 32 - 1) / (THREADS / 32);
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
-// xp[p] = x[src_tok[p]] for p < offsets[E].  The output is walked as a flat array of
-// 16-byte vectors; each thread moves VPT vectors that are THREADS apart, so a warp's
-// accesses are contiguous and every thread has VPT loads in flight.
+// xp[p] = x[src_tok[p]] for p < offsets[E].  One warp per destination row; the row is
+// copied in batches of 16 vectors per lane whose loads are all issued first.
 __global__ void __launch_bounds__(THREADS)
 permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
                const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap, int nvec,
                uint4* __restrict__ xp, int* err) {
+  constexpr int B = 16;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
   int64_t n_rows = offsets[E];
   if (n_rows < 0 || n_rows > rows_cap) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
+    if (gw == 0 && lane == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
     n_rows = n_rows < 0 ? 0 : rows_cap;
   }
-  const int64_t total = n_rows * nvec;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * THREADS * VPT;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * THREADS * VPT + threadIdx.x;
-       base < total; base += step) {
-    uint4 v[VPT];
-    int64_t dst[VPT];
-#pragma unroll
-    for (int u = 0; u < VPT; ++u) {
-      const int64_t idx = base + static_cast<int64_t>(u) * THREADS;
-      dst[u] = -1;
-      if (idx < total) {
-        const int64_t p = idx / nvec;
-        const int c = static_cast<int>(idx - p * nvec);
-        const int t = __ldg(src_tok + p);
-        if (t < 0 || t >= T) {
-          flag_error(err, MOE_DEVERR_BAD_INDEX);
-        } else {
-          v[u] = __ldg(x + static_cast<int64_t>(t) * nvec + c);
-          dst[u] = idx;
-        }
-      }
+  for (int64_t p = gw; p < n_rows; p += nw) {
+    const int t = __ldg(src_tok + p);
+    if (t < 0 || t >= T) {
+      if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
+      continue;
     }
+    const uint4* src = x + static_cast<int64_t>(t) * nvec;
+    uint4* dst = xp + p * nvec;
+    for (int c0 = lane; c0 < nvec; c0 += 32 * B) {
+      uint4 v[B];
 #pragma unroll
-    for (int u = 0; u < VPT; ++u)
-      if (dst[u] >= 0) xp[dst[u]] = v[u];
+      for (int b = 0; b < B; ++b)
+        if (c0 + 32 * b < nvec) v[b] = __ldg(src + c0 + 32 * b);
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+        if (c0 + 32 * b < nvec) dst[c0 + 32 * b] = v[b];
+    }
   }
 }
 
@@ -110,7 +102,7 @@ __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ dest_row,
                const float* __restrict__ w, const uint4* __restrict__ add, int64_t T, int k,
                int nvec, int64_t rows_cap, uint4* __restrict__ y, int* err) {
-  constexpr int B = 16 / KMAX;
+  constexpr int B = KMAX == 6 ? 3 : 16 / KMAX;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
@@ -168,7 +160,7 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ dest_row,
                    int64_t T, int E, int k, int nvec, int gate, float scale, int64_t rows_cap,
                    uint4* __restrict__ dyp, float* __restrict__ dlogits, int* err) {
-  constexpr int B = KMAX >= 8 ? 1 : 16 / (KMAX + 2);
+  constexpr int B = KMAX >= 6 ? 2 : 16 / (KMAX + 2);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * THREADS) >> 5;
@@ -265,16 +257,10 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
 cudaError_t launch_permute(const void* x, const int32_t* src_tok, const int32_t* offsets, int E,
                            int64_t T, int64_t rows_cap, int d, void* xp, int* err,
                            cudaStream_t st) {
-  permute_kernel<<<grid_flat(rows_cap * (d / 8)), THREADS, 0, st>>>(
+  permute_kernel<<<grid_warps(rows_cap), THREADS, 0, st>>>(
       static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d / 8,
       static_cast<uint4*>(xp), err);
   return cudaGetLastError();
-}
-
-int grid_warps(int64_t warps) {
-  const int64_t need = (warps + THREADS / 32 - 1) / (THREADS / 32);
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
-  return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
 cudaError_t launch_combine(const void* rows, const int32_t* dest_row, const float* w,
@@ -287,6 +273,7 @@ cudaError_t launch_combine(const void* rows, const int32_t* dest_row, const floa
                                                rows_cap, static_cast<uint4*>(y), err)
   if (k <= 2) MOE_COMBINE(2);
   else if (k <= 4) MOE_COMBINE(4);
+  else if (k <= 6) MOE_COMBINE(6);
   else MOE_COMBINE(8);
 #undef MOE_COMBINE
   return cudaGetLastError();
@@ -304,6 +291,7 @@ cudaError_t launch_combine_bwd(const void* dy, const void* yp, const float* logi
       dest_row, T, E, k, d / 8, gate, scale, rows_cap, static_cast<uint4*>(dyp), dlogits, err)
   if (k <= 2) MOE_COMBINE_BWD(2);
   else if (k <= 4) MOE_COMBINE_BWD(4);
+  else if (k <= 6) MOE_COMBINE_BWD(6);
   else MOE_COMBINE_BWD(8);
 #undef MOE_COMBINE_BWD
   return cudaGetLastError();
