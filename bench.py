@@ -120,24 +120,33 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, value: float) -> float:
+def _reduce(world, value: float, op) -> float:
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    device = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(world, value: float) -> float:
+    import torch.distributed as dist
+    return _reduce(world, value, dist.ReduceOp.MAX) if world > 1 else value
 
 
 def sum_over_ranks(world, value: float) -> float:
-    if world == 1:
-        return value
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(world, value, dist.ReduceOp.SUM) if world > 1 else value
+
+
+def replica_throughput(world, tokens_local: float, ms_local: float):
+    """Whole-job throughput of independent replicas: all ranks' tokens over the slowest
+    rank's time.  Returns (tokens_total, ms_max, tokens_per_s)."""
+    ms_max = max_over_ranks(world, ms_local)
+    tokens_total = sum_over_ranks(world, tokens_local)
+    return tokens_total, ms_max, tokens_total / (ms_max / 1e3)
 
 
 # --------------------------------------------------------------------------- oracle timing
@@ -301,10 +310,9 @@ def bench_ours(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device status after timing: {tde.moe_status_string(st)} {fl:#x}")
 
-    total_ms_max = max_over_ranks(world, total_ms)
+    tokens_total, total_ms_max, value = replica_throughput(world, float(c.T * args.steps),
+                                                           total_ms)
     ms_per_step = total_ms_max / args.steps
-    tokens_total = sum_over_ranks(world, float(c.T * args.steps))
-    value = tokens_total / (total_ms_max / 1e3)
 
     e2e_value = None
     h2d = d2h = 0

@@ -272,6 +272,17 @@ moe_status_t moe_layer_bwd(const moe_config_t *cfg, const void *ctx, const float
                            const void *W1s, const void *W2s, void *dx, void *dW1, void *dW2,
                            void *dW1s, void *dW2s, float *dlogits, void *ws, void *stream);
 
+/*
+ * Diagnostics: exercises the device-side failure path without a GPU fault.  Enqueues one
+ * small kernel that waits on an mbarrier nothing will ever complete, with the same bounded
+ * wait the grouped GEMM uses, limited to `budget_cycles` SM clock cycles (clamped to
+ * 2e9, about one second).  When the wait gives up it sets MOE_DEVERR_TIMEOUT in the error
+ * word of `ws` and returns normally, so moe_status() then reports MOE_ERR_TIMEOUT and
+ * the context stays usable.  (Not part of the layer; there is no counterpart on the
+ * pages.)
+ */
+moe_status_t moe_selftest_wait_timeout(void *ws, int64_t budget_cycles, void *stream);
+
 /* Synchronise `stream`, then read and clear the device error word in `ws`.
  * Returns MOE_OK, MOE_ERR_DEVICE_FLAG or MOE_ERR_TIMEOUT (MOE_DEVERR_TIMEOUT set),
  * or MOE_ERR_CUDA; *flags (may be NULL) receives the MOE_DEVERR_* bits. */

@@ -21,7 +21,7 @@ __all__ = [
     "moe_capacity_from_factor", "moe_workspace_size", "moe_ctx_offsets", "moe_ws_init",
     "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_combine_bwd",
     "moe_grouped_ffn_bwd", "moe_unpermute_reduce", "moe_layer_fwd", "moe_layer_bwd",
-    "moe_status", "moe_status_string", "ctx_views", "MoELayer", "CTX_FIELDS",
+    "moe_status", "moe_status_string", "moe_selftest_wait_timeout", "ctx_views", "MoELayer", "CTX_FIELDS",
 ]
 
 GATES = {"softmax": 0, "sigmoid": 1}
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "moe_layer_fwd": ([cfgp] + [P] * 10, I32),
             "moe_layer_bwd": ([cfgp] + [P] * 16, I32),
             "moe_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], I32),
+            "moe_selftest_wait_timeout": ([P, I64, P], I32),
             "moe_status_string": ([I32], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -207,6 +208,12 @@ def moe_layer_bwd(cfg, ctx, logits, x, dy, W1, W2, W1s, W2s, dx, dW1, dW2, dW1s,
     _check(lib().moe_layer_bwd(_cfg(cfg), _p(ctx), _p(logits), _p(x), _p(dy), _p(W1), _p(W2),
                                _p(W1s), _p(W2s), _p(dx), _p(dW1), _p(dW2), _p(dW1s), _p(dW2s),
                                _p(dlogits), _p(ws), _s(stream)), "moe_layer_bwd")
+
+
+def moe_selftest_wait_timeout(ws, budget_cycles, stream=None):
+    """Enqueue a bounded wait that is never satisfied (see include/moe.h)."""
+    _check(lib().moe_selftest_wait_timeout(_p(ws), int(budget_cycles), _s(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_status(ws, stream=None):

@@ -173,6 +173,20 @@ moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
   return MOE_OK;
 }
 
+// A wait that nothing will complete: the bounded wait gives up, flags the timeout and the
+// kernel returns (the path every pipeline wait of the grouped GEMM takes on a stall).
+__global__ void selftest_wait_kernel(int* err, long long budget) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, err, budget);
+}
+
 }  // namespace
 
 extern "C" {
@@ -379,6 +393,14 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float
   MOE_TRY(launch_combine(dxp, dest_row, nullptr, dxs, cfg->T, cfg->k, cfg->d, cfg->T * cfg->k,
                          dx, err, st));
   return MOE_OK;
+}
+
+moe_status_t moe_selftest_wait_timeout(void* ws, int64_t budget_cycles, void* stream) {
+  if (!ptrs_ok(ws) || budget_cycles <= 0) return MOE_ERR_INVALID_ARG;
+  const long long budget = budget_cycles > 2000000000LL ? 2000000000LL : budget_cycles;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<int*>(ws),
+                                                                        budget);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status_t moe_status(void* ws, void* stream, int32_t* flags) {
