@@ -6,7 +6,9 @@
 // (one launch over the ragged, variable-M per-expert groups of a sorted-by-expert
 // layout).  X-MoE verdict page, key machinery: the groups are the padding-free
 // buffer's expert segments -- no segment is padded; a tile that crosses a segment's
-// end masks its stores, and a K-block that crosses it is zero-filled in shared memory.
+// end masks its stores, and in the weight-gradient GEMMs (K = the segment's rows) each
+// segment gets its own copy of the operand maps whose row extent ends at the segment's
+// end, so the rows of a K block past it load as zeros.
 //
 // One persistent kernel per mode, 192 threads per CTA, one CTA per SM:
 //   warp 0      TMA producer: 128B-swizzled tiles of A and B into a shared-memory ring
@@ -60,7 +62,7 @@ struct Geo {
 constexpr int BK = 64;
 constexpr int BN = 256;
 constexpr int CHUNK_BYTES = 64 * BK * 2;     // one 64-element x 64-row MN-major box: 8 KB
-constexpr int NUM_THREADS = 224;   // producer, MMA, 4 epilogue warps, tail fixer
+constexpr int NUM_THREADS = 192;   // producer, MMA, 4 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_G = 256;
 constexpr int MAX_STAGES = 6;
@@ -69,8 +71,6 @@ constexpr long long WAIT_BUDGET = 4000000000LL;   // clock cycles (about 2 s)
 struct Ctl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  uint64_t tailb[MAX_STAGES];
-  uint64_t tailpeer[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -103,6 +103,8 @@ struct KParams {
   __nv_bfloat16* out1;
   const __nv_bfloat16* aux;
   int* err;
+  // WGRAD: per-segment copies of the two operand maps (row extent = segment end), or null
+  const CUtensorMap* gmaps;
 };
 
 template <int MODE>
@@ -218,8 +220,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);   // the leader's arrive (+ both CTAs' bytes)
       mbar_init(smem_u32(&ctl->empty[s]), 1);
-      mbar_init(smem_u32(&ctl->tailb[s]), 1);
-      mbar_init(smem_u32(&ctl->tailpeer[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -302,12 +302,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    const CUtensorMap* mA = &tmA;
+    const CUtensorMap* mB = &tmB;
+    int map_g = -1;
     for (int tile = unit; tile < total && ok; tile += num_units) {
       int g, mt, nt;
       map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
       const int seg0 = ctl->gstart[g];
       const int seg_rows = ctl->gstart[g + 1] - seg0;
       const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
+      if (MODE == GEMM_WGRAD && p.gmaps != nullptr && g != map_g && nkb > 0) {
+        // this segment's maps end at its last row: a K block that crosses the end loads
+        // the rows past it as zeros (they belong to the next expert, or are unwritten)
+        mA = p.gmaps + 2 * g;
+        mB = mA + 1;
+        map_g = g;
+        if (lane == 0) {
+          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(mA)
+                       : "memory");
+          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(mB)
+                       : "memory");
+        }
+        __syncwarp();
+      }
       for (int kb = 0; kb < nkb; ++kb) {
         if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, WAIT_BUDGET)) {
           ok = false;
@@ -317,24 +334,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t sb = sa + GE::A_BYTES;
         const uint32_t full_local = smem_u32(&ctl->full[s]);
         const uint32_t full_leader = PAIR == 2 ? mapa_shared(full_local, 0) : full_local;
-        const int valid = seg_rows - kb * BK;
-        if (MODE != GEMM_WGRAD || valid >= BK) {
-          // the leader's single arrive announces both CTAs' bytes; the peer's copies count
-          // down the leader's barrier directly (its stage is free, so the leader's barrier
-          // for this stage has already completed its previous phase)
-          if (lane == 0) {
-            if (leader) mbar_arrive_expect_tx(full_local, PAIR * GE::STAGE_BYTES);
-            issue_loads<MODE, PAIR>(&tmA, &tmB, p, sa, sb, full_leader, PAIR == 2, rank, g, mt,
-                                    nt, seg0, kb);
-          }
-        } else {
-          // K block crossing the segment end: land it on a CTA-local barrier; the tail
-          // fixer warp zeroes the rows past the end and releases the stage
-          if (lane == 0) {
-            mbar_arrive_expect_tx(smem_u32(&ctl->tailb[s]), GE::STAGE_BYTES);
-            issue_loads<MODE, PAIR>(&tmA, &tmB, p, sa, sb, smem_u32(&ctl->tailb[s]), false, rank,
-                                    g, mt, nt, seg0, kb);
-          }
+        // the leader's single arrive announces both CTAs' bytes; the peer's copies count
+        // down the leader's barrier directly (its stage is free, so the leader's barrier
+        // for this stage has already completed its previous phase)
+        if (lane == 0) {
+          if (leader) mbar_arrive_expect_tx(full_local, PAIR * GE::STAGE_BYTES);
+          issue_loads<MODE, PAIR>(mA, mB, p, sa, sb, full_leader, PAIR == 2, rank, g, mt, nt,
+                                  seg0, kb);
         }
         if (++s == STAGES) {
           s = 0;
@@ -499,22 +505,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
         const bool valid = prow < seg_end;
         const int f = p.f;
+        // the saved pre-activations a, b of this row: 32 columns per chunk, fetched one
+        // chunk ahead into registers so their latency overlaps the previous chunk's work
+        const uint4* arow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f);
+        const uint4* brow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + f);
+        auto chunk_ok = [&](int c) { return valid && nt * BN + c * 32 < f; };
+        uint4 na[4], nb[4];
+        if (chunk_ok(0)) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            na[v] = __ldg(arow + (nt * BN) / 8 + v);
+            nb[v] = __ldg(brow + (nt * BN) / 8 + v);
+          }
+        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          uint4 ca[4], cb[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            ca[v] = na[v];
+            cb[v] = nb[v];
+          }
+          if (c + 1 < BN / 32 && chunk_ok(c + 1)) {
+            const int nn = (nt * BN + (c + 1) * 32) / 8;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              na[v] = __ldg(arow + nn + v);
+              nb[v] = __ldg(brow + nn + v);
+            }
+          }
           uint32_t ra[32];
           tmem_ld32(taddr + c * 32, ra);
           tmem_ld_wait();
           const int n0 = nt * BN + c * 32;
-          if (valid && n0 < f) {
-            const uint4* sa_ = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + n0);
-            const uint4* sb_ = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + f + n0);
+          if (chunk_ok(c)) {
             uint4* da_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
             uint4* db_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float a[8], b[8], da[8], db[8];
-              unpack8(__ldg(sa_ + v), a);
-              unpack8(__ldg(sb_ + v), b);
+              unpack8(ca[v], a);
+              unpack8(cb[v], b);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float dh = __uint_as_float(ra[v * 8 + e]);
@@ -584,50 +615,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
     }
     if (GE::TMA_STORE && lane == 0) bulk_wait_group_all();   // stores done before exit
-  } else if (MODE == GEMM_WGRAD) {
-    // ------------------------------------------------------------ tail fixer (warp 6)
-    // Walks the same tiles as the producer; for each K block that crosses its segment's
-    // end: waits for that block's copies, zeroes the rows past the end in both operands
-    // and releases the stage to the MMA issuer (in a pair, after the peer CTA has too).
-    int s = 0;
-    uint32_t tail_ph = 0, peer_ph = 0;
-    for (int tile = unit; tile < total; tile += num_units) {
-      int g, mt, nt;
-      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
-      const int seg_rows = ctl->gstart[g + 1] - ctl->gstart[g];
-      const int nkb = ceil_div(seg_rows, BK);
-      const int valid = seg_rows - (nkb - 1) * BK;
-      if (nkb > 0 && valid < BK) {
-        const int st = (s + nkb - 1) % STAGES;
-        const uint32_t tb = smem_u32(&ctl->tailb[st]);
-        if (!warp_wait(tb, (tail_ph >> st) & 1u, abort_flag, p.err, WAIT_BUDGET)) break;
-        tail_ph ^= 1u << st;
-        const uint32_t sa = smem_base + st * GE::STAGE_BYTES;
-        const uint32_t sb = sa + GE::A_BYTES;
-        constexpr int CHUNKS = 2 + GE::BN_CTA / 64;   // 64 x 64 boxes in A and B
-        for (int idx = lane; idx < CHUNKS * 64 * 8; idx += 32) {
-          const int chunk = idx >> 9, r = (idx >> 3) & 63, c = idx & 7;
-          if (r >= valid) {
-            const uint32_t base = chunk < 2 ? sa + chunk * CHUNK_BYTES
-                                            : sb + (chunk - 2) * CHUNK_BYTES;
-            st_shared_zero16(base + r * 128 + c * 16);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        const uint32_t tp = smem_u32(&ctl->tailpeer[st]);
-        if (PAIR == 2 && !leader) {
-          if (lane == 0) mbar_arrive_cluster_release(mapa_shared(tp, 0));
-        } else {
-          if (PAIR == 2) {
-            if (!warp_wait(tp, (peer_ph >> st) & 1u, abort_flag, p.err, WAIT_BUDGET)) break;
-            peer_ph ^= 1u << st;
-          }
-          if (lane == 0) mbar_arrive(smem_u32(&ctl->full[st]));
-        }
-      }
-      s = (s + nkb) % STAGES;
-    }
   }
 
   // ---------------------------------------------------------------- teardown
@@ -639,6 +626,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (PAIR == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// One thread per segment: copy the two operand maps of the weight-gradient GEMM into
+// device memory and set their row extent to the segment's end (offsets[g+1]).
+__global__ void prep_segment_maps(const __grid_constant__ CUtensorMap tmA,
+                                  const __grid_constant__ CUtensorMap tmB,
+                                  const int32_t* __restrict__ offsets, int G, long long rows_cap,
+                                  CUtensorMap* out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= G) return;
+  long long end = offsets[g + 1];
+  end = end < 1 ? 1 : (end > rows_cap ? rows_cap : end);
+  const uint4* sa = reinterpret_cast<const uint4*>(&tmA);
+  const uint4* sb = reinterpret_cast<const uint4*>(&tmB);
+  uint4* da = reinterpret_cast<uint4*>(out + 2 * g);
+  uint4* db = reinterpret_cast<uint4*>(out + 2 * g + 1);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    da[i] = sa[i];
+    db[i] = sb[i];
+  }
+  const uint32_t e32 = static_cast<uint32_t>(end);
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(da),
+               "r"(e32)
+               : "memory");
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(db),
+               "r"(e32)
+               : "memory");
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ host side
@@ -746,6 +762,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
   kp.out1 = static_cast<__nv_bfloat16*>(a.out1);
   kp.aux = static_cast<const __nv_bfloat16*>(a.aux);
   kp.err = a.err;
+  kp.gmaps = nullptr;
   const uint64_t G = static_cast<uint64_t>(kp.G);
   const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
   const uint64_t d = static_cast<uint64_t>(a.d), f = static_cast<uint64_t>(a.f);
@@ -799,6 +816,17 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
              make_map_3d(&tc, a.out0, static_cast<uint64_t>(a.wg_N),
                          static_cast<uint64_t>(a.wg_M), G);
         if (!ok) return cudaErrorInvalidValue;
+        if (a.uniform_rows <= 0) {
+          // segments end inside the buffers: per-segment maps, prepared on the device
+          if (!a.seg_maps || (reinterpret_cast<uintptr_t>(a.seg_maps) & 127u))
+            return cudaErrorInvalidValue;
+          CUtensorMap* maps = static_cast<CUtensorMap*>(a.seg_maps);
+          prep_segment_maps<<<(kp.G + 63) / 64, 64, 0, st>>>(ta, tb, a.offsets, kp.G, a.rows_cap,
+                                                             maps);
+          const cudaError_t e = cudaGetLastError();
+          if (e != cudaSuccess) return e;
+          kp.gmaps = maps;
+        }
         return launch_mode<GEMM_WGRAD, 2>(ta, tb, tc, kp, st);
       }
     default:

@@ -68,7 +68,12 @@ struct GroupedGemmArgs {
   void* out1;      // FC1: h
   const void* aux; // DGRAD2: ab (saved FC1 output)
   int* err;
+  // WGRAD over segments: device scratch for 2 * G tensor maps (128-byte aligned) whose row
+  // extent ends at each segment's end, so rows past it load as zeros
+  void* seg_maps;
 };
+
+constexpr size_t SEG_MAP_BYTES = 128;   // one CUtensorMap
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st);
 

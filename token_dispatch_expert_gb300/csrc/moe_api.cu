@@ -82,7 +82,7 @@ CtxLayout ctx_layout(const moe_config_t* c) {
 }
 
 struct WsLayout {
-  size_t route, dyp, dab, dxp, dab_s, dx_s, total;
+  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -92,6 +92,7 @@ WsLayout ws_layout(const moe_config_t* c) {
   WsLayout L;
   size_t o = WS_HEADER_BYTES;
   L.route = o; o += align_up(route_scratch_bytes(c->T, c->E));
+  L.maps = o;  o += align_up(2 * static_cast<size_t>(c->E) * SEG_MAP_BYTES);
   L.dyp = o;   o += align_up(R * d * 2);
   L.dab = o;   o += align_up(R * 2 * f * 2);
   L.dxp = o;   o += align_up(R * d * 2);
@@ -153,7 +154,7 @@ moe_status_t ffn_fwd(const moe_config_t* c, const void* xp, const int32_t* offse
 moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
                      const int32_t* offsets, int64_t uniform_rows, int f, const void* W1,
                      const void* W2, const void* ab, const void* h, void* dab, void* dxp,
-                     void* dW1, void* dW2, int* err, cudaStream_t st) {
+                     void* dW1, void* dW2, void* seg_maps, int* err, cudaStream_t st) {
   GroupedGemmArgs g2 = gemm_args(GEMM_DGRAD2_SWIGLU, c, offsets, uniform_rows, c->d, f, dyp, W2,
                                  dab, nullptr, ab, err);
   MOE_TRY(launch_grouped_gemm(g2, st));
@@ -161,6 +162,7 @@ moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
                                  nullptr, nullptr, err);
   w2.wg_M = c->d;
   w2.wg_N = f;
+  w2.seg_maps = seg_maps;
   MOE_TRY(launch_grouped_gemm(w2, st));
   GroupedGemmArgs g1 = gemm_args(GEMM_DGRAD1, c, offsets, uniform_rows, c->d, f, dab, W1, dxp,
                                  nullptr, nullptr, err);
@@ -169,6 +171,7 @@ moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
                                  nullptr, nullptr, err);
   w1.wg_M = 2 * f;
   w1.wg_N = c->d;
+  w1.seg_maps = seg_maps;
   MOE_TRY(launch_grouped_gemm(w1, st));
   return MOE_OK;
 }
@@ -296,7 +299,8 @@ moe_status_t moe_grouped_ffn_bwd(const moe_config_t* cfg, const void* dyp, const
   if (!ptrs_ok(dyp, xp, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2, ws))
     return MOE_ERR_INVALID_ARG;
   return ffn_bwd(cfg, dyp, xp, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
-                 static_cast<int*>(ws), static_cast<cudaStream_t>(stream));
+                 at<uint8_t>(ws, ws_layout(cfg).maps), static_cast<int*>(ws),
+                 static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_unpermute_reduce(const moe_config_t* cfg, const void* dxp,
@@ -379,14 +383,14 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float
                              dlogits, err, st));
   s = ffn_bwd(cfg, dyp, at<uint8_t>(ctx, C.off[MOE_CTX_XP]), offsets, 0, cfg->ffn, W1, W2,
               at<uint8_t>(ctx, C.off[MOE_CTX_AB]), at<uint8_t>(ctx, C.off[MOE_CTX_H]), dab, dxp,
-              dW1, dW2, err, st);
+              dW1, dW2, at<uint8_t>(ws, W.maps), err, st);
   if (s != MOE_OK) return s;
   const void* dxs = nullptr;
   if (cfg->ffn_shared) {
     void* dxsw = at<uint8_t>(ws, W.dx_s);
     s = ffn_bwd(cfg, dy, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s,
                 at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]), at<uint8_t>(ctx, C.off[MOE_CTX_H_S]),
-                at<uint8_t>(ws, W.dab_s), dxsw, dW1s, dW2s, err, st);
+                at<uint8_t>(ws, W.dab_s), dxsw, dW1s, dW2s, nullptr, err, st);
     if (s != MOE_OK) return s;
     dxs = dxsw;
   }
