@@ -108,3 +108,57 @@ def test_grouped_ffn_bwd(name):
         assert_close(f"dW1[{e}]", g1[e], oracle.bf16(r_dW1[e]))
         assert_close(f"dW2[{e}]", g2[e], oracle.bf16(r_dW2[e]))
     assert tde.moe_status(ws) == (0, 0)
+
+
+def test_grouped_ffn_segment_edges():
+    """Segment sizes chosen to hit the tile cases of the CTA-pair path: an empty segment,
+    one row, segment ends 1, 64, 127, 128, 129 and 255 rows into a 256-row tile, segments
+    of several tiles, and an N tail (f = 192)."""
+    sizes = [1, 64, 127, 128, 129, 255, 300, 600, 0, 385]
+    E = len(sizes)
+    n = sum(sizes)
+    c = MoEConfig("edges", T=n, d=256, E=E, k=1, f=192)
+    assert n / E >= 192          # average rows per group: the pair path is taken
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    inp = gen_inputs_host(c)
+    xp = inp["x"]
+    cfg = cfg_c(c)
+    ws = new_ws(cfg)
+    R = c.T * c.k
+    ab = torch.empty((R, 2 * c.f), dtype=torch.bfloat16, device="cuda")
+    h = torch.empty((R, c.f), dtype=torch.bfloat16, device="cuda")
+    yp = torch.empty((R, c.d), dtype=torch.bfloat16, device="cuda")
+    tde.moe_grouped_ffn(cfg, dev(xp), dev(off), dev(inp["W1"]), dev(inp["W2"]), ab, h, yp, ws)
+    r_ab = np.empty((n, 2 * c.f)); r_h = np.empty((n, c.f)); r_yp = np.empty((n, c.d))
+    for e in range(E):
+        s, t = int(off[e]), int(off[e + 1])
+        r_ab[s:t], r_h[s:t], r_yp[s:t] = oracle.ffn_fwd_rows(xp[s:t], inp["W1"][e], inp["W2"][e])
+    assert_close("ab", f64(ab), r_ab)
+    assert_close("h", f64(h), r_h)
+    assert_close("yp", f64(yp), r_yp)
+    # backward from the oracle's saved tensors
+    dyp = gen_rows_bf16("dyp_edges", R, c.d)
+    dab = torch.empty((R, 2 * c.f), dtype=torch.bfloat16, device="cuda")
+    dxp = torch.empty((R, c.d), dtype=torch.bfloat16, device="cuda")
+    dW1 = torch.full((E, 2 * c.f, c.d), 7.0, dtype=torch.bfloat16, device="cuda")
+    dW2 = torch.full((E, c.d, c.f), 7.0, dtype=torch.bfloat16, device="cuda")
+    tde.moe_grouped_ffn_bwd(cfg, dev(dyp), dev(xp), dev(off), dev(inp["W1"]), dev(inp["W2"]),
+                            torch.from_numpy(r_ab).to(torch.bfloat16).cuda(),
+                            torch.from_numpy(r_h).to(torch.bfloat16).cuda(), dab, dxp, dW1, dW2,
+                            ws)
+    r_dab = np.empty((n, 2 * c.f)); r_dxp = np.empty((n, c.d))
+    g1, g2 = f64(dW1), f64(dW2)
+    for e in range(E):
+        s, t = int(off[e]), int(off[e + 1])
+        r_dab[s:t], r_dxp[s:t] = oracle.ffn_bwd_rows(dyp[s:t], r_ab[s:t], inp["W1"][e],
+                                                     inp["W2"][e])
+        w1, w2 = oracle.layer.ffn_wgrad_rows(oracle.layer._f64(xp[s:t]), r_h[s:t],
+                                             oracle.layer._f64(dyp[s:t]), r_dab[s:t], c.d, c.f)
+        if t == s:
+            assert (g1[e] == 0).all() and (g2[e] == 0).all()
+        else:
+            assert_close(f"dW1[{e}]", g1[e], oracle.bf16(w1))
+            assert_close(f"dW2[{e}]", g2[e], oracle.bf16(w2))
+    assert_close("dab", f64(dab), r_dab)
+    assert_close("dxp", f64(dxp), r_dxp)
+    assert tde.moe_status(ws) == (0, 0)
