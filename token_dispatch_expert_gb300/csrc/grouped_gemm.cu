@@ -98,6 +98,7 @@ struct KParams {
   int wg_m_tiles;
   int num_kb;          // K blocks of the fixed-K modes
   int n_out;           // valid output columns of the accumulator's N axis
+  int wg_n_fast;       // WGRAD: walk N tiles fastest (when there are fewer N than M tiles)
   const int32_t* offsets;
   __nv_bfloat16* out0;
   __nv_bfloat16* out1;
@@ -121,11 +122,18 @@ template <int MODE, int PAIR>
 __device__ __forceinline__ void map_tile(const Ctl* ctl, const KParams& p, int tile, int& g,
                                          int& mt, int& nt) {
   if (MODE == GEMM_WGRAD) {
+    // consecutive tiles share the operand chunk of the dimension with more tiles, so that
+    // operand streams through once while the smaller one is re-read from L2
     const int per = p.wg_m_tiles * p.num_n_tiles;
     g = tile / per;
     const int r = tile - g * per;
-    nt = r / p.wg_m_tiles;
-    mt = r - nt * p.wg_m_tiles;
+    if (p.wg_n_fast) {
+      mt = r / p.num_n_tiles;
+      nt = r - mt * p.num_n_tiles;
+    } else {
+      nt = r / p.wg_m_tiles;
+      mt = r - nt * p.wg_m_tiles;
+    }
   } else {
     int lo = 0, hi = p.G;   // tprefix[0] = 0 <= tile < tprefix[G]
     while (hi - lo > 1) {
@@ -808,6 +816,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
     case GEMM_WGRAD:
       kp.num_n_tiles = (a.wg_N + BN - 1) / BN;
       kp.wg_m_tiles = (a.wg_M + 256 - 1) / 256;
+      kp.wg_n_fast = kp.wg_m_tiles > kp.num_n_tiles ? 1 : 0;
       kp.n_out = a.wg_N;
       {
         CUtensorMap tc;
