@@ -49,7 +49,12 @@
  *     are not renormalised after drops;
  *   - assignments to an expert are ranked by ascending token index; the first `cap`
  *     are kept (cap = 0: unlimited);
- *   - unselected logits get a zero gradient (selection is piecewise constant).
+ *   - unselected logits get a zero gradient (selection is piecewise constant);
+ *   - routing variants: an optional per-expert selection bias is added to the fp32 logits
+ *     (in fp32) for the top-k choice only (DeepSeek-V3-style balancing bias); with
+ *     negative-score dropping, an assignment whose raw logit is negative is dropped
+ *     before the capacity ranking and is not counted (X-MoE verdict page, major comment
+ *     on section 5.6: DeepSpeed-MoE also drops negative-score tokens).
  */
 #include <math.h>
 #include <stdint.h>
@@ -107,7 +112,7 @@ static int ranks_before(float la, int ea, float lb, int eb)
  *   logits    [T,E] fp32 (read only)
  *   topk_idx  [T,k] expert of slot j, in rank order
  *   topk_w    [T,k] gate weight of slot j
- *   counts    [E]   assignments routed to e
+ *   counts    [E]   assignments routed to e (eligible ones: not negative-dropped)
  *   kept      [E]   min(counts, cap)
  *   offsets   [E+1] exclusive scan of kept (offsets[E] = rows kept)
  *   dest_row  [T,k] row of slot (t,j) in the expert-ordered buffer, or -1 if dropped
@@ -117,35 +122,44 @@ static int ranks_before(float la, int ea, float lb, int eb)
  * Returns the number of NaN logits seen.
  */
 int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
-                  const float *logits, int32_t *topk_idx, double *topk_w,
-                  int32_t *counts, int32_t *kept, int32_t *offsets, int32_t *dest_row,
-                  int32_t *src_tok, int32_t *src_slot, uint8_t *drop_mask)
+                  const float *logits, const float *select_bias, int drop_negative,
+                  int32_t *topk_idx, double *topk_w, int32_t *counts, int32_t *kept,
+                  int32_t *offsets, int32_t *dest_row, int32_t *src_tok, int32_t *src_slot,
+                  uint8_t *drop_mask)
 {
     int64_t nan_seen = 0;
     int *order = (int *)malloc(sizeof(int) * (size_t)E);
+    float *key = (float *)malloc(sizeof(float) * (size_t)E);
     int32_t *rank = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T * k));
+    uint8_t *ineligible = (uint8_t *)malloc((size_t)(T * k));
 
-    /* 1. selection: order experts by (logit desc, id asc), take the first k */
+    /* 1. selection: order experts by (key desc, id asc), take the first k.  The key is the
+     *    logit, or with a selection bias the fp32 sum logit + bias (the bias steers the
+     *    choice only; the gate weights below use the raw logits). */
     for (int64_t t = 0; t < T; ++t) {
         const float *l = logits + t * E;
         for (int e = 0; e < E; ++e) {
             if (isnan(l[e]))
                 ++nan_seen;
             order[e] = e;
+            key[e] = select_bias ? (float)(l[e] + select_bias[e]) : l[e];
         }
         /* insertion sort: plain and obviously stable w.r.t. the key */
         for (int i = 1; i < E; ++i) {
             int cur = order[i], j = i - 1;
-            while (j >= 0 && ranks_before(l[cur], cur, l[order[j]], order[j])) {
+            while (j >= 0 && ranks_before(key[cur], cur, key[order[j]], order[j])) {
                 order[j + 1] = order[j];
                 --j;
             }
             order[j + 1] = cur;
         }
-        for (int j = 0; j < k; ++j)
+        for (int j = 0; j < k; ++j) {
             topk_idx[t * k + j] = order[j];
+            /* negative-score dropping: an assignment whose raw logit is negative */
+            ineligible[t * k + j] = (uint8_t)(drop_negative && l[order[j]] < 0.0f);
+        }
 
-        /* 2. gate weights over the selected k */
+        /* 2. gate weights over the selected k (raw logits) */
         double sel[64];
         for (int j = 0; j < k; ++j)
             sel[j] = (double)l[order[j]];
@@ -168,13 +182,19 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
         }
     }
 
-    /* 3. histogram and rank of each assignment among its expert's, by ascending t */
+    /* 3. histogram of the eligible assignments and the rank of each among its expert's,
+     *    by ascending t */
     for (int e = 0; e < E; ++e)
         counts[e] = 0;
     for (int64_t t = 0; t < T; ++t)
         for (int j = 0; j < k; ++j) {
-            int e = topk_idx[t * k + j];
-            rank[t * k + j] = counts[e];
+            int64_t s = t * k + j;
+            if (ineligible[s]) {
+                rank[s] = -1;
+                continue;
+            }
+            int e = topk_idx[s];
+            rank[s] = counts[e];
             counts[e] += 1;
         }
 
@@ -195,7 +215,7 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
         for (int j = 0; j < k; ++j) {
             int64_t s = t * k + j;
             int e = topk_idx[s];
-            if (cap > 0 && rank[s] >= cap) {
+            if (ineligible[s] || (cap > 0 && rank[s] >= cap)) {
                 dest_row[s] = -1;
                 drop_mask[s] = 1;
             } else {
@@ -207,7 +227,9 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
             }
         }
     free(order);
+    free(key);
     free(rank);
+    free(ineligible);
     return nan_seen;
 }
 

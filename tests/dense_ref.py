@@ -32,14 +32,17 @@ def selection(logits: np.ndarray, k: int) -> np.ndarray:
     return order[:, :k]
 
 
-def keep_mask(sel: np.ndarray, E: int, cap: int) -> tuple:
+def keep_mask(sel: np.ndarray, E: int, cap: int, eligible=None) -> tuple:
+    """mask: selected; keep: selected, eligible and within the first `cap` eligible tokens
+    of the expert in token order."""
     T, k = sel.shape
     mask = np.zeros((T, E), np.int64)
     np.put_along_axis(mask, sel, 1, axis=-1)
-    rank = np.cumsum(mask, axis=0) - 1
-    keep = mask.copy()
+    elig = mask if eligible is None else mask * eligible
+    rank = np.cumsum(elig, axis=0) - 1
+    keep = elig.copy()
     if cap > 0:
-        keep = mask * (rank < cap)
+        keep = elig * (rank < cap)
     return mask, keep
 
 
@@ -60,8 +63,12 @@ def swiglu(x, W1, W2, rnd=False):
 def dense_layer(cfg, inp: dict, rnd=False, requires_grad=False):
     """Returns (y, leaves) where leaves maps input names to leaf tensors."""
     lg_np = np.asarray(inp["logits"], np.float32)
-    sel = selection(lg_np, cfg.k)
-    mask, keep = keep_mask(sel, cfg.E, cfg.capacity)
+    key = lg_np
+    if getattr(cfg, "select_bias", None) is not None:
+        key = (lg_np + np.asarray(cfg.select_bias, np.float32)[None, :]).astype(np.float32)
+    sel = selection(key, cfg.k)
+    eligible = (lg_np >= 0).astype(np.int64) if getattr(cfg, "drop_negative", False) else None
+    mask, keep = keep_mask(sel, cfg.E, cfg.capacity, eligible)
     leaves = {n: as_t(inp[n]) for n in ("x", "W1", "W2", "W1s", "W2s") if n in inp}
     leaves["logits"] = torch.tensor(lg_np.astype(np.float64))
     if requires_grad:

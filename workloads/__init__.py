@@ -48,6 +48,10 @@ class MoEConfig:
     cap_factor: float | None = None   # capacity factor c; None = unlimited
     zipf_s: float | None = None       # Zipf exponent of the expert bias (None = no bias)
     zipf_alpha: float = 1.0           # scale of the Zipf bias
+    # routing variants
+    select_bias: tuple | None = None  # per-expert bias added to the logits for selection only
+    drop_negative: bool = False       # drop assignments whose raw logit is negative
+    recompute: bool = False           # backward recomputes FC1 instead of saving ab, h
 
     @property
     def R(self) -> int:
@@ -111,6 +115,12 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     """Exact widening of raw bf16 bit patterns to float64."""
     u = (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16)
     return u.view(np.float32).astype(np.float64)
+
+
+def gen_select_bias(cfg: MoEConfig, scale: float = 1.0, seed: int = 0) -> tuple:
+    """A per-expert selection bias (as a balancing controller would hold): N(0, scale^2)."""
+    z = _rng(seed, cfg.name, "select_bias").standard_normal(cfg.E, dtype=np.float32) * scale
+    return tuple(float(v) for v in z.astype(np.float32))
 
 
 def zipf_bias(cfg: MoEConfig, seed: int = 0) -> np.ndarray:
