@@ -50,8 +50,8 @@ def _load():
         lib.orc_bf16.argtypes = [f64]
         lib.orc_bf16.restype = f64
         lib.orc_round_bf16_array.argtypes = [P, i64]
-        lib.orc_route.argtypes = [i64, i32, i32, i32, f64, i64, P, P, i32, P, P, P, P, P, P,
-                                  P, P, P]
+        lib.orc_route.argtypes = [i64, i32, i32, i32, f64, i64, P, P, i32, i32, P, P, P, P, P,
+                                  P, P, P, P]
         lib.orc_route.restype = i64
         lib.orc_permute.argtypes = [i64, i32, P, P, P]
         lib.orc_ffn_fwd_rows.argtypes = [i64, i32, i32, P, P, P, i32, P, P, P]
@@ -110,7 +110,7 @@ def route(cfg, logits: np.ndarray) -> dict:
     bias_a = None if bias is None else _c(bias, np.float32)
     nan = lib.orc_route(T, E, k, GATE[cfg.gate], float(cfg.route_scale), int(cfg.capacity),
                         _p(lg), _p(bias_a), int(getattr(cfg, "drop_negative", False)),
-                        _p(r["topk_idx"]), _p(r["topk_w"]), _p(r["counts"]),
+                        int(getattr(cfg, "drop_by_score", False)), _p(r["topk_idx"]), _p(r["topk_w"]), _p(r["counts"]),
                         _p(r["kept"]), _p(r["offsets"]), _p(r["dest_row"]), _p(r["src_tok"]),
                         _p(r["src_slot"]), _p(r["drop_mask"]))
     r["nan_logits"] = int(nan)

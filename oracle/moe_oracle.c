@@ -54,7 +54,12 @@
  *     (in fp32) for the top-k choice only (DeepSeek-V3-style balancing bias); with
  *     negative-score dropping, an assignment whose raw logit is negative is dropped
  *     before the capacity ranking and is not counted (X-MoE verdict page, major comment
- *     on section 5.6: DeepSpeed-MoE also drops negative-score tokens).
+ *     on section 5.6: DeepSpeed-MoE also drops negative-score tokens);
+ *   - drop by score: when an expert overflows its capacity, the `cap` assignments it keeps
+ *     are those with the largest raw fp32 logit (ties: lower token index first) instead of
+ *     the first `cap` in token order; the kept rows still sit in token order inside the
+ *     expert's segment.  The score is the logit itself, the same quantity the selection
+ *     compares (for the sigmoid gate this is the order of the gate scores).
  */
 #include <math.h>
 #include <stdint.h>
@@ -123,7 +128,7 @@ static int ranks_before(float la, int ea, float lb, int eb)
  */
 int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
                   const float *logits, const float *select_bias, int drop_negative,
-                  int32_t *topk_idx, double *topk_w, int32_t *counts, int32_t *kept,
+                  int drop_by_score, int32_t *topk_idx, double *topk_w, int32_t *counts, int32_t *kept,
                   int32_t *offsets, int32_t *dest_row, int32_t *src_tok, int32_t *src_slot,
                   uint8_t *drop_mask)
 {
@@ -198,6 +203,39 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
             counts[e] += 1;
         }
 
+    /* 3b. drop by score: for an overflowing expert, keep its `cap` best-scored
+     *     assignments and re-rank the kept ones by ascending t (others get rank -1) */
+    if (drop_by_score && cap > 0) {
+        int64_t *list = (int64_t *)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
+        for (int e = 0; e < E; ++e) {
+            if (counts[e] <= cap)
+                continue;
+            int64_t n = 0;                 /* e's assignments (slot ids), by ascending t */
+            for (int64_t s = 0; s < T * k; ++s)
+                if (!ineligible[s] && topk_idx[s] == e)
+                    list[n++] = s;
+            /* selection of the best `cap` by repeated scans: plain and obviously right */
+            uint8_t *keep = (uint8_t *)calloc((size_t)n, 1);
+            for (int64_t c = 0; c < cap; ++c) {
+                int64_t best = -1;
+                for (int64_t i = 0; i < n; ++i) {
+                    if (keep[i])
+                        continue;
+                    if (best < 0 ||
+                        ranks_before(logits[(list[i] / k) * E + e], (int)(list[i] / k),
+                                     logits[(list[best] / k) * E + e], (int)(list[best] / k)))
+                        best = i;
+                }
+                keep[best] = 1;
+            }
+            int32_t r = 0;
+            for (int64_t i = 0; i < n; ++i)
+                rank[list[i]] = keep[i] ? r++ : -1;
+            free(keep);
+        }
+        free(list);
+    }
+
     /* 4. capacity (drop only on overflow) and exclusive scan of the kept counts */
     offsets[0] = 0;
     for (int e = 0; e < E; ++e) {
@@ -215,7 +253,7 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
         for (int j = 0; j < k; ++j) {
             int64_t s = t * k + j;
             int e = topk_idx[s];
-            if (ineligible[s] || (cap > 0 && rank[s] >= cap)) {
+            if (ineligible[s] || rank[s] < 0 || (cap > 0 && rank[s] >= cap)) {
                 dest_row[s] = -1;
                 drop_mask[s] = 1;
             } else {

@@ -6,7 +6,8 @@ EVERY token with dense torch float64 matmuls and masks the result:
     y = sum_e keep[t,e] * w[t,e] * FFN_e(x[t])  (+ FFN_shared(x[t]))
 
 Selection uses numpy's lexsort (key: logit descending, expert id ascending); the
-capacity rule keeps the first `cap` tokens (in token order) of each expert; the
+capacity rule keeps the first `cap` tokens (in token order) of each expert, or with
+drop-by-score the `cap` with the largest logit (lexsort again); the
 gate weights come from torch.softmax over all E experts renormalised over the
 selected ones, or from torch.sigmoid normalised over the selected ones.  Gradients
 come from torch autograd.  Nothing here is shared with oracle/ (no import, no helper).
@@ -32,17 +33,25 @@ def selection(logits: np.ndarray, k: int) -> np.ndarray:
     return order[:, :k]
 
 
-def keep_mask(sel: np.ndarray, E: int, cap: int, eligible=None) -> tuple:
+def keep_mask(sel: np.ndarray, E: int, cap: int, eligible=None, score=None) -> tuple:
     """mask: selected; keep: selected, eligible and within the first `cap` eligible tokens
-    of the expert in token order."""
+    of the expert in token order -- or, given `score` [T, E], within the `cap` eligible
+    tokens of the expert with the largest score (ties: lower token first)."""
     T, k = sel.shape
     mask = np.zeros((T, E), np.int64)
     np.put_along_axis(mask, sel, 1, axis=-1)
     elig = mask if eligible is None else mask * eligible
     rank = np.cumsum(elig, axis=0) - 1
     keep = elig.copy()
-    if cap > 0:
+    if cap > 0 and score is None:
         keep = elig * (rank < cap)
+    elif cap > 0:
+        for e in range(E):
+            toks = np.flatnonzero(elig[:, e])
+            if toks.size > cap:
+                best = toks[np.lexsort((toks, -score[toks, e].astype(np.float64)))[:cap]]
+                keep[:, e] = 0
+                keep[best, e] = 1
     return mask, keep
 
 
@@ -68,7 +77,8 @@ def dense_layer(cfg, inp: dict, rnd=False, requires_grad=False):
         key = (lg_np + np.asarray(cfg.select_bias, np.float32)[None, :]).astype(np.float32)
     sel = selection(key, cfg.k)
     eligible = (lg_np >= 0).astype(np.int64) if getattr(cfg, "drop_negative", False) else None
-    mask, keep = keep_mask(sel, cfg.E, cfg.capacity, eligible)
+    score = lg_np if getattr(cfg, "drop_by_score", False) else None
+    mask, keep = keep_mask(sel, cfg.E, cfg.capacity, eligible, score)
     leaves = {n: as_t(inp[n]) for n in ("x", "W1", "W2", "W1s", "W2s") if n in inp}
     leaves["logits"] = torch.tensor(lg_np.astype(np.float64))
     if requires_grad:

@@ -51,6 +51,7 @@ class MoEConfig:
     # routing variants
     select_bias: tuple | None = None  # per-expert bias added to the logits for selection only
     drop_negative: bool = False       # drop assignments whose raw logit is negative
+    drop_by_score: bool = False       # on overflow keep the best-scored, not the earliest
     recompute: bool = False           # backward recomputes FC1 instead of saving ab, h
 
     @property
