@@ -220,16 +220,24 @@ def bench_ours(args, world, rank, local):
     import torch
 
     import token_dispatch_expert_gb300 as tde
-    from workloads import CONFIGS, PROFILE_CONFIGS, gen_inputs_device
+    from workloads import CONFIGS, PROFILE_CONFIGS, gen_inputs_device, gen_select_bias
 
     c = CONFIGS.get(args.config) or PROFILE_CONFIGS[args.config]
+    if args.select_bias:
+        c = c.replace(select_bias=gen_select_bias(c, args.select_bias))
+    c = c.replace(drop_negative=args.drop_negative, recompute=args.recompute,
+                  drop_by_score=args.drop_by_score)
     torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     tde.lib()
-    cfg = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity)
+    bias_t = (torch.tensor(c.select_bias, dtype=torch.float32, device=dev)
+              if c.select_bias is not None else None)
+    cfg = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity,
+                          select_bias=bias_t, drop_negative=c.drop_negative,
+                          recompute=c.recompute, drop_by_score=c.drop_by_score)
     g = gen_inputs_device(c, dev, seed=rank)
     R = c.T * c.k
     ws_b, ctx_b = tde.moe_workspace_size(cfg)
@@ -258,8 +266,30 @@ def bench_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     PHASES = ["route", "permute", "ffn_fwd", "combine", "combine_bwd", "ffn_bwd",
               "unpermute_reduce"]
+    if c.recompute:
+        # FC1 is recomputed inside the backward: the step runs through the two whole-layer
+        # calls, timed as two phases
+        PHASES = ["layer_fwd", "layer_bwd"]
+        l_outs = {"dx": dx, "dW1": dW1, "dW2": dW2, "dlogits": dl}
+        if shared:
+            l_outs["dW1s"] = shared["dW1"]; l_outs["dW2s"] = shared["dW2"]
+
+    def step_layer(ev):
+        if ev is not None:
+            ev[0].record(stream)
+        tde.moe_layer_fwd(cfg, g["logits"], g["x"], g["W1"], g["W2"], g.get("W1s"),
+                          g.get("W2s"), y, ctx, ws)
+        if ev is not None:
+            ev[1].record(stream)
+        tde.moe_layer_bwd(cfg, ctx, g["logits"], g["x"], g["dy"], g["W1"], g["W2"],
+                          g.get("W1s"), g.get("W2s"), dx, dW1, dW2, l_outs.get("dW1s"),
+                          l_outs.get("dW2s"), dl, ws)
+        if ev is not None:
+            ev[2].record(stream)
 
     def step(ev):
+        if c.recompute:
+            return step_layer(ev)
         # ev: len(PHASES) + 1 events recorded at the phase boundaries (or None)
         def mark(i):
             if ev is not None:
@@ -295,6 +325,10 @@ def bench_ours(args, world, rank, local):
         mark(7)
 
     launches_per_step = 3 + 1 + 2 + 1 + 1 + 4 + 1 + (6 if shared else 0)
+    if c.recompute:
+        launches_per_step += 1 + (1 if shared else 0)   # the recomputed FC1
+    if c.drop_by_score and c.capacity > 0:
+        launches_per_step += 2                          # score scatter + select
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
@@ -324,7 +358,10 @@ def bench_ours(args, world, rank, local):
     for ev in step_events:
         for i, ph in enumerate(PHASES):
             phase_ms[ph] += ev[i].elapsed_time(ev[i + 1]) / args.steps
-    gemm_ms = (phase_ms["ffn_fwd"] + phase_ms["ffn_bwd"]) * args.steps
+    if c.recompute:   # the GEMMs are not separable from the rest of the two layer calls
+        gemm_ms = total_ms
+    else:
+        gemm_ms = (phase_ms["ffn_fwd"] + phase_ms["ffn_bwd"]) * args.steps
     st, fl = tde.moe_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after timing: {tde.moe_status_string(st)} {fl:#x}")
@@ -379,6 +416,8 @@ def bench_ours(args, world, rank, local):
 
     peaks, peak_src = load_peaks()
     flops = gemm_flops(c, rows_kept)
+    if c.recompute:   # FC1 again in the backward: 4*d*f per kept row (+ shared per token)
+        flops += 4.0 * c.d * c.f * rows_kept + (4.0 * c.d * c.fs * c.T if c.fs else 0.0)
     gemm_s_per_step = gemm_ms / args.steps / 1e3
     achieved = flops / gemm_s_per_step / 1e12
     # the GEMMs run inside a continuous loop of steps (the power cap engages): the sustained
@@ -398,6 +437,8 @@ def bench_ours(args, world, rank, local):
     hbm = float(peaks["hbm_gbs"])
     mem = {}
     for ph, b in mem_bytes.items():
+        if ph not in phase_ms:
+            continue
         gbs = b / (phase_ms[ph] * 1e-3) / 1e9
         mem[ph] = {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
                    "us": round(phase_ms[ph] * 1e3, 2), "bytes": b}
@@ -416,11 +457,18 @@ def bench_ours(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) tokens/logits, N(0,0.02) bf16 weights)",
         "config": {"workload": f"{c.name}: T={c.T} d={c.d} E={c.E} top-{c.k} "
                                f"{c.gate} f={c.f}" + (f" shared fs={c.fs}" if c.fs else "")
-                               + (f" capacity {c.capacity}" if c.capacity else ""),
+                               + (f" capacity {c.capacity}" if c.capacity else "")
+                               + (f" select-bias N(0,{args.select_bias}^2)"
+                                  if args.select_bias else "")
+                               + (" drop-negative" if c.drop_negative else "")
+                               + (" drop-by-score" if c.drop_by_score else "")
+                               + (" recompute-FC1" if c.recompute else ""),
                    "tokens_per_step": c.T, "rows_kept": rows_kept,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: each step streams >10 GB of weights/grads (> 129 MB L2)"},
-        "roofline": {"kernel": "grouped_gemm (tcgen05; FC1, FC2, 2 dgrad, 2 wgrad per step)",
+        "roofline": {"kernel": ("whole step, GEMM flops incl. the recomputed FC1 over the "
+                                "step time" if c.recompute else
+                                "grouped_gemm (tcgen05; FC1, FC2, 2 dgrad, 2 wgrad per step)"),
                      "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "frac_of_burst": round(achieved / burst, 4),
@@ -436,7 +484,7 @@ def bench_ours(args, world, rank, local):
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h},
-        "permute_gbs": mem["permute"]["GB/s"],
+        "permute_gbs": mem["permute"]["GB/s"] if "permute" in mem else None,
         "memory_kernels": dict(mem, hbm_peak_gbs=hbm,
                                note=f"hbm_gbs of {peak_src}; CUDA events per phase, live"),
         "phase_ms": {k2: round(v2, 4) for k2, v2 in phase_ms.items()},
@@ -502,6 +550,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--select-bias", type=float, default=0.0,
+                    help="std of a seeded per-expert selection-only bias (0: none)")
+    ap.add_argument("--drop-negative", action="store_true",
+                    help="drop selections whose raw logit is negative")
+    ap.add_argument("--drop-by-score", action="store_true",
+                    help="an expert over capacity keeps its best-scored assignments")
+    ap.add_argument("--recompute", action="store_true",
+                    help="backward recomputes FC1 instead of saving its outputs")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -90,6 +90,22 @@ typedef struct {
     int32_t gate;         /* moe_gate_t                                                */
     float route_scale;    /* 1.0 for softmax; the sigmoid gate's scale (e.g. 2.5)      */
     int32_t capacity;     /* per-expert capacity; 0 = unlimited                        */
+    /* Routing variants and memory trade-off (zero-initialise for the plain layer): */
+    const float *select_bias; /* [E] device fp32, or NULL: added (fp32) to the logits for the
+                                 top-k choice only -- the gate weights use the raw logits
+                                 (a DeepSeek-V3-style balancing bias)                     */
+    int32_t drop_negative;    /* 1: an assignment whose raw logit is negative is dropped
+                                 before the capacity ranking and is not counted (DeepSpeed-
+                                 MoE's rule, X-MoE verdict page, major comment on 5.6)    */
+    int32_t recompute;        /* 1: selective rematerialisation -- ctx keeps neither ab nor
+                                 h (nor ab_s, h_s); moe_layer_bwd recomputes FC1 from the
+                                 saved xp (MegaScale-MoE notes: selective activation
+                                 rematerialisation).  Results are bit-identical.         */
+    int32_t drop_by_score;    /* 1 (with capacity > 0): an expert over capacity keeps the
+                                 assignments with the largest raw logit (ties: lower token)
+                                 instead of the earliest tokens; kept rows stay in token
+                                 order inside its segment.  Needs (E+1 + T*k)*4 more bytes
+                                 of ws.                                                   */
 } moe_config_t;
 
 /* Index of each saved tensor inside the forward context `ctx` (see moe_ctx_offsets). */
@@ -138,7 +154,8 @@ moe_status_t moe_ws_init(void *ws, void *stream);
  *   topk_idx [T,k] out: the k best experts per token, by logit descending, ties to
  *            the lower id, NaN below -inf.  topk_w [T,k] out: gate weights computed
  *            over all k before any drop.
- *   counts [E], kept [E] = min(counts, capacity), offsets [E+1] = exclusive scan of
+ *   counts [E] (assignments routed to e that were not dropped for a negative score),
+ *            kept [E] = min(counts, capacity), offsets [E+1] = exclusive scan of
  *            kept; dest_row [T,k] = offsets[e] + (rank of t among e's tokens by
  *            ascending t), or -1 if that rank >= capacity; src_tok [T*k] / src_slot
  *            [T*k] (= t*k+j) invert dest_row (-1 past offsets[E]); drop_mask [T,k].

@@ -22,7 +22,13 @@ MAX_TOL = 2e-2
 
 
 def cfg_c(c):
-    return tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity)
+    bias = None
+    if getattr(c, "select_bias", None) is not None:
+        bias = torch.tensor(np.asarray(c.select_bias, np.float32), device="cuda")
+    return tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity,
+                           select_bias=bias, drop_negative=getattr(c, "drop_negative", False),
+                           recompute=getattr(c, "recompute", False),
+                           drop_by_score=getattr(c, "drop_by_score", False))
 
 
 def dev(a, device="cuda"):

@@ -39,7 +39,8 @@ def test_binding_names_match_the_header():
 
 
 def cfg_of(c):
-    return tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity)
+    return tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity,
+                           recompute=c.recompute)
 
 
 def test_capacity_from_factor(L):
@@ -64,6 +65,18 @@ def test_workspace_and_ctx_layout(L):
         # the saved activations alone: xp, ab, h, yp
         assert ctx >= R * (c.d + 2 * c.f + c.f + c.d) * 2
         assert ws >= 256
+        # recompute moves ab and h (and the shared expert's) out of ctx into ws
+        rc = cfg_of(c.replace(recompute=True))
+        ws_r, ctx_r = tde.moe_workspace_size(rc)
+        moved = (R * 3 * c.f + c.T * 3 * c.fs) * 2
+        assert ctx - ctx_r >= moved
+        assert ws_r - ws >= moved
+        # drop by score (with a capacity) needs one word per assignment more in ws
+        bs = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale,
+                             c.capacity or 1, drop_by_score=True)
+        plain = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale,
+                                c.capacity or 1)
+        assert tde.moe_workspace_size(bs)[0] - tde.moe_workspace_size(plain)[0] >= R * 4
 
 
 @pytest.mark.parametrize("bad,status", [
@@ -75,6 +88,10 @@ def test_workspace_and_ctx_layout(L):
     (dict(T=0), 1),
     (dict(gate=7), 1),
     (dict(capacity=-1), 1),
+    (dict(drop_negative=2), 1),
+    (dict(recompute=-1), 1),
+    (dict(select_bias=2), 1),      # not 4-byte aligned
+    (dict(drop_by_score=3), 1),
 ])
 def test_invalid_configs_rejected_before_launch(L, bad, status):
     base = dict(T=64, d=128, E=8, k=2, ffn=128, ffn_shared=0, gate=0, route_scale=1.0,

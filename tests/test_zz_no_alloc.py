@@ -40,7 +40,8 @@ def route_both(c, logits):
 
 
 def test_noalloc_route_matches_moe_route_twice():
-    for c in (CONFIGS["capacity"], CONFIGS["qwen3"].replace(name="q_small", T=1000)):
+    for c in (CONFIGS["capacity"], CONFIGS["qwen3"].replace(name="q_small", T=1000),
+              CONFIGS["capacity"].replace(name="cap_score", drop_by_score=True)):
         logits = dev(gen_logits(c))
         ref, got, flags = route_both(c, logits)
         for k in KEYS:

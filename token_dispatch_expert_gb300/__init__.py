@@ -36,7 +36,9 @@ class MoEConfigC(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("ffn", ctypes.c_int32), ("ffn_shared", ctypes.c_int32),
                 ("gate", ctypes.c_int32), ("route_scale", ctypes.c_float),
-                ("capacity", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("select_bias", ctypes.c_void_p),
+                ("drop_negative", ctypes.c_int32), ("recompute", ctypes.c_int32),
+                ("drop_by_score", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):
@@ -87,10 +89,15 @@ def lib() -> ctypes.CDLL:
 
 
 def make_config(T, d, E, k, ffn, ffn_shared=0, gate="softmax", route_scale=1.0,
-                capacity=0) -> MoEConfigC:
-    return MoEConfigC(int(T), int(d), int(E), int(k), int(ffn), int(ffn_shared),
-                      GATES[gate] if isinstance(gate, str) else int(gate), float(route_scale),
-                      int(capacity))
+                capacity=0, select_bias=None, drop_negative=False,
+                recompute=False, drop_by_score=False) -> MoEConfigC:
+    """select_bias: a float32 device tensor [E] (kept alive by the returned config) or None."""
+    cfg = MoEConfigC(int(T), int(d), int(E), int(k), int(ffn), int(ffn_shared),
+                     GATES[gate] if isinstance(gate, str) else int(gate), float(route_scale),
+                     int(capacity), _p(select_bias), int(bool(drop_negative)),
+                     int(bool(recompute)), int(bool(drop_by_score)))
+    cfg._keep = select_bias
+    return cfg
 
 
 def _p(t):
@@ -240,6 +247,9 @@ def ctx_views(cfg, ctx):
         "yp": (torch.bfloat16, (R, d)), "ab_s": (torch.bfloat16, (T, 2 * fs)),
         "h_s": (torch.bfloat16, (T, fs)), "ys": (torch.bfloat16, (T, d if fs else 0)),
     }
+    if cfg.recompute:   # FC1's outputs are not kept in ctx
+        for name, cols in (("ab", 2 * f), ("h", f), ("ab_s", 2 * fs), ("h_s", fs)):
+            spec[name] = (torch.bfloat16, (0, cols))
     out = {}
     for i, name in enumerate(CTX_FIELDS):
         dt, shape = spec[name]

@@ -5,23 +5,46 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
 
 // Number of 32-token chunks the routing histogram is built from.
 inline int64_t route_chunks(int64_t T) { return (T + 31) / 32; }
 
-// Scratch bytes the routing step needs inside ws (after the 256-byte header).
-inline size_t route_scratch_bytes(int64_t T, int E) {
-  return static_cast<size_t>(route_chunks(T)) * static_cast<size_t>(E) * sizeof(int32_t);
+// Scratch the routing step needs inside ws (after the 256-byte header): the per-chunk,
+// per-expert counts; with drop-by-score also each expert's base among all eligible
+// assignments (E+1 ints) and one 32-bit word per assignment (score key, then final rank).
+struct RouteScratch {
+  size_t chunk, cnt_base, list, total;
+};
+inline RouteScratch route_scratch_layout(int64_t T, int E, int k, bool by_score) {
+  auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  RouteScratch r;
+  r.chunk = 0;
+  size_t o = up(static_cast<size_t>(route_chunks(T)) * static_cast<size_t>(E) * 4);
+  r.cnt_base = o;
+  if (by_score) o += up(static_cast<size_t>(E + 1) * 4);
+  r.list = o;
+  if (by_score) o += up(static_cast<size_t>(T) * static_cast<size_t>(k) * 4);
+  r.total = o;
+  return r;
+}
+inline bool route_by_score(const moe_config_t* c) {
+  return c->drop_by_score != 0 && c->capacity > 0;
+}
+inline size_t route_scratch_bytes(const moe_config_t* c) {
+  return route_scratch_layout(c->T, c->E, c->k, route_by_score(c)).total;
 }
 
 constexpr size_t WS_HEADER_BYTES = 256;
 
-cudaError_t launch_route(const float* logits, int64_t T, int E, int k, int gate, float scale,
-                         int capacity, int32_t* topk_idx, float* topk_w, int32_t* counts,
-                         int32_t* kept, int32_t* offsets, int32_t* dest_row, int32_t* src_tok,
-                         int32_t* src_slot, uint8_t* drop_mask, int32_t* chunk_scratch,
-                         int* err, cudaStream_t st);
+// F1 + F2 for config `c` (its routing variants included); scratch: route_scratch_bytes(c)
+// bytes, 256-byte aligned.
+cudaError_t launch_route(const moe_config_t* c, const float* logits, int32_t* topk_idx,
+                         float* topk_w, int32_t* counts, int32_t* kept, int32_t* offsets,
+                         int32_t* dest_row, int32_t* src_tok, int32_t* src_slot,
+                         uint8_t* drop_mask, void* scratch, int* err, cudaStream_t st);
 
 cudaError_t launch_permute(const void* x, const int32_t* src_tok, const int32_t* offsets,
                            int E, int64_t T, int64_t rows_cap, int d, void* xp, int* err,

@@ -24,6 +24,12 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->gate != MOE_GATE_SOFTMAX_TOPK && c->gate != MOE_GATE_SIGMOID_TOPK)
     return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
+  if ((c->drop_negative != 0 && c->drop_negative != 1) ||
+      (c->recompute != 0 && c->recompute != 1) ||
+      (c->drop_by_score != 0 && c->drop_by_score != 1))
+    return MOE_ERR_INVALID_ARG;
+  if (c->select_bias && (reinterpret_cast<uintptr_t>(c->select_bias) & 3u))
+    return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->k > 8) return MOE_ERR_UNSUPPORTED;
   if (c->d % 64 || c->ffn % 64 || c->ffn_shared % 64) return MOE_ERR_UNSUPPORTED;
   if (c->T * static_cast<int64_t>(c->k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
@@ -65,11 +71,12 @@ CtxLayout ctx_layout(const moe_config_t* c) {
   sz[MOE_CTX_SRC_SLOT] = R * 4;
   sz[MOE_CTX_DROP_MASK] = R;
   sz[MOE_CTX_XP] = R * d * 2;
-  sz[MOE_CTX_AB] = R * 2 * f * 2;
-  sz[MOE_CTX_H] = R * f * 2;
+  const bool keep_act = !c->recompute;   // with recompute, FC1's outputs live in ws
+  sz[MOE_CTX_AB] = keep_act ? R * 2 * f * 2 : 0;
+  sz[MOE_CTX_H] = keep_act ? R * f * 2 : 0;
   sz[MOE_CTX_YP] = R * d * 2;
-  sz[MOE_CTX_AB_S] = T * 2 * fs * 2;
-  sz[MOE_CTX_H_S] = T * fs * 2;
+  sz[MOE_CTX_AB_S] = keep_act ? T * 2 * fs * 2 : 0;
+  sz[MOE_CTX_H_S] = keep_act ? T * fs * 2 : 0;
   sz[MOE_CTX_YS] = fs ? T * d * 2 : 0;
   CtxLayout L;
   size_t o = 0;
@@ -82,7 +89,7 @@ CtxLayout ctx_layout(const moe_config_t* c) {
 }
 
 struct WsLayout {
-  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, total;
+  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, ab, h, ab_s, h_s, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -91,13 +98,19 @@ WsLayout ws_layout(const moe_config_t* c) {
   const size_t R = T * k;
   WsLayout L;
   size_t o = WS_HEADER_BYTES;
-  L.route = o; o += align_up(route_scratch_bytes(c->T, c->E));
+  L.route = o; o += align_up(route_scratch_bytes(c));
   L.maps = o;  o += align_up(2 * static_cast<size_t>(c->E) * SEG_MAP_BYTES);
   L.dyp = o;   o += align_up(R * d * 2);
   L.dab = o;   o += align_up(R * 2 * f * 2);
   L.dxp = o;   o += align_up(R * d * 2);
   L.dab_s = o; o += align_up(T * 2 * fs * 2);
   L.dx_s = o;  o += align_up(fs ? T * d * 2 : 0);
+  // selective rematerialisation: FC1's outputs are scratch, recomputed by the backward
+  const bool rc = c->recompute != 0;
+  L.ab = o;    o += align_up(rc ? R * 2 * f * 2 : 0);
+  L.h = o;     o += align_up(rc ? R * f * 2 : 0);
+  L.ab_s = o;  o += align_up(rc ? T * 2 * fs * 2 : 0);
+  L.h_s = o;   o += align_up(rc ? T * fs * 2 : 0);
   L.total = o;
   return L;
 }
@@ -237,11 +250,9 @@ moe_status_t moe_route(const moe_config_t* cfg, const float* logits, int32_t* to
                drop_mask, ws))
     return MOE_ERR_INVALID_ARG;
   WsLayout W = ws_layout(cfg);
-  return cuda_status(launch_route(logits, cfg->T, cfg->E, cfg->k, cfg->gate, cfg->route_scale,
-                                  cfg->capacity, topk_idx, topk_w, counts, kept, offsets,
-                                  dest_row, src_tok, src_slot, drop_mask,
-                                  at<int32_t>(ws, W.route), static_cast<int*>(ws),
-                                  static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_route(cfg, logits, topk_idx, topk_w, counts, kept, offsets,
+                                  dest_row, src_tok, src_slot, drop_mask, at<uint8_t>(ws, W.route),
+                                  static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* src_tok,
@@ -327,29 +338,30 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const float* logits, const v
   CtxLayout C = ctx_layout(cfg);
   WsLayout W = ws_layout(cfg);
   int32_t* offsets = at<int32_t>(ctx, C.off[MOE_CTX_OFFSETS]);
-  MOE_TRY(launch_route(logits, cfg->T, cfg->E, cfg->k, cfg->gate, cfg->route_scale,
-                       cfg->capacity, at<int32_t>(ctx, C.off[MOE_CTX_TOPK_IDX]),
+  MOE_TRY(launch_route(cfg, logits, at<int32_t>(ctx, C.off[MOE_CTX_TOPK_IDX]),
                        at<float>(ctx, C.off[MOE_CTX_TOPK_W]),
                        at<int32_t>(ctx, C.off[MOE_CTX_COUNTS]),
                        at<int32_t>(ctx, C.off[MOE_CTX_KEPT]), offsets,
                        at<int32_t>(ctx, C.off[MOE_CTX_DEST_ROW]),
                        at<int32_t>(ctx, C.off[MOE_CTX_SRC_TOK]),
                        at<int32_t>(ctx, C.off[MOE_CTX_SRC_SLOT]),
-                       at<uint8_t>(ctx, C.off[MOE_CTX_DROP_MASK]), at<int32_t>(ws, W.route), err,
+                       at<uint8_t>(ctx, C.off[MOE_CTX_DROP_MASK]), at<uint8_t>(ws, W.route), err,
                        st));
   void* xp = at<uint8_t>(ctx, C.off[MOE_CTX_XP]);
   MOE_TRY(launch_permute(x, at<int32_t>(ctx, C.off[MOE_CTX_SRC_TOK]), offsets, cfg->E, cfg->T,
                          cfg->T * cfg->k, cfg->d, xp, err, st));
   void* yp = at<uint8_t>(ctx, C.off[MOE_CTX_YP]);
-  s = ffn_fwd(cfg, xp, offsets, 0, cfg->ffn, W1, W2, at<uint8_t>(ctx, C.off[MOE_CTX_AB]),
-              at<uint8_t>(ctx, C.off[MOE_CTX_H]), yp, err, st);
+  const bool rc = cfg->recompute != 0;
+  void* ab = rc ? at<uint8_t>(ws, W.ab) : at<uint8_t>(ctx, C.off[MOE_CTX_AB]);
+  void* h = rc ? at<uint8_t>(ws, W.h) : at<uint8_t>(ctx, C.off[MOE_CTX_H]);
+  s = ffn_fwd(cfg, xp, offsets, 0, cfg->ffn, W1, W2, ab, h, yp, err, st);
   if (s != MOE_OK) return s;
   const void* ys = nullptr;
   if (cfg->ffn_shared) {
     void* ysw = at<uint8_t>(ctx, C.off[MOE_CTX_YS]);
-    s = ffn_fwd(cfg, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s,
-                at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]), at<uint8_t>(ctx, C.off[MOE_CTX_H_S]), ysw,
-                err, st);
+    void* ab_s = rc ? at<uint8_t>(ws, W.ab_s) : at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]);
+    void* h_s = rc ? at<uint8_t>(ws, W.h_s) : at<uint8_t>(ctx, C.off[MOE_CTX_H_S]);
+    s = ffn_fwd(cfg, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s, ab_s, h_s, ysw, err, st);
     if (s != MOE_OK) return s;
     ys = ysw;
   }
@@ -376,20 +388,41 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float
   void* dyp = at<uint8_t>(ws, W.dyp);
   void* dab = at<uint8_t>(ws, W.dab);
   void* dxp = at<uint8_t>(ws, W.dxp);
+  const bool rc = cfg->recompute != 0;
+  const void* xp_saved = at<uint8_t>(ctx, C.off[MOE_CTX_XP]);
+  const void* ab = at<uint8_t>(ctx, C.off[MOE_CTX_AB]);
+  const void* h = at<uint8_t>(ctx, C.off[MOE_CTX_H]);
+  const void* ab_s = at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]);
+  const void* h_s = at<uint8_t>(ctx, C.off[MOE_CTX_H_S]);
+  if (rc) {
+    // selective rematerialisation: rerun FC1 (+ SwiGLU) from the saved permuted tokens;
+    // the grouped GEMM is deterministic, so ab and h equal the forward's bit for bit
+    GroupedGemmArgs a1 = gemm_args(GEMM_FC1_SWIGLU, cfg, offsets, 0, cfg->d, cfg->ffn, xp_saved,
+                                   W1, at<uint8_t>(ws, W.ab), at<uint8_t>(ws, W.h), nullptr, err);
+    MOE_TRY(launch_grouped_gemm(a1, st));
+    ab = at<uint8_t>(ws, W.ab);
+    h = at<uint8_t>(ws, W.h);
+    if (cfg->ffn_shared) {
+      GroupedGemmArgs a2 = gemm_args(GEMM_FC1_SWIGLU, cfg, nullptr, cfg->T, cfg->d,
+                                     cfg->ffn_shared, x, W1s, at<uint8_t>(ws, W.ab_s),
+                                     at<uint8_t>(ws, W.h_s), nullptr, err);
+      MOE_TRY(launch_grouped_gemm(a2, st));
+      ab_s = at<uint8_t>(ws, W.ab_s);
+      h_s = at<uint8_t>(ws, W.h_s);
+    }
+  }
   MOE_TRY(launch_combine_bwd(dy, at<uint8_t>(ctx, C.off[MOE_CTX_YP]), logits,
                              at<int32_t>(ctx, C.off[MOE_CTX_TOPK_IDX]),
                              at<float>(ctx, C.off[MOE_CTX_TOPK_W]), dest_row, cfg->T, cfg->E,
                              cfg->k, cfg->d, cfg->gate, cfg->route_scale, cfg->T * cfg->k, dyp,
                              dlogits, err, st));
-  s = ffn_bwd(cfg, dyp, at<uint8_t>(ctx, C.off[MOE_CTX_XP]), offsets, 0, cfg->ffn, W1, W2,
-              at<uint8_t>(ctx, C.off[MOE_CTX_AB]), at<uint8_t>(ctx, C.off[MOE_CTX_H]), dab, dxp,
-              dW1, dW2, at<uint8_t>(ws, W.maps), err, st);
+  s = ffn_bwd(cfg, dyp, xp_saved, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
+              at<uint8_t>(ws, W.maps), err, st);
   if (s != MOE_OK) return s;
   const void* dxs = nullptr;
   if (cfg->ffn_shared) {
     void* dxsw = at<uint8_t>(ws, W.dx_s);
-    s = ffn_bwd(cfg, dy, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s,
-                at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]), at<uint8_t>(ctx, C.off[MOE_CTX_H_S]),
+    s = ffn_bwd(cfg, dy, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s, ab_s, h_s,
                 at<uint8_t>(ws, W.dab_s), dxsw, dW1s, dW2s, nullptr, err, st);
     if (s != MOE_OK) return s;
     dxs = dxsw;

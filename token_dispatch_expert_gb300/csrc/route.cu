@@ -21,6 +21,16 @@
 //      scan of kept gives the segment offsets.
 //   3. route_assign: one thread per (t, j): rank = chunk base + rank in chunk; kept
 //      slots get dest_row = offsets[e] + rank and fill the inverse maps.
+// Routing variants: an optional per-expert bias enters the selection key only (fp32
+// logit + bias), the gate weights use the raw logits; with negative-score dropping an
+// assignment whose raw logit is negative never enters the histogram and is dropped (X-MoE
+// verdict page, major comment on section 5.6: DeepSpeed-MoE's rule).  With drop-by-score
+// two kernels run between 2 and 3: route_score_scatter writes the score key of every
+// assignment of an over-capacity expert at its token-order position in a per-expert list,
+// and route_score_select (one CTA per expert) finds the cap-th largest key by a 4-pass
+// 8-bit radix select, keeps the keys above it plus the earliest of the keys equal to it,
+// and overwrites the list with each assignment's rank among the kept (or -1); the assign
+// step then reads its rank from there.
 #include <mutex>
 
 #include "common.cuh"
@@ -44,10 +54,13 @@ __device__ __forceinline__ uint32_t order_key(float x, bool& is_nan) {
 
 template <int VPL>
 __global__ void __launch_bounds__(ROUTE_THREADS)
-route_topk_chunk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int gate,
-                        float scale, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+route_topk_chunk_kernel(const float* __restrict__ logits, const float* __restrict__ select_bias,
+                        int drop_negative, int64_t T, int E, int k, int gate, float scale,
+                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                         int32_t* __restrict__ rank_out, int32_t* __restrict__ chunk_cnt,
                         int64_t nch, int* err) {
+  // s_idx: the selected expert, or -1 for an empty token slot or an assignment dropped for
+  // its negative score (it takes no place in the histogram)
   __shared__ int s_idx[CHUNK][8];
   __shared__ uint32_t s_bits[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -72,7 +85,9 @@ route_topk_chunk_kernel(const float* __restrict__ logits, int64_t T, int E, int 
       const int e = lane + 32 * s;
       if (e < E) {
         v[s] = row[e];
-        const uint32_t kf = order_key(v[s], nan_here);
+        // the selection key: the logit, or (fp32) logit + bias; the weights use the logit
+        const float kv = select_bias ? v[s] + __ldg(select_bias + e) : v[s];
+        const uint32_t kf = order_key(kv, nan_here);
         key[s] = (static_cast<unsigned long long>(kf) << 32) | (0xFFFFu - static_cast<uint32_t>(e));
       } else {
         v[s] = 0.0f;
@@ -143,10 +158,17 @@ route_topk_chunk_kernel(const float* __restrict__ logits, int64_t T, int E, int 
         my_e = sel_e[j];
         my_w = w[j];
       }
+    float my_l = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j == lane) my_l = sel_l[j];
     if (lane < k) {
       topk_idx[t * k + lane] = my_e;
       topk_w[t * k + lane] = my_w;
-      s_idx[tl][lane] = my_e;
+      // negative-score dropping: out of the histogram, marked dropped by the assign step
+      const bool drop = drop_negative && my_l < 0.0f;
+      s_idx[tl][lane] = drop ? -1 : my_e;
+      if (drop) rank_out[t * k + lane] = -1;
     }
   }
   __syncthreads();
@@ -165,8 +187,9 @@ route_topk_chunk_kernel(const float* __restrict__ logits, int64_t T, int E, int 
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
                   int32_t* __restrict__ counts, int32_t* __restrict__ kept,
-                  int32_t* __restrict__ offsets) {
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ cnt_base) {
   __shared__ int s_kept[256];
+  __shared__ int s_cnt[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = warp; e < E; e += 32) {
     int32_t* col = chunk_cnt + static_cast<int64_t>(e) * nch;
@@ -183,16 +206,20 @@ route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
       counts[e] = running;
       kept[e] = kp;
       s_kept[e] = kp;
+      s_cnt[e] = running;
     }
   }
   __syncthreads();
-  if (warp == 0) {
+  // warp 0: exclusive scan of kept -> offsets; warp 1: of counts -> cnt_base (by score)
+  if (warp == 0 || (warp == 1 && cnt_base)) {
+    const int* src = warp == 0 ? s_kept : s_cnt;
+    int32_t* dst = warp == 0 ? offsets : cnt_base;
     int vals[8];
     int sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      vals[i] = e < E ? s_kept[e] : 0;
+      vals[i] = e < E ? src[e] : 0;
       sum += vals[i];
     }
     const int incl = warp_incl_scan(sum);
@@ -200,19 +227,122 @@ route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      if (e < E) offsets[e] = run;
+      if (e < E) dst[e] = run;
       run += vals[i];
     }
-    if (lane == 31) offsets[E] = incl;
+    if (lane == 31) dst[E] = incl;
+  }
+}
+
+// Drop by score, step a: thread per slot.  An eligible assignment to an expert over
+// capacity writes its score key (the order-preserving bits of its raw fp32 logit) at
+// list[cnt_base[e] + r], r its rank among the expert's assignments by token.
+__global__ void __launch_bounds__(256)
+route_score_scatter_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
+                           const int32_t* __restrict__ in_chunk_rank, int64_t T, int k, int E,
+                           int cap, const int32_t* __restrict__ chunk_base, int64_t nch,
+                           const int32_t* __restrict__ counts,
+                           const int32_t* __restrict__ cnt_base, uint32_t* __restrict__ list) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= T * k) return;
+  const int in_chunk = in_chunk_rank[i];
+  const int e = topk_idx[i];
+  if (in_chunk < 0 || counts[e] <= cap) return;
+  const int64_t t = i / k;
+  const int r = chunk_base[static_cast<int64_t>(e) * nch + t / CHUNK] + in_chunk;
+  bool nan_seen = false;
+  list[cnt_base[e] + r] = order_key(logits[t * E + e], nan_seen);
+}
+
+constexpr int SELECT_THREADS = 1024;
+
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the block total.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& excl) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int incl = warp_incl_scan(v);
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = s_warp[lane];
+    const int wi = warp_incl_scan(w);
+    s_warp[lane] = wi - w;          // exclusive base of each warp
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  excl = s_warp[warp] + incl - v;
+  const int total = s_warp[32];
+  __syncthreads();                  // s_warp is reused by the next call
+  return total;
+}
+
+// Drop by score, step b: one CTA per expert over capacity.  Finds K, the cap-th largest
+// key of the expert's list (4 passes of an 8-bit radix select, most significant digit
+// first; the histogram is counted with shared-memory atomics, an order-free sum), then in
+// token order keeps every key > K and the first `need` keys == K (need = cap - #(key > K)),
+// and overwrites the list with each assignment's rank among the kept, or -1.
+__global__ void __launch_bounds__(SELECT_THREADS)
+route_score_select_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ cnt_base,
+                          int cap, uint32_t* __restrict__ list) {
+  __shared__ int s_hist[256];
+  __shared__ int s_warp[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int e = blockIdx.x;
+  const int n = counts[e];
+  if (n <= cap) return;
+  uint32_t* lst = list + cnt_base[e];
+  uint32_t prefix = 0u, mask = 0u;
+  int remaining = cap;              // rank (1-based, from the top) still to locate
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += SELECT_THREADS) s_hist[b] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += SELECT_THREADS) {
+      const uint32_t key = lst[i];
+      if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int cum = 0, dg = 255;
+      for (; dg > 0; --dg) {
+        if (cum + s_hist[dg] >= remaining) break;
+        cum += s_hist[dg];
+      }
+      s_prefix = prefix | (static_cast<uint32_t>(dg) << shift);
+      s_remaining = remaining - cum;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    remaining = s_remaining;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  const uint32_t K = prefix;
+  const int need = remaining;       // how many keys equal to K are kept (>= 1)
+  int ties_before = 0, kept_before = 0;
+#pragma unroll 1
+  for (int base = 0; base < n; base += SELECT_THREADS) {
+    const int i = base + threadIdx.x;
+    const uint32_t key = i < n ? lst[i] : 0u;
+    const int eq = (i < n && key == K) ? 1 : 0;
+    int tie_rank;
+    const int ties = block_excl_scan(eq, s_warp, tie_rank);
+    const int keep = (i < n && (key > K || (eq && ties_before + tie_rank < need))) ? 1 : 0;
+    int kept_rank;
+    const int kept_n = block_excl_scan(keep, s_warp, kept_rank);
+    if (i < n) lst[i] = keep ? static_cast<uint32_t>(kept_before + kept_rank) : 0xFFFFFFFFu;
+    ties_before += ties;
+    kept_before += kept_n;
   }
 }
 
 __global__ void __launch_bounds__(256)
 route_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, int cap,
                     const int32_t* __restrict__ chunk_base, int64_t nch,
-                    const int32_t* __restrict__ offsets, int32_t* __restrict__ dest_row,
-                    int32_t* __restrict__ src_tok, int32_t* __restrict__ src_slot,
-                    uint8_t* __restrict__ drop_mask) {
+                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
+                    const int32_t* __restrict__ cnt_base, const int32_t* __restrict__ score_rank,
+                    int32_t* __restrict__ dest_row, int32_t* __restrict__ src_tok,
+                    int32_t* __restrict__ src_slot, uint8_t* __restrict__ drop_mask) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t R = T * k;
   if (i >= R) return;
@@ -223,8 +353,11 @@ route_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int 
   }
   const int64_t t = i / k;
   const int e = topk_idx[i];
-  const int r = chunk_base[static_cast<int64_t>(e) * nch + t / CHUNK] + dest_row[i];
-  if (cap > 0 && r >= cap) {
+  const int in_chunk = dest_row[i];   // rank inside the chunk, or -1: negative-score drop
+  int r = in_chunk < 0 ? -1 : chunk_base[static_cast<int64_t>(e) * nch + t / CHUNK] + in_chunk;
+  // drop by score: an over-capacity expert's rank comes from the select step
+  if (score_rank && r >= 0 && counts[e] > cap) r = score_rank[cnt_base[e] + r];
+  if (r < 0 || (cap > 0 && r >= cap)) {
     dest_row[i] = -1;
     drop_mask[i] = 1;
   } else {
@@ -238,27 +371,42 @@ route_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int 
 
 }  // namespace
 
-cudaError_t launch_route(const float* logits, int64_t T, int E, int k, int gate, float scale,
-                         int capacity, int32_t* topk_idx, float* topk_w, int32_t* counts,
-                         int32_t* kept, int32_t* offsets, int32_t* dest_row, int32_t* src_tok,
-                         int32_t* src_slot, uint8_t* drop_mask, int32_t* chunk_scratch,
-                         int* err, cudaStream_t st) {
+cudaError_t launch_route(const moe_config_t* c, const float* logits, int32_t* topk_idx,
+                         float* topk_w, int32_t* counts, int32_t* kept, int32_t* offsets,
+                         int32_t* dest_row, int32_t* src_tok, int32_t* src_slot,
+                         uint8_t* drop_mask, void* scratch, int* err, cudaStream_t st) {
+  const int64_t T = c->T;
+  const int E = c->E, k = c->k, cap = c->capacity;
+  const bool by_score = route_by_score(c);
+  const RouteScratch L = route_scratch_layout(T, E, k, by_score);
+  uint8_t* sb = static_cast<uint8_t*>(scratch);
+  int32_t* chunk_scratch = reinterpret_cast<int32_t*>(sb + L.chunk);
+  int32_t* cnt_base = by_score ? reinterpret_cast<int32_t*>(sb + L.cnt_base) : nullptr;
+  uint32_t* list = by_score ? reinterpret_cast<uint32_t*>(sb + L.list) : nullptr;
   const int64_t nch = route_chunks(T);
   const dim3 g1(static_cast<unsigned>(nch));
-#define MOE_ROUTE_LAUNCH(V)                                                                  \
-  route_topk_chunk_kernel<V><<<g1, ROUTE_THREADS, 0, st>>>(logits, T, E, k, gate, scale,    \
-                                                            topk_idx, topk_w, dest_row,      \
-                                                            chunk_scratch, nch, err)
+#define MOE_ROUTE_LAUNCH(V)                                                                   \
+  route_topk_chunk_kernel<V><<<g1, ROUTE_THREADS, 0, st>>>(                                   \
+      logits, c->select_bias, c->drop_negative, T, E, k, c->gate, c->route_scale, topk_idx,  \
+      topk_w, dest_row, chunk_scratch, nch, err)
   if (E <= 32) MOE_ROUTE_LAUNCH(1);
   else if (E <= 64) MOE_ROUTE_LAUNCH(2);
   else if (E <= 128) MOE_ROUTE_LAUNCH(4);
   else MOE_ROUTE_LAUNCH(8);
 #undef MOE_ROUTE_LAUNCH
-  route_scan_kernel<<<1, 1024, 0, st>>>(chunk_scratch, nch, E, capacity, counts, kept, offsets);
+  route_scan_kernel<<<1, 1024, 0, st>>>(chunk_scratch, nch, E, cap, counts, kept, offsets,
+                                        cnt_base);
   const int64_t R = T * k;
-  route_assign_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(
-      topk_idx, T, k, E, capacity, chunk_scratch, nch, offsets, dest_row, src_tok, src_slot,
-      drop_mask);
+  const unsigned g_slots = static_cast<unsigned>((R + 255) / 256);
+  if (by_score) {
+    route_score_scatter_kernel<<<g_slots, 256, 0, st>>>(logits, topk_idx, dest_row, T, k, E, cap,
+                                                        chunk_scratch, nch, counts, cnt_base,
+                                                        list);
+    route_score_select_kernel<<<E, SELECT_THREADS, 0, st>>>(counts, cnt_base, cap, list);
+  }
+  route_assign_kernel<<<g_slots, 256, 0, st>>>(
+      topk_idx, T, k, E, cap, chunk_scratch, nch, offsets, counts, cnt_base,
+      reinterpret_cast<const int32_t*>(list), dest_row, src_tok, src_slot, drop_mask);
   return cudaGetLastError();
 }
 
@@ -317,15 +465,14 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const float* 
     if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return MOE_ERR_INVALID_ARG;
   if (dev_flags_or_null && (reinterpret_cast<uintptr_t>(dev_flags_or_null) & 3u))
     return MOE_ERR_INVALID_ARG;
-  if (moe::route_scratch_bytes(cfg->T, cfg->E) > MOE_NOALLOC_ROUTE_SCRATCH_BYTES)
+  if (moe::route_scratch_bytes(cfg) > MOE_NOALLOC_ROUTE_SCRATCH_BYTES)
     return MOE_ERR_UNSUPPORTED;   // the fixed scratch is too small for this T x E
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   int32_t* scratch = nullptr;
   if (moe::noalloc_scratch(dev, &scratch) != cudaSuccess || !scratch) return MOE_ERR_CUDA;
-  const cudaError_t e = moe::launch_route(
-      logits, cfg->T, cfg->E, cfg->k, cfg->gate, cfg->route_scale, cfg->capacity, topk_idx,
-      topk_w, counts, kept, offsets, dest_row, src_tok, src_slot, drop_mask, scratch,
-      dev_flags_or_null, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = moe::launch_route(cfg, logits, topk_idx, topk_w, counts, kept, offsets,
+                                          dest_row, src_tok, src_slot, drop_mask, scratch,
+                                          dev_flags_or_null, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
