@@ -299,10 +299,15 @@ def bench_ours(args, world, rank, local):
                       v["offsets"], v["dest_row"], v["src_tok"], v["src_slot"], v["drop_mask"],
                       ws)
         mark(1)
-        tde.moe_permute(cfg, g["x"], v["src_tok"], v["offsets"], v["xp"], ws)
-        mark(2)
-        tde.moe_grouped_ffn(cfg, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"], v["h"],
-                            v["yp"], ws)
+        if args.fuse_gather:   # the permute folded into FC1's loads: no xp
+            mark(2)
+            tde.moe_grouped_ffn_gather(cfg, g["x"], v["src_tok"], v["offsets"], g["W1"],
+                                       g["W2"], v["ab"], v["h"], v["yp"], ws)
+        else:
+            tde.moe_permute(cfg, g["x"], v["src_tok"], v["offsets"], v["xp"], ws)
+            mark(2)
+            tde.moe_grouped_ffn(cfg, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"], v["h"],
+                                v["yp"], ws)
         if shared:
             tde.moe_grouped_ffn(shared["cfg"], g["x"], shared["off"], g["W1s"], g["W2s"],
                                 shared["ab"], shared["h"], shared["ys"], ws)
@@ -313,8 +318,12 @@ def bench_ours(args, world, rank, local):
         tde.moe_combine_bwd(cfg, g["dy"], v["yp"], g["logits"], v["topk_idx"], v["topk_w"],
                             v["dest_row"], dyp, dl, ws)
         mark(5)
-        tde.moe_grouped_ffn_bwd(cfg, dyp, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"],
-                                v["h"], dab, dxp, dW1, dW2, ws)
+        if args.fuse_gather:
+            tde.moe_grouped_ffn_bwd_gather(cfg, dyp, g["x"], v["src_tok"], v["offsets"], g["W1"],
+                                           g["W2"], v["ab"], v["h"], dab, dxp, dW1, dW2, ws)
+        else:
+            tde.moe_grouped_ffn_bwd(cfg, dyp, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"],
+                                    v["h"], dab, dxp, dW1, dW2, ws)
         if shared:
             tde.moe_grouped_ffn_bwd(shared["cfg"], g["dy"], g["x"], shared["off"], g["W1s"],
                                     g["W2s"], shared["ab"], shared["h"], shared["dab"],
@@ -324,7 +333,11 @@ def bench_ours(args, world, rank, local):
                                  dx, ws)
         mark(7)
 
-    launches_per_step = 3 + 1 + 2 + 1 + 1 + 4 + 1 + (6 if shared else 0)
+    # route 3, permute 1, FC1+FC2 2, combine 1, combine-bwd 1, backward GEMMs 4 plus the two
+    # per-segment map preparations, reduce 1; the shared expert 2 + 4
+    launches_per_step = 3 + 1 + 2 + 1 + 1 + 6 + 1 + (6 if shared else 0)
+    if args.fuse_gather:
+        launches_per_step -= 1
     if c.recompute:
         launches_per_step += 1 + (1 if shared else 0)   # the recomputed FC1
     if c.drop_by_score and c.capacity > 0:
@@ -554,6 +567,8 @@ def main():
                     help="std of a seeded per-expert selection-only bias (0: none)")
     ap.add_argument("--drop-negative", action="store_true",
                     help="drop selections whose raw logit is negative")
+    ap.add_argument("--fuse-gather", action="store_true",
+                    help="fold the permute into the FC1 and dW1 operand loads")
     ap.add_argument("--drop-by-score", action="store_true",
                     help="an expert over capacity keeps its best-scored assignments")
     ap.add_argument("--recompute", action="store_true",

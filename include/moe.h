@@ -223,6 +223,19 @@ moe_status_t moe_grouped_ffn(const moe_config_t *cfg, const void *xp, const int3
                              void *ws, void *stream);
 
 /*
+ * F3 + F4 + F5 fused: moe_grouped_ffn with the permute folded into FC1's operand loads
+ * (Primus MoE blog, MegaMoE section: the dispatch fused into the FC1 grouped GEMM, here
+ * on one GPU: tensor-memory-accelerator gathers of the token rows, no xp buffer).
+ *   Row p of expert e is computed from x[src_tok[p]]; outputs as moe_grouped_ffn.
+ *   x [T,d] bf16, src_tok [T*k] int32 (entries < offsets[E] must lie in [0,T); a bad one
+ *   sets MOE_DEVERR_BAD_INDEX and row 0 is read instead).
+ */
+moe_status_t moe_grouped_ffn_gather(const moe_config_t *cfg, const void *x,
+                                    const int32_t *src_tok, const int32_t *offsets,
+                                    const void *W1, const void *W2, void *ab, void *h, void *yp,
+                                    void *ws, void *stream);
+
+/*
  * F7: combine = unpermute and scale (Primus MoE blog, Figure 7, last step).
  *   y[t] = sum_{j = 0..k-1, dest_row[t,j] >= 0} topk_w[t,j] * yp[dest_row[t,j]]
  *          (+ ys[t] if ys_or_null is not NULL), fp32 accumulation, bf16 out [T,d].
@@ -258,6 +271,18 @@ moe_status_t moe_grouped_ffn_bwd(const moe_config_t *cfg, const void *dyp, const
                                  const int32_t *offsets, const void *W1, const void *W2,
                                  const void *ab, const void *h, void *dab, void *dxp, void *dW1,
                                  void *dW2, void *ws, void *stream);
+
+/*
+ * B2..B5 with the FC1 weight gradient gathering its operand from x: as
+ * moe_grouped_ffn_bwd with xp[p] = x[src_tok[p]] read straight from x
+ * (dW1[e] = dab_e^T x[src_tok]_e); no xp buffer exists.  Same index rules as
+ * moe_grouped_ffn_gather.
+ */
+moe_status_t moe_grouped_ffn_bwd_gather(const moe_config_t *cfg, const void *dyp, const void *x,
+                                        const int32_t *src_tok, const int32_t *offsets,
+                                        const void *W1, const void *W2, const void *ab,
+                                        const void *h, void *dab, void *dxp, void *dW1,
+                                        void *dW2, void *ws, void *stream);
 
 /*
  * B6: un-permute reduce (Primus MoE blog, MegaMoE section: "the FC1 data-gradient

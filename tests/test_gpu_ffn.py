@@ -162,3 +162,75 @@ def test_grouped_ffn_segment_edges():
     assert_close("dab", f64(dab), r_dab)
     assert_close("dxp", f64(dxp), r_dxp)
     assert tde.moe_status(ws) == (0, 0)
+
+
+@pytest.mark.parametrize("name", list(CASES) + ["edges"])
+def test_gather_fused_ffn_is_bit_identical(name):
+    """The permute folded into FC1's operand loads (and into the FC1 weight gradient's):
+    the gathered rows are the same bf16 values the permute would have written, so every
+    output must equal the unfused path bit for bit."""
+    if name == "edges":
+        sizes = [1, 64, 127, 128, 129, 255, 300, 600, 0, 385]
+        c = MoEConfig("edges_g", T=sum(sizes), d=320, E=len(sizes), k=1, f=192)
+        off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        # a scrambled token order: row p of the buffer reads token perm[p]
+        perm = np.random.default_rng(5).permutation(c.T).astype(np.int32)
+        inp = gen_inputs_host(c)
+        src_tok, n = perm, c.T
+    else:
+        c = CASES[name]
+        inp, o, n, _ = setup(c)
+        off, src_tok = o["offsets"], o["src_tok"]
+    R = c.T * c.k
+    cfg = cfg_c(c)
+    ws = new_ws(cfg)
+    x, W1, W2 = dev(inp["x"]), dev(inp["W1"]), dev(inp["W2"])
+    d_off, d_src = dev(off), dev(src_tok)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    xp = torch.full((R, c.d), float("nan"), **bf)
+    tde.moe_permute(cfg, x, d_src, d_off, xp, ws)
+    out_u = [torch.full(s, float("nan"), **bf) for s in [(R, 2 * c.f), (R, c.f), (R, c.d)]]
+    out_g = [torch.full(s, float("nan"), **bf) for s in [(R, 2 * c.f), (R, c.f), (R, c.d)]]
+    tde.moe_grouped_ffn(cfg, xp, d_off, W1, W2, *out_u, ws)
+    tde.moe_grouped_ffn_gather(cfg, x, d_src, d_off, W1, W2, *out_g, ws)
+    torch.cuda.synchronize()
+    for a, b, nm in zip(out_u, out_g, ("ab", "h", "yp")):
+        assert torch.equal(a[:n], b[:n]), nm
+    dyp = dev(gen_rows_bf16("dyp_g", R, c.d))
+    ab, h = out_u[0], out_u[1]
+
+    def bwd(fn, src):
+        dab = torch.empty((R, 2 * c.f), **bf)
+        dxp = torch.empty((R, c.d), **bf)
+        dW1 = torch.full((c.E, 2 * c.f, c.d), 7.0, **bf)
+        dW2 = torch.full((c.E, c.d, c.f), 7.0, **bf)
+        fn(cfg, dyp, *src, d_off, W1, W2, ab, h, dab, dxp, dW1, dW2, ws)
+        torch.cuda.synchronize()
+        return dab, dxp, dW1, dW2
+
+    u = bwd(tde.moe_grouped_ffn_bwd, (xp,))
+    g = bwd(tde.moe_grouped_ffn_bwd_gather, (x, d_src))
+    for a, b, nm in zip(u, g, ("dab", "dxp", "dW1", "dW2")):
+        if nm in ("dab", "dxp"):
+            a, b = a[:n], b[:n]
+        assert torch.equal(a, b), nm
+    assert tde.moe_status(ws) == (0, 0)
+
+
+def test_gather_flags_bad_source_rows():
+    """An out-of-range source row is flagged (MOE_DEVERR_BAD_INDEX) and row 0 read instead;
+    nothing outside x is touched."""
+    c = MoEConfig("badg", T=256, d=128, E=2, k=1, f=128)
+    inp = gen_inputs_host(c)
+    cfg = cfg_c(c)
+    ws = new_ws(cfg)
+    off = dev(np.array([0, 100, 256], np.int32))
+    src = np.arange(256, dtype=np.int32)
+    src[17] = 256            # one past the end
+    src[200] = -3
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    ab, h, yp = (torch.empty(s, **bf) for s in [(256, 256), (256, 128), (256, 128)])
+    tde.moe_grouped_ffn_gather(cfg, dev(inp["x"]), dev(src), off, dev(inp["W1"]), dev(inp["W2"]),
+                               ab, h, yp, ws)
+    st, flags = tde.moe_status(ws)
+    assert flags & tde.DEVERR["BAD_INDEX"]

@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             "moe_route_noalloc": ([cfgp] + [P] * 12, I32),
             "moe_permute": ([cfgp] + [P] * 6, I32),
             "moe_grouped_ffn": ([cfgp] + [P] * 9, I32),
+            "moe_grouped_ffn_gather": ([cfgp] + [P] * 10, I32),
+            "moe_grouped_ffn_bwd_gather": ([cfgp] + [P] * 14, I32),
             "moe_combine": ([cfgp] + [P] * 7, I32),
             "moe_combine_bwd": ([cfgp] + [P] * 10, I32),
             "moe_grouped_ffn_bwd": ([cfgp] + [P] * 13, I32),
@@ -191,6 +193,20 @@ def moe_combine_bwd(cfg, dy, yp, logits, topk_idx, topk_w, dest_row, dyp, dlogit
     _check(lib().moe_combine_bwd(_cfg(cfg), _p(dy), _p(yp), _p(logits), _p(topk_idx), _p(topk_w),
                                  _p(dest_row), _p(dyp), _p(dlogits), _p(ws), _s(stream)),
            "moe_combine_bwd")
+
+
+def moe_grouped_ffn_gather(cfg, x, src_tok, offsets, W1, W2, ab, h, yp, ws, stream=None):
+    _check(lib().moe_grouped_ffn_gather(_cfg(cfg), _p(x), _p(src_tok), _p(offsets), _p(W1),
+                                        _p(W2), _p(ab), _p(h), _p(yp), _p(ws), _s(stream)),
+           "moe_grouped_ffn_gather")
+
+
+def moe_grouped_ffn_bwd_gather(cfg, dyp, x, src_tok, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2,
+                               ws, stream=None):
+    _check(lib().moe_grouped_ffn_bwd_gather(_cfg(cfg), _p(dyp), _p(x), _p(src_tok), _p(offsets),
+                                            _p(W1), _p(W2), _p(ab), _p(h), _p(dab), _p(dxp),
+                                            _p(dW1), _p(dW2), _p(ws), _s(stream)),
+           "moe_grouped_ffn_bwd_gather")
 
 
 def moe_grouped_ffn_bwd(cfg, dyp, xp, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2, ws,

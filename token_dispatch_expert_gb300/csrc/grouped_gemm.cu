@@ -106,6 +106,9 @@ struct KParams {
   int* err;
   // WGRAD: per-segment copies of the two operand maps (row extent = segment end), or null
   const CUtensorMap* gmaps;
+  // gathered operand rows (FC1's A, WGRAD's B): source row of each row-buffer row
+  const int32_t* gidx;
+  int gather_rows;
 };
 
 template <int MODE>
@@ -162,8 +165,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(FULL_MASK, mbar_wait_bounded(bar, parity, abort, err, budget));
 }
 
-// Issue this CTA's share of the copies of one K block into stage (sa, sb).
-template <int MODE, int PAIR>
+// Source row of row-buffer row r for a gathered operand; an out-of-range entry is flagged
+// and replaced by row 0, so no copy ever leaves the source matrix.
+__device__ __forceinline__ int gather_row(const KParams& p, int r) {
+  int v = __ldg(p.gidx + r);
+  if (static_cast<unsigned>(v) >= static_cast<unsigned>(p.gather_rows)) {
+    flag_error(p.err, MOE_DEVERR_BAD_INDEX);
+    v = 0;
+  }
+  return v;
+}
+
+// Issue this CTA's share of the copies of one K block into stage (sa, sb).  With GATHER,
+// the gathered operand (FC1's A, WGRAD's B) is left to the caller's gather4 copies.
+template <int MODE, int PAIR, bool GATHER>
 __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                             const KParams& p, uint32_t sa, uint32_t sb,
                                             uint32_t bar, bool pair_form, int rank, int g,
@@ -176,7 +191,7 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
   const int k0 = kb * BK;
   const int arow = seg0 + mt * GE::TILE_M + 128 * rank;
   if (MODE == GEMM_FC1_SWIGLU) {
-    load(sa, tmA, k0, arow);
+    if (!GATHER) load(sa, tmA, k0, arow);
     const int wrow = g * 2 * p.f + nt * (BN / 2);
     if (PAIR == 1) {
       load(sb, tmB, k0, wrow);                        // gate rows -> accumulator cols 0..127
@@ -197,13 +212,15 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
 #pragma unroll
     for (int j = 0; j < 2; ++j)
       load(sa + j * CHUNK_BYTES, tmA, mt * GE::TILE_M + rank * 128 + 64 * j, seg0 + k0);
+    if (!GATHER) {
 #pragma unroll
-    for (int j = 0; j < GE::BN_CTA / 64; ++j)
-      load(sb + j * CHUNK_BYTES, tmB, nt * BN + rank * GE::BN_CTA + 64 * j, seg0 + k0);
+      for (int j = 0; j < GE::BN_CTA / 64; ++j)
+        load(sb + j * CHUNK_BYTES, tmB, nt * BN + rank * GE::BN_CTA + 64 * j, seg0 + k0);
+    }
   }
 }
 
-template <int MODE, int PAIR>
+template <int MODE, int PAIR, bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -321,19 +338,43 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
       if (MODE == GEMM_WGRAD && p.gmaps != nullptr && g != map_g && nkb > 0) {
         // this segment's maps end at its last row: a K block that crosses the end loads
-        // the rows past it as zeros (they belong to the next expert, or are unwritten)
+        // the rows past it as zeros (they belong to the next expert, or are unwritten).
+        // A gathered B keeps the source map: its rows past the end repeat the segment's
+        // last row and meet A's zero rows.
         mA = p.gmaps + 2 * g;
-        mB = mA + 1;
+        mB = GATHER ? &tmB : mA + 1;
         map_g = g;
         if (lane == 0) {
           asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(mA)
                        : "memory");
-          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(mB)
-                       : "memory");
+          if (!GATHER)
+            asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(mB)
+                         : "memory");
         }
         __syncwarp();
       }
+      // gathered rows.  FC1: this CTA's 128 A rows of the tile, 4 per lane, fixed for the
+      // tile.  WGRAD: the 64 K rows of a K block, 4 per lane of lanes 0..15, fetched one K
+      // block ahead.  Rows past the segment's end take its last row.
+      const int seg_last = seg0 + seg_rows - 1;
+      int gi[4] = {0, 0, 0, 0};
+      if (GATHER && nkb > 0) {
+        if (MODE == GEMM_FC1_SWIGLU) {
+          const int r0 = seg0 + mt * GE::TILE_M + 128 * rank + 4 * lane;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) gi[q] = gather_row(p, min(r0 + q, seg_last));
+        } else if (MODE == GEMM_WGRAD && lane < 16) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) gi[q] = gather_row(p, min(seg0 + 4 * lane + q, seg_last));
+        }
+      }
       for (int kb = 0; kb < nkb; ++kb) {
+        int gc[4] = {gi[0], gi[1], gi[2], gi[3]};
+        if (GATHER && MODE == GEMM_WGRAD && lane < 16 && kb + 1 < nkb) {
+          const int r0 = seg0 + (kb + 1) * BK + 4 * lane;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) gi[q] = gather_row(p, min(r0 + q, seg_last));
+        }
         if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, WAIT_BUDGET)) {
           ok = false;
           break;
@@ -347,8 +388,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // for this stage has already completed its previous phase)
         if (lane == 0) {
           if (leader) mbar_arrive_expect_tx(full_local, PAIR * GE::STAGE_BYTES);
-          issue_loads<MODE, PAIR>(mA, mB, p, sa, sb, full_leader, PAIR == 2, rank, g, mt, nt,
-                                  seg0, kb);
+          issue_loads<MODE, PAIR, GATHER>(mA, mB, p, sa, sb, full_leader, PAIR == 2, rank, g,
+                                          mt, nt, seg0, kb);
+        }
+        if (GATHER) {
+          __syncwarp();
+          const int k0 = kb * BK;
+          auto g4 = [&](uint32_t dst, const CUtensorMap* m, int x) {
+            if (PAIR == 2) tma_gather4_pair(dst, m, full_leader, x, gc[0], gc[1], gc[2], gc[3]);
+            else tma_gather4(dst, m, full_leader, x, gc[0], gc[1], gc[2], gc[3]);
+          };
+          if (MODE == GEMM_FC1_SWIGLU) {
+            g4(sa + lane * 512, mA, k0);              // rows 4*lane .. 4*lane+3 of the tile
+          } else if (MODE == GEMM_WGRAD && lane < 16) {
+            // K rows 4*lane.. of each 64-column chunk; a chunk past the last column (an N
+            // tail) re-reads the last chunk instead: its output columns are never stored
+#pragma unroll
+            for (int j = 0; j < GE::BN_CTA / 64; ++j)
+              g4(sb + j * CHUNK_BYTES + lane * 512, mB,
+                 min(nt * BN + rank * GE::BN_CTA + 64 * j, p.wg_N - 64));
+          }
         }
         if (++s == STAGES) {
           s = 0;
@@ -710,10 +769,10 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
-template <int MODE, int PAIR>
+template <int MODE, int PAIR, bool GATHER = false>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         const KParams& kp, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<MODE, PAIR>;
+  auto kern = grouped_gemm_kernel<MODE, PAIR, GATHER>;
   constexpr size_t SMEM = smem_bytes<MODE, PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
@@ -745,12 +804,12 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp);
 }
 
-template <int MODE>
+template <int MODE, bool GATHER = false>
 cudaError_t launch_pick(bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
                         const KParams& kp, cudaStream_t st) {
   // the output map is used by the weight-gradient mode only; the others pass tb through
-  return pair ? launch_mode<MODE, 2>(ta, tb, tb, kp, st)
-              : launch_mode<MODE, 1>(ta, tb, tb, kp, st);
+  return pair ? launch_mode<MODE, 2, GATHER>(ta, tb, tb, kp, st)
+              : launch_mode<MODE, 1, GATHER>(ta, tb, tb, kp, st);
 }
 
 }  // namespace
@@ -771,6 +830,12 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
   kp.aux = static_cast<const __nv_bfloat16*>(a.aux);
   kp.err = a.err;
   kp.gmaps = nullptr;
+  const bool gather = a.gather_idx != nullptr;
+  if (gather && (!a.gather_src || a.gather_rows < 1 || a.gather_rows > INT32_MAX ||
+                 (a.mode != GEMM_FC1_SWIGLU && a.mode != GEMM_WGRAD)))
+    return cudaErrorInvalidValue;
+  kp.gidx = a.gather_idx;
+  kp.gather_rows = static_cast<int>(a.gather_rows);
   const uint64_t G = static_cast<uint64_t>(kp.G);
   const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
   const uint64_t d = static_cast<uint64_t>(a.d), f = static_cast<uint64_t>(a.f);
@@ -789,9 +854,12 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
       kp.num_n_tiles = (a.f + BN / 2 - 1) / (BN / 2);
       kp.num_kb = a.d / BK;
       kp.n_out = a.f;
-      ok = make_map(&ta, a.A, d, rows, 128) && make_map(&tb, a.B, d, G * 2 * f, BN / 2);
+      ok = (gather ? make_map(&ta, a.gather_src, d, static_cast<uint64_t>(a.gather_rows), 1)
+                   : make_map(&ta, a.A, d, rows, 128)) &&
+           make_map(&tb, a.B, d, G * 2 * f, BN / 2);
       if (!ok) return cudaErrorInvalidValue;
-      return launch_pick<GEMM_FC1_SWIGLU>(pair, ta, tb, kp, st);
+      return gather ? launch_pick<GEMM_FC1_SWIGLU, true>(pair, ta, tb, kp, st)
+                    : launch_pick<GEMM_FC1_SWIGLU>(pair, ta, tb, kp, st);
     case GEMM_FC2:
       kp.num_n_tiles = (a.d + BN - 1) / BN;
       kp.num_kb = a.f / BK;
@@ -821,7 +889,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
       {
         CUtensorMap tc;
         ok = make_map(&ta, a.A, static_cast<uint64_t>(a.wg_M), rows, 64) &&
-             make_map(&tb, a.B, static_cast<uint64_t>(a.wg_N), rows, 64) &&
+             (gather ? make_map(&tb, a.gather_src, static_cast<uint64_t>(a.wg_N),
+                                static_cast<uint64_t>(a.gather_rows), 1)
+                     : make_map(&tb, a.B, static_cast<uint64_t>(a.wg_N), rows, 64)) &&
              make_map_3d(&tc, a.out0, static_cast<uint64_t>(a.wg_N),
                          static_cast<uint64_t>(a.wg_M), G);
         if (!ok) return cudaErrorInvalidValue;
@@ -836,7 +906,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
           if (e != cudaSuccess) return e;
           kp.gmaps = maps;
         }
-        return launch_mode<GEMM_WGRAD, 2>(ta, tb, tc, kp, st);
+        return gather ? launch_mode<GEMM_WGRAD, 2, true>(ta, tb, tc, kp, st)
+                      : launch_mode<GEMM_WGRAD, 2>(ta, tb, tc, kp, st);
       }
     default:
       return cudaErrorInvalidValue;

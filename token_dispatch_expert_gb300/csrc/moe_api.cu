@@ -152,11 +152,25 @@ GroupedGemmArgs gemm_args(int mode, const moe_config_t* c, const int32_t* offset
   return a;
 }
 
+// Rows of the FC1 input taken from x through src_tok (the fused permute), or none.
+struct Gather {
+  const int32_t* idx = nullptr;
+  const void* src = nullptr;
+  int64_t rows = 0;
+};
+
+void set_gather(GroupedGemmArgs& a, const Gather& gx) {
+  a.gather_idx = gx.idx;
+  a.gather_src = gx.src;
+  a.gather_rows = gx.rows;
+}
+
 moe_status_t ffn_fwd(const moe_config_t* c, const void* xp, const int32_t* offsets,
                      int64_t uniform_rows, int f, const void* W1, const void* W2, void* ab,
-                     void* h, void* yp, int* err, cudaStream_t st) {
+                     void* h, void* yp, int* err, cudaStream_t st, Gather gx = {}) {
   GroupedGemmArgs a1 = gemm_args(GEMM_FC1_SWIGLU, c, offsets, uniform_rows, c->d, f, xp, W1, ab,
                                  h, nullptr, err);
+  set_gather(a1, gx);
   MOE_TRY(launch_grouped_gemm(a1, st));
   GroupedGemmArgs a2 =
       gemm_args(GEMM_FC2, c, offsets, uniform_rows, c->d, f, h, W2, yp, nullptr, nullptr, err);
@@ -167,7 +181,8 @@ moe_status_t ffn_fwd(const moe_config_t* c, const void* xp, const int32_t* offse
 moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
                      const int32_t* offsets, int64_t uniform_rows, int f, const void* W1,
                      const void* W2, const void* ab, const void* h, void* dab, void* dxp,
-                     void* dW1, void* dW2, void* seg_maps, int* err, cudaStream_t st) {
+                     void* dW1, void* dW2, void* seg_maps, int* err, cudaStream_t st,
+                     Gather gx = {}) {
   GroupedGemmArgs g2 = gemm_args(GEMM_DGRAD2_SWIGLU, c, offsets, uniform_rows, c->d, f, dyp, W2,
                                  dab, nullptr, ab, err);
   MOE_TRY(launch_grouped_gemm(g2, st));
@@ -185,6 +200,7 @@ moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
   w1.wg_M = 2 * f;
   w1.wg_N = c->d;
   w1.seg_maps = seg_maps;
+  set_gather(w1, gx);
   MOE_TRY(launch_grouped_gemm(w1, st));
   return MOE_OK;
 }
@@ -275,6 +291,21 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* xp, const int3
                  static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_grouped_ffn_gather(const moe_config_t* cfg, const void* x,
+                                    const int32_t* src_tok, const int32_t* offsets,
+                                    const void* W1, const void* W2, void* ab, void* h, void* yp,
+                                    void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(x, src_tok, offsets, W1, W2, ab, h, yp, ws)) return MOE_ERR_INVALID_ARG;
+  Gather gx;
+  gx.idx = src_tok;
+  gx.src = x;
+  gx.rows = cfg->T;
+  return ffn_fwd(cfg, nullptr, offsets, 0, cfg->ffn, W1, W2, ab, h, yp, static_cast<int*>(ws),
+                 static_cast<cudaStream_t>(stream), gx);
+}
+
 moe_status_t moe_combine(const moe_config_t* cfg, const void* yp, const int32_t* dest_row,
                          const float* topk_w, const void* ys_or_null, void* y, void* ws,
                          void* stream) {
@@ -312,6 +343,24 @@ moe_status_t moe_grouped_ffn_bwd(const moe_config_t* cfg, const void* dyp, const
   return ffn_bwd(cfg, dyp, xp, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
                  at<uint8_t>(ws, ws_layout(cfg).maps), static_cast<int*>(ws),
                  static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_ffn_bwd_gather(const moe_config_t* cfg, const void* dyp, const void* x,
+                                        const int32_t* src_tok, const int32_t* offsets,
+                                        const void* W1, const void* W2, const void* ab,
+                                        const void* h, void* dab, void* dxp, void* dW1,
+                                        void* dW2, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(dyp, x, src_tok, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2, ws))
+    return MOE_ERR_INVALID_ARG;
+  Gather gx;
+  gx.idx = src_tok;
+  gx.src = x;
+  gx.rows = cfg->T;
+  return ffn_bwd(cfg, dyp, nullptr, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
+                 at<uint8_t>(ws, ws_layout(cfg).maps), static_cast<int*>(ws),
+                 static_cast<cudaStream_t>(stream), gx);
 }
 
 moe_status_t moe_unpermute_reduce(const moe_config_t* cfg, const void* dxp,
