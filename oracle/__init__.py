@@ -22,6 +22,10 @@ from .layer import (  # noqa: F401
     unpermute_reduce,
     ffn_fwd_rows,
     ffn_bwd_rows,
+    e4m3,
+    e4m3_code,
+    mx_quantize_rows,
+    ffn_fwd_rows_mx,
     HostSource,
     TorchSource,
 )

@@ -55,6 +55,12 @@ def _load():
         lib.orc_route.restype = i64
         lib.orc_permute.argtypes = [i64, i32, P, P, P]
         lib.orc_ffn_fwd_rows.argtypes = [i64, i32, i32, P, P, P, i32, P, P, P]
+        lib.orc_e4m3.argtypes = [f64]
+        lib.orc_e4m3.restype = f64
+        lib.orc_e4m3_code.argtypes = [f64]
+        lib.orc_e4m3_code.restype = ctypes.c_uint8
+        lib.orc_mx_quantize_rows.argtypes = [i64, i32, P, P, P, P]
+        lib.orc_ffn_fwd_rows_mx.argtypes = [i64, i32, i32, P, P, P, P, P, P, P, P]
         lib.orc_ffn_bwd_rows.argtypes = [i64, i32, i32, P, P, P, P, i32, P, P]
         lib.orc_ffn_wgrad_rows.argtypes = [i64, i32, i32, P, P, P, P, P, P]
         lib.orc_combine.argtypes = [i64, P, i32, i32, P, P, P, P, P, i32, P]
@@ -128,6 +134,43 @@ def ffn_fwd_rows(xr, W1e, W2e, rnd=True):
     if n:
         lib.orc_ffn_fwd_rows(n, d, f, _p(xr), _p(W1e), _p(W2e), int(rnd), _p(ab), _p(h), _p(yp))
     return ab, h, yp
+
+
+def e4m3(v: float) -> float:
+    """Round to the nearest FP8 E4M3 value (ties to even), saturating at +-448."""
+    return float(_load().orc_e4m3(float(v)))
+
+
+def e4m3_code(q: float) -> int:
+    return int(_load().orc_e4m3_code(float(q)))
+
+
+def mx_quantize_rows(v):
+    """MXFP8 of each row of v [rows, cols] in blocks of 32: (E4M3 codes uint8 [rows, cols],
+    E8M0 scale codes uint8 [rows, cols/32], dequantised float64 [rows, cols])."""
+    v = _f64(v)
+    rows, cols = v.shape
+    assert cols % 32 == 0
+    codes = np.empty((rows, cols), np.uint8)
+    scales = np.empty((rows, cols // 32), np.uint8)
+    deq = np.empty((rows, cols))
+    if rows:
+        _load().orc_mx_quantize_rows(rows, cols, _p(v), _p(codes), _p(scales), _p(deq))
+    return codes, scales, deq
+
+
+def ffn_fwd_rows_mx(xr, W1e, W2e):
+    """The expert FFN forward on MXFP8 operands: (ab, h, yp, h codes, h scales)."""
+    lib = _load()
+    xr, W1e, W2e = _f64(xr), _f64(W1e), _f64(W2e)
+    n, d = xr.shape
+    f = W1e.shape[0] // 2
+    ab = np.empty((n, 2 * f)); h = np.empty((n, f)); yp = np.empty((n, d))
+    hc = np.empty((n, f), np.uint8); hs = np.empty((n, f // 32), np.uint8)
+    if n:
+        lib.orc_ffn_fwd_rows_mx(n, d, f, _p(xr), _p(W1e), _p(W2e), _p(ab), _p(h), _p(yp),
+                                _p(hc), _p(hs))
+    return ab, h, yp, hc, hs
 
 
 def ffn_bwd_rows(dyp, ab, W1e, W2e, rnd=True):

@@ -27,6 +27,12 @@
  *               expert).
  *   combine     unpermute-and-scale: y[t] = sum over kept slots of w * yp[row].
  *               Primus MoE blog, Figure 7 dataflow, last step.
+ *   mxfp8       MX block quantisation (OCP Microscaling formats v1.0: one E8M0 power-of-two
+ *               scale per block of 32 consecutive elements along the contraction axis,
+ *               elements in FP8 E4M3) and the expert FFN forward on quantised operands,
+ *               with h quantised from its stored bf16 value.  Primus MoE blog, FP8
+ *               section (MXFP8 recipe, OCP E4M3 expert GEMMs) and MegaMoE section (the
+ *               SwiGLU step quantises its own output).
  *   backward    dispatch(dy) -> FC2 data-grad, FC1 data-grad -> combine/reduce,
  *               plus the two variable-K weight gradients.  Primus MoE blog,
  *               MegaMoE section ("dispatch/combine duality") and the JAX grouped
@@ -226,7 +232,8 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
                                      logits[(list[best] / k) * E + e], (int)(list[best] / k)))
                         best = i;
                 }
-                keep[best] = 1;
+                if (best >= 0)     /* always: n > cap */
+                    keep[best] = 1;
             }
             int32_t r = 0;
             for (int64_t i = 0; i < n; ++i)
@@ -503,4 +510,144 @@ void orc_unpermute_reduce(int64_t n_tok, const int64_t *toks, int k, int d,
             dx[q * d + i] = rb(s, rnd);
         }
     }
+}
+
+/* ------------------------------------------------------------------------------------
+ * MXFP8 (OCP Microscaling formats v1.0, from the definitions)
+ *
+ * E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinities; normal
+ * values (1 + m/8) * 2^(e-7) for e = 1..15 (e = 15, m = 7 is NaN), largest 448;
+ * subnormals (m/8) * 2^-6.  A conversion rounds to the nearest value, ties to an even
+ * mantissa, and saturates: magnitudes above 448 become 448.
+ *
+ * MX block of 32 values v: shared exponent X = floor(log2(max |v|)) - 8 (8 = the exponent
+ * of E4M3's largest normal), clamped to [-127, 127]; an all-zero block takes -127.  The
+ * scale is stored as the E8M0 code X + 127; the elements as E4M3(v / 2^X).  The value a
+ * block element stands for is E4M3 * 2^X.
+ * ------------------------------------------------------------------------------------ */
+double orc_e4m3(double v)
+{
+    if (isnan(v))
+        return v;
+    double a = fabs(v);
+    if (a >= 448.0)
+        return copysign(448.0, v);
+    if (a == 0.0)
+        return v;
+    int e;
+    frexp(a, &e);                 /* a = m * 2^e, 0.5 <= m < 1: floor(log2 a) = e - 1 */
+    int E = e - 1;
+    if (E < -6)
+        E = -6;                   /* subnormal range: fixed spacing 2^-9 */
+    double q = ldexp(nearbyint(ldexp(a, 3 - E)), E - 3);   /* 3 mantissa bits */
+    if (q > 448.0)
+        q = 448.0;
+    return copysign(q, v);
+}
+
+/* the E4M3 bit pattern of an exactly representable value q */
+uint8_t orc_e4m3_code(double q)
+{
+    uint8_t sign = signbit(q) ? 0x80 : 0x00;
+    double a = fabs(q);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);
+    int E = e - 1;
+    if (E < -6)   /* subnormal: m/8 * 2^-6 */
+        return (uint8_t)(sign | (uint8_t)nearbyint(a * 512.0));
+    int m = (int)nearbyint(ldexp(a, -E) * 8.0) - 8;
+    return (uint8_t)(sign | (uint8_t)((E + 7) << 3) | (uint8_t)m);
+}
+
+/* Quantise each row of v [rows, cols] (cols a multiple of 32) in blocks of 32 along the
+ * row.  codes [rows, cols] E4M3 bit patterns, scales [rows, cols/32] E8M0 codes, deq
+ * [rows, cols] the values the quantised row stands for (any output may be NULL). */
+void orc_mx_quantize_rows(int64_t rows, int cols, const double *v, uint8_t *codes,
+                          uint8_t *scales, double *deq)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < cols / 32; ++b) {
+            const double *blk = v + r * cols + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i)
+                if (fabs(blk[i]) > amax)
+                    amax = fabs(blk[i]);
+            int X = -127;
+            if (amax > 0.0) {
+                int e;
+                frexp(amax, &e);
+                X = (e - 1) - 8;
+                if (X < -127)
+                    X = -127;
+                if (X > 127)
+                    X = 127;
+            }
+            if (scales)
+                scales[r * (cols / 32) + b] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; ++i) {
+                double q = orc_e4m3(ldexp(blk[i], -X));
+                if (codes)
+                    codes[r * cols + b * 32 + i] = orc_e4m3_code(q);
+                if (deq)
+                    deq[r * cols + b * 32 + i] = ldexp(q, X);
+            }
+        }
+    }
+}
+
+/*
+ * The expert FFN forward with MXFP8 GEMM operands, n rows of one expert.
+ *   xq   = MX(xr) along d;      W1q = MX(W1e) along d (per output row)
+ *   [a|b] = bf16(xq W1q^T);     h = bf16(silu(a) * b)
+ *   hq   = MX(h) along f (from the stored bf16 h);   W2q = MX(W2e) along f
+ *   yp   = bf16(hq W2q^T)
+ * Accumulation in double.  hq_codes [n,f] / hq_scales [n,f/32] receive h's quantisation.
+ */
+void orc_ffn_fwd_rows_mx(int64_t n, int d, int f, const double *xr, const double *W1e,
+                         const double *W2e, double *ab, double *h, double *yp,
+                         uint8_t *hq_codes, uint8_t *hq_scales)
+{
+    double *xq = (double *)malloc(sizeof(double) * (size_t)(n * d + 1));
+    double *w1q = (double *)malloc(sizeof(double) * (size_t)(2 * (int64_t)f * d));
+    double *w2q = (double *)malloc(sizeof(double) * (size_t)((int64_t)d * f));
+    double *hq = (double *)malloc(sizeof(double) * (size_t)(n * f + 1));
+    orc_mx_quantize_rows(n, d, xr, NULL, NULL, xq);
+    orc_mx_quantize_rows(2 * (int64_t)f, d, W1e, NULL, NULL, w1q);
+    orc_mx_quantize_rows(d, f, W2e, NULL, NULL, w2q);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const double *x = xq + r * d;
+        double *abr = ab + r * 2 * f;
+        double *hr = h + r * f;
+        for (int c = 0; c < 2 * f; ++c) {
+            const double *w = w1q + (int64_t)c * d;
+            double s = 0.0;
+            for (int i = 0; i < d; ++i)
+                s += x[i] * w[i];
+            abr[c] = orc_bf16(s);
+        }
+        for (int c = 0; c < f; ++c) {
+            double a = abr[c], b = abr[f + c];
+            hr[c] = orc_bf16(a / (1.0 + exp(-a)) * b);
+        }
+    }
+    orc_mx_quantize_rows(n, f, h, hq_codes, hq_scales, hq);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const double *hr = hq + r * f;
+        for (int i = 0; i < d; ++i) {
+            const double *w = w2q + (int64_t)i * f;
+            double s = 0.0;
+            for (int c = 0; c < f; ++c)
+                s += hr[c] * w[c];
+            yp[r * d + i] = orc_bf16(s);
+        }
+    }
+    free(xq);
+    free(w1q);
+    free(w2q);
+    free(hq);
 }

@@ -1,0 +1,137 @@
+"""Pins of the oracle's MXFP8 arithmetic (the NEXT-2 row).
+
+* E4M3 rounding and encoding: every finite code round-trips; random values (normal,
+  subnormal, ties) agree with torch's float8_e4m3fn conversion, which rounds to nearest
+  even; magnitudes above 448 saturate (torch's cast does not, so those are checked by hand).
+* MX block quantisation: hand-worked blocks (tests/golden/mxfp8_blocks_hand_worked.json),
+  the scale rule against numpy's frexp, the per-block error bound, and scale invariance
+  (multiplying a block by 2^j shifts its scale code by j and keeps its element codes).
+* The MXFP8 FFN forward: equal to the plain FFN when every operand is exactly
+  representable; otherwise equal to a torch float64 composition of the pinned quantiser.
+CPU only."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import bf16_bits_to_f64, gen_rows_bf16
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def torch_e4m3(v):
+    return torch.tensor(v, dtype=torch.float64).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_every_finite_code_round_trips():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c, v in enumerate(vals):
+        if np.isnan(v):
+            assert c in (0x7F, 0xFF)
+            continue
+        assert oracle.e4m3(v) == v
+        assert oracle.e4m3_code(v) == c, (c, v)
+
+
+def test_rounding_matches_torch_in_range():
+    rng = np.random.default_rng(11)
+    v = np.concatenate([
+        rng.standard_normal(20000) * 50,                       # normals
+        rng.standard_normal(5000) * 2.0 ** -8,                 # subnormal range
+        (rng.integers(-900, 900, 5000) + 0.5) * 2.0 ** -9,     # subnormal ties
+        (rng.integers(16, 31, 3000) * 2 + 1) * 2.0 ** rng.integers(-7, 4, 3000),  # ties
+    ])
+    v = v[np.abs(v) <= 448.0]
+    ours = np.array([oracle.e4m3(x) for x in v])
+    np.testing.assert_array_equal(ours, torch_e4m3(v))
+
+
+def test_saturation():
+    for v, q in [(448.0, 448.0), (449.0, 448.0), (463.9, 448.0), (464.0, 448.0),
+                 (500.0, 448.0), (1e30, 448.0), (-1e5, -448.0), (-450.0, -448.0)]:
+        assert oracle.e4m3(v) == q
+    assert oracle.e4m3_code(448.0) == 0x7E and oracle.e4m3_code(-448.0) == 0xFE
+
+
+def test_hand_worked_blocks():
+    g = json.load(open(os.path.join(HERE, "golden", "mxfp8_blocks_hand_worked.json")))
+    v = np.zeros((len(g["blocks"]), 32))
+    exp_codes = np.zeros((len(g["blocks"]), 32), np.uint8)
+    for i, b in enumerate(g["blocks"]):
+        for k, x in b["values"].items():
+            v[i, int(k)] = x
+        for k, c in b["codes"].items():
+            exp_codes[i, int(k)] = c
+    codes, scales, deq = oracle.mx_quantize_rows(v)
+    np.testing.assert_array_equal(scales[:, 0], [b["scale"] for b in g["blocks"]])
+    np.testing.assert_array_equal(codes, exp_codes)
+
+
+def test_scale_rule_error_bound_and_invariance():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((64, 256)) * np.exp(rng.uniform(-20, 20, (64, 1)))
+    x[5, 32:64] = 0.0
+    codes, scales, deq = oracle.mx_quantize_rows(x)
+    blocks = x.reshape(64, 8, 32)
+    amax = np.abs(blocks).max(-1)
+    _, e = np.frexp(amax)
+    X = np.where(amax > 0, np.clip(e - 1 - 8, -127, 127), -127)
+    np.testing.assert_array_equal(scales.astype(int), X + 127)
+    err = np.abs(deq - x).reshape(64, 8, 32).max(-1)
+    assert (err <= amax / 8 + 1e-300).all()               # saturation costs at most 1/8
+    # scale invariance: x * 2^j -> the same element codes, scale codes shifted by j
+    c2, s2, d2 = oracle.mx_quantize_rows(x * 2.0 ** 5)
+    np.testing.assert_array_equal(c2, codes)
+    nz = amax > 0
+    np.testing.assert_array_equal(s2.astype(int)[nz], scales.astype(int)[nz] + 5)
+    np.testing.assert_array_equal(d2, deq * 2.0 ** 5)
+
+
+def exactly_representable(shape, rng):
+    """Values j/8, |j| <= 14, every block of 32 holding one value of magnitude in [1, 2):
+    the block scale is 2^-8 and every element maps to an E4M3 value exactly."""
+    j = rng.integers(-14, 15, shape)
+    j[..., ::32] = rng.choice([-12, -8, 8, 12], size=j[..., ::32].shape)
+    return j / 8.0
+
+
+def test_mx_ffn_equals_plain_ffn_on_representable_operands():
+    rng = np.random.default_rng(9)
+    n, d, f = 40, 128, 64
+    x = exactly_representable((n, d), rng)
+    W1 = exactly_representable((2 * f, d), rng)
+    W2 = exactly_representable((d, f), rng)
+    for m in (x, W1, W2):
+        np.testing.assert_array_equal(oracle.mx_quantize_rows(m)[2], m)
+    ab, h, yp, hc, hs = oracle.ffn_fwd_rows_mx(x, W1, W2)
+    ab0, h0, _ = oracle.ffn_fwd_rows(x, W1, W2)
+    np.testing.assert_array_equal(ab, ab0)
+    np.testing.assert_array_equal(h, h0)
+
+
+def test_mx_ffn_matches_torch_composition():
+    n, d, f = 33, 96, 64
+    x = bf16_bits_to_f64(gen_rows_bf16("mx_x", n, d))
+    W1 = bf16_bits_to_f64(gen_rows_bf16("mx_w1", 2 * f, d, std=0.05))
+    W2 = bf16_bits_to_f64(gen_rows_bf16("mx_w2", d, f, std=0.05))
+    ab, h, yp, hc, hs = oracle.ffn_fwd_rows_mx(x, W1, W2)
+
+    def bf(t):
+        return t.to(torch.bfloat16).to(torch.float64)
+
+    q = lambda m: torch.tensor(oracle.mx_quantize_rows(m)[2])
+    ab_t = bf(q(x) @ q(W1).T)
+    a, b = ab_t[:, :f], ab_t[:, f:]
+    h_t = bf(torch.nn.functional.silu(a) * b)
+    hq = oracle.mx_quantize_rows(h_t.numpy())
+    y_t = bf(torch.tensor(hq[2]) @ q(W2).T)
+    np.testing.assert_allclose(ab, ab_t.numpy(), rtol=0, atol=0)
+    np.testing.assert_array_equal(h, h_t.numpy())
+    np.testing.assert_array_equal(hc, hq[0])
+    np.testing.assert_array_equal(hs, hq[1])
+    np.testing.assert_allclose(yp, y_t.numpy(), rtol=2 ** -8, atol=1e-12)
