@@ -237,7 +237,8 @@ def bench_ours(args, world, rank, local):
               if c.select_bias is not None else None)
     cfg = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity,
                           select_bias=bias_t, drop_negative=c.drop_negative,
-                          recompute=c.recompute, drop_by_score=c.drop_by_score)
+                          recompute=c.recompute, drop_by_score=c.drop_by_score,
+                          mxfp8=args.mxfp8)
     g = gen_inputs_device(c, dev, seed=rank)
     R = c.T * c.k
     ws_b, ctx_b = tde.moe_workspace_size(cfg)
@@ -287,37 +288,64 @@ def bench_ours(args, world, rank, local):
         if ev is not None:
             ev[2].record(stream)
 
+    if args.mxfp8:
+        # the routed experts' forward in MXFP8; the weights are re-quantised every step
+        # (the conservative case: no reuse across micro-batches), timed as their own phase
+        PHASES = ["mx_weight_quant"] + PHASES
+        nbytes, _ = tde.moe_mx_weights_size(cfg)
+        wq = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        mxb = dict(xq=torch.empty((R, c.d), **u8), xs=torch.empty((R, c.d // 32), **u8),
+                   hq=torch.empty((R, c.f), **u8), hs=torch.empty((R, c.f // 32), **u8))
+        if args.mx_cache_weights:
+            # weight-quantisation caching: the blob is made once, as when one optimizer
+            # step's weights serve many micro-batches
+            tde.moe_mx_quantize_weights(cfg, g["W1"], g["W2"], wq)
+
     def step(ev):
         if c.recompute:
             return step_layer(ev)
         # ev: len(PHASES) + 1 events recorded at the phase boundaries (or None)
-        def mark(i):
+        n_mark = [0]
+
+        def mark():
             if ev is not None:
-                ev[i].record(stream)
-        mark(0)
+                ev[n_mark[0]].record(stream)
+            n_mark[0] += 1
+        mark()
+        if args.mxfp8:
+            if not args.mx_cache_weights:
+                tde.moe_mx_quantize_weights(cfg, g["W1"], g["W2"], wq)
+            mark()
         tde.moe_route(cfg, g["logits"], v["topk_idx"], v["topk_w"], v["counts"], v["kept"],
                       v["offsets"], v["dest_row"], v["src_tok"], v["src_slot"], v["drop_mask"],
                       ws)
-        mark(1)
-        if args.fuse_gather:   # the permute folded into FC1's loads: no xp
-            mark(2)
+        mark()
+        if args.mxfp8:         # permute + quantise (bf16 xp kept for the backward)
+            tde.moe_mx_permute_quant(cfg, g["x"], v["src_tok"], v["offsets"], v["xp"],
+                                     mxb["xq"], mxb["xs"], ws)
+            mark()
+            tde.moe_grouped_ffn_mx(cfg, mxb["xq"], mxb["xs"], v["offsets"], wq, v["ab"], v["h"],
+                                   mxb["hq"], mxb["hs"], v["yp"], ws)
+        elif args.fuse_gather:   # the permute folded into FC1's loads: no xp
+            mark()
             tde.moe_grouped_ffn_gather(cfg, g["x"], v["src_tok"], v["offsets"], g["W1"],
                                        g["W2"], v["ab"], v["h"], v["yp"], ws)
         else:
             tde.moe_permute(cfg, g["x"], v["src_tok"], v["offsets"], v["xp"], ws)
-            mark(2)
+            mark()
             tde.moe_grouped_ffn(cfg, v["xp"], v["offsets"], g["W1"], g["W2"], v["ab"], v["h"],
                                 v["yp"], ws)
         if shared:
             tde.moe_grouped_ffn(shared["cfg"], g["x"], shared["off"], g["W1s"], g["W2s"],
                                 shared["ab"], shared["h"], shared["ys"], ws)
-        mark(3)
+        mark()
         tde.moe_combine(cfg, v["yp"], v["dest_row"], v["topk_w"],
                         shared["ys"] if shared else None, y, ws)
-        mark(4)
+        mark()
         tde.moe_combine_bwd(cfg, g["dy"], v["yp"], g["logits"], v["topk_idx"], v["topk_w"],
                             v["dest_row"], dyp, dl, ws)
-        mark(5)
+        mark()
         if args.fuse_gather:
             tde.moe_grouped_ffn_bwd_gather(cfg, dyp, g["x"], v["src_tok"], v["offsets"], g["W1"],
                                            g["W2"], v["ab"], v["h"], dab, dxp, dW1, dW2, ws)
@@ -328,10 +356,10 @@ def bench_ours(args, world, rank, local):
             tde.moe_grouped_ffn_bwd(shared["cfg"], g["dy"], g["x"], shared["off"], g["W1s"],
                                     g["W2s"], shared["ab"], shared["h"], shared["dab"],
                                     shared["dx"], shared["dW1"], shared["dW2"], ws)
-        mark(6)
+        mark()
         tde.moe_unpermute_reduce(cfg, dxp, v["dest_row"], shared["dx"] if shared else None,
                                  dx, ws)
-        mark(7)
+        mark()
 
     # route 3, permute 1, FC1+FC2 2, combine 1, combine-bwd 1, backward GEMMs 4 plus the two
     # per-segment map preparations, reduce 1; the shared expert 2 + 4
@@ -342,6 +370,8 @@ def bench_ours(args, world, rank, local):
         launches_per_step += 1 + (1 if shared else 0)   # the recomputed FC1
     if c.drop_by_score and c.capacity > 0:
         launches_per_step += 2                          # score scatter + select
+    if args.mxfp8 and not args.mx_cache_weights:
+        launches_per_step += 2                          # the two weight-quantisation kernels
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
@@ -404,7 +434,13 @@ def bench_ours(args, world, rank, local):
             d_logits.copy_(h_logits, non_blocking=True)
             d_x.copy_(h_x, non_blocking=True)
             d_dy.copy_(h_dy, non_blocking=True)
-            yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"), y=y)
+            if args.mxfp8:
+                if not args.mx_cache_weights:
+                    tde.moe_mx_quantize_weights(cfg, g["W1"], g["W2"], wq)
+                yy = layer.forward_mx(d_logits, d_x, wq, g.get("W1s"), g.get("W2s"), y=y)
+            else:
+                yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
+                                   y=y)
             layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
                            out=outs)
             h_y.copy_(yy, non_blocking=True)
@@ -437,6 +473,25 @@ def bench_ours(args, world, rank, local):
     # measured peak is the denominator; the burst fraction is reported beside it
     peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     burst = float(peaks["bf16_tflops"])
+    mx_line = None
+    if args.mxfp8:
+        # the forward's routed GEMMs run at the E4M3 rate: 2x the measured bf16 peak (the
+        # nominal dense ratio 4.5 / 2.25 PFLOP/s).  The step's ideal GEMM time is the sum of
+        # the forward (at that rate) and everything else (bf16); the peak reported is the
+        # flop rate that ideal time stands for.
+        fwd_mx = 6.0 * c.d * c.f * rows_kept
+        ideal_s = fwd_mx / (2 * peak * 1e12) + (flops - fwd_mx) / (peak * 1e12)
+        ideal_b = fwd_mx / (2 * burst * 1e12) + (flops - fwd_mx) / (burst * 1e12)
+        # (the ffn_fwd phase also holds the bf16 shared expert when there is one)
+        mx_line = {"ffn_fwd_tflops": None if c.fs else
+                   round(fwd_mx / (phase_ms["ffn_fwd"] * 1e-3) / 1e12, 1),
+                   "fp8_peak_sustained": 2 * peak, "fp8_peak_burst": 2 * burst,
+                   "weight_quant_ms": round(phase_ms["mx_weight_quant"], 4),
+                   "note": ("weights quantised once before timing (cached)"
+                            if args.mx_cache_weights else
+                            "weights re-quantised every step (included in value)")}
+        peak = round(flops / ideal_s / 1e12, 1)
+        burst = round(flops / ideal_b / 1e12, 1)
     # algorithmic bytes of the HBM-bound steps (each source row read once, each
     # destination row written once, index arrays counted)
     T_, d_, k_, E_ = c.T, c.d, c.k, c.E
@@ -466,7 +521,7 @@ def bench_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "mxfp8 fwd (routed) + bf16" if args.mxfp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens/logits, N(0,0.02) bf16 weights)",
         "config": {"workload": f"{c.name}: T={c.T} d={c.d} E={c.E} top-{c.k} "
                                f"{c.gate} f={c.f}" + (f" shared fs={c.fs}" if c.fs else "")
@@ -475,7 +530,10 @@ def bench_ours(args, world, rank, local):
                                   if args.select_bias else "")
                                + (" drop-negative" if c.drop_negative else "")
                                + (" drop-by-score" if c.drop_by_score else "")
-                               + (" recompute-FC1" if c.recompute else ""),
+                               + (" recompute-FC1" if c.recompute else "")
+                               + (" MXFP8-forward" if args.mxfp8 else "")
+                               + (" cached-weight-quant" if args.mxfp8 and args.mx_cache_weights
+                                  else ""),
                    "tokens_per_step": c.T, "rows_kept": rows_kept,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: each step streams >10 GB of weights/grads (> 129 MB L2)"},
@@ -485,8 +543,11 @@ def bench_ours(args, world, rank, local):
                      "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "frac_of_burst": round(achieved / burst, 4),
-                     "peak_source": f"bf16_tflops_sustained of {peak_src} (kernel timed "
-                                    f"inside a continuous step loop); burst {burst}",
+                     "peak_source": (f"bf16_tflops_sustained of {peak_src} (kernel timed "
+                                     f"inside a continuous step loop); burst {burst}"
+                                     if not args.mxfp8 else
+                                     f"flop-weighted: routed forward at 2x, the rest at 1x "
+                                     f"bf16_tflops_sustained of {peak_src}; burst {burst}"),
                      "traffic": GEMM_TRAFFIC_PER_LAUNCH.get(c.name),
                      "traffic_note": "DRAM bytes per launch, average of the 6 GEMM launches "
                                      "(ncu on the mixtral_e2 shape x4)",
@@ -494,6 +555,7 @@ def bench_ours(args, world, rank, local):
                          gemm_algorithmic_bytes(c, rows_kept) / 6),
                      "gemm_ms_per_step": round(gemm_ms / args.steps, 4),
                      "gemm_share_of_step": round(gemm_ms / total_ms, 4)},
+        "mxfp8": mx_line,
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h},
@@ -569,6 +631,10 @@ def main():
                     help="drop selections whose raw logit is negative")
     ap.add_argument("--fuse-gather", action="store_true",
                     help="fold the permute into the FC1 and dW1 operand loads")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="routed experts' forward GEMMs on MXFP8 operands (backward bf16)")
+    ap.add_argument("--mx-cache-weights", action="store_true",
+                    help="with --mxfp8: quantise the weights once, outside the timed steps")
     ap.add_argument("--drop-by-score", action="store_true",
                     help="an expert over capacity keeps its best-scored assignments")
     ap.add_argument("--recompute", action="store_true",

@@ -106,6 +106,10 @@ typedef struct {
                                  instead of the earliest tokens; kept rows stay in token
                                  order inside its segment.  Needs (E+1 + T*k)*4 more bytes
                                  of ws.                                                   */
+    int32_t mxfp8;            /* 1: the routed experts' forward GEMMs run on MXFP8 operands
+                                 (moe_layer_fwd_mx); needs d and ffn multiples of 128 and
+                                 T*k*(d + ffn)*33/32 more bytes of ws for the quantised
+                                 activations.  The backward stays bf16.                   */
 } moe_config_t;
 
 /* Index of each saved tensor inside the forward context `ctx` (see moe_ctx_offsets). */
@@ -293,6 +297,56 @@ moe_status_t moe_grouped_ffn_bwd_gather(const moe_config_t *cfg, const void *dyp
 moe_status_t moe_unpermute_reduce(const moe_config_t *cfg, const void *dxp,
                                   const int32_t *dest_row, const void *dxs_or_null, void *dx,
                                   void *ws, void *stream);
+
+/*
+ * ---- MXFP8 forward of the routed experts (Primus MoE blog, FP8 section: the MXFP8 recipe
+ * with OCP E4M3 elements for the expert grouped GEMMs, weight-quantisation caching;
+ * MegaMoE section: the SwiGLU step quantises its own output).  MX rule (OCP Microscaling
+ * formats v1.0): blocks of 32 consecutive elements along the contraction axis share the
+ * scale 2^X, X = floor(log2(max |v|)) - 8 clamped to [-127, 127] (-127 for an all-zero
+ * block), stored as the E8M0 code X + 127; elements are E4M3(v / 2^X), rounded to
+ * nearest (ties to even) and saturated at +-448.  d and ffn must be multiples of 128.
+ */
+
+/* Bytes of the quantised-weight blob for cfg's routed experts, and the byte offsets of its
+ * four parts: offsets[0] W1 codes [E][2f][d] E4M3, offsets[1] W1 scales, offsets[2] W2
+ * codes [E][d][f], offsets[3] W2 scales.  The scales are stored in 512-byte atoms: atom
+ * ((e*(f/128) + nb)*(d/128) + kb)*2 + half holds, at byte 16*(m%32) + 4*(m/32) + j, the
+ * scale of W1 row e*2f + half*f + nb*128 + m, elements 32*(4*kb + j) .. +31; W2 atom
+ * ((e*ceil(d/256) + nt)*(f/128) + kb)*2 + half covers W2 row e*d + nt*256 + half*128 + m.
+ * Atom bytes of rows past an expert's end hold 127.  Host-only; offsets may be NULL. */
+moe_status_t moe_mx_weights_size(const moe_config_t *cfg, size_t *bytes, size_t *offsets);
+
+/* Quantise W1 [E,2f,d] and W2 [E,d,f] (bf16) into the blob (device, 256-byte aligned,
+ * moe_mx_weights_size bytes).  The caller keeps the blob while the weights are unchanged
+ * (weight-quantisation caching). */
+moe_status_t moe_mx_quantize_weights(const moe_config_t *cfg, const void *W1, const void *W2,
+                                     void *wq, void *stream);
+
+/* F3 with MXFP8 output: for p < offsets[E], xq[p] = E4M3 codes of x[src_tok[p]] and
+ * x_sf[p] = its E8M0 scales ([T*k][d] and [T*k][d/32] bytes); with xp_or_null also the
+ * bf16 copy xp[p] = x[src_tok[p]] (the backward's saved input). */
+moe_status_t moe_mx_permute_quant(const moe_config_t *cfg, const void *x,
+                                  const int32_t *src_tok, const int32_t *offsets,
+                                  void *xp_or_null, void *xq, uint8_t *x_sf, void *ws,
+                                  void *stream);
+
+/* F4 + F5 on MXFP8 operands (block-scaled tensor-core MMAs, fp32 accumulation):
+ *   [a|b] = bf16(deq(xq) deq(W1q[e])^T) -> ab;  h = bf16(silu(a) b) -> h;
+ *   hq, h_sf = MX(h) along f (the SwiGLU epilogue quantises its bf16 output);
+ *   yp = bf16(deq(hq) deq(W2q[e])^T).
+ * Shapes as moe_grouped_ffn; hq [T*k][f], h_sf [T*k][f/32] bytes. */
+moe_status_t moe_grouped_ffn_mx(const moe_config_t *cfg, const void *xq, const uint8_t *x_sf,
+                                const int32_t *offsets, const void *wq, void *ab, void *h,
+                                uint8_t *hq, uint8_t *h_sf, void *yp, void *ws, void *stream);
+
+/* Whole forward with the routed experts in MXFP8 (cfg->mxfp8 = 1): route -> permute and
+ * quantise -> MXFP8 grouped FFN -> (bf16 shared expert) -> combine.  ctx receives the same
+ * tensors as moe_layer_fwd (xp, ab, h, yp in bf16), so moe_layer_bwd runs unchanged; the
+ * quantised activations live in ws.  wq: the blob of moe_mx_quantize_weights. */
+moe_status_t moe_layer_fwd_mx(const moe_config_t *cfg, const float *logits, const void *x,
+                              const void *wq, const void *W1s, const void *W2s, void *y,
+                              void *ctx, void *ws, void *stream);
 
 /*
  * Whole forward: route -> permute -> grouped FFN -> (shared expert) -> combine.

@@ -240,10 +240,12 @@ def unpermute_reduce(cfg, dest_row, dxp, dxs=None, toks=None, row_of=None, rnd=T
 
 
 # --------------------------------------------------------------------------- full layer
-def layer_fwd(cfg, inp: dict, rnd: bool = True, r: dict | None = None) -> dict:
+def layer_fwd(cfg, inp: dict, rnd: bool = True, r: dict | None = None, mx: bool = False) -> dict:
     """Whole forward on the host, every token and every expert.
 
-    inp holds logits (f32 [T,E]) and x, W1, W2 (+ W1s, W2s) as bf16 bits or float64."""
+    inp holds logits (f32 [T,E]) and x, W1, W2 (+ W1s, W2s) as bf16 bits or float64.
+    mx: the routed experts' GEMMs on MXFP8 operands (ffn_fwd_rows_mx); the shared expert
+    stays bf16 (the MXFP8 recipe covers the routed-expert grouped GEMMs)."""
     if r is None:
         r = route(cfg, inp["logits"])
     x = _f64(inp["x"])
@@ -253,10 +255,17 @@ def layer_fwd(cfg, inp: dict, rnd: bool = True, r: dict | None = None) -> dict:
     xp = np.empty((n_rows, cfg.d))
     _load().orc_permute(n_rows, cfg.d, _p(r["src_tok"]), _p(x), _p(xp))
     ab = np.empty((n_rows, 2 * cfg.f)); h = np.empty((n_rows, cfg.f)); yp = np.empty((n_rows, cfg.d))
+    hq = np.zeros((n_rows, cfg.f), np.uint8) if mx else None
+    hs = np.zeros((n_rows, cfg.f // 32), np.uint8) if mx else None
     for e in range(cfg.E):
         s, t = int(off[e]), int(off[e + 1])
-        ab[s:t], h[s:t], yp[s:t] = ffn_fwd_rows(xp[s:t], W1[e], W2[e], rnd)
+        if mx:
+            ab[s:t], h[s:t], yp[s:t], hq[s:t], hs[s:t] = ffn_fwd_rows_mx(xp[s:t], W1[e], W2[e])
+        else:
+            ab[s:t], h[s:t], yp[s:t] = ffn_fwd_rows(xp[s:t], W1[e], W2[e], rnd)
     out = dict(route=r, xp=xp, ab=ab, h=h, yp=yp)
+    if mx:
+        out["hq"], out["h_sf"] = hq, hs
     ys = None
     if cfg.fs:
         out["ab_s"], out["h_s"], ys = ffn_fwd_rows(x, inp["W1s"], inp["W2s"], rnd)

@@ -38,7 +38,7 @@ class MoEConfigC(ctypes.Structure):
                 ("gate", ctypes.c_int32), ("route_scale", ctypes.c_float),
                 ("capacity", ctypes.c_int32), ("select_bias", ctypes.c_void_p),
                 ("drop_negative", ctypes.c_int32), ("recompute", ctypes.c_int32),
-                ("drop_by_score", ctypes.c_int32)]
+                ("drop_by_score", ctypes.c_int32), ("mxfp8", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):
@@ -77,6 +77,12 @@ def lib() -> ctypes.CDLL:
             "moe_grouped_ffn_bwd": ([cfgp] + [P] * 13, I32),
             "moe_unpermute_reduce": ([cfgp] + [P] * 6, I32),
             "moe_layer_fwd": ([cfgp] + [P] * 10, I32),
+            "moe_mx_weights_size": ([cfgp, ctypes.POINTER(ctypes.c_size_t),
+                                     ctypes.POINTER(ctypes.c_size_t)], I32),
+            "moe_mx_quantize_weights": ([cfgp] + [P] * 4, I32),
+            "moe_mx_permute_quant": ([cfgp] + [P] * 8, I32),
+            "moe_grouped_ffn_mx": ([cfgp] + [P] * 11, I32),
+            "moe_layer_fwd_mx": ([cfgp] + [P] * 9, I32),
             "moe_layer_bwd": ([cfgp] + [P] * 16, I32),
             "moe_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], I32),
             "moe_selftest_wait_timeout": ([P, I64, P], I32),
@@ -92,12 +98,12 @@ def lib() -> ctypes.CDLL:
 
 def make_config(T, d, E, k, ffn, ffn_shared=0, gate="softmax", route_scale=1.0,
                 capacity=0, select_bias=None, drop_negative=False,
-                recompute=False, drop_by_score=False) -> MoEConfigC:
+                recompute=False, drop_by_score=False, mxfp8=False) -> MoEConfigC:
     """select_bias: a float32 device tensor [E] (kept alive by the returned config) or None."""
     cfg = MoEConfigC(int(T), int(d), int(E), int(k), int(ffn), int(ffn_shared),
                      GATES[gate] if isinstance(gate, str) else int(gate), float(route_scale),
                      int(capacity), _p(select_bias), int(bool(drop_negative)),
-                     int(bool(recompute)), int(bool(drop_by_score)))
+                     int(bool(recompute)), int(bool(drop_by_score)), int(bool(mxfp8)))
     cfg._keep = select_bias
     return cfg
 
@@ -209,6 +215,36 @@ def moe_grouped_ffn_bwd_gather(cfg, dyp, x, src_tok, offsets, W1, W2, ab, h, dab
            "moe_grouped_ffn_bwd_gather")
 
 
+def moe_mx_weights_size(cfg):
+    """(bytes, [offsets of W1 codes, W1 scales, W2 codes, W2 scales]) of the MXFP8 blob."""
+    b = ctypes.c_size_t(0)
+    offs = (ctypes.c_size_t * 4)()
+    _check(lib().moe_mx_weights_size(_cfg(cfg), ctypes.byref(b), offs), "moe_mx_weights_size")
+    return b.value, [o for o in offs]
+
+
+def moe_mx_quantize_weights(cfg, W1, W2, wq, stream=None):
+    _check(lib().moe_mx_quantize_weights(_cfg(cfg), _p(W1), _p(W2), _p(wq), _s(stream)),
+           "moe_mx_quantize_weights")
+
+
+def moe_mx_permute_quant(cfg, x, src_tok, offsets, xp, xq, x_sf, ws, stream=None):
+    _check(lib().moe_mx_permute_quant(_cfg(cfg), _p(x), _p(src_tok), _p(offsets), _p(xp),
+                                      _p(xq), _p(x_sf), _p(ws), _s(stream)),
+           "moe_mx_permute_quant")
+
+
+def moe_grouped_ffn_mx(cfg, xq, x_sf, offsets, wq, ab, h, hq, h_sf, yp, ws, stream=None):
+    _check(lib().moe_grouped_ffn_mx(_cfg(cfg), _p(xq), _p(x_sf), _p(offsets), _p(wq), _p(ab),
+                                    _p(h), _p(hq), _p(h_sf), _p(yp), _p(ws), _s(stream)),
+           "moe_grouped_ffn_mx")
+
+
+def moe_layer_fwd_mx(cfg, logits, x, wq, W1s, W2s, y, ctx, ws, stream=None):
+    _check(lib().moe_layer_fwd_mx(_cfg(cfg), _p(logits), _p(x), _p(wq), _p(W1s), _p(W2s), _p(y),
+                                  _p(ctx), _p(ws), _s(stream)), "moe_layer_fwd_mx")
+
+
 def moe_grouped_ffn_bwd(cfg, dyp, xp, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2, ws,
                         stream=None):
     _check(lib().moe_grouped_ffn_bwd(_cfg(cfg), _p(dyp), _p(xp), _p(offsets), _p(W1), _p(W2),
@@ -297,6 +333,23 @@ class MoELayer:
         if y is None:
             y = torch.empty_like(x)
         moe_layer_fwd(self.cfg, logits, x, W1, W2, W1s, W2s, y, self.ctx, self.ws, stream)
+        return y
+
+    def quantize_weights(self, W1, W2, stream=None):
+        """MXFP8 blob of the routed weights (cache it while W1, W2 are unchanged)."""
+        import torch
+        nbytes, _ = moe_mx_weights_size(self.cfg)
+        wq = torch.empty(nbytes, dtype=torch.uint8, device=W1.device)
+        moe_mx_quantize_weights(self.cfg, W1, W2, wq, stream)
+        return wq
+
+    def forward_mx(self, logits, x, wq, W1s=None, W2s=None, y=None, stream=None):
+        """Forward with the routed experts in MXFP8 (config made with mxfp8=True); the
+        backward is the same bf16 call as after forward()."""
+        import torch
+        if y is None:
+            y = torch.empty_like(x)
+        moe_layer_fwd_mx(self.cfg, logits, x, wq, W1s, W2s, y, self.ctx, self.ws, stream)
         return y
 
     def backward(self, logits, x, dy, W1, W2, W1s=None, W2s=None, out=None, stream=None):

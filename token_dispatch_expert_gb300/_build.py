@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libmoe_gb300.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["route.cu", "dispatch.cu", "grouped_gemm.cu", "moe_api.cu"]
+SOURCES = ["route.cu", "dispatch.cu", "grouped_gemm.cu", "mx.cu", "moe_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

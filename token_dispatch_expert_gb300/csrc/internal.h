@@ -106,4 +106,37 @@ constexpr size_t SEG_MAP_BYTES = 128;   // one CUtensorMap
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st);
 
+// ----------------------------------------------------------------- MXFP8 forward
+// Byte offsets inside the quantised-weight blob: E4M3 codes of W1 [E][2f][d] and W2
+// [E][d][f], and their E8M0 scales in 512-byte atoms ([E][f/128][d/128][2][512] and
+// [E][ceil(d/256)][f/128][2][512]); every part 256-byte aligned.
+struct MxWeightLayout {
+  size_t w1q, w1sf, w2q, w2sf, total;
+};
+MxWeightLayout mx_weight_layout(int E, int d, int f);
+
+cudaError_t launch_mx_quant_weights(const void* W1, const void* W2, int E, int d, int f,
+                                    void* blob, cudaStream_t st);
+
+cudaError_t launch_mx_permute_quant(const void* x, const int32_t* src_tok,
+                                    const int32_t* offsets, int E, int64_t T, int64_t rows_cap,
+                                    int d, void* xp_or_null, void* xq, uint8_t* x_sf, int* err,
+                                    cudaStream_t st);
+
+struct MxFfnArgs {
+  int E, d, f;
+  int64_t rows_cap;
+  const int32_t* offsets;
+  const void* xq;        // [rows_cap][d] E4M3
+  const uint8_t* x_sf;   // [rows_cap][d/32] E8M0
+  const void* wq;        // quantised-weight blob
+  void* ab;              // [rows_cap][2f] bf16
+  void* h;               // [rows_cap][f] bf16
+  uint8_t* hq;           // [rows_cap][f] E4M3
+  uint8_t* h_sf;         // [rows_cap][f/32] E8M0
+  void* yp;              // [rows_cap][d] bf16
+  int* err;
+};
+cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st);
+
 }  // namespace moe

@@ -26,12 +26,14 @@ moe_status_t validate(const moe_config_t* c) {
   if (!std::isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
   if ((c->drop_negative != 0 && c->drop_negative != 1) ||
       (c->recompute != 0 && c->recompute != 1) ||
-      (c->drop_by_score != 0 && c->drop_by_score != 1))
+      (c->drop_by_score != 0 && c->drop_by_score != 1) || (c->mxfp8 != 0 && c->mxfp8 != 1))
     return MOE_ERR_INVALID_ARG;
   if (c->select_bias && (reinterpret_cast<uintptr_t>(c->select_bias) & 3u))
     return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->k > 8) return MOE_ERR_UNSUPPORTED;
   if (c->d % 64 || c->ffn % 64 || c->ffn_shared % 64) return MOE_ERR_UNSUPPORTED;
+  // MXFP8: K blocks of 128 elements; the backward's FC1 rerun would be bf16, not MXFP8
+  if (c->mxfp8 && (c->d % 128 || c->ffn % 128 || c->recompute)) return MOE_ERR_UNSUPPORTED;
   if (c->T * static_cast<int64_t>(c->k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
   // 2f rows x d of one expert must be addressable with int32 tile coordinates
   if (static_cast<int64_t>(c->E) * 2 * c->ffn >= (int64_t(1) << 31) ||
@@ -89,7 +91,7 @@ CtxLayout ctx_layout(const moe_config_t* c) {
 }
 
 struct WsLayout {
-  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, ab, h, ab_s, h_s, total;
+  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, ab, h, ab_s, h_s, xq, x_sf, hq, h_sf, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -111,6 +113,12 @@ WsLayout ws_layout(const moe_config_t* c) {
   L.h = o;     o += align_up(rc ? R * f * 2 : 0);
   L.ab_s = o;  o += align_up(rc ? T * 2 * fs * 2 : 0);
   L.h_s = o;   o += align_up(rc ? T * fs * 2 : 0);
+  // MXFP8 forward: the quantised activations and their scales
+  const bool mx = c->mxfp8 != 0;
+  L.xq = o;    o += align_up(mx ? R * d : 0);
+  L.x_sf = o;  o += align_up(mx ? R * d / 32 : 0);
+  L.hq = o;    o += align_up(mx ? R * f : 0);
+  L.h_sf = o;  o += align_up(mx ? R * f / 32 : 0);
   L.total = o;
   return L;
 }
@@ -411,6 +419,128 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const float* logits, const v
     void* ab_s = rc ? at<uint8_t>(ws, W.ab_s) : at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]);
     void* h_s = rc ? at<uint8_t>(ws, W.h_s) : at<uint8_t>(ctx, C.off[MOE_CTX_H_S]);
     s = ffn_fwd(cfg, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s, ab_s, h_s, ysw, err, st);
+    if (s != MOE_OK) return s;
+    ys = ysw;
+  }
+  MOE_TRY(launch_combine(yp, at<int32_t>(ctx, C.off[MOE_CTX_DEST_ROW]),
+                         at<float>(ctx, C.off[MOE_CTX_TOPK_W]), ys, cfg->T, cfg->k, cfg->d,
+                         cfg->T * cfg->k, y, err, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_mx_weights_size(const moe_config_t* cfg, size_t* bytes, size_t* offsets) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->d % 128 || cfg->ffn % 128) return MOE_ERR_UNSUPPORTED;
+  const MxWeightLayout L = mx_weight_layout(cfg->E, cfg->d, cfg->ffn);
+  if (bytes) *bytes = L.total;
+  if (offsets) {
+    offsets[0] = L.w1q;
+    offsets[1] = L.w1sf;
+    offsets[2] = L.w2q;
+    offsets[3] = L.w2sf;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_mx_quantize_weights(const moe_config_t* cfg, const void* W1, const void* W2,
+                                     void* wq, void* stream) {
+  size_t bytes = 0;
+  moe_status_t s = moe_mx_weights_size(cfg, &bytes, nullptr);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(W1, W2, wq) || (reinterpret_cast<uintptr_t>(wq) & 255u)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_mx_quant_weights(W1, W2, cfg->E, cfg->d, cfg->ffn, wq,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_mx_permute_quant(const moe_config_t* cfg, const void* x, const int32_t* src_tok,
+                                  const int32_t* offsets, void* xp_or_null, void* xq,
+                                  uint8_t* x_sf, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->d % 128) return MOE_ERR_UNSUPPORTED;
+  if (!ptrs_ok(x, src_tok, offsets, xq, x_sf, ws)) return MOE_ERR_INVALID_ARG;
+  if (xp_or_null && !aligned16(xp_or_null)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_mx_permute_quant(x, src_tok, offsets, cfg->E, cfg->T,
+                                             cfg->T * cfg->k, cfg->d, xp_or_null, xq, x_sf,
+                                             static_cast<int*>(ws),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_ffn_mx(const moe_config_t* cfg, const void* xq, const uint8_t* x_sf,
+                                const int32_t* offsets, const void* wq, void* ab, void* h,
+                                uint8_t* hq, uint8_t* h_sf, void* yp, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->d % 128 || cfg->ffn % 128) return MOE_ERR_UNSUPPORTED;
+  if (!ptrs_ok(xq, x_sf, offsets, wq, ab, h, hq, h_sf, yp, ws)) return MOE_ERR_INVALID_ARG;
+  MxFfnArgs a{};
+  a.E = cfg->E;
+  a.d = cfg->d;
+  a.f = cfg->ffn;
+  a.rows_cap = cfg->T * cfg->k;
+  a.offsets = offsets;
+  a.xq = xq;
+  a.x_sf = x_sf;
+  a.wq = wq;
+  a.ab = ab;
+  a.h = h;
+  a.hq = hq;
+  a.h_sf = h_sf;
+  a.yp = yp;
+  a.err = static_cast<int*>(ws);
+  return cuda_status(launch_mx_ffn(a, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_fwd_mx(const moe_config_t* cfg, const float* logits, const void* x,
+                              const void* wq, const void* W1s, const void* W2s, void* y,
+                              void* ctx, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!cfg->mxfp8) return MOE_ERR_INVALID_ARG;
+  if (!ptrs_ok(logits, x, wq, y, ctx, ws)) return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared && !ptrs_ok(W1s, W2s)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(ws);
+  CtxLayout C = ctx_layout(cfg);
+  WsLayout W = ws_layout(cfg);
+  int32_t* offsets = at<int32_t>(ctx, C.off[MOE_CTX_OFFSETS]);
+  const int32_t* src_tok = at<int32_t>(ctx, C.off[MOE_CTX_SRC_TOK]);
+  MOE_TRY(launch_route(cfg, logits, at<int32_t>(ctx, C.off[MOE_CTX_TOPK_IDX]),
+                       at<float>(ctx, C.off[MOE_CTX_TOPK_W]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_COUNTS]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_KEPT]), offsets,
+                       at<int32_t>(ctx, C.off[MOE_CTX_DEST_ROW]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_SRC_TOK]),
+                       at<int32_t>(ctx, C.off[MOE_CTX_SRC_SLOT]),
+                       at<uint8_t>(ctx, C.off[MOE_CTX_DROP_MASK]), at<uint8_t>(ws, W.route), err,
+                       st));
+  void* xp = at<uint8_t>(ctx, C.off[MOE_CTX_XP]);
+  MOE_TRY(launch_mx_permute_quant(x, src_tok, offsets, cfg->E, cfg->T, cfg->T * cfg->k, cfg->d,
+                                  xp, at<uint8_t>(ws, W.xq), at<uint8_t>(ws, W.x_sf), err, st));
+  MxFfnArgs a{};
+  a.E = cfg->E;
+  a.d = cfg->d;
+  a.f = cfg->ffn;
+  a.rows_cap = cfg->T * cfg->k;
+  a.offsets = offsets;
+  a.xq = at<uint8_t>(ws, W.xq);
+  a.x_sf = at<uint8_t>(ws, W.x_sf);
+  a.wq = wq;
+  a.ab = at<uint8_t>(ctx, C.off[MOE_CTX_AB]);
+  a.h = at<uint8_t>(ctx, C.off[MOE_CTX_H]);
+  a.hq = at<uint8_t>(ws, W.hq);
+  a.h_sf = at<uint8_t>(ws, W.h_sf);
+  void* yp = at<uint8_t>(ctx, C.off[MOE_CTX_YP]);
+  a.yp = yp;
+  a.err = err;
+  MOE_TRY(launch_mx_ffn(a, st));
+  const void* ys = nullptr;
+  if (cfg->ffn_shared) {   // the shared expert stays bf16
+    void* ysw = at<uint8_t>(ctx, C.off[MOE_CTX_YS]);
+    s = ffn_fwd(cfg, x, nullptr, cfg->T, cfg->ffn_shared, W1s, W2s,
+                at<uint8_t>(ctx, C.off[MOE_CTX_AB_S]), at<uint8_t>(ctx, C.off[MOE_CTX_H_S]), ysw,
+                err, st);
     if (s != MOE_OK) return s;
     ys = ysw;
   }

@@ -1,0 +1,720 @@
+// mx.cu -- the MXFP8 forward of the routed experts: quantisation kernels and the
+// block-scaled grouped GEMMs (FC1 + SwiGLU + quantisation of h, FC2).
+//
+// "MoE Training Optimization with Primus", FP8 section: the MXFP8 recipe (OCP E4M3
+// elements with per-block power-of-two scales) for the routed-expert grouped GEMMs, and
+// weight-quantisation caching; MegaMoE section: the SwiGLU step quantises its own output,
+// so the cast is never a separate pass.  Block rule (OCP Microscaling formats v1.0): a
+// block is 32 consecutive elements along the contraction axis; its scale is the E8M0
+// power of two 2^X with X = floor(log2(max |v|)) - 8 (8 = the exponent of E4M3's largest
+// value, 448), clamped to [-127, 127], -127 for an all-zero block; elements are v / 2^X
+// rounded to E4M3 (nearest, ties to even, saturating at 448).
+//
+// Tensor-core path: tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale, M 128 x N 256 x
+// K 32 per instruction, E4M3 operands in 128-byte-swizzled shared memory (one K block =
+// 128 elements = one 128-byte row), fp32 accumulation in TMEM.  The scales live in TMEM:
+// the MMA reads row m's scale of A from lane m, column base + m/32, byte = the sub-block
+// (0..3) named in the instruction descriptor, and column n's scale of B from lane n%32 of
+// every lane quarter, column base + n/32.  tcgen05.cp.32x128b.warpx4 produces exactly that
+// from a 512-byte "atom" in shared memory: byte 16*(m%32) + 4*(m/32) + k holds the scale of
+// row m, sub-block k (the layout was measured with an in-bounds probe on GB300).
+//
+// The weights' scales are written once, already in atom order (the quantised weights are
+// cached by the caller); the activations' scales are row-major [rows][K/32] and the
+// producer warp rearranges each K block's 128 rows into an atom with plain loads.
+//
+// TMEM holds one 256-column accumulator and 4 stages x 12 scale columns.  There is no
+// room for a second accumulator, so eight epilogue warps (two per lane quarter, each
+// taking half the columns) copy the accumulator into registers and release it at once;
+// the next tile's MMAs then overlap the epilogue's arithmetic and stores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp8.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int MX_BK = 128;                 // E4M3 elements (bytes) per K block
+constexpr int MX_STAGES = 4;
+constexpr int MX_A_BYTES = 128 * MX_BK;    // 16 KB
+constexpr int MX_B_BYTES = 256 * MX_BK;    // 32 KB
+constexpr int MX_SFA_BYTES = 512;
+constexpr int MX_SFB_BYTES = 1024;
+constexpr int MX_STAGE_BYTES = 51200;      // A | B | SFA | SFB, rounded up to 1 KB
+constexpr int MX_THREADS = 320;            // producer, MMA, 8 epilogue warps
+constexpr int MX_EPI_WARPS = 8;
+constexpr uint32_t MX_TMEM_COLS = 512;
+constexpr uint32_t MX_SF_COL0 = 256;       // scale slots: 12 columns per stage
+constexpr int MX_MAX_G = 256;
+constexpr long long MX_WAIT_BUDGET = 4000000000LL;
+
+static_assert(MX_A_BYTES + MX_B_BYTES + MX_SFA_BYTES + MX_SFB_BYTES <= MX_STAGE_BYTES, "stage");
+
+// ------------------------------------------------------------------ quantisation helpers
+// X = floor(log2(amax)) - 8, clamped to [-127, 127]; -127 when amax is 0 (or subnormal,
+// whose floor(log2) lies below -127 anyway).
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (e == 0) return -127;
+  const int X = e - 127 - 8;
+  return X < -127 ? -127 : X;   // at most 254 - 135 = 119: never above 127
+}
+
+// 2^n for n in [-126, 127] (normal fp32)
+__device__ __forceinline__ float exp2_int(int n) {
+  return __uint_as_float(static_cast<uint32_t>(n + 127) << 23);
+}
+
+// two values -> two E4M3 codes (round to nearest even, saturate to +-448); a in the low byte
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                                        __NV_E4M3));
+}
+
+// Quantise one block of 32 values: 32 codes into c[8] (4 per word, element 0 lowest),
+// returns the E8M0 scale code.
+__device__ __forceinline__ uint32_t mx_block(const float* v, uint32_t* c) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int X = mx_exponent(amax);
+  const float inv = exp2_int(-X);   // -X in [-119, 127]: exact scaling
+#pragma unroll
+  for (int w = 0; w < 8; ++w)
+    c[w] = e4m3x2(v[4 * w] * inv, v[4 * w + 1] * inv) |
+           (e4m3x2(v[4 * w + 2] * inv, v[4 * w + 3] * inv) << 16);
+  return static_cast<uint32_t>(X + 127);
+}
+
+// Byte offset of (row m of a 128-row block, sub-block k) inside a scale atom.
+__host__ __device__ __forceinline__ int atom_byte(int m, int k) {
+  return 16 * (m & 31) + 4 * (m >> 5) + k;
+}
+
+// ------------------------------------------------------------------ F3 + quantisation
+// Warp per destination row p < offsets[E]: x[src_tok[p]] (bf16, d elements) is quantised
+// into xq[p] (E4M3) and x_sf[p] (E8M0 per 32 elements); with xp != null the bf16 row is
+// also copied (the backward's saved input).  Lane l takes blocks l, l+32, ...
+constexpr int QTHREADS = 256;
+
+__global__ void __launch_bounds__(QTHREADS)
+mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
+                        const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap,
+                        int d, uint4* __restrict__ xp, uint4* __restrict__ xq,
+                        uint8_t* __restrict__ x_sf, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * QTHREADS + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * QTHREADS) >> 5;
+  int64_t n_rows = offsets[E];
+  if (n_rows < 0 || n_rows > rows_cap) {
+    if (gw == 0 && lane == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
+    n_rows = n_rows < 0 ? 0 : rows_cap;
+  }
+  const int nb = d / 32;
+  for (int64_t p = gw; p < n_rows; p += nw) {
+    const int t = __ldg(src_tok + p);
+    if (t < 0 || t >= T) {
+      if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
+      continue;
+    }
+    const uint4* src = x + static_cast<int64_t>(t) * (d / 8);
+    for (int b = lane; b < nb; b += 32) {
+      uint4 raw[4];
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        raw[i] = __ldg(src + 4 * b + i);
+        unpack8(raw[i], v + 8 * i);
+      }
+      if (xp) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xp[p * (d / 8) + 4 * b + i] = raw[i];
+      }
+      uint32_t c[8];
+      const uint32_t s = mx_block(v, c);
+      uint4* dq = xq + p * (d / 16) + 2 * b;
+      dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
+      x_sf[p * nb + b] = static_cast<uint8_t>(s);
+    }
+  }
+}
+
+// Weight quantisation, warp per weight row.  W1 [E][2f][d]: codes row-major into w1q,
+// scales into atoms [E][f/128][d/128][2 halves][512 B] (half 0: gate rows, 1: up rows).
+// W2 [E][d][f]: codes into w2q, scales into atoms [E][ceil(d/256)][f/128][2][512 B].
+__global__ void __launch_bounds__(QTHREADS)
+mx_weight_quant_kernel(const uint4* __restrict__ W, int64_t n_rows, int rows_per_expert,
+                       int K, int which, int f, int n_blocks_mn, uint4* __restrict__ wq,
+                       uint8_t* __restrict__ atoms) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * QTHREADS + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * QTHREADS) >> 5;
+  const int nb = K / 32, KB = K / 128;
+  for (int64_t r = gw; r < n_rows; r += nw) {
+    const int64_t e = r / rows_per_expert;
+    const int re = static_cast<int>(r - e * rows_per_expert);
+    int half, blk, m;
+    if (which == 0) {   // W1: gate rows [0, f), up rows [f, 2f); 128-row blocks per half
+      half = re >= f ? 1 : 0;
+      const int rr = re - half * f;
+      blk = rr >> 7;
+      m = rr & 127;
+    } else {            // W2: 256-row N tiles, two 128-row halves each
+      blk = re >> 8;
+      half = (re >> 7) & 1;
+      m = re & 127;
+    }
+    const uint4* src = W + r * (K / 8);
+    for (int b = lane; b < nb; b += 32) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) unpack8(__ldg(src + 4 * b + i), v + 8 * i);
+      uint32_t c[8];
+      const uint32_t s = mx_block(v, c);
+      uint4* dq = wq + r * (K / 16) + 2 * b;
+      dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
+      const int kb = b >> 2, k1 = b & 3;
+      const int64_t atom = ((e * n_blocks_mn + blk) * KB + kb) * 2 + half;
+      atoms[atom * 512 + atom_byte(m, k1)] = static_cast<uint8_t>(s);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ block-scaled GEMM
+struct MxCtl {
+  uint64_t full[MX_STAGES];
+  uint64_t empty[MX_STAGES];
+  uint64_t tfull;
+  uint64_t tempty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int bad;
+  int pad;
+  int gstart[MX_MAX_G + 2];
+  int tprefix[MX_MAX_G + 2];
+};
+
+constexpr size_t MX_SMEM = 1024 + MX_STAGES * MX_STAGE_BYTES + sizeof(MxCtl);
+
+struct MxParams {
+  int G;
+  long long rows_cap;
+  int d, f;
+  int num_n_tiles;
+  int num_kb;
+  int n_out;
+  int kb_sf;                  // bytes per row of the A scales (K / 32)
+  int n_blocks_mn;            // B atom blocks per expert (W1: f/128, W2: ceil(d/256))
+  const int32_t* offsets;
+  const uint8_t* a_sf;        // [rows_cap][K/32] E8M0, row-major
+  const uint8_t* b_atoms;     // weight scale atoms
+  __nv_bfloat16* out0;        // FC1: ab  FC2: yp
+  __nv_bfloat16* out1;        // FC1: h
+  uint8_t* out_q;             // FC1: hq  [rows_cap][f] E4M3
+  uint8_t* out_sf;            // FC1: h_sf [rows_cap][f/32] E8M0
+  int* err;
+};
+
+__device__ __forceinline__ int mx_ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  return make_smem_desc(saddr, 16, 1024);
+}
+// no-swizzle descriptor of a 32-row x 16-byte scale atom (8-row core matrices 128 B apart)
+__device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+// kind::mxf8f6f4 instruction descriptor: E4M3 x E4M3, K-major A and B, UE8M0 scales;
+// [4,6) B scale sub-block, [7,10) A type, [10,13) B type, [17,23) N>>3, [23] scale type
+// UE8M0, [24,29) M>>4, [29,31) A scale sub-block.
+__device__ __forceinline__ uint32_t idesc_mx(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
+         (static_cast<uint32_t>(sf_id) << 29);
+}
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mx_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             int* err, long long budget) {
+  return __all_sync(FULL_MASK, mbar_wait_bounded(bar, parity, abort, err, budget));
+}
+
+__device__ __forceinline__ float silu_mx(float a) { return a / (1.0f + expf(-a)); }
+__device__ __forceinline__ float bf16r(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+template <int MODE>   // GEMM_FC1_SWIGLU or GEMM_FC2
+__global__ void __launch_bounds__(MX_THREADS, 1)
+mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  MxCtl* ctl = reinterpret_cast<MxCtl*>(smem + MX_STAGES * MX_STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  volatile int* abort_flag = &ctl->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < MX_STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->tfull), 1);
+    mbar_init(smem_u32(&ctl->tempty), MX_EPI_WARPS);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    fence_mbar_init();
+    ctl->abort = 0;
+    ctl->bad = 0;
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  for (int g = threadIdx.x; g <= p.G; g += MX_THREADS) ctl->gstart[g] = p.offsets[g];
+  __syncthreads();
+  if (warp == 0) {
+    const int per = mx_ceil_div(p.G, 32);
+    int local = 0, bad = 0;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < p.G) {
+        const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
+        if (b < a || a < 0 || b > p.rows_cap) bad = 1;
+        local += b < a ? 0 : mx_ceil_div(b - a, 128) * p.num_n_tiles;
+      }
+    }
+    const int incl = warp_incl_scan(local);
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int g = lane * per + i;
+      if (g < p.G) {
+        ctl->tprefix[g] = run;
+        const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
+        run += b < a ? 0 : mx_ceil_div(b - a, 128) * p.num_n_tiles;
+      }
+    }
+    if (lane == 31) ctl->tprefix[p.G] = incl;
+    if (ctl->gstart[0] != 0) bad = 1;
+    bad = __any_sync(FULL_MASK, bad);
+    if (lane == 0 && bad) {
+      ctl->bad = 1;
+      if (blockIdx.x == 0) flag_error(p.err, MOE_DEVERR_BAD_OFFSETS);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), MX_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int total = ctl->bad ? 0 : ctl->tprefix[p.G];
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  auto map_tile = [&](int tile, int& g, int& mt, int& nt) {
+    int lo = 0, hi = p.G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ctl->tprefix[mid] <= tile) lo = mid;
+      else hi = mid;
+    }
+    g = lo;
+    const int local = tile - ctl->tprefix[g];
+    const int mtg = mx_ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], 128);
+    nt = local / mtg;
+    mt = local - nt * mtg;
+  };
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer (whole warp)
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    const int nkb = p.num_kb;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int g, mt, nt;
+      map_tile(tile, g, mt, nt);
+      const int seg0 = ctl->gstart[g];
+      const int seg_last = ctl->gstart[g + 1] - 1;
+      const int row0 = seg0 + mt * 128;
+      // this lane's four A rows of the tile (rows past the segment read its last row;
+      // their outputs are never stored)
+      const uint8_t* sf_row[4];
+#pragma unroll
+      for (int m1 = 0; m1 < 4; ++m1)
+        sf_row[m1] = p.a_sf + static_cast<long long>(min(row0 + lane + 32 * m1, seg_last)) * p.kb_sf;
+      uint32_t nxt[4];
+#pragma unroll
+      for (int m1 = 0; m1 < 4; ++m1) nxt[m1] = __ldg(reinterpret_cast<const uint32_t*>(sf_row[m1]));
+      const uint8_t* b_atom =
+          p.b_atoms + (static_cast<long long>(g) * p.n_blocks_mn + nt) * nkb * 1024;
+      for (int kb = 0; kb < nkb; ++kb) {
+        uint32_t cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        if (kb + 1 < nkb) {
+#pragma unroll
+          for (int m1 = 0; m1 < 4; ++m1)
+            nxt[m1] = __ldg(reinterpret_cast<const uint32_t*>(sf_row[m1] + 4 * (kb + 1)));
+        }
+        if (!mx_warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, MX_WAIT_BUDGET)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_base + s * MX_STAGE_BYTES;
+        const uint32_t sb = sa + MX_A_BYTES;
+        const uint32_t ssfa = sb + MX_B_BYTES;
+        const uint32_t ssfb = ssfa + MX_SFA_BYTES;
+        // the A scales of this K block: lane m0 writes bytes 16*m0 .. 16*m0+15 of the atom
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ssfa + 16 * lane),
+                     "r"(cur[0]), "r"(cur[1]), "r"(cur[2]), "r"(cur[3])
+                     : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t full = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(full, MX_A_BYTES + MX_B_BYTES + MX_SFB_BYTES);
+          const int k0 = kb * MX_BK;
+          tma_load_2d(sa, &tmA, full, k0, row0);
+          if (MODE == GEMM_FC1_SWIGLU) {
+            const int wrow = g * 2 * p.f + nt * 128;
+            tma_load_2d(sb, &tmB, full, k0, wrow);                          // gate rows
+            tma_load_2d(sb + MX_B_BYTES / 2, &tmB, full, k0, wrow + p.f);   // up rows
+          } else {
+            const int wrow = g * p.d + nt * 256;
+            tma_load_2d(sb, &tmB, full, k0, wrow);
+            tma_load_2d(sb + MX_B_BYTES / 2, &tmB, full, k0, wrow + 128);
+          }
+          bulk_load(ssfb, b_atom + kb * 1024, MX_SFB_BYTES, full);
+        }
+        if (++s == MX_STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    for (int i = 0; i < MX_STAGES && ok; ++i) {
+      if (!mx_warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, MX_WAIT_BUDGET / 4))
+        break;
+      if (++s == MX_STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    int s = 0;
+    uint32_t ph = 0;
+    int it = 0;
+    bool ok = true, issued_any = false;
+    const int nkb = p.num_kb;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      if (!mx_warp_wait(smem_u32(&ctl->tempty), (it & 1) ^ 1u, abort_flag, p.err,
+                        MX_WAIT_BUDGET)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mx_warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, MX_WAIT_BUDGET)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_base + s * MX_STAGE_BYTES;
+        const uint32_t sb = sa + MX_A_BYTES;
+        const uint32_t ssfa = sb + MX_B_BYTES;
+        const uint32_t ssfb = ssfa + MX_SFA_BYTES;
+        const uint32_t sf_col = tmem_base + MX_SF_COL0 + 12u * static_cast<uint32_t>(s);
+        if (lane == 0) {
+          tc_cp_atom(sf_col, sdesc_atom(ssfa));             // A: 128 rows x 4 sub-blocks
+          tc_cp_atom(sf_col + 4, sdesc_atom(ssfb));         // B: columns 0..127
+          tc_cp_atom(sf_col + 8, sdesc_atom(ssfb + 512));   // B: columns 128..255
+#pragma unroll
+          for (int kk = 0; kk < MX_BK / 32; ++kk)
+            tc_mma_mx(tmem_base, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32),
+                      idesc_mx(128, 256, kk), sf_col, sf_col + 4, (kb | kk) != 0 ? 1u : 0u);
+          tc_commit(smem_u32(&ctl->empty[s]));
+        }
+        issued_any = true;
+        __syncwarp();
+        if (++s == MX_STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(smem_u32(&ctl->tfull));
+      __syncwarp();
+    }
+    if (!ok && issued_any && lane == 0) {
+      tc_commit(smem_u32(&ctl->drain));
+      long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < MX_WAIT_BUDGET / 4) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue (8 warps)
+    const int q = warp & 3;                  // the lane quarter this warp may access
+    const int hh = (warp - 2) >> 2;          // which half of the columns
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      int g, mt, nt;
+      map_tile(tile, g, mt, nt);
+      const long long prow = static_cast<long long>(ctl->gstart[g]) + mt * 128 + r_in_tile;
+      const bool valid = prow < ctl->gstart[g + 1];
+      if (!mx_warp_wait(smem_u32(&ctl->tfull), it & 1, abort_flag, p.err, MX_WAIT_BUDGET)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      uint32_t acc[128];
+      if (MODE == GEMM_FC1_SWIGLU) {
+        // gate columns [64 hh, 64 hh + 64) and the matching up columns 128 + ...
+        tmem_ld32(taddr + 64 * hh, acc);
+        tmem_ld32(taddr + 64 * hh + 32, acc + 32);
+        tmem_ld32(taddr + 128 + 64 * hh, acc + 64);
+        tmem_ld32(taddr + 128 + 64 * hh + 32, acc + 96);
+      } else {
+        tmem_ld32(taddr + 128 * hh, acc);
+        tmem_ld32(taddr + 128 * hh + 32, acc + 32);
+        tmem_ld32(taddr + 128 * hh + 64, acc + 64);
+        tmem_ld32(taddr + 128 * hh + 96, acc + 96);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty));   // the accumulator is free
+      if (!valid) continue;
+      if (MODE == GEMM_FC1_SWIGLU) {
+        const int f = p.f;
+        const int n0 = nt * 128 + 64 * hh;     // f is a multiple of 128: always in range
+        uint4* ab_a = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
+        uint4* ab_b = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
+        uint4* hp = reinterpret_cast<uint4*>(p.out1 + prow * f + n0);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          float h[32];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float a[8], b[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              a[e] = bf16r(__uint_as_float(acc[32 * blk + 8 * v + e]));
+              b[e] = bf16r(__uint_as_float(acc[64 + 32 * blk + 8 * v + e]));
+              h[8 * v + e] = bf16r(silu_mx(a[e]) * b[e]);
+            }
+            ab_a[4 * blk + v] = pack8(a);
+            ab_b[4 * blk + v] = pack8(b);
+            hp[4 * blk + v] = pack8(h + 8 * v);
+          }
+          // the SwiGLU step quantises its own (bf16) output for FC2
+          uint32_t c[8];
+          const uint32_t sc = mx_block(h, c);
+          uint4* dq = reinterpret_cast<uint4*>(p.out_q + prow * f + n0 + 32 * blk);
+          dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
+          dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
+          p.out_sf[prow * (f / 32) + n0 / 32 + blk] = static_cast<uint8_t>(sc);
+        }
+      } else {
+        const int n0 = nt * 256 + 128 * hh;
+        if (n0 < p.n_out) {                    // d is a multiple of 128: all or nothing
+          uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * p.n_out + n0);
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(acc[8 * v + e]);
+            o[v] = pack8(x);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, MX_TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 mx_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D byte tensor map over a row-major [rows, cols] E4M3 matrix, 128-byte swizzle, box =
+// 128 columns (bytes) x 128 rows, zero fill out of bounds.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  auto enc = mx_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+int grid_rows(int64_t rows) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (rows + (QTHREADS / 32) - 1) / (QTHREADS / 32);
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+template <int MODE>
+cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const MxParams& kp,
+                           cudaStream_t st) {
+  auto kern = mx_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(MX_SMEM));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  kern<<<sms, MX_THREADS, MX_SMEM, st>>>(ta, tb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+MxWeightLayout mx_weight_layout(int E, int d, int f) {
+  auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  MxWeightLayout L;
+  const size_t Es = static_cast<size_t>(E), ds = static_cast<size_t>(d),
+               fs = static_cast<size_t>(f);
+  size_t o = 0;
+  L.w1q = o;  o += up(Es * 2 * fs * ds);
+  L.w1sf = o; o += up(Es * (fs / 128) * (ds / 128) * 1024);
+  L.w2q = o;  o += up(Es * ds * fs);
+  L.w2sf = o; o += up(Es * ((ds + 255) / 256) * (fs / 128) * 1024);
+  L.total = o;
+  return L;
+}
+
+cudaError_t launch_mx_quant_weights(const void* W1, const void* W2, int E, int d, int f,
+                                    void* blob, cudaStream_t st) {
+  const MxWeightLayout L = mx_weight_layout(E, d, f);
+  uint8_t* b = static_cast<uint8_t*>(blob);
+  // atom bytes of rows past an expert's last row are never written: give them scale 1
+  cudaError_t e = cudaMemsetAsync(b + L.w1sf, 127, L.w2q - L.w1sf, st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(b + L.w2sf, 127, L.total - L.w2sf, st);
+  if (e != cudaSuccess) return e;
+  const int64_t r1 = static_cast<int64_t>(E) * 2 * f, r2 = static_cast<int64_t>(E) * d;
+  mx_weight_quant_kernel<<<grid_rows(r1), QTHREADS, 0, st>>>(
+      static_cast<const uint4*>(W1), r1, 2 * f, d, 0, f, f / 128,
+      reinterpret_cast<uint4*>(b + L.w1q), b + L.w1sf);
+  mx_weight_quant_kernel<<<grid_rows(r2), QTHREADS, 0, st>>>(
+      static_cast<const uint4*>(W2), r2, d, f, 1, f, (d + 255) / 256,
+      reinterpret_cast<uint4*>(b + L.w2q), b + L.w2sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_permute_quant(const void* x, const int32_t* src_tok,
+                                    const int32_t* offsets, int E, int64_t T, int64_t rows_cap,
+                                    int d, void* xp_or_null, void* xq, uint8_t* x_sf, int* err,
+                                    cudaStream_t st) {
+  mx_permute_quant_kernel<<<grid_rows(rows_cap), QTHREADS, 0, st>>>(
+      static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d,
+      static_cast<uint4*>(xp_or_null), static_cast<uint4*>(xq), x_sf, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
+  if (a.E < 1 || a.E > MX_MAX_G || a.d % 128 || a.f % 128) return cudaErrorInvalidValue;
+  const MxWeightLayout L = mx_weight_layout(a.E, a.d, a.f);
+  const uint8_t* wb = static_cast<const uint8_t*>(a.wq);
+  const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
+  const uint64_t E = static_cast<uint64_t>(a.E), d = static_cast<uint64_t>(a.d),
+                 f = static_cast<uint64_t>(a.f);
+  MxParams kp{};
+  kp.G = a.E;
+  kp.rows_cap = a.rows_cap;
+  kp.d = a.d;
+  kp.f = a.f;
+  kp.offsets = a.offsets;
+  kp.err = a.err;
+  CUtensorMap ta, tb;
+  // FC1: [a|b] = xq W1q^T (K = d), SwiGLU, h quantised
+  kp.num_n_tiles = a.f / 128;
+  kp.num_kb = a.d / MX_BK;
+  kp.n_out = a.f;
+  kp.kb_sf = a.d / 32;
+  kp.n_blocks_mn = a.f / 128;
+  kp.a_sf = a.x_sf;
+  kp.b_atoms = wb + L.w1sf;
+  kp.out0 = static_cast<__nv_bfloat16*>(a.ab);
+  kp.out1 = static_cast<__nv_bfloat16*>(a.h);
+  kp.out_q = a.hq;
+  kp.out_sf = a.h_sf;
+  if (!make_map_u8(&ta, a.xq, d, rows) || !make_map_u8(&tb, wb + L.w1q, d, E * 2 * f))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_mx_mode<GEMM_FC1_SWIGLU>(ta, tb, kp, st);
+  if (e != cudaSuccess) return e;
+  // FC2: yp = hq W2q^T (K = f)
+  kp.num_n_tiles = (a.d + 255) / 256;
+  kp.num_kb = a.f / MX_BK;
+  kp.n_out = a.d;
+  kp.kb_sf = a.f / 32;
+  kp.n_blocks_mn = (a.d + 255) / 256;
+  kp.a_sf = a.h_sf;
+  kp.b_atoms = wb + L.w2sf;
+  kp.out0 = static_cast<__nv_bfloat16*>(a.yp);
+  kp.out1 = nullptr;
+  kp.out_q = nullptr;
+  kp.out_sf = nullptr;
+  if (!make_map_u8(&ta, a.hq, f, rows) || !make_map_u8(&tb, wb + L.w2q, f, E * d))
+    return cudaErrorInvalidValue;
+  return launch_mx_mode<GEMM_FC2>(ta, tb, kp, st);
+}
+
+}  // namespace moe
