@@ -295,8 +295,12 @@ def bench_ours(args, world, rank, local):
         nbytes, _ = tde.moe_mx_weights_size(cfg)
         wq = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         u8 = dict(dtype=torch.uint8, device=dev)
-        mxb = dict(xq=torch.empty((R, c.d), **u8), xs=torch.empty((R, c.d // 32), **u8),
-                   hq=torch.empty((R, c.f), **u8), hs=torch.empty((R, c.f // 32), **u8))
+        # the activation scales are atoms tiled by 128 rows per expert segment: sized by
+        # the library, not by rows x K/32
+        mxb = dict(xq=torch.empty((R, c.d), **u8),
+                   xs=torch.empty(tde.moe_mx_act_scales_size(cfg, c.d), **u8),
+                   hq=torch.empty((R, c.f), **u8),
+                   hs=torch.empty(tde.moe_mx_act_scales_size(cfg, c.f), **u8))
         if args.mx_cache_weights:
             # weight-quantisation caching: the blob is made once, as when one optimizer
             # step's weights serve many micro-batches

@@ -317,15 +317,24 @@ moe_status_t moe_unpermute_reduce(const moe_config_t *cfg, const void *dxp,
  * Atom bytes of rows past an expert's end hold 127.  Host-only; offsets may be NULL. */
 moe_status_t moe_mx_weights_size(const moe_config_t *cfg, size_t *bytes, size_t *offsets);
 
+/* Bytes of an activation scale array for contraction length K (d for x, ffn for h).
+ * Activation scales are stored in 512-byte atoms tiled by 128 rows inside each expert
+ * segment: for row p of expert e, local row l = p - offsets[e], m = l % 128, the scale of
+ * elements 32*(4*kb + j) .. +31 sits in atom ((offsets[e] >> 7) + e + l/128) * (K/128) + kb
+ * at byte 16*(m%32) + 4*(m/32) + j; bytes of rows past a segment's end are unspecified.
+ * Size: ((T*k >> 7) + E + 1) * (K/128) * 512.  Host-only. */
+moe_status_t moe_mx_act_scales_size(const moe_config_t *cfg, int32_t K, size_t *bytes);
+
 /* Quantise W1 [E,2f,d] and W2 [E,d,f] (bf16) into the blob (device, 256-byte aligned,
  * moe_mx_weights_size bytes).  The caller keeps the blob while the weights are unchanged
  * (weight-quantisation caching). */
 moe_status_t moe_mx_quantize_weights(const moe_config_t *cfg, const void *W1, const void *W2,
                                      void *wq, void *stream);
 
-/* F3 with MXFP8 output: for p < offsets[E], xq[p] = E4M3 codes of x[src_tok[p]] and
- * x_sf[p] = its E8M0 scales ([T*k][d] and [T*k][d/32] bytes); with xp_or_null also the
- * bf16 copy xp[p] = x[src_tok[p]] (the backward's saved input). */
+/* F3 with MXFP8 output: for p < offsets[E], xq[p] = E4M3 codes of x[src_tok[p]] ([T*k][d]
+ * bytes) and its E8M0 scales into x_sf (activation atoms, moe_mx_act_scales_size(cfg, d)
+ * bytes); with xp_or_null also the bf16 copy xp[p] = x[src_tok[p]] (the backward's saved
+ * input). */
 moe_status_t moe_mx_permute_quant(const moe_config_t *cfg, const void *x,
                                   const int32_t *src_tok, const int32_t *offsets,
                                   void *xp_or_null, void *xq, uint8_t *x_sf, void *ws,
@@ -335,7 +344,8 @@ moe_status_t moe_mx_permute_quant(const moe_config_t *cfg, const void *x,
  *   [a|b] = bf16(deq(xq) deq(W1q[e])^T) -> ab;  h = bf16(silu(a) b) -> h;
  *   hq, h_sf = MX(h) along f (the SwiGLU epilogue quantises its bf16 output);
  *   yp = bf16(deq(hq) deq(W2q[e])^T).
- * Shapes as moe_grouped_ffn; hq [T*k][f], h_sf [T*k][f/32] bytes. */
+ * Shapes as moe_grouped_ffn; hq [T*k][f] bytes; x_sf and h_sf are activation atoms
+ * (moe_mx_act_scales_size with K = d and K = ffn). */
 moe_status_t moe_grouped_ffn_mx(const moe_config_t *cfg, const void *xq, const uint8_t *x_sf,
                                 const int32_t *offsets, const void *wq, void *ab, void *h,
                                 uint8_t *hq, uint8_t *h_sf, void *yp, void *ws, void *stream);

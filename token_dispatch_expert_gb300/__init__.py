@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "moe_mx_weights_size": ([cfgp, ctypes.POINTER(ctypes.c_size_t),
                                      ctypes.POINTER(ctypes.c_size_t)], I32),
             "moe_mx_quantize_weights": ([cfgp] + [P] * 4, I32),
+            "moe_mx_act_scales_size": ([cfgp, I32, ctypes.POINTER(ctypes.c_size_t)], I32),
             "moe_mx_permute_quant": ([cfgp] + [P] * 8, I32),
             "moe_grouped_ffn_mx": ([cfgp] + [P] * 11, I32),
             "moe_layer_fwd_mx": ([cfgp] + [P] * 9, I32),
@@ -221,6 +222,13 @@ def moe_mx_weights_size(cfg):
     offs = (ctypes.c_size_t * 4)()
     _check(lib().moe_mx_weights_size(_cfg(cfg), ctypes.byref(b), offs), "moe_mx_weights_size")
     return b.value, [o for o in offs]
+
+
+def moe_mx_act_scales_size(cfg, K) -> int:
+    b = ctypes.c_size_t(0)
+    _check(lib().moe_mx_act_scales_size(_cfg(cfg), int(K), ctypes.byref(b)),
+           "moe_mx_act_scales_size")
+    return b.value
 
 
 def moe_mx_quantize_weights(cfg, W1, W2, wq, stream=None):

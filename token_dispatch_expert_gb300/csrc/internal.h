@@ -115,6 +115,12 @@ struct MxWeightLayout {
 };
 MxWeightLayout mx_weight_layout(int E, int d, int f);
 
+// Bytes of an activation scale array (atoms tiled by 128 rows inside each expert
+// segment: block (offsets[e] >> 7) + e + l/128 for local row l, K/128 atoms per block).
+inline size_t mx_act_scale_bytes(int64_t rows_cap, int E, int K) {
+  return static_cast<size_t>((rows_cap >> 7) + E + 1) * static_cast<size_t>(K / 128) * 512;
+}
+
 cudaError_t launch_mx_quant_weights(const void* W1, const void* W2, int E, int d, int f,
                                     void* blob, cudaStream_t st);
 
@@ -128,12 +134,12 @@ struct MxFfnArgs {
   int64_t rows_cap;
   const int32_t* offsets;
   const void* xq;        // [rows_cap][d] E4M3
-  const uint8_t* x_sf;   // [rows_cap][d/32] E8M0
+  const uint8_t* x_sf;   // activation scale atoms (mx_act_scale_bytes(rows_cap, E, d))
   const void* wq;        // quantised-weight blob
   void* ab;              // [rows_cap][2f] bf16
   void* h;               // [rows_cap][f] bf16
   uint8_t* hq;           // [rows_cap][f] E4M3
-  uint8_t* h_sf;         // [rows_cap][f/32] E8M0
+  uint8_t* h_sf;         // activation scale atoms (mx_act_scale_bytes(rows_cap, E, f))
   void* yp;              // [rows_cap][d] bf16
   int* err;
 };

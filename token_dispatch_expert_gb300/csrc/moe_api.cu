@@ -116,9 +116,9 @@ WsLayout ws_layout(const moe_config_t* c) {
   // MXFP8 forward: the quantised activations and their scales
   const bool mx = c->mxfp8 != 0;
   L.xq = o;    o += align_up(mx ? R * d : 0);
-  L.x_sf = o;  o += align_up(mx ? R * d / 32 : 0);
+  L.x_sf = o;  o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, c->d) : 0);
   L.hq = o;    o += align_up(mx ? R * f : 0);
-  L.h_sf = o;  o += align_up(mx ? R * f / 32 : 0);
+  L.h_sf = o;  o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, c->ffn) : 0);
   L.total = o;
   return L;
 }
@@ -440,6 +440,14 @@ moe_status_t moe_mx_weights_size(const moe_config_t* cfg, size_t* bytes, size_t*
     offsets[2] = L.w2q;
     offsets[3] = L.w2sf;
   }
+  return MOE_OK;
+}
+
+moe_status_t moe_mx_act_scales_size(const moe_config_t* cfg, int32_t K, size_t* bytes) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (K <= 0 || K % 128 || !bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = mx_act_scale_bytes(cfg->T * cfg->k, cfg->E, K);
   return MOE_OK;
 }
 

@@ -19,9 +19,17 @@
 // from a 512-byte "atom" in shared memory: byte 16*(m%32) + 4*(m/32) + k holds the scale of
 // row m, sub-block k (the layout was measured with an in-bounds probe on GB300).
 //
-// The weights' scales are written once, already in atom order (the quantised weights are
-// cached by the caller); the activations' scales are row-major [rows][K/32] and the
-// producer warp rearranges each K block's 128 rows into an atom with plain loads.
+// Every scale is stored in atom order, so a stage's scales arrive by TMA like its
+// operands: the weights' when they are quantised (cached by the caller), the activations'
+// by the kernels that produce them -- tiled by 128 rows inside each expert segment (atom
+// block (offsets[e] >> 7) + e + l/128 for local row l), so a tile's rows always fill whole
+// atoms whatever the segment's start.
+//
+// Long segments run on CTA pairs (cta_group::2, M 256 x N 256): each CTA holds 128 rows of
+// A and 128 rows of B; the MMA reads each CTA's A scales from that CTA's TMEM and, for its
+// 128 output rows, the B scales of all 256 columns from the same CTA's TMEM, so both CTAs
+// load the whole B scale pair; tcgen05.cp.cta_group::2 issued by the leader copies each
+// CTA's own shared-memory atoms into its own TMEM (measured with a second probe).
 //
 // TMEM holds one 256-column accumulator and 4 stages x 12 scale columns.  There is no
 // room for a second accumulator, so eight epilogue warps (two per lane quarter, each
@@ -40,20 +48,14 @@ namespace moe {
 namespace {
 
 constexpr int MX_BK = 128;                 // E4M3 elements (bytes) per K block
-constexpr int MX_STAGES = 4;
-constexpr int MX_A_BYTES = 128 * MX_BK;    // 16 KB
-constexpr int MX_B_BYTES = 256 * MX_BK;    // 32 KB
-constexpr int MX_SFA_BYTES = 512;
-constexpr int MX_SFB_BYTES = 1024;
-constexpr int MX_STAGE_BYTES = 51200;      // A | B | SFA | SFB, rounded up to 1 KB
+constexpr int MX_SFA_BYTES = 512;          // one scale atom
+constexpr int MX_SFB_BYTES = 1024;         // a pair of atoms: 256 B rows
 constexpr int MX_THREADS = 320;            // producer, MMA, 8 epilogue warps
 constexpr int MX_EPI_WARPS = 8;
 constexpr uint32_t MX_TMEM_COLS = 512;
-constexpr uint32_t MX_SF_COL0 = 256;       // scale slots: 12 columns per stage
+constexpr uint32_t MX_SF_COL0 = 256;       // scale slots: 12 columns per stage (up to 6)
 constexpr int MX_MAX_G = 256;
 constexpr long long MX_WAIT_BUDGET = 4000000000LL;
-
-static_assert(MX_A_BYTES + MX_B_BYTES + MX_SFA_BYTES + MX_SFB_BYTES <= MX_STAGE_BYTES, "stage");
 
 // ------------------------------------------------------------------ quantisation helpers
 // X = floor(log2(amax)) - 8, clamped to [-127, 127]; -127 when amax is 0 (or subnormal,
@@ -96,10 +98,31 @@ __host__ __device__ __forceinline__ int atom_byte(int m, int k) {
   return 16 * (m & 31) + 4 * (m >> 5) + k;
 }
 
+// Byte of the scale of sub-block j (32 elements) of K block kb, for local row l of
+// expert e (segment start seg0), in an activation atom array with KB K blocks per row.
+__host__ __device__ __forceinline__ long long act_atom_byte(int seg0, int e, int l, int KB,
+                                                            int kb, int j) {
+  const long long blk = (seg0 >> 7) + e + (l >> 7);
+  return (blk * KB + kb) * 512 + atom_byte(l & 127, j);
+}
+
+// Expert of row p: the e with offsets[e] <= p < offsets[e+1] (binary search; empty
+// segments are skipped because their start equals the next one's).
+__device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ offsets, int E, int64_t p) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(offsets + mid) <= p) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // ------------------------------------------------------------------ F3 + quantisation
 // Warp per destination row p < offsets[E]: x[src_tok[p]] (bf16, d elements) is quantised
-// into xq[p] (E4M3) and x_sf[p] (E8M0 per 32 elements); with xp != null the bf16 row is
-// also copied (the backward's saved input).  Lane l takes blocks l, l+32, ...
+// into xq[p] (E4M3) and its scales (E8M0 per 32 elements, into the activation atoms); with
+// xp != null the bf16 row is also copied (the backward's saved input).  Lane l takes
+// blocks l, l+32, ...
 constexpr int QTHREADS = 256;
 
 __global__ void __launch_bounds__(QTHREADS)
@@ -123,6 +146,9 @@ mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
       continue;
     }
     const uint4* src = x + static_cast<int64_t>(t) * (d / 8);
+    const int e = expert_of_row(offsets, E, p);
+    const int seg0 = __ldg(offsets + e);
+    const int l = static_cast<int>(p - seg0);
     for (int b = lane; b < nb; b += 32) {
       uint4 raw[4];
       float v[32];
@@ -140,7 +166,7 @@ mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
       uint4* dq = xq + p * (d / 16) + 2 * b;
       dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
       dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
-      x_sf[p * nb + b] = static_cast<uint8_t>(s);
+      x_sf[act_atom_byte(seg0, e, l, d / 128, b >> 2, b & 3)] = static_cast<uint8_t>(s);
     }
   }
 }
@@ -188,9 +214,25 @@ mx_weight_quant_kernel(const uint4* __restrict__ W, int64_t n_rows, int rows_per
 }
 
 // ------------------------------------------------------------------ block-scaled GEMM
+// Per CTA and stage: A 128 rows x 128 B, B 128 rows (pair: this CTA's half of N) or 256
+// rows (one CTA) x 128 B, the A scale atom (512 B) and the B scale pair (1 KB).
+template <int PAIR>
+struct MxGeo {
+  static constexpr int B_ROWS = 256 / PAIR;
+  static constexpr int A_BYTES = 128 * MX_BK;
+  static constexpr int B_BYTES = B_ROWS * MX_BK;
+  static constexpr int SFA_OFF = A_BYTES + B_BYTES;
+  static constexpr int SFB_OFF = SFA_OFF + MX_SFA_BYTES;
+  static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + MX_SFA_BYTES + MX_SFB_BYTES;
+  static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+  static constexpr int TILE_M = 128 * PAIR;
+};
+static_assert(MX_SF_COL0 + 12 * 6 <= MX_TMEM_COLS, "scale slots");
+
 struct MxCtl {
-  uint64_t full[MX_STAGES];
-  uint64_t empty[MX_STAGES];
+  uint64_t full[6];
+  uint64_t empty[6];
   uint64_t tfull;
   uint64_t tempty;
   uint64_t drain;
@@ -202,7 +244,10 @@ struct MxCtl {
   int tprefix[MX_MAX_G + 2];
 };
 
-constexpr size_t MX_SMEM = 1024 + MX_STAGES * MX_STAGE_BYTES + sizeof(MxCtl);
+template <int PAIR>
+constexpr size_t mx_smem_bytes() {
+  return 1024 + MxGeo<PAIR>::STAGES * MxGeo<PAIR>::STAGE_BYTES + sizeof(MxCtl);
+}
 
 struct MxParams {
   int G;
@@ -211,15 +256,12 @@ struct MxParams {
   int num_n_tiles;
   int num_kb;
   int n_out;
-  int kb_sf;                  // bytes per row of the A scales (K / 32)
   int n_blocks_mn;            // B atom blocks per expert (W1: f/128, W2: ceil(d/256))
   const int32_t* offsets;
-  const uint8_t* a_sf;        // [rows_cap][K/32] E8M0, row-major
-  const uint8_t* b_atoms;     // weight scale atoms
   __nv_bfloat16* out0;        // FC1: ab  FC2: yp
   __nv_bfloat16* out1;        // FC1: h
   uint8_t* out_q;             // FC1: hq  [rows_cap][f] E4M3
-  uint8_t* out_sf;            // FC1: h_sf [rows_cap][f/32] E8M0
+  uint8_t* out_sf;            // FC1: h's scales, activation atoms with f/128 K blocks
   int* err;
 };
 
@@ -244,28 +286,35 @@ __device__ __forceinline__ uint32_t idesc_mx(int M, int N, int sf_id) {
          (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) |
          (static_cast<uint32_t>(sf_id) << 29);
 }
+template <int PAIR>
 __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
-      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-      : "memory");
+  if (PAIR == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
 }
+template <int PAIR>
 __device__ __forceinline__ void tc_cp_atom(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
+  if (PAIR == 2)
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool mx_warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
@@ -278,25 +327,35 @@ __device__ __forceinline__ float bf16r(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-template <int MODE>   // GEMM_FC1_SWIGLU or GEMM_FC2
+// tmA: the activation codes [rows, K] (box 128 x 128); tmB: the weight codes (box 128 x
+// 128); tmSA: the activation scale atoms viewed as [*, 256] bytes (box 256 x 2 = one atom);
+// tmSB: the weight scale atoms viewed as [*, 256] bytes (box 256 x 4 = one atom pair).
+template <int MODE, int PAIR>   // MODE: GEMM_FC1_SWIGLU or GEMM_FC2
 __global__ void __launch_bounds__(MX_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                const MxParams p) {
+  using GE = MxGeo<PAIR>;
+  constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  MxCtl* ctl = reinterpret_cast<MxCtl*>(smem + MX_STAGES * MX_STAGE_BYTES);
+  MxCtl* ctl = reinterpret_cast<MxCtl*>(smem + STAGES * GE::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   volatile int* abort_flag = &ctl->abort;
+  const int rank = PAIR == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit = blockIdx.x / PAIR;
+  const int num_units = gridDim.x / PAIR;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < MX_STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     mbar_init(smem_u32(&ctl->tfull), 1);
-    mbar_init(smem_u32(&ctl->tempty), MX_EPI_WARPS);
+    mbar_init(smem_u32(&ctl->tempty), MX_EPI_WARPS * PAIR);
     mbar_init(smem_u32(&ctl->drain), 1);
     fence_mbar_init();
     ctl->abort = 0;
@@ -305,6 +364,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmSA);
+    tma_prefetch_desc(&tmSB);
   }
   for (int g = threadIdx.x; g <= p.G; g += MX_THREADS) ctl->gstart[g] = p.offsets[g];
   __syncthreads();
@@ -316,7 +377,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (g < p.G) {
         const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
         if (b < a || a < 0 || b > p.rows_cap) bad = 1;
-        local += b < a ? 0 : mx_ceil_div(b - a, 128) * p.num_n_tiles;
+        local += b < a ? 0 : mx_ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
       }
     }
     const int incl = warp_incl_scan(local);
@@ -326,7 +387,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (g < p.G) {
         ctl->tprefix[g] = run;
         const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
-        run += b < a ? 0 : mx_ceil_div(b - a, 128) * p.num_n_tiles;
+        run += b < a ? 0 : mx_ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
       }
     }
     if (lane == 31) ctl->tprefix[p.G] = incl;
@@ -338,11 +399,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), MX_TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR == 2) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), MX_TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), MX_TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR == 2) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
   const int total = ctl->bad ? 0 : ctl->tprefix[p.G];
   const uint32_t tmem_base = ctl->tmem_base;
@@ -356,148 +423,155 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     g = lo;
     const int local = tile - ctl->tprefix[g];
-    const int mtg = mx_ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], 128);
+    const int mtg = mx_ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], GE::TILE_M);
     nt = local / mtg;
     mt = local - nt * mtg;
   };
 
   if (warp == 0) {
-    // -------------------------------------------------------------- producer (whole warp)
+    // -------------------------------------------------------------- producer (lane 0)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     const int nkb = p.num_kb;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = unit; tile < total && ok; tile += num_units) {
       int g, mt, nt;
       map_tile(tile, g, mt, nt);
       const int seg0 = ctl->gstart[g];
-      const int seg_last = ctl->gstart[g + 1] - 1;
-      const int row0 = seg0 + mt * 128;
-      // this lane's four A rows of the tile (rows past the segment read its last row;
-      // their outputs are never stored)
-      const uint8_t* sf_row[4];
-#pragma unroll
-      for (int m1 = 0; m1 < 4; ++m1)
-        sf_row[m1] = p.a_sf + static_cast<long long>(min(row0 + lane + 32 * m1, seg_last)) * p.kb_sf;
-      uint32_t nxt[4];
-#pragma unroll
-      for (int m1 = 0; m1 < 4; ++m1) nxt[m1] = __ldg(reinterpret_cast<const uint32_t*>(sf_row[m1]));
-      const uint8_t* b_atom =
-          p.b_atoms + (static_cast<long long>(g) * p.n_blocks_mn + nt) * nkb * 1024;
+      const int lrow = mt * GE::TILE_M + 128 * rank;            // this CTA's first local row
+      const int row0 = seg0 + lrow;
+      const int a_atom_blk = (seg0 >> 7) + g + (lrow >> 7);     // its activation atom block
+      const int b_atom = (g * p.n_blocks_mn + nt) * nkb;        // weight atom pair index
       for (int kb = 0; kb < nkb; ++kb) {
-        uint32_t cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
-        if (kb + 1 < nkb) {
-#pragma unroll
-          for (int m1 = 0; m1 < 4; ++m1)
-            nxt[m1] = __ldg(reinterpret_cast<const uint32_t*>(sf_row[m1] + 4 * (kb + 1)));
-        }
         if (!mx_warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, MX_WAIT_BUDGET)) {
           ok = false;
           break;
         }
-        const uint32_t sa = smem_base + s * MX_STAGE_BYTES;
-        const uint32_t sb = sa + MX_A_BYTES;
-        const uint32_t ssfa = sb + MX_B_BYTES;
-        const uint32_t ssfb = ssfa + MX_SFA_BYTES;
-        // the A scales of this K block: lane m0 writes bytes 16*m0 .. 16*m0+15 of the atom
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ssfa + 16 * lane),
-                     "r"(cur[0]), "r"(cur[1]), "r"(cur[2]), "r"(cur[3])
-                     : "memory");
-        fence_proxy_async_smem();
-        __syncwarp();
         if (lane == 0) {
-          const uint32_t full = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(full, MX_A_BYTES + MX_B_BYTES + MX_SFB_BYTES);
+          const uint32_t sa = smem_base + s * GE::STAGE_BYTES;
+          const uint32_t sb = sa + GE::A_BYTES;
+          const uint32_t full_local = smem_u32(&ctl->full[s]);
+          const uint32_t full = PAIR == 2 ? mapa_shared(full_local, 0) : full_local;
+          // the leader's single arrive announces both CTAs' bytes
+          if (leader) mbar_arrive_expect_tx(full_local, PAIR * GE::LOAD_BYTES);
+          auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+            if (PAIR == 2) tma_load_2d_pair(dst, m, full, x, y);
+            else tma_load_2d(dst, m, full, x, y);
+          };
           const int k0 = kb * MX_BK;
-          tma_load_2d(sa, &tmA, full, k0, row0);
+          load(sa, &tmA, k0, row0);
           if (MODE == GEMM_FC1_SWIGLU) {
             const int wrow = g * 2 * p.f + nt * 128;
-            tma_load_2d(sb, &tmB, full, k0, wrow);                          // gate rows
-            tma_load_2d(sb + MX_B_BYTES / 2, &tmB, full, k0, wrow + p.f);   // up rows
+            if (PAIR == 2) {
+              load(sb, &tmB, k0, wrow + rank * p.f);                // CTA 0 gate, CTA 1 up
+            } else {
+              load(sb, &tmB, k0, wrow);
+              load(sb + 128 * MX_BK, &tmB, k0, wrow + p.f);
+            }
           } else {
             const int wrow = g * p.d + nt * 256;
-            tma_load_2d(sb, &tmB, full, k0, wrow);
-            tma_load_2d(sb + MX_B_BYTES / 2, &tmB, full, k0, wrow + 128);
+            if (PAIR == 2) {
+              load(sb, &tmB, k0, wrow + rank * 128);
+            } else {
+              load(sb, &tmB, k0, wrow);
+              load(sb + 128 * MX_BK, &tmB, k0, wrow + 128);
+            }
           }
-          bulk_load(ssfb, b_atom + kb * 1024, MX_SFB_BYTES, full);
+          load(sa + GE::SFA_OFF, &tmSA, 0, (a_atom_blk * nkb + kb) * 2);
+          load(sa + GE::SFB_OFF, &tmSB, 0, (b_atom + kb) * 4);
         }
-        if (++s == MX_STAGES) {
+        __syncwarp();
+        if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
       }
     }
-    for (int i = 0; i < MX_STAGES && ok; ++i) {
+    for (int i = 0; i < STAGES && ok; ++i) {
       if (!mx_warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, MX_WAIT_BUDGET / 4))
         break;
-      if (++s == MX_STAGES) {
+      if (++s == STAGES) {
         s = 0;
         ph ^= 1u;
       }
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
-    int s = 0;
-    uint32_t ph = 0;
-    int it = 0;
-    bool ok = true, issued_any = false;
-    const int nkb = p.num_kb;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-      if (!mx_warp_wait(smem_u32(&ctl->tempty), (it & 1) ^ 1u, abort_flag, p.err,
-                        MX_WAIT_BUDGET)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!mx_warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, MX_WAIT_BUDGET)) {
+    // -------------------------------------------------------------- MMA issuer (leader)
+    if (leader) {
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true, issued_any = false;
+      const int nkb = p.num_kb;
+      for (int tile = unit; tile < total && ok; tile += num_units, ++it) {
+        if (!mx_warp_wait(smem_u32(&ctl->tempty), (it & 1) ^ 1u, abort_flag, p.err,
+                          MX_WAIT_BUDGET)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_base + s * MX_STAGE_BYTES;
-        const uint32_t sb = sa + MX_A_BYTES;
-        const uint32_t ssfa = sb + MX_B_BYTES;
-        const uint32_t ssfb = ssfa + MX_SFA_BYTES;
-        const uint32_t sf_col = tmem_base + MX_SF_COL0 + 12u * static_cast<uint32_t>(s);
-        if (lane == 0) {
-          tc_cp_atom(sf_col, sdesc_atom(ssfa));             // A: 128 rows x 4 sub-blocks
-          tc_cp_atom(sf_col + 4, sdesc_atom(ssfb));         // B: columns 0..127
-          tc_cp_atom(sf_col + 8, sdesc_atom(ssfb + 512));   // B: columns 128..255
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mx_warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, MX_WAIT_BUDGET)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * GE::STAGE_BYTES;
+          const uint32_t sb = sa + GE::A_BYTES;
+          // one scale slot per stage: a slot is rewritten only after the MMAs that read it
+          // have completed (the producer refilled that stage after their commit)
+          const uint32_t sf_col = tmem_base + MX_SF_COL0 + 12u * static_cast<uint32_t>(s);
+          if (lane == 0) {
+            // each CTA's own atoms into its own TMEM: A scales (its 128 rows) and the B
+            // scales of all 256 columns
+            tc_cp_atom<PAIR>(sf_col, sdesc_atom(sa + GE::SFA_OFF));
+            tc_cp_atom<PAIR>(sf_col + 4, sdesc_atom(sa + GE::SFB_OFF));
+            tc_cp_atom<PAIR>(sf_col + 8, sdesc_atom(sa + GE::SFB_OFF + 512));
 #pragma unroll
-          for (int kk = 0; kk < MX_BK / 32; ++kk)
-            tc_mma_mx(tmem_base, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32),
-                      idesc_mx(128, 256, kk), sf_col, sf_col + 4, (kb | kk) != 0 ? 1u : 0u);
-          tc_commit(smem_u32(&ctl->empty[s]));
+            for (int kk = 0; kk < MX_BK / 32; ++kk)
+              tc_mma_mx<PAIR>(tmem_base, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32),
+                              idesc_mx(GE::TILE_M, 256, kk), sf_col, sf_col + 4,
+                              (kb | kk) != 0 ? 1u : 0u);
+            if (PAIR == 2) tc_commit_pair_mc(smem_u32(&ctl->empty[s]), 0x3);
+            else tc_commit(smem_u32(&ctl->empty[s]));
+          }
+          issued_any = true;
+          __syncwarp();
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        issued_any = true;
+        if (!ok) break;
+        if (lane == 0) {
+          if (PAIR == 2) tc_commit_pair_mc(smem_u32(&ctl->tfull), 0x3);
+          else tc_commit(smem_u32(&ctl->tfull));
+        }
         __syncwarp();
-        if (++s == MX_STAGES) {
-          s = 0;
-          ph ^= 1u;
+      }
+      if (!ok && issued_any && lane == 0) {
+        if (PAIR == 2) tc_commit_pair(smem_u32(&ctl->drain));
+        else tc_commit(smem_u32(&ctl->drain));
+        long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < MX_WAIT_BUDGET / 4) {
         }
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(smem_u32(&ctl->tfull));
       __syncwarp();
     }
-    if (!ok && issued_any && lane == 0) {
-      tc_commit(smem_u32(&ctl->drain));
-      long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < MX_WAIT_BUDGET / 4) {
-      }
-    }
-    __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue (8 warps)
     const int q = warp & 3;                  // the lane quarter this warp may access
     const int hh = (warp - 2) >> 2;          // which half of the columns
-    const int r_in_tile = q * 32 + lane;
+    const int r_in_tile = rank * 128 + q * 32 + lane;
+    const uint32_t tempty_leader =
+        PAIR == 2 ? mapa_shared(smem_u32(&ctl->tempty), 0) : smem_u32(&ctl->tempty);
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = unit; tile < total; tile += num_units, ++it) {
       int g, mt, nt;
       map_tile(tile, g, mt, nt);
-      const long long prow = static_cast<long long>(ctl->gstart[g]) + mt * 128 + r_in_tile;
+      const int seg0 = ctl->gstart[g];
+      const int lrow = mt * GE::TILE_M + r_in_tile;
+      const long long prow = static_cast<long long>(seg0) + lrow;
       const bool valid = prow < ctl->gstart[g + 1];
       if (!mx_warp_wait(smem_u32(&ctl->tfull), it & 1, abort_flag, p.err, MX_WAIT_BUDGET)) break;
       tc_fence_after();
@@ -518,7 +592,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty));   // the accumulator is free
+      if (lane == 0) {   // the accumulator is free (the leader counts both CTAs' warps)
+        if (PAIR == 2) mbar_arrive_remote(tempty_leader);
+        else mbar_arrive(tempty_leader);
+      }
       if (!valid) continue;
       if (MODE == GEMM_FC1_SWIGLU) {
         const int f = p.f;
@@ -548,7 +625,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint4* dq = reinterpret_cast<uint4*>(p.out_q + prow * f + n0 + 32 * blk);
           dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
           dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
-          p.out_sf[prow * (f / 32) + n0 / 32 + blk] = static_cast<uint8_t>(sc);
+          const int sub = n0 / 32 + blk;        // 32-element block of h's row
+          p.out_sf[act_atom_byte(seg0, g, lrow, f / 128, sub >> 2, sub & 3)] =
+              static_cast<uint8_t>(sc);
         }
       } else {
         const int n0 = nt * 256 + 128 * hh;
@@ -566,9 +645,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR == 2) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, MX_TMEM_COLS);
+  if (warp == 1) {
+    if (PAIR == 2) tmem_dealloc_pair(tmem_base, MX_TMEM_COLS);
+    else tmem_dealloc(tmem_base, MX_TMEM_COLS);
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -586,17 +669,19 @@ PFN_cuTensorMapEncodeTiled_v12000 mx_encode_fn() {
   return fn;
 }
 
-// 2-D byte tensor map over a row-major [rows, cols] E4M3 matrix, 128-byte swizzle, box =
-// 128 columns (bytes) x 128 rows, zero fill out of bounds.
-bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// 2-D byte tensor map over a row-major [rows, cols] matrix: swizzled E4M3 tiles (box 128 x
+// 128, 128-byte swizzle) or plain scale atoms (box 256 x box_rows, no swizzle).
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                 uint32_t box_cols, uint32_t box_rows, bool swizzle) {
   auto enc = mx_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
@@ -610,18 +695,38 @@ int grid_rows(int64_t rows) {
   return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
-template <int MODE>
-cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const MxParams& kp,
-                           cudaStream_t st) {
-  auto kern = mx_gemm_kernel<MODE>;
+template <int MODE, int PAIR>
+cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                           const CUtensorMap& tsb, const MxParams& kp, cudaStream_t st) {
+  auto kern = mx_gemm_kernel<MODE, PAIR>;
+  constexpr size_t SMEM = mx_smem_bytes<PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(MX_SMEM));
+                                       static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  kern<<<sms, MX_THREADS, MX_SMEM, st>>>(ta, tb, kp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(MX_THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = st;
+  if (PAIR == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+      clusters = sms / 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  } else {
+    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+  }
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, kp);
 }
 
 }  // namespace
@@ -676,6 +781,8 @@ cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
   const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
   const uint64_t E = static_cast<uint64_t>(a.E), d = static_cast<uint64_t>(a.d),
                  f = static_cast<uint64_t>(a.f);
+  // long segments on CTA pairs, as in the bf16 GEMMs
+  const bool pair = static_cast<double>(a.rows_cap) / a.E >= 192.0;
   MxParams kp{};
   kp.G = a.E;
   kp.rows_cap = a.rows_cap;
@@ -683,38 +790,49 @@ cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
   kp.f = a.f;
   kp.offsets = a.offsets;
   kp.err = a.err;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tsa, tsb;
+  auto launch = [&](int mode) {
+    if (mode == GEMM_FC1_SWIGLU)
+      return pair ? launch_mx_mode<GEMM_FC1_SWIGLU, 2>(ta, tb, tsa, tsb, kp, st)
+                  : launch_mx_mode<GEMM_FC1_SWIGLU, 1>(ta, tb, tsa, tsb, kp, st);
+    return pair ? launch_mx_mode<GEMM_FC2, 2>(ta, tb, tsa, tsb, kp, st)
+                : launch_mx_mode<GEMM_FC2, 1>(ta, tb, tsa, tsb, kp, st);
+  };
   // FC1: [a|b] = xq W1q^T (K = d), SwiGLU, h quantised
+  const uint64_t KB1 = d / 128, NB1 = f / 128;
   kp.num_n_tiles = a.f / 128;
   kp.num_kb = a.d / MX_BK;
   kp.n_out = a.f;
-  kp.kb_sf = a.d / 32;
   kp.n_blocks_mn = a.f / 128;
-  kp.a_sf = a.x_sf;
-  kp.b_atoms = wb + L.w1sf;
   kp.out0 = static_cast<__nv_bfloat16*>(a.ab);
   kp.out1 = static_cast<__nv_bfloat16*>(a.h);
   kp.out_q = a.hq;
   kp.out_sf = a.h_sf;
-  if (!make_map_u8(&ta, a.xq, d, rows) || !make_map_u8(&tb, wb + L.w1q, d, E * 2 * f))
+  if (!make_map_u8(&ta, a.xq, d, rows, 128, 128, true) ||
+      !make_map_u8(&tb, wb + L.w1q, d, E * 2 * f, 128, 128, true) ||
+      !make_map_u8(&tsa, a.x_sf, 256, mx_act_scale_bytes(a.rows_cap, a.E, a.d) / 256, 256, 2,
+                   false) ||
+      !make_map_u8(&tsb, wb + L.w1sf, 256, E * NB1 * KB1 * 4, 256, 4, false))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_mx_mode<GEMM_FC1_SWIGLU>(ta, tb, kp, st);
+  cudaError_t e = launch(GEMM_FC1_SWIGLU);
   if (e != cudaSuccess) return e;
   // FC2: yp = hq W2q^T (K = f)
-  kp.num_n_tiles = (a.d + 255) / 256;
+  const uint64_t KB2 = f / 128, NT2 = (d + 255) / 256;
+  kp.num_n_tiles = static_cast<int>(NT2);
   kp.num_kb = a.f / MX_BK;
   kp.n_out = a.d;
-  kp.kb_sf = a.f / 32;
-  kp.n_blocks_mn = (a.d + 255) / 256;
-  kp.a_sf = a.h_sf;
-  kp.b_atoms = wb + L.w2sf;
+  kp.n_blocks_mn = static_cast<int>(NT2);
   kp.out0 = static_cast<__nv_bfloat16*>(a.yp);
   kp.out1 = nullptr;
   kp.out_q = nullptr;
   kp.out_sf = nullptr;
-  if (!make_map_u8(&ta, a.hq, f, rows) || !make_map_u8(&tb, wb + L.w2q, f, E * d))
+  if (!make_map_u8(&ta, a.hq, f, rows, 128, 128, true) ||
+      !make_map_u8(&tb, wb + L.w2q, f, E * d, 128, 128, true) ||
+      !make_map_u8(&tsa, a.h_sf, 256, mx_act_scale_bytes(a.rows_cap, a.E, a.f) / 256, 256, 2,
+                   false) ||
+      !make_map_u8(&tsb, wb + L.w2sf, 256, E * NT2 * KB2 * 4, 256, 4, false))
     return cudaErrorInvalidValue;
-  return launch_mx_mode<GEMM_FC2>(ta, tb, kp, st);
+  return launch(GEMM_FC2);
 }
 
 }  // namespace moe
