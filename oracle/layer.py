@@ -349,7 +349,8 @@ class TorchSource:
         return self._np(self.inp[name])
 
 
-def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True) -> dict:
+def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True,
+                  mx: bool = False) -> dict:
     """The exact layer restricted to a subset of outputs (for configurations too big
     to evaluate in full on the host):
 
@@ -360,7 +361,10 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
       dW1s, dW2s entries     likewise for the shared expert, if any.
 
     Every value is computed from the inputs alone through the same steps as the full
-    layer; only the rows/columns that the requested outputs depend on are evaluated."""
+    layer; only the rows/columns that the requested outputs depend on are evaluated.
+    mx: the routed experts' forward on MXFP8 operands (as layer_fwd(mx=True)); the
+    restriction stays exact because every MX block lies inside one token row or one
+    weight row."""
     r = route(cfg, src.logits)
     k, d, f = cfg.k, cfg.d, cfg.f
     toks = np.unique(np.asarray(tokens, np.int64))
@@ -382,7 +386,10 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     for e in np.unique(eid):           # each expert's weights are fetched once
         sel = np.nonzero(eid == e)[0]
         W1e, W2e = src.expert("W1", int(e)), src.expert("W2", int(e))
-        ab, _, yp[sel] = ffn_fwd_rows(xp[sel], W1e, W2e, rnd)
+        if mx:
+            ab, _, yp[sel], _, _ = ffn_fwd_rows_mx(xp[sel], W1e, W2e)
+        else:
+            ab, _, yp[sel] = ffn_fwd_rows(xp[sel], W1e, W2e, rnd)
         _, dxp[sel] = ffn_bwd_rows(dyp[sel], ab, W1e, W2e, rnd)
         del W1e, W2e
     out = {"route": r, "tokens": toks}
@@ -415,7 +422,7 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
             dyp_e = src.rows("dy", tk) * w[:, None]
             if rnd:
                 dyp_e = bf16(dyp_e)
-            g1, g2 = _wgrad_cols(xr, dyp_e, W1e, W2e, wcols, wrows, rnd)
+            g1, g2 = _wgrad_cols(xr, dyp_e, W1e, W2e, wcols, wrows, rnd, mx=mx)
             dW1[e] = g1; dW2[e] = g2
         out["dW1"] = dW1; out["dW2"] = dW2
         out["wcols"] = wcols; out["wrows"] = wrows
@@ -426,14 +433,21 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     return out
 
 
-def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd):
+def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False):
     """dW2[drows][:, cols] and dW1[[cols, f+cols]][:, drows] of one expert from all its rows,
     evaluating only the FFN columns `cols` (exact: a, b, h, dh, da, db of column c depend
-    on column c alone).  Uses the oracle's row steps on the column-restricted weights."""
+    on column c alone).  Uses the oracle's row steps on the column-restricted weights.
+    mx: a and b from MXFP8 operands (x rows and W1 rows are whole MX rows), h from them."""
     f = W1e.shape[0] // 2
     W1c = np.concatenate([W1e[cols], W1e[f + cols]])       # [2m, d]  (gate cols, up cols)
     W2c = np.ascontiguousarray(W2e[:, cols])                # [d, m]
-    ab, h, _ = ffn_fwd_rows(xr, W1c, W2c, rnd)              # ab = [a_cols | b_cols]
+    if mx:
+        m = len(cols)
+        ab = bf16(mx_quantize_rows(xr)[2] @ mx_quantize_rows(W1c)[2].T)
+        a, b = ab[:, :m], ab[:, m:]
+        h = bf16(a / (1.0 + np.exp(-a)) * b)
+    else:
+        ab, h, _ = ffn_fwd_rows(xr, W1c, W2c, rnd)          # ab = [a_cols | b_cols]
     dab, _ = ffn_bwd_rows(dyp, ab, W1c, W2c, rnd)           # [da_cols | db_cols]
     m = len(cols)
     dW2 = (dyp[:, drows].T @ h)                              # [len(drows), m]

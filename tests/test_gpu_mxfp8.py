@@ -214,3 +214,38 @@ def test_layer_fwd_mx_then_bf16_backward(name):
     y16 = tde.MoELayer(cfg_c(c)).forward(g["logits"], g["x"], g["W1"], g["W2"])
     diff = np.linalg.norm(f64(y) - f64(y16)) / np.linalg.norm(f64(y16))
     assert 1e-4 < diff < 0.1, diff
+
+
+@pytest.mark.parametrize("name", ["mixtral", "qwen3", "dsv3", "capacity"])
+def test_layer_mx_full_size_sampled(name):
+    """The benchmark's MXFP8 configuration at full size (CTA pairs where the benchmark takes
+    them): routing bit-exact in full; y, dx and dlogits of sampled tokens and sampled
+    weight-gradient entries against the oracle's exact restriction."""
+    from workloads import CONFIGS, gen_inputs_device
+    c = CONFIGS[name]
+    g = gen_inputs_device(c, "cuda")
+    cfg = mx_cfg(c)
+    layer = tde.MoELayer(cfg)
+    wq = layer.quantize_weights(g["W1"], g["W2"])
+    y = layer.forward_mx(g["logits"], g["x"], wq, g.get("W1s"), g.get("W2s"))
+    gr = layer.backward(g["logits"], g["x"], g["dy"], g["W1"], g["W2"], g.get("W1s"),
+                        g.get("W2s"))
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    src = oracle.TorchSource(g)
+    rng = np.random.default_rng(1)
+    toks = rng.choice(c.T, size=16, replace=False)
+    kept = oracle.route(c, src.logits)["kept"]
+    experts = [int(np.argmax(kept))]
+    wcols = np.sort(rng.choice(c.f, size=4, replace=False))
+    wrows = np.sort(rng.choice(c.d, size=8, replace=False))
+    s = oracle.layer_sampled(c, src, toks, experts, wcols, wrows, mx=True)
+    tk = torch.as_tensor(s["tokens"]).cuda()
+    assert_close("y", f64(y[tk]), s["y"])
+    assert_close("dx", f64(gr["dx"][tk]), s["dx"])
+    assert_close("dlogits", f64(gr["dlogits"][tk]), s["dlogits"])
+    for e in experts:
+        wc = torch.as_tensor(wcols).cuda(); wr = torch.as_tensor(wrows).cuda()
+        assert_close(f"dW1 gate[{e}]", f64(gr["dW1"][e][wc][:, wr]), s["dW1"][e][0])
+        assert_close(f"dW1 up[{e}]", f64(gr["dW1"][e][wc + c.f][:, wr]), s["dW1"][e][1])
+        assert_close(f"dW2[{e}]", f64(gr["dW2"][e][wr][:, wc]), s["dW2"][e])

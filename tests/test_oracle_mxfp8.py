@@ -135,3 +135,32 @@ def test_mx_ffn_matches_torch_composition():
     np.testing.assert_array_equal(hc, hq[0])
     np.testing.assert_array_equal(hs, hq[1])
     np.testing.assert_allclose(yp, y_t.numpy(), rtol=2 ** -8, atol=1e-12)
+
+
+def test_sampled_mx_layer_matches_full_mx_layer():
+    """layer_sampled(mx=True) is an exact restriction of layer_fwd(mx=True) + layer_bwd."""
+    from workloads import MoEConfig, gen_inputs_host
+    cfg = MoEConfig("mx_sample", T=96, d=128, E=4, k=2, f=128, cap_factor=0.8, zipf_s=1.1)
+    inp = gen_inputs_host(cfg)
+    f = oracle.layer_fwd(cfg, inp, mx=True)
+    b = oracle.layer_bwd(cfg, inp, f)
+    toks = [0, 5, 17, 95, 42]
+    experts = [0, 3]
+    wcols = np.array([0, 7, 63, 100])
+    wrows = np.array([1, 2, 63, 127])
+    s = oracle.layer_sampled(cfg, oracle.HostSource(inp), toks, experts, wcols, wrows, mx=True)
+    tk = np.array(sorted(toks))
+    np.testing.assert_array_equal(s["y"], f["y"][tk])
+    np.testing.assert_array_equal(s["dx"], b["dx"][tk])
+    np.testing.assert_allclose(s["dlogits"], b["dlogits"][tk], rtol=1e-12, atol=1e-14)
+    one_ulp = 2.0 ** -7      # rows summed in another order before the final rounding
+    for e in experts:
+        np.testing.assert_allclose(s["dW1"][e][0], b["dW1"][e][np.ix_(wcols, wrows)],
+                                   rtol=one_ulp, atol=1e-30)
+        np.testing.assert_allclose(s["dW1"][e][1], b["dW1"][e][np.ix_(wcols + cfg.f, wrows)],
+                                   rtol=one_ulp, atol=1e-30)
+        np.testing.assert_allclose(s["dW2"][e], b["dW2"][e][np.ix_(wrows, wcols)],
+                                   rtol=one_ulp, atol=1e-30)
+    # and it differs from the bf16 layer (the quantisation is really applied)
+    f16 = oracle.layer_fwd(cfg, inp)
+    assert (f16["y"] != f["y"]).any()
