@@ -26,6 +26,7 @@ from .layer import (  # noqa: F401
     e4m3_code,
     mx_quantize_rows,
     ffn_fwd_rows_mx,
+    ffn_bwd_rows_mx,
     HostSource,
     TorchSource,
 )

@@ -61,6 +61,7 @@ def _load():
         lib.orc_e4m3_code.restype = ctypes.c_uint8
         lib.orc_mx_quantize_rows.argtypes = [i64, i32, P, P, P, P]
         lib.orc_ffn_fwd_rows_mx.argtypes = [i64, i32, i32, P, P, P, P, P, P, P, P]
+        lib.orc_ffn_bwd_rows_mx.argtypes = [i64, i32, i32, P, P, P, P, P, P, P, P]
         lib.orc_ffn_bwd_rows.argtypes = [i64, i32, i32, P, P, P, P, i32, P, P]
         lib.orc_ffn_wgrad_rows.argtypes = [i64, i32, i32, P, P, P, P, P, P]
         lib.orc_combine.argtypes = [i64, P, i32, i32, P, P, P, P, P, i32, P]
@@ -173,6 +174,20 @@ def ffn_fwd_rows_mx(xr, W1e, W2e):
     return ab, h, yp, hc, hs
 
 
+def ffn_bwd_rows_mx(dyp, ab, W1e, W2e):
+    """The expert FFN's data gradients on MXFP8 operands: (dab, dxp, dab codes, dab scales)."""
+    lib = _load()
+    dyp, ab, W1e, W2e = _f64(dyp), _f64(ab), _f64(W1e), _f64(W2e)
+    n, d = dyp.shape
+    f = W1e.shape[0] // 2
+    dab = np.empty((n, 2 * f)); dxr = np.empty((n, d))
+    dc = np.empty((n, 2 * f), np.uint8); ds = np.empty((n, 2 * f // 32), np.uint8)
+    if n:
+        lib.orc_ffn_bwd_rows_mx(n, d, f, _p(dyp), _p(ab), _p(W1e), _p(W2e), _p(dab), _p(dxr),
+                                _p(dc), _p(ds))
+    return dab, dxr, dc, ds
+
+
 def ffn_bwd_rows(dyp, ab, W1e, W2e, rnd=True):
     lib = _load()
     dyp, ab, W1e, W2e = _f64(dyp), _f64(ab), _f64(W1e), _f64(W2e)
@@ -274,8 +289,10 @@ def layer_fwd(cfg, inp: dict, rnd: bool = True, r: dict | None = None, mx: bool 
     return out
 
 
-def layer_bwd(cfg, inp: dict, fwd: dict, rnd: bool = True) -> dict:
-    """Whole backward on the host given the forward's saved tensors and inp['dy']."""
+def layer_bwd(cfg, inp: dict, fwd: dict, rnd: bool = True, mx: bool = False) -> dict:
+    """Whole backward on the host given the forward's saved tensors and inp['dy'].
+    mx: the routed experts' data-gradient GEMMs on MXFP8 operands (ffn_bwd_rows_mx); the
+    weight gradients and the shared expert stay bf16."""
     r = fwd["route"]
     off = r["offsets"]
     x = _f64(inp["x"]); dy = _f64(inp["dy"])
@@ -286,7 +303,10 @@ def layer_bwd(cfg, inp: dict, fwd: dict, rnd: bool = True) -> dict:
     dW1 = np.zeros((cfg.E, 2 * cfg.f, cfg.d)); dW2 = np.zeros((cfg.E, cfg.d, cfg.f))
     for e in range(cfg.E):
         s, t = int(off[e]), int(off[e + 1])
-        dab[s:t], dxp[s:t] = ffn_bwd_rows(dyp[s:t], fwd["ab"][s:t], W1[e], W2[e], rnd)
+        if mx:
+            dab[s:t], dxp[s:t], _, _ = ffn_bwd_rows_mx(dyp[s:t], fwd["ab"][s:t], W1[e], W2[e])
+        else:
+            dab[s:t], dxp[s:t] = ffn_bwd_rows(dyp[s:t], fwd["ab"][s:t], W1[e], W2[e], rnd)
         dW1[e], dW2[e] = ffn_wgrad_rows(fwd["xp"][s:t], fwd["h"][s:t], dyp[s:t], dab[s:t],
                                         cfg.d, cfg.f)
     out = dict(dyp=dyp, dlogits=dlogits, dab=dab, dxp=dxp)

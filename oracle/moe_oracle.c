@@ -30,7 +30,9 @@
  *   mxfp8       MX block quantisation (OCP Microscaling formats v1.0: one E8M0 power-of-two
  *               scale per block of 32 consecutive elements along the contraction axis,
  *               elements in FP8 E4M3) and the expert FFN forward on quantised operands,
- *               with h quantised from its stored bf16 value.  Primus MoE blog, FP8
+ *               with h quantised from its stored bf16 value, and the data-gradient
+ *               GEMMs of the backward on MXFP8 operands (each quantised along its own
+ *               contraction axis; the weight gradients stay bf16).  Primus MoE blog, FP8
  *               section (MXFP8 recipe, OCP E4M3 expert GEMMs) and MegaMoE section (the
  *               SwiGLU step quantises its own output).
  *   backward    dispatch(dy) -> FC2 data-grad, FC1 data-grad -> combine/reduce,
@@ -650,4 +652,65 @@ void orc_ffn_fwd_rows_mx(int64_t n, int d, int f, const double *xr, const double
     free(w1q);
     free(w2q);
     free(hq);
+}
+
+/*
+ * The expert FFN's data gradients with MXFP8 GEMM operands (the weight gradients stay
+ * bf16), n rows of one expert.  Each GEMM quantises along its own contraction axis:
+ *   dyq  = MX(dyp) along d;      W2t = MX(W2e^T) along d   (W2e^T is [f][d])
+ *   dh   = dyq W2t^T (double);   [da | db] = bf16 of the SwiGLU backward from ab -> dab
+ *   dabq = MX(dab) along 2f (from the stored bf16 dab);  W1t = MX(W1e^T) along 2f ([d][2f])
+ *   dxr  = bf16(dabq W1t^T)
+ * dab_codes [n,2f] / dab_scales [n,2f/32] receive dab's quantisation.
+ */
+void orc_ffn_bwd_rows_mx(int64_t n, int d, int f, const double *dyp, const double *ab,
+                         const double *W1e, const double *W2e, double *dab, double *dxr,
+                         uint8_t *dab_codes, uint8_t *dab_scales)
+{
+    double *dyq = (double *)malloc(sizeof(double) * (size_t)(n * d + 1));
+    double *w2t = (double *)malloc(sizeof(double) * (size_t)((int64_t)f * d));
+    double *w1t = (double *)malloc(sizeof(double) * (size_t)((int64_t)d * 2 * f));
+    double *dabq = (double *)malloc(sizeof(double) * (size_t)(n * 2 * f + 1));
+    /* transposes, then quantise their rows */
+    for (int i = 0; i < d; ++i)
+        for (int c = 0; c < f; ++c)
+            w2t[(int64_t)c * d + i] = W2e[(int64_t)i * f + c];
+    for (int c = 0; c < 2 * f; ++c)
+        for (int i = 0; i < d; ++i)
+            w1t[(int64_t)i * 2 * f + c] = W1e[(int64_t)c * d + i];
+    orc_mx_quantize_rows(f, d, w2t, NULL, NULL, w2t);
+    orc_mx_quantize_rows(d, 2 * f, w1t, NULL, NULL, w1t);
+    orc_mx_quantize_rows(n, d, dyp, NULL, NULL, dyq);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const double *g = dyq + r * d;
+        const double *abr = ab + r * 2 * f;
+        double *dr = dab + r * 2 * f;
+        for (int c = 0; c < f; ++c) {
+            const double *w = w2t + (int64_t)c * d;
+            double dh = 0.0;
+            for (int i = 0; i < d; ++i)
+                dh += g[i] * w[i];
+            double a = abr[c], b = abr[f + c];
+            double sg = 1.0 / (1.0 + exp(-a));
+            dr[c] = orc_bf16(dh * b * (sg * (1.0 + a * (1.0 - sg))));
+            dr[f + c] = orc_bf16(dh * (a * sg));
+        }
+    }
+    orc_mx_quantize_rows(n, 2 * f, dab, dab_codes, dab_scales, dabq);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const double *q = dabq + r * 2 * f;
+        for (int i = 0; i < d; ++i) {
+            const double *w = w1t + (int64_t)i * 2 * f;
+            double s2 = 0.0;
+            for (int c = 0; c < 2 * f; ++c)
+                s2 += q[c] * w[c];
+            dxr[r * d + i] = orc_bf16(s2);
+        }
+    }
+    free(dyq);
+    free(w2t);
+    free(w1t);
+    free(dabq);
 }

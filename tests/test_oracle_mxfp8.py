@@ -164,3 +164,52 @@ def test_sampled_mx_layer_matches_full_mx_layer():
     # and it differs from the bf16 layer (the quantisation is really applied)
     f16 = oracle.layer_fwd(cfg, inp)
     assert (f16["y"] != f["y"]).any()
+
+
+def test_mx_bwd_equals_plain_bwd_on_representable_operands():
+    """With every GEMM operand exactly representable in MXFP8 (along both axes for the
+    weights), the MXFP8 data gradients equal the plain ones exactly."""
+    rng = np.random.default_rng(12)
+    n, d, f = 32, 128, 64
+    W1 = exactly_representable((2 * f, d), rng)
+    W2 = exactly_representable((d, f), rng)
+    # the transposes must be representable too: a value of magnitude in [1,2) in every
+    # 32-block along the other axis as well
+    W1[:, ::32] = 1.0
+    W1[::32, :] = 1.0
+    W2[:, ::32] = 1.0
+    W2[::32, :] = 1.0
+    for m in (W1, W2, W1.T.copy(), W2.T.copy()):
+        np.testing.assert_array_equal(oracle.mx_quantize_rows(m)[2], m)
+    dyp = exactly_representable((n, d), rng)
+    ab = exactly_representable((n, 2 * f), rng) / 4
+    dab_mx, dx_mx, dc, ds = oracle.ffn_bwd_rows_mx(dyp, ab, W1, W2)
+    dab, dx = oracle.ffn_bwd_rows(dyp, ab, W1, W2)
+    np.testing.assert_array_equal(dab_mx, dab)
+    # dab itself is generally not representable: the second GEMM sees its quantisation
+    dabq = oracle.mx_quantize_rows(dab)[2]
+    dx_ref = oracle.bf16(dabq @ W1)
+    np.testing.assert_allclose(dx_mx, dx_ref, rtol=2 ** -8, atol=1e-30)
+    np.testing.assert_array_equal(dc, oracle.mx_quantize_rows(dab)[0])
+    np.testing.assert_array_equal(ds, oracle.mx_quantize_rows(dab)[1])
+
+
+def test_mx_bwd_matches_torch_composition():
+    n, d, f = 40, 96, 64
+    dyp = bf16_bits_to_f64(gen_rows_bf16("mxb_dy", n, d))
+    ab = bf16_bits_to_f64(gen_rows_bf16("mxb_ab", n, 2 * f))
+    W1 = bf16_bits_to_f64(gen_rows_bf16("mxb_w1", 2 * f, d, std=0.05))
+    W2 = bf16_bits_to_f64(gen_rows_bf16("mxb_w2", d, f, std=0.05))
+    dab, dx, dc, ds = oracle.ffn_bwd_rows_mx(dyp, ab, W1, W2)
+
+    def bf(t):
+        return t.to(torch.bfloat16).to(torch.float64)
+
+    q = lambda m: torch.tensor(oracle.mx_quantize_rows(np.ascontiguousarray(m))[2])
+    dh = q(dyp) @ q(W2.T).T                                # contraction over d
+    a, b = torch.tensor(ab[:, :f]), torch.tensor(ab[:, f:])
+    s = torch.sigmoid(a)
+    dab_t = torch.cat([bf(dh * b * s * (1 + a * (1 - s))), bf(dh * a * s)], dim=1)
+    np.testing.assert_allclose(dab, dab_t.numpy(), rtol=2 ** -7, atol=1e-12)
+    dx_t = bf(q(dab) @ q(W1.T).T)                          # contraction over 2f
+    np.testing.assert_allclose(dx, dx_t.numpy(), rtol=2 ** -7, atol=1e-10)
