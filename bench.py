@@ -350,7 +350,10 @@ def bench_ours(args, world, rank, local):
         tde.moe_combine_bwd(cfg, g["dy"], v["yp"], g["logits"], v["topk_idx"], v["topk_w"],
                             v["dest_row"], dyp, dl, ws)
         mark()
-        if args.fuse_gather:
+        if args.mxfp8:   # the data-gradient GEMMs on MXFP8 operands, weight gradients bf16
+            tde.moe_grouped_ffn_bwd_mx(cfg, dyp, v["xp"], v["offsets"], wq, v["ab"], v["h"], dab,
+                                       dxp, dW1, dW2, ws)
+        elif args.fuse_gather:
             tde.moe_grouped_ffn_bwd_gather(cfg, dyp, g["x"], v["src_tok"], v["offsets"], g["W1"],
                                            g["W2"], v["ab"], v["h"], dab, dxp, dW1, dW2, ws)
         else:
@@ -374,8 +377,10 @@ def bench_ours(args, world, rank, local):
         launches_per_step += 1 + (1 if shared else 0)   # the recomputed FC1
     if c.drop_by_score and c.capacity > 0:
         launches_per_step += 2                          # score scatter + select
+    if args.mxfp8:
+        launches_per_step += 1                          # dyp quantised for the data gradients
     if args.mxfp8 and not args.mx_cache_weights:
-        launches_per_step += 2                          # the two weight-quantisation kernels
+        launches_per_step += 4                          # the four weight-quantisation kernels
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
@@ -445,8 +450,11 @@ def bench_ours(args, world, rank, local):
             else:
                 yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
                                    y=y)
-            layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
-                           out=outs)
+            if args.mxfp8:
+                layer.backward_mx(d_logits, d_x, d_dy, wq, g.get("W1s"), g.get("W2s"), out=outs)
+            else:
+                layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
+                               out=outs)
             h_y.copy_(yy, non_blocking=True)
             h_dx.copy_(outs["dx"], non_blocking=True)
             h_dl.copy_(outs["dlogits"], non_blocking=True)
@@ -483,12 +491,14 @@ def bench_ours(args, world, rank, local):
         # nominal dense ratio 4.5 / 2.25 PFLOP/s).  The step's ideal GEMM time is the sum of
         # the forward (at that rate) and everything else (bf16); the peak reported is the
         # flop rate that ideal time stands for.
-        fwd_mx = 6.0 * c.d * c.f * rows_kept
+        # routed FC1 + FC2 (6 d f per row) and the two data gradients (6 d f per row) run at
+        # the E4M3 rate; the weight gradients and the shared expert at the bf16 rate
+        fwd_mx = 12.0 * c.d * c.f * rows_kept
         ideal_s = fwd_mx / (2 * peak * 1e12) + (flops - fwd_mx) / (peak * 1e12)
         ideal_b = fwd_mx / (2 * burst * 1e12) + (flops - fwd_mx) / (burst * 1e12)
         # (the ffn_fwd phase also holds the bf16 shared expert when there is one)
         mx_line = {"ffn_fwd_tflops": None if c.fs else
-                   round(fwd_mx / (phase_ms["ffn_fwd"] * 1e-3) / 1e12, 1),
+                   round(fwd_mx / 2 / (phase_ms["ffn_fwd"] * 1e-3) / 1e12, 1),
                    "fp8_peak_sustained": 2 * peak, "fp8_peak_burst": 2 * burst,
                    "weight_quant_ms": round(phase_ms["mx_weight_quant"], 4),
                    "note": ("weights quantised once before timing (cached)"
@@ -525,7 +535,7 @@ def bench_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp8 fwd (routed) + bf16" if args.mxfp8 else "bf16",
+        "dtype": "mxfp8 (routed fwd + dgrad) + bf16" if args.mxfp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens/logits, N(0,0.02) bf16 weights)",
         "config": {"workload": f"{c.name}: T={c.T} d={c.d} E={c.E} top-{c.k} "
                                f"{c.gate} f={c.f}" + (f" shared fs={c.fs}" if c.fs else "")
@@ -550,8 +560,9 @@ def bench_ours(args, world, rank, local):
                      "peak_source": (f"bf16_tflops_sustained of {peak_src} (kernel timed "
                                      f"inside a continuous step loop); burst {burst}"
                                      if not args.mxfp8 else
-                                     f"flop-weighted: routed forward at 2x, the rest at 1x "
-                                     f"bf16_tflops_sustained of {peak_src}; burst {burst}"),
+                                     f"flop-weighted: routed FC1, FC2 and data gradients at "
+                                     f"2x, the rest at 1x bf16_tflops_sustained of "
+                                     f"{peak_src}; burst {burst}"),
                      "traffic": GEMM_TRAFFIC_PER_LAUNCH.get(c.name),
                      "traffic_note": "DRAM bytes per launch, average of the 6 GEMM launches "
                                      "(ncu on the mixtral_e2 shape x4)",
@@ -636,7 +647,8 @@ def main():
     ap.add_argument("--fuse-gather", action="store_true",
                     help="fold the permute into the FC1 and dW1 operand loads")
     ap.add_argument("--mxfp8", action="store_true",
-                    help="routed experts' forward GEMMs on MXFP8 operands (backward bf16)")
+                    help="routed experts' forward and data-gradient GEMMs on MXFP8 operands "
+                         "(weight gradients bf16)")
     ap.add_argument("--mx-cache-weights", action="store_true",
                     help="with --mxfp8: quantise the weights once, outside the timed steps")
     ap.add_argument("--drop-by-score", action="store_true",

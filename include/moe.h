@@ -107,9 +107,10 @@ typedef struct {
                                  order inside its segment.  Needs (E+1 + T*k)*4 more bytes
                                  of ws.                                                   */
     int32_t mxfp8;            /* 1: the routed experts' forward GEMMs run on MXFP8 operands
-                                 (moe_layer_fwd_mx); needs d and ffn multiples of 128 and
-                                 T*k*(d + ffn)*33/32 more bytes of ws for the quantised
-                                 activations.  The backward stays bf16.                   */
+                                 (moe_layer_fwd_mx), and with moe_layer_bwd_mx the data-
+                                 gradient GEMMs of the backward too; needs d and ffn
+                                 multiples of 128 and more ws for the quantised
+                                 activations.  The weight gradients stay bf16.            */
 } moe_config_t;
 
 /* Index of each saved tensor inside the forward context `ctx` (see moe_ctx_offsets). */
@@ -309,12 +310,18 @@ moe_status_t moe_unpermute_reduce(const moe_config_t *cfg, const void *dxp,
  */
 
 /* Bytes of the quantised-weight blob for cfg's routed experts, and the byte offsets of its
- * four parts: offsets[0] W1 codes [E][2f][d] E4M3, offsets[1] W1 scales, offsets[2] W2
- * codes [E][d][f], offsets[3] W2 scales.  The scales are stored in 512-byte atoms: atom
+ * eight parts: offsets[0] W1 codes [E][2f][d] E4M3, offsets[1] W1 scales, offsets[2] W2
+ * codes [E][d][f], offsets[3] W2 scales (the forward's, quantised along d and f);
+ * offsets[4] W2^T codes [E][f][d] quantised along d, offsets[5] their scales, offsets[6]
+ * W1^T codes [E][d][2f] quantised along 2f, offsets[7] their scales (the backward's data
+ * gradients).  The transposes' scale atoms ((e*ceil(C/256) + nt)*(K/128) + kb)*2 + half
+ * cover rows e*C + nt*256 + half*128 + m of the transpose (C = f or d rows per expert,
+ * K = d or 2f).  The scales are stored in 512-byte atoms: atom
  * ((e*(f/128) + nb)*(d/128) + kb)*2 + half holds, at byte 16*(m%32) + 4*(m/32) + j, the
  * scale of W1 row e*2f + half*f + nb*128 + m, elements 32*(4*kb + j) .. +31; W2 atom
  * ((e*ceil(d/256) + nt)*(f/128) + kb)*2 + half covers W2 row e*d + nt*256 + half*128 + m.
- * Atom bytes of rows past an expert's end hold 127.  Host-only; offsets may be NULL. */
+ * Atom bytes of rows past an expert's end hold 127.  Host-only; offsets (8 entries) may be
+ * NULL. */
 moe_status_t moe_mx_weights_size(const moe_config_t *cfg, size_t *bytes, size_t *offsets);
 
 /* Bytes of an activation scale array for contraction length K (d for x, ffn for h).
@@ -357,6 +364,24 @@ moe_status_t moe_grouped_ffn_mx(const moe_config_t *cfg, const void *xq, const u
 moe_status_t moe_layer_fwd_mx(const moe_config_t *cfg, const float *logits, const void *x,
                               const void *wq, const void *W1s, const void *W2s, void *y,
                               void *ctx, void *ws, void *stream);
+
+/* B2..B5 with the data-gradient GEMMs on MXFP8 operands (cfg->mxfp8 = 1): dyp is
+ * quantised along d; dh = deq(MX(dyp)) deq(W2^T codes), the SwiGLU backward gives dab
+ * (bf16 out) which is quantised along 2f; dxp = bf16(deq(MX(dab)) deq(W1^T codes)).  The
+ * weight gradients dW1, dW2 are computed from the bf16 xp, h, dyp and dab as in
+ * moe_grouped_ffn_bwd.  wq: the blob of moe_mx_quantize_weights.  The quantised dyp and
+ * dab live in ws. */
+moe_status_t moe_grouped_ffn_bwd_mx(const moe_config_t *cfg, const void *dyp, const void *xp,
+                                    const int32_t *offsets, const void *wq, const void *ab,
+                                    const void *h, void *dab, void *dxp, void *dW1, void *dW2,
+                                    void *ws, void *stream);
+
+/* Whole backward with the routed experts' data gradients in MXFP8 (cfg->mxfp8 = 1); as
+ * moe_layer_bwd otherwise (the shared expert and the weight gradients stay bf16). */
+moe_status_t moe_layer_bwd_mx(const moe_config_t *cfg, const void *ctx, const float *logits,
+                              const void *x, const void *dy, const void *wq, const void *W1s,
+                              const void *W2s, void *dx, void *dW1, void *dW2, void *dW1s,
+                              void *dW2s, float *dlogits, void *ws, void *stream);
 
 /*
  * Whole forward: route -> permute -> grouped FFN -> (shared expert) -> combine.

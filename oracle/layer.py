@@ -370,7 +370,7 @@ class TorchSource:
 
 
 def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True,
-                  mx: bool = False) -> dict:
+                  mx: bool = False, mx_bwd: bool = False) -> dict:
     """The exact layer restricted to a subset of outputs (for configurations too big
     to evaluate in full on the host):
 
@@ -382,9 +382,10 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
 
     Every value is computed from the inputs alone through the same steps as the full
     layer; only the rows/columns that the requested outputs depend on are evaluated.
-    mx: the routed experts' forward on MXFP8 operands (as layer_fwd(mx=True)); the
-    restriction stays exact because every MX block lies inside one token row or one
-    weight row."""
+    mx: the routed experts' forward on MXFP8 operands (as layer_fwd(mx=True)); mx_bwd:
+    their data-gradient GEMMs too (as layer_bwd(mx=True)).  The restriction stays exact
+    because every MX block lies inside one token row or one row of a weight (or of its
+    transpose)."""
     r = route(cfg, src.logits)
     k, d, f = cfg.k, cfg.d, cfg.f
     toks = np.unique(np.asarray(tokens, np.int64))
@@ -410,7 +411,10 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
             ab, _, yp[sel], _, _ = ffn_fwd_rows_mx(xp[sel], W1e, W2e)
         else:
             ab, _, yp[sel] = ffn_fwd_rows(xp[sel], W1e, W2e, rnd)
-        _, dxp[sel] = ffn_bwd_rows(dyp[sel], ab, W1e, W2e, rnd)
+        if mx_bwd:
+            _, dxp[sel], _, _ = ffn_bwd_rows_mx(dyp[sel], ab, W1e, W2e)
+        else:
+            _, dxp[sel] = ffn_bwd_rows(dyp[sel], ab, W1e, W2e, rnd)
         del W1e, W2e
     out = {"route": r, "tokens": toks}
     ys = dxs = None
@@ -442,7 +446,7 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
             dyp_e = src.rows("dy", tk) * w[:, None]
             if rnd:
                 dyp_e = bf16(dyp_e)
-            g1, g2 = _wgrad_cols(xr, dyp_e, W1e, W2e, wcols, wrows, rnd, mx=mx)
+            g1, g2 = _wgrad_cols(xr, dyp_e, W1e, W2e, wcols, wrows, rnd, mx=mx, mx_bwd=mx_bwd)
             dW1[e] = g1; dW2[e] = g2
         out["dW1"] = dW1; out["dW2"] = dW2
         out["wcols"] = wcols; out["wrows"] = wrows
@@ -453,7 +457,7 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     return out
 
 
-def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False):
+def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False, mx_bwd=False):
     """dW2[drows][:, cols] and dW1[[cols, f+cols]][:, drows] of one expert from all its rows,
     evaluating only the FFN columns `cols` (exact: a, b, h, dh, da, db of column c depend
     on column c alone).  Uses the oracle's row steps on the column-restricted weights.
@@ -468,7 +472,16 @@ def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False):
         h = bf16(a / (1.0 + np.exp(-a)) * b)
     else:
         ab, h, _ = ffn_fwd_rows(xr, W1c, W2c, rnd)          # ab = [a_cols | b_cols]
-    dab, _ = ffn_bwd_rows(dyp, ab, W1c, W2c, rnd)           # [da_cols | db_cols]
+    if mx_bwd:
+        # dh from MXFP8 dyp (along d) and W2^T rows of these columns (along d), then the
+        # SwiGLU backward; only dab (bf16) enters the weight gradients
+        dh = mx_quantize_rows(dyp)[2] @ mx_quantize_rows(np.ascontiguousarray(W2c.T))[2].T
+        a, b = ab[:, :len(cols)], ab[:, len(cols):]
+        sg = 1.0 / (1.0 + np.exp(-a))
+        dab = np.concatenate([bf16(dh * b * (sg * (1.0 + a * (1.0 - sg)))),
+                              bf16(dh * (a * sg))], axis=1)
+    else:
+        dab, _ = ffn_bwd_rows(dyp, ab, W1c, W2c, rnd)       # [da_cols | db_cols]
     m = len(cols)
     dW2 = (dyp[:, drows].T @ h)                              # [len(drows), m]
     dW1 = (dab.T @ xr[:, drows])                             # [2m, len(drows)]

@@ -7,8 +7,9 @@
   starts from each side's own bf16 h, which may differ by one bf16 step at a few
   elements: its codes must agree wherever both sides quantised the same value, and
   almost everywhere overall.
-* The layer: moe_layer_fwd_mx against the oracle's MXFP8 forward, and the (bf16)
-  backward that follows it against the oracle's backward from the same saved tensors.
+* The layer: moe_layer_fwd_mx against the oracle's MXFP8 forward, followed by either the
+  bf16 backward or moe_layer_bwd_mx (data gradients in MXFP8), each against the oracle's
+  backward of the same kind from the same saved tensors.
 """
 
 import numpy as np
@@ -92,6 +93,25 @@ def test_weight_quantisation_bit_exact():
     for (row, b), v in g2.items():
         assert v == s2[row, b], (row, b)
     assert len(g2) == s2.size
+    # the backward's transposes: W2^T [E][f][d] along d, W1^T [E][d][2f] along 2f
+    w2t = np.concatenate([inp["W2"][e].T for e in range(E)])          # [E*f, d]
+    w1t = np.concatenate([inp["W1"][e].T for e in range(E)])          # [E*d, 2f]
+    ct2, st2, _ = oracle.mx_quantize_rows(np.ascontiguousarray(w2t))
+    ct1, st1, _ = oracle.mx_quantize_rows(np.ascontiguousarray(w1t))
+    np.testing.assert_array_equal(blob[offs[4]:offs[4] + w2t.size].reshape(w2t.shape), ct2)
+    np.testing.assert_array_equal(blob[offs[6]:offs[6] + w1t.size].reshape(w1t.shape), ct1)
+    for off_at, C, K, st in ((offs[5], f, d, st2), (offs[7], d, 2 * f, st1)):
+        NTt, KBt = (C + 255) // 256, K // 128
+
+        def t_row(blk, half, m, C=C, NTt=NTt):
+            e, nt = blk // NTt, blk % NTt
+            r = nt * 256 + half * 128 + m
+            return e * C + r if r < C else None
+
+        gt = unatom(blob[off_at:off_at + E * NTt * KBt * 1024], NTt, KBt, t_row)
+        for (row, b), v in gt.items():
+            assert v == st[row, b], (row, b)
+        assert len(gt) == st.size
 
 
 def act_scales_rowmajor(buf, off, n, K):
@@ -216,11 +236,88 @@ def test_layer_fwd_mx_then_bf16_backward(name):
     assert 1e-4 < diff < 0.1, diff
 
 
+@pytest.mark.parametrize("name", list(CASES))
+def test_grouped_ffn_bwd_mx_against_oracle(name):
+    """The data gradients on MXFP8 operands (dyp and dab quantised along their contraction
+    axes, the weights' transposes from the blob) and the bf16 weight gradients."""
+    c = CASES[name]
+    inp, o, n = route_and_inputs(c)
+    cfg = mx_cfg(c)
+    ws = new_ws(cfg)
+    R = c.T * c.k
+    off = o["offsets"]
+    xp = inp["x"][o["src_tok"][:n]]
+    ab = np.empty((n, 2 * c.f)); h = np.empty((n, c.f))
+    for e in range(c.E):
+        s_, t_ = int(off[e]), int(off[e + 1])
+        ab[s_:t_], h[s_:t_], _, _, _ = oracle.ffn_fwd_rows_mx(xp[s_:t_], inp["W1"][e],
+                                                              inp["W2"][e])
+    from workloads import gen_rows_bf16
+    dyp = gen_rows_bf16("dyp_mxb", R, c.d)
+
+    def rows_bf16(a, cols):
+        t = torch.full((R, cols), float("nan"), dtype=torch.bfloat16)
+        t[:n] = torch.from_numpy(np.asarray(a)).to(torch.bfloat16)
+        return t.cuda()
+
+    nbytes, _ = tde.moe_mx_weights_size(cfg)
+    wq = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    tde.moe_mx_quantize_weights(cfg, dev(inp["W1"]), dev(inp["W2"]), wq)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    xp_t = rows_bf16(oracle.layer._f64(xp), c.d)
+    dab = torch.empty((R, 2 * c.f), **bf); dxp = torch.empty((R, c.d), **bf)
+    dW1 = torch.full((c.E, 2 * c.f, c.d), 7.0, **bf)
+    dW2 = torch.full((c.E, c.d, c.f), 7.0, **bf)
+    tde.moe_grouped_ffn_bwd_mx(cfg, dev(dyp), xp_t, dev(off), wq, rows_bf16(ab, 2 * c.f),
+                               rows_bf16(h, c.f), dab, dxp, dW1, dW2, ws)
+    torch.cuda.synchronize()
+    assert tde.moe_status(ws) == (0, 0)
+    dyp64 = oracle.layer._f64(dyp)
+    r_dab = np.empty((n, 2 * c.f)); r_dxp = np.empty((n, c.d))
+    g1, g2 = f64(dW1), f64(dW2)
+    for e in range(c.E):
+        s_, t_ = int(off[e]), int(off[e + 1])
+        r_dab[s_:t_], r_dxp[s_:t_], _, _ = oracle.ffn_bwd_rows_mx(dyp64[s_:t_], ab[s_:t_],
+                                                                  inp["W1"][e], inp["W2"][e])
+        w1, w2 = oracle.layer.ffn_wgrad_rows(oracle.layer._f64(xp[s_:t_]), h[s_:t_],
+                                             dyp64[s_:t_], r_dab[s_:t_], c.d, c.f)
+        if t_ == s_:
+            assert (g1[e] == 0).all() and (g2[e] == 0).all()
+            continue
+        assert_close(f"dW1[{e}]", g1[e], oracle.bf16(w1))
+        assert_close(f"dW2[{e}]", g2[e], oracle.bf16(w2))
+    assert_close("dab", f64(dab[:n]), r_dab)
+    assert_close("dxp", f64(dxp[:n]), r_dxp)
+
+
+@pytest.mark.parametrize("name", ["small", "many", "pair", "fine"])
+def test_layer_mx_forward_and_backward(name):
+    c = CASES[name]
+    inp = gen_inputs_host(c)
+    cfg = mx_cfg(c)
+    g = {k: dev(v) for k, v in inp.items()}
+    layer = tde.MoELayer(cfg)
+    wq = layer.quantize_weights(g["W1"], g["W2"])
+    y = layer.forward_mx(g["logits"], g["x"], wq)
+    gr = layer.backward_mx(g["logits"], g["x"], g["dy"], wq)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    fo = oracle.layer_fwd(c, inp, mx=True)
+    bo = oracle.layer_bwd(c, inp, fo, mx=True)
+    assert_close("y", f64(y), fo["y"])
+    assert_close("dx", f64(gr["dx"]), bo["dx"])
+    assert_close("dlogits", f64(gr["dlogits"]), bo["dlogits"])
+    for e in range(c.E):
+        if fo["route"]["kept"][e]:
+            assert_close(f"dW1[{e}]", f64(gr["dW1"][e]), bo["dW1"][e])
+            assert_close(f"dW2[{e}]", f64(gr["dW2"][e]), bo["dW2"][e])
+
+
 @pytest.mark.parametrize("name", ["mixtral", "qwen3", "dsv3", "capacity"])
 def test_layer_mx_full_size_sampled(name):
     """The benchmark's MXFP8 configuration at full size (CTA pairs where the benchmark takes
-    them): routing bit-exact in full; y, dx and dlogits of sampled tokens and sampled
-    weight-gradient entries against the oracle's exact restriction."""
+    them; forward and data gradients in MXFP8): y, dx and dlogits of sampled tokens and
+    sampled weight-gradient entries against the oracle's exact restriction."""
     from workloads import CONFIGS, gen_inputs_device
     c = CONFIGS[name]
     g = gen_inputs_device(c, "cuda")
@@ -228,8 +325,7 @@ def test_layer_mx_full_size_sampled(name):
     layer = tde.MoELayer(cfg)
     wq = layer.quantize_weights(g["W1"], g["W2"])
     y = layer.forward_mx(g["logits"], g["x"], wq, g.get("W1s"), g.get("W2s"))
-    gr = layer.backward(g["logits"], g["x"], g["dy"], g["W1"], g["W2"], g.get("W1s"),
-                        g.get("W2s"))
+    gr = layer.backward_mx(g["logits"], g["x"], g["dy"], wq, g.get("W1s"), g.get("W2s"))
     torch.cuda.synchronize()
     assert layer.status() == (0, 0)
     src = oracle.TorchSource(g)
@@ -239,7 +335,7 @@ def test_layer_mx_full_size_sampled(name):
     experts = [int(np.argmax(kept))]
     wcols = np.sort(rng.choice(c.f, size=4, replace=False))
     wrows = np.sort(rng.choice(c.d, size=8, replace=False))
-    s = oracle.layer_sampled(c, src, toks, experts, wcols, wrows, mx=True)
+    s = oracle.layer_sampled(c, src, toks, experts, wcols, wrows, mx=True, mx_bwd=True)
     tk = torch.as_tensor(s["tokens"]).cuda()
     assert_close("y", f64(y[tk]), s["y"])
     assert_close("dx", f64(gr["dx"][tk]), s["dx"])

@@ -137,18 +137,21 @@ def test_mx_ffn_matches_torch_composition():
     np.testing.assert_allclose(yp, y_t.numpy(), rtol=2 ** -8, atol=1e-12)
 
 
-def test_sampled_mx_layer_matches_full_mx_layer():
-    """layer_sampled(mx=True) is an exact restriction of layer_fwd(mx=True) + layer_bwd."""
+@pytest.mark.parametrize("mx_bwd", [False, True])
+def test_sampled_mx_layer_matches_full_mx_layer(mx_bwd):
+    """layer_sampled(mx=True[, mx_bwd]) is an exact restriction of layer_fwd(mx=True) +
+    layer_bwd(mx=mx_bwd)."""
     from workloads import MoEConfig, gen_inputs_host
     cfg = MoEConfig("mx_sample", T=96, d=128, E=4, k=2, f=128, cap_factor=0.8, zipf_s=1.1)
     inp = gen_inputs_host(cfg)
     f = oracle.layer_fwd(cfg, inp, mx=True)
-    b = oracle.layer_bwd(cfg, inp, f)
+    b = oracle.layer_bwd(cfg, inp, f, mx=mx_bwd)
     toks = [0, 5, 17, 95, 42]
     experts = [0, 3]
     wcols = np.array([0, 7, 63, 100])
     wrows = np.array([1, 2, 63, 127])
-    s = oracle.layer_sampled(cfg, oracle.HostSource(inp), toks, experts, wcols, wrows, mx=True)
+    s = oracle.layer_sampled(cfg, oracle.HostSource(inp), toks, experts, wcols, wrows, mx=True,
+                             mx_bwd=mx_bwd)
     tk = np.array(sorted(toks))
     np.testing.assert_array_equal(s["y"], f["y"][tk])
     np.testing.assert_array_equal(s["dx"], b["dx"][tk])

@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             "moe_mx_permute_quant": ([cfgp] + [P] * 8, I32),
             "moe_grouped_ffn_mx": ([cfgp] + [P] * 11, I32),
             "moe_layer_fwd_mx": ([cfgp] + [P] * 9, I32),
+            "moe_grouped_ffn_bwd_mx": ([cfgp] + [P] * 12, I32),
+            "moe_layer_bwd_mx": ([cfgp] + [P] * 15, I32),
             "moe_layer_bwd": ([cfgp] + [P] * 16, I32),
             "moe_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], I32),
             "moe_selftest_wait_timeout": ([P, I64, P], I32),
@@ -217,9 +219,10 @@ def moe_grouped_ffn_bwd_gather(cfg, dyp, x, src_tok, offsets, W1, W2, ab, h, dab
 
 
 def moe_mx_weights_size(cfg):
-    """(bytes, [offsets of W1 codes, W1 scales, W2 codes, W2 scales]) of the MXFP8 blob."""
+    """(bytes, offsets of the MXFP8 blob's parts: W1 codes, W1 scales, W2 codes, W2 scales,
+    W2^T codes, W2^T scales, W1^T codes, W1^T scales)."""
     b = ctypes.c_size_t(0)
-    offs = (ctypes.c_size_t * 4)()
+    offs = (ctypes.c_size_t * 8)()
     _check(lib().moe_mx_weights_size(_cfg(cfg), ctypes.byref(b), offs), "moe_mx_weights_size")
     return b.value, [o for o in offs]
 
@@ -251,6 +254,20 @@ def moe_grouped_ffn_mx(cfg, xq, x_sf, offsets, wq, ab, h, hq, h_sf, yp, ws, stre
 def moe_layer_fwd_mx(cfg, logits, x, wq, W1s, W2s, y, ctx, ws, stream=None):
     _check(lib().moe_layer_fwd_mx(_cfg(cfg), _p(logits), _p(x), _p(wq), _p(W1s), _p(W2s), _p(y),
                                   _p(ctx), _p(ws), _s(stream)), "moe_layer_fwd_mx")
+
+
+def moe_grouped_ffn_bwd_mx(cfg, dyp, xp, offsets, wq, ab, h, dab, dxp, dW1, dW2, ws,
+                           stream=None):
+    _check(lib().moe_grouped_ffn_bwd_mx(_cfg(cfg), _p(dyp), _p(xp), _p(offsets), _p(wq), _p(ab),
+                                        _p(h), _p(dab), _p(dxp), _p(dW1), _p(dW2), _p(ws),
+                                        _s(stream)), "moe_grouped_ffn_bwd_mx")
+
+
+def moe_layer_bwd_mx(cfg, ctx, logits, x, dy, wq, W1s, W2s, dx, dW1, dW2, dW1s, dW2s, dlogits,
+                     ws, stream=None):
+    _check(lib().moe_layer_bwd_mx(_cfg(cfg), _p(ctx), _p(logits), _p(x), _p(dy), _p(wq),
+                                  _p(W1s), _p(W2s), _p(dx), _p(dW1), _p(dW2), _p(dW1s), _p(dW2s),
+                                  _p(dlogits), _p(ws), _s(stream)), "moe_layer_bwd_mx")
 
 
 def moe_grouped_ffn_bwd(cfg, dyp, xp, offsets, W1, W2, ab, h, dab, dxp, dW1, dW2, ws,
@@ -359,6 +376,25 @@ class MoELayer:
             y = torch.empty_like(x)
         moe_layer_fwd_mx(self.cfg, logits, x, wq, W1s, W2s, y, self.ctx, self.ws, stream)
         return y
+
+    def backward_mx(self, logits, x, dy, wq, W1s=None, W2s=None, out=None, stream=None):
+        """Backward with the data-gradient GEMMs in MXFP8 (after forward_mx); `out` as in
+        backward(); the weight-gradient shapes come from the config."""
+        import torch
+        c = self.cfg
+        if out is None:
+            bf = dict(dtype=torch.bfloat16, device=x.device)
+            out = {"dx": torch.empty_like(x),
+                   "dW1": torch.empty((c.E, 2 * c.ffn, c.d), **bf),
+                   "dW2": torch.empty((c.E, c.d, c.ffn), **bf),
+                   "dlogits": torch.empty_like(logits)}
+            if c.ffn_shared:
+                out["dW1s"] = torch.empty_like(W1s)
+                out["dW2s"] = torch.empty_like(W2s)
+        moe_layer_bwd_mx(c, self.ctx, logits, x, dy, wq, W1s, W2s, out["dx"], out["dW1"],
+                         out["dW2"], out.get("dW1s"), out.get("dW2s"), out["dlogits"], self.ws,
+                         stream)
+        return out
 
     def backward(self, logits, x, dy, W1, W2, W1s=None, W2s=None, out=None, stream=None):
         import torch

@@ -110,8 +110,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st);
 // Byte offsets inside the quantised-weight blob: E4M3 codes of W1 [E][2f][d] and W2
 // [E][d][f], and their E8M0 scales in 512-byte atoms ([E][f/128][d/128][2][512] and
 // [E][ceil(d/256)][f/128][2][512]); every part 256-byte aligned.
+// The backward's parts: W2^T [E][f][d] quantised along d with atoms
+// [E][ceil(f/256)][d/128][2][512], and W1^T [E][d][2f] quantised along 2f with atoms
+// [E][ceil(d/256)][2f/128][2][512].
 struct MxWeightLayout {
-  size_t w1q, w1sf, w2q, w2sf, total;
+  size_t w1q, w1sf, w2q, w2sf, w2tq, w2tsf, w1tq, w1tsf, total;
 };
 MxWeightLayout mx_weight_layout(int E, int d, int f);
 
@@ -144,5 +147,24 @@ struct MxFfnArgs {
   int* err;
 };
 cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st);
+
+// The backward's data gradients on MXFP8 operands: DGRAD2 (dh from dyq and the W2^T codes,
+// the SwiGLU backward from ab -> dab bf16 and its MXFP8 form), then DGRAD1 (dxp from the
+// dab codes and the W1^T codes).
+struct MxDgradArgs {
+  int E, d, f;
+  int64_t rows_cap;
+  const int32_t* offsets;
+  const void* dyq;       // [rows_cap][d] E4M3
+  const uint8_t* dy_sf;  // activation scale atoms (K = d)
+  const void* wq;        // quantised-weight blob
+  const void* ab;        // [rows_cap][2f] bf16 (saved)
+  void* dab;             // [rows_cap][2f] bf16 out
+  uint8_t* dabq;         // [rows_cap][2f] E4M3 out
+  uint8_t* dab_sf;       // activation scale atoms (K = 2f) out
+  void* dxp;             // [rows_cap][d] bf16 out
+  int* err;
+};
+cudaError_t launch_mx_ffn_dgrad(const MxDgradArgs& a, cudaStream_t st);
 
 }  // namespace moe

@@ -91,7 +91,8 @@ CtxLayout ctx_layout(const moe_config_t* c) {
 }
 
 struct WsLayout {
-  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, ab, h, ab_s, h_s, xq, x_sf, hq, h_sf, total;
+  size_t route, maps, dyp, dab, dxp, dab_s, dx_s, ab, h, ab_s, h_s, xq, x_sf, hq, h_sf, dyq,
+      dy_sf, dabq, dab_sf, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -119,6 +120,11 @@ WsLayout ws_layout(const moe_config_t* c) {
   L.x_sf = o;  o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, c->d) : 0);
   L.hq = o;    o += align_up(mx ? R * f : 0);
   L.h_sf = o;  o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, c->ffn) : 0);
+  // ... and the backward's: dyp and dab in MXFP8
+  L.dyq = o;   o += align_up(mx ? R * d : 0);
+  L.dy_sf = o; o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, c->d) : 0);
+  L.dabq = o;  o += align_up(mx ? R * 2 * f : 0);
+  L.dab_sf = o; o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, 2 * c->ffn) : 0);
   L.total = o;
   return L;
 }
@@ -439,6 +445,10 @@ moe_status_t moe_mx_weights_size(const moe_config_t* cfg, size_t* bytes, size_t*
     offsets[1] = L.w1sf;
     offsets[2] = L.w2q;
     offsets[3] = L.w2sf;
+    offsets[4] = L.w2tq;
+    offsets[5] = L.w2tsf;
+    offsets[6] = L.w1tq;
+    offsets[7] = L.w1tsf;
   }
   return MOE_OK;
 }
@@ -558,14 +568,70 @@ moe_status_t moe_layer_fwd_mx(const moe_config_t* cfg, const float* logits, cons
   return MOE_OK;
 }
 
-moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float* logits,
-                           const void* x, const void* dy, const void* W1, const void* W2,
-                           const void* W1s, const void* W2s, void* dx, void* dW1, void* dW2,
-                           void* dW1s, void* dW2s, float* dlogits, void* ws, void* stream) {
+namespace {
+// The MXFP8 backward of the routed experts' FFN: quantise dyp, DGRAD2 and DGRAD1 on MXFP8
+// operands, then the two bf16 weight gradients.
+moe_status_t ffn_bwd_mx(const moe_config_t* c, const void* dyp, const void* xp,
+                        const int32_t* offsets, const void* wq, const void* ab, const void* h,
+                        void* dab, void* dxp, void* dW1, void* dW2, void* ws, cudaStream_t st) {
+  const WsLayout W = ws_layout(c);
+  int* err = static_cast<int*>(ws);
+  const int64_t R = c->T * c->k;
+  MOE_TRY(launch_mx_permute_quant(dyp, nullptr, offsets, c->E, R, R, c->d, nullptr,
+                                  at<uint8_t>(ws, W.dyq), at<uint8_t>(ws, W.dy_sf), err, st));
+  MxDgradArgs a{};
+  a.E = c->E;
+  a.d = c->d;
+  a.f = c->ffn;
+  a.rows_cap = R;
+  a.offsets = offsets;
+  a.dyq = at<uint8_t>(ws, W.dyq);
+  a.dy_sf = at<uint8_t>(ws, W.dy_sf);
+  a.wq = wq;
+  a.ab = ab;
+  a.dab = dab;
+  a.dabq = at<uint8_t>(ws, W.dabq);
+  a.dab_sf = at<uint8_t>(ws, W.dab_sf);
+  a.dxp = dxp;
+  a.err = err;
+  MOE_TRY(launch_mx_ffn_dgrad(a, st));
+  void* maps = at<uint8_t>(ws, W.maps);
+  GroupedGemmArgs w2 = gemm_args(GEMM_WGRAD, c, offsets, 0, c->d, c->ffn, dyp, h, dW2, nullptr,
+                                 nullptr, err);
+  w2.wg_M = c->d;
+  w2.wg_N = c->ffn;
+  w2.seg_maps = maps;
+  MOE_TRY(launch_grouped_gemm(w2, st));
+  GroupedGemmArgs w1 = gemm_args(GEMM_WGRAD, c, offsets, 0, c->d, c->ffn, dab, xp, dW1, nullptr,
+                                 nullptr, err);
+  w1.wg_M = 2 * c->ffn;
+  w1.wg_N = c->d;
+  w1.seg_maps = maps;
+  MOE_TRY(launch_grouped_gemm(w1, st));
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_grouped_ffn_bwd_mx(const moe_config_t* cfg, const void* dyp, const void* xp,
+                                    const int32_t* offsets, const void* wq, const void* ab,
+                                    const void* h, void* dab, void* dxp, void* dW1, void* dW2,
+                                    void* ws, void* stream) {
   moe_status_t s = validate(cfg);
   if (s != MOE_OK) return s;
-  if (!ptrs_ok(ctx, logits, x, dy, W1, W2, dx, dW1, dW2, dlogits, ws)) return MOE_ERR_INVALID_ARG;
-  if (cfg->ffn_shared && !ptrs_ok(W1s, W2s, dW1s, dW2s)) return MOE_ERR_INVALID_ARG;
+  if (!cfg->mxfp8) return MOE_ERR_INVALID_ARG;
+  if (!ptrs_ok(dyp, xp, offsets, wq, ab, h, dab, dxp, dW1, dW2, ws)) return MOE_ERR_INVALID_ARG;
+  return ffn_bwd_mx(cfg, dyp, xp, offsets, wq, ab, h, dab, dxp, dW1, dW2, ws,
+                    static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+// The whole backward; wq != null runs the routed experts' data gradients on MXFP8 operands.
+moe_status_t layer_bwd(const moe_config_t* cfg, const void* ctx, const float* logits,
+                       const void* x, const void* dy, const void* W1, const void* W2,
+                       const void* wq, const void* W1s, const void* W2s, void* dx, void* dW1,
+                       void* dW2, void* dW1s, void* dW2s, float* dlogits, void* ws,
+                       void* stream) {
+  moe_status_t s = MOE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* err = static_cast<int*>(ws);
   CtxLayout C = ctx_layout(cfg);
@@ -603,8 +669,11 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float
                              at<float>(ctx, C.off[MOE_CTX_TOPK_W]), dest_row, cfg->T, cfg->E,
                              cfg->k, cfg->d, cfg->gate, cfg->route_scale, cfg->T * cfg->k, dyp,
                              dlogits, err, st));
-  s = ffn_bwd(cfg, dyp, xp_saved, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
-              at<uint8_t>(ws, W.maps), err, st);
+  if (wq)
+    s = ffn_bwd_mx(cfg, dyp, xp_saved, offsets, wq, ab, h, dab, dxp, dW1, dW2, ws, st);
+  else
+    s = ffn_bwd(cfg, dyp, xp_saved, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
+                at<uint8_t>(ws, W.maps), err, st);
   if (s != MOE_OK) return s;
   const void* dxs = nullptr;
   if (cfg->ffn_shared) {
@@ -617,6 +686,32 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float
   MOE_TRY(launch_combine(dxp, dest_row, nullptr, dxs, cfg->T, cfg->k, cfg->d, cfg->T * cfg->k,
                          dx, err, st));
   return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* ctx, const float* logits,
+                           const void* x, const void* dy, const void* W1, const void* W2,
+                           const void* W1s, const void* W2s, void* dx, void* dW1, void* dW2,
+                           void* dW1s, void* dW2s, float* dlogits, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(ctx, logits, x, dy, W1, W2, dx, dW1, dW2, dlogits, ws)) return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared && !ptrs_ok(W1s, W2s, dW1s, dW2s)) return MOE_ERR_INVALID_ARG;
+  return layer_bwd(cfg, ctx, logits, x, dy, W1, W2, nullptr, W1s, W2s, dx, dW1, dW2, dW1s, dW2s,
+                   dlogits, ws, stream);
+}
+
+moe_status_t moe_layer_bwd_mx(const moe_config_t* cfg, const void* ctx, const float* logits,
+                              const void* x, const void* dy, const void* wq, const void* W1s,
+                              const void* W2s, void* dx, void* dW1, void* dW2, void* dW1s,
+                              void* dW2s, float* dlogits, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!cfg->mxfp8) return MOE_ERR_INVALID_ARG;
+  if (!ptrs_ok(ctx, logits, x, dy, wq, dx, dW1, dW2, dlogits, ws)) return MOE_ERR_INVALID_ARG;
+  if (cfg->ffn_shared && !ptrs_ok(W1s, W2s, dW1s, dW2s)) return MOE_ERR_INVALID_ARG;
+  return layer_bwd(cfg, ctx, logits, x, dy, nullptr, nullptr, wq, W1s, W2s, dx, dW1, dW2, dW1s,
+                   dW2s, dlogits, ws, stream);
 }
 
 moe_status_t moe_selftest_wait_timeout(void* ws, int64_t budget_cycles, void* stream) {

@@ -93,6 +93,23 @@ __device__ __forceinline__ uint32_t mx_block(const float* v, uint32_t* c) {
   return static_cast<uint32_t>(X + 127);
 }
 
+// mx_block on 32 bf16 values packed in 4 uint4 (element 0 in the low half of v[0].x).
+__device__ __forceinline__ uint32_t mx_block_bf16(const uint4* v, uint32_t* c) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+  auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
+  auto hi = [](uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); };
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo(w[i])), fabsf(hi(w[i]))));
+  const int X = mx_exponent(amax);
+  const float inv = exp2_int(-X);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    c[q] = e4m3x2(lo(w[2 * q]) * inv, hi(w[2 * q]) * inv) |
+           (e4m3x2(lo(w[2 * q + 1]) * inv, hi(w[2 * q + 1]) * inv) << 16);
+  return static_cast<uint32_t>(X + 127);
+}
+
 // Byte offset of (row m of a 128-row block, sub-block k) inside a scale atom.
 __host__ __device__ __forceinline__ int atom_byte(int m, int k) {
   return 16 * (m & 31) + 4 * (m >> 5) + k;
@@ -140,7 +157,8 @@ mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
   }
   const int nb = d / 32;
   for (int64_t p = gw; p < n_rows; p += nw) {
-    const int t = __ldg(src_tok + p);
+    // src_tok == null: the rows are quantised in place (x has rows_cap rows, t = p)
+    const int t = src_tok ? __ldg(src_tok + p) : static_cast<int>(p);
     if (t < 0 || t >= T) {
       if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
       continue;
@@ -213,6 +231,45 @@ mx_weight_quant_kernel(const uint4* __restrict__ W, int64_t n_rows, int rows_per
   }
 }
 
+// Transposed weight quantisation for the data-gradient GEMMs: for each expert, Wt = W^T
+// ([C][Rk] from W [Rk][C]) quantised along Rk (the contraction axis of the backward GEMM),
+// codes row-major into wtq and scales into atoms [E][ceil(C/256)][Rk/128][2][512] (the
+// weight-atom layout of a B operand with N = C).  One CTA takes a 128 (Rk) x 64 (C) tile
+// through shared memory: coalesced row reads, then one thread per (column, 32-row block).
+constexpr int TQ_ROWS = 128, TQ_COLS = 64;
+
+__global__ void __launch_bounds__(256)
+mx_weight_quant_t_kernel(const __nv_bfloat16* __restrict__ W, int Rk, int C,
+                         uint8_t* __restrict__ wtq, uint8_t* __restrict__ atoms) {
+  __shared__ __nv_bfloat16 tile[TQ_ROWS][TQ_COLS + 2];   // +2: stagger the banks
+  const int e = blockIdx.z;
+  const int r0 = blockIdx.y * TQ_ROWS, c0 = blockIdx.x * TQ_COLS;
+  const __nv_bfloat16* src = W + static_cast<long long>(e) * Rk * C;
+  for (int i = threadIdx.x; i < TQ_ROWS * TQ_COLS / 2; i += blockDim.x) {
+    const int r = i / (TQ_COLS / 2), c2 = (i % (TQ_COLS / 2)) * 2;
+    const __nv_bfloat162 v =
+        *reinterpret_cast<const __nv_bfloat162*>(src + static_cast<long long>(r0 + r) * C + c0 + c2);
+    tile[r][c2] = v.x;
+    tile[r][c2 + 1] = v.y;
+  }
+  __syncthreads();
+  const int c = threadIdx.x % TQ_COLS, blk = threadIdx.x / TQ_COLS;   // 4 blocks of 32 rows
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[32 * blk + i][c]);
+  uint32_t code[8];
+  const uint32_t sc = mx_block(v, code);
+  const int col = c0 + c;                                   // the output row (N index)
+  uint4* dq = reinterpret_cast<uint4*>(wtq + (static_cast<long long>(e) * C + col) * Rk + r0 +
+                                       32 * blk);
+  dq[0] = make_uint4(code[0], code[1], code[2], code[3]);
+  dq[1] = make_uint4(code[4], code[5], code[6], code[7]);
+  const int KB = Rk / 128, NT = (C + 255) / 256;
+  const int kb = r0 / 128, j = blk;                          // r0 is a multiple of 128
+  const long long atom = ((static_cast<long long>(e) * NT + col / 256) * KB + kb) * 2 + ((col >> 7) & 1);
+  atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
+}
+
 // ------------------------------------------------------------------ block-scaled GEMM
 // Per CTA and stage: A 128 rows x 128 B, B 128 rows (pair: this CTA's half of N) or 256
 // rows (one CTA) x 128 B, the A scale atom (512 B) and the B scale pair (1 KB).
@@ -257,11 +314,14 @@ struct MxParams {
   int num_kb;
   int n_out;
   int n_blocks_mn;            // B atom blocks per expert (W1: f/128, W2: ceil(d/256))
+  int b_rows;                 // B rows per expert for the 256-row N tiles (FC2 d, DGRAD2 f,
+                              // DGRAD1 d)
   const int32_t* offsets;
-  __nv_bfloat16* out0;        // FC1: ab  FC2: yp
+  const __nv_bfloat16* aux;   // DGRAD2: the saved pre-activations ab [rows][2f]
+  __nv_bfloat16* out0;        // FC1: ab  FC2: yp  DGRAD2: dab  DGRAD1: dxp
   __nv_bfloat16* out1;        // FC1: h
-  uint8_t* out_q;             // FC1: hq  [rows_cap][f] E4M3
-  uint8_t* out_sf;            // FC1: h's scales, activation atoms with f/128 K blocks
+  uint8_t* out_q;             // FC1: hq [rows_cap][f]   DGRAD2: dab codes [rows_cap][2f]
+  uint8_t* out_sf;            // FC1: h's scales (K blocks f/128)  DGRAD2: dab's (2f/128)
   int* err;
 };
 
@@ -468,8 +528,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               load(sb, &tmB, k0, wrow);
               load(sb + 128 * MX_BK, &tmB, k0, wrow + p.f);
             }
-          } else {
-            const int wrow = g * p.d + nt * 256;
+          } else {   // FC2 (W2), DGRAD2 (W2^T), DGRAD1 (W1^T): 256-row N tiles
+            const int wrow = g * p.b_rows + nt * 256;
             if (PAIR == 2) {
               load(sb, &tmB, k0, wrow + rank * 128);
             } else {
@@ -629,7 +689,58 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           p.out_sf[act_atom_byte(seg0, g, lrow, f / 128, sub >> 2, sub & 3)] =
               static_cast<uint8_t>(sc);
         }
-      } else {
+      } else if (MODE == GEMM_DGRAD2_SWIGLU) {
+        // dh of columns [n0, n0 + 128) of f; the SwiGLU backward from the saved a, b gives
+        // da, db (bf16, for the bf16 weight gradient) and their MXFP8 form (for DGRAD1)
+        const int f = p.f;
+        const int n0 = nt * 256 + 128 * hh;
+        if (n0 < f) {                          // f is a multiple of 128: all or nothing
+          const uint4* arow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + n0);
+          const uint4* brow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + f + n0);
+          uint4* da_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
+          uint4* db_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {        // 32 columns = one MX block per chunk
+            uint4 pda[4], pdb[4];              // da, db as bf16 (what is stored)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float a[8], b[8], da[8], db[8];
+              unpack8(__ldg(arow + 4 * c + v), a);
+              unpack8(__ldg(brow + 4 * c + v), b);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float dh = __uint_as_float(acc[32 * c + 8 * v + e]);
+                const float sg = 1.0f / (1.0f + expf(-a[e]));
+                const float silu = a[e] * sg;
+                const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
+                da[e] = dh * b[e] * dsilu;
+                db[e] = dh * silu;
+              }
+              pda[v] = pack8(da);
+              pdb[v] = pack8(db);
+              da_[4 * c + v] = pda[v];
+              db_[4 * c + v] = pdb[v];
+            }
+            // dab quantised along 2f from its bf16 value (a block never straddles the
+            // da | db boundary)
+            uint32_t code[8];
+            uint32_t sc = mx_block_bf16(pda, code);
+            uint4* qa = reinterpret_cast<uint4*>(p.out_q + prow * 2 * f + n0 + 32 * c);
+            qa[0] = make_uint4(code[0], code[1], code[2], code[3]);
+            qa[1] = make_uint4(code[4], code[5], code[6], code[7]);
+            int sub = (n0 + 32 * c) / 32;
+            p.out_sf[act_atom_byte(seg0, g, lrow, 2 * f / 128, sub >> 2, sub & 3)] =
+                static_cast<uint8_t>(sc);
+            sc = mx_block_bf16(pdb, code);
+            uint4* qb = reinterpret_cast<uint4*>(p.out_q + prow * 2 * f + f + n0 + 32 * c);
+            qb[0] = make_uint4(code[0], code[1], code[2], code[3]);
+            qb[1] = make_uint4(code[4], code[5], code[6], code[7]);
+            sub = (f + n0 + 32 * c) / 32;
+            p.out_sf[act_atom_byte(seg0, g, lrow, 2 * f / 128, sub >> 2, sub & 3)] =
+                static_cast<uint8_t>(sc);
+          }
+        }
+      } else {   // FC2, DGRAD1: plain bf16 rows
         const int n0 = nt * 256 + 128 * hh;
         if (n0 < p.n_out) {                    // d is a multiple of 128: all or nothing
           uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * p.n_out + n0);
@@ -741,6 +852,11 @@ MxWeightLayout mx_weight_layout(int E, int d, int f) {
   L.w1sf = o; o += up(Es * (fs / 128) * (ds / 128) * 1024);
   L.w2q = o;  o += up(Es * ds * fs);
   L.w2sf = o; o += up(Es * ((ds + 255) / 256) * (fs / 128) * 1024);
+  // the backward's data-gradient operands: W2^T [E][f][d] along d, W1^T [E][d][2f] along 2f
+  L.w2tq = o;  o += up(Es * fs * ds);
+  L.w2tsf = o; o += up(Es * ((fs + 255) / 256) * (ds / 128) * 1024);
+  L.w1tq = o;  o += up(Es * ds * 2 * fs);
+  L.w1tsf = o; o += up(Es * ((ds + 255) / 256) * (2 * fs / 128) * 1024);
   L.total = o;
   return L;
 }
@@ -752,7 +868,11 @@ cudaError_t launch_mx_quant_weights(const void* W1, const void* W2, int E, int d
   // atom bytes of rows past an expert's last row are never written: give them scale 1
   cudaError_t e = cudaMemsetAsync(b + L.w1sf, 127, L.w2q - L.w1sf, st);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(b + L.w2sf, 127, L.total - L.w2sf, st);
+  e = cudaMemsetAsync(b + L.w2sf, 127, L.w2tq - L.w2sf, st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(b + L.w2tsf, 127, L.w1tq - L.w2tsf, st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(b + L.w1tsf, 127, L.total - L.w1tsf, st);
   if (e != cudaSuccess) return e;
   const int64_t r1 = static_cast<int64_t>(E) * 2 * f, r2 = static_cast<int64_t>(E) * d;
   mx_weight_quant_kernel<<<grid_rows(r1), QTHREADS, 0, st>>>(
@@ -761,6 +881,11 @@ cudaError_t launch_mx_quant_weights(const void* W1, const void* W2, int E, int d
   mx_weight_quant_kernel<<<grid_rows(r2), QTHREADS, 0, st>>>(
       static_cast<const uint4*>(W2), r2, d, f, 1, f, (d + 255) / 256,
       reinterpret_cast<uint4*>(b + L.w2q), b + L.w2sf);
+  // W2 [E][d][f] -> W2^T along d;  W1 [E][2f][d] -> W1^T along 2f
+  mx_weight_quant_t_kernel<<<dim3(f / TQ_COLS, d / TQ_ROWS, E), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(W2), d, f, b + L.w2tq, b + L.w2tsf);
+  mx_weight_quant_t_kernel<<<dim3(d / TQ_COLS, 2 * f / TQ_ROWS, E), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(W1), 2 * f, d, b + L.w1tq, b + L.w1tsf);
   return cudaGetLastError();
 }
 
@@ -773,6 +898,26 @@ cudaError_t launch_mx_permute_quant(const void* x, const int32_t* src_tok,
       static_cast<uint4*>(xp_or_null), static_cast<uint4*>(xq), x_sf, err);
   return cudaGetLastError();
 }
+
+namespace {
+cudaError_t launch_mx_any(int mode, bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
+                          const CUtensorMap& tsa, const CUtensorMap& tsb, const MxParams& kp,
+                          cudaStream_t st) {
+#define MOE_MX_CASE(M)                                                   \
+  case M:                                                                \
+    return pair ? launch_mx_mode<M, 2>(ta, tb, tsa, tsb, kp, st)         \
+                : launch_mx_mode<M, 1>(ta, tb, tsa, tsb, kp, st);
+  switch (mode) {
+    MOE_MX_CASE(GEMM_FC1_SWIGLU)
+    MOE_MX_CASE(GEMM_FC2)
+    MOE_MX_CASE(GEMM_DGRAD2_SWIGLU)
+    MOE_MX_CASE(GEMM_DGRAD1)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_MX_CASE
+}
+}  // namespace
 
 cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
   if (a.E < 1 || a.E > MX_MAX_G || a.d % 128 || a.f % 128) return cudaErrorInvalidValue;
@@ -792,11 +937,7 @@ cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
   kp.err = a.err;
   CUtensorMap ta, tb, tsa, tsb;
   auto launch = [&](int mode) {
-    if (mode == GEMM_FC1_SWIGLU)
-      return pair ? launch_mx_mode<GEMM_FC1_SWIGLU, 2>(ta, tb, tsa, tsb, kp, st)
-                  : launch_mx_mode<GEMM_FC1_SWIGLU, 1>(ta, tb, tsa, tsb, kp, st);
-    return pair ? launch_mx_mode<GEMM_FC2, 2>(ta, tb, tsa, tsb, kp, st)
-                : launch_mx_mode<GEMM_FC2, 1>(ta, tb, tsa, tsb, kp, st);
+    return launch_mx_any(mode, pair, ta, tb, tsa, tsb, kp, st);
   };
   // FC1: [a|b] = xq W1q^T (K = d), SwiGLU, h quantised
   const uint64_t KB1 = d / 128, NB1 = f / 128;
@@ -822,6 +963,7 @@ cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
   kp.num_kb = a.f / MX_BK;
   kp.n_out = a.d;
   kp.n_blocks_mn = static_cast<int>(NT2);
+  kp.b_rows = a.d;
   kp.out0 = static_cast<__nv_bfloat16*>(a.yp);
   kp.out1 = nullptr;
   kp.out_q = nullptr;
@@ -833,6 +975,61 @@ cudaError_t launch_mx_ffn(const MxFfnArgs& a, cudaStream_t st) {
       !make_map_u8(&tsb, wb + L.w2sf, 256, E * NT2 * KB2 * 4, 256, 4, false))
     return cudaErrorInvalidValue;
   return launch(GEMM_FC2);
+}
+
+cudaError_t launch_mx_ffn_dgrad(const MxDgradArgs& a, cudaStream_t st) {
+  if (a.E < 1 || a.E > MX_MAX_G || a.d % 128 || a.f % 128) return cudaErrorInvalidValue;
+  const MxWeightLayout L = mx_weight_layout(a.E, a.d, a.f);
+  const uint8_t* wb = static_cast<const uint8_t*>(a.wq);
+  const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
+  const uint64_t E = static_cast<uint64_t>(a.E), d = static_cast<uint64_t>(a.d),
+                 f = static_cast<uint64_t>(a.f);
+  const bool pair = static_cast<double>(a.rows_cap) / a.E >= 192.0;
+  MxParams kp{};
+  kp.G = a.E;
+  kp.rows_cap = a.rows_cap;
+  kp.d = a.d;
+  kp.f = a.f;
+  kp.offsets = a.offsets;
+  kp.err = a.err;
+  CUtensorMap ta, tb, tsa, tsb;
+  // DGRAD2: dh = dyq W2^T-quantised (K = d, N = f), SwiGLU backward, dab quantised
+  const uint64_t NT_f = (f + 255) / 256, KB_d = d / 128;
+  kp.num_n_tiles = static_cast<int>(NT_f);
+  kp.num_kb = a.d / MX_BK;
+  kp.n_out = a.f;
+  kp.n_blocks_mn = static_cast<int>(NT_f);
+  kp.b_rows = a.f;
+  kp.aux = static_cast<const __nv_bfloat16*>(a.ab);
+  kp.out0 = static_cast<__nv_bfloat16*>(a.dab);
+  kp.out_q = a.dabq;
+  kp.out_sf = a.dab_sf;
+  if (!make_map_u8(&ta, a.dyq, d, rows, 128, 128, true) ||
+      !make_map_u8(&tb, wb + L.w2tq, d, E * f, 128, 128, true) ||
+      !make_map_u8(&tsa, a.dy_sf, 256, mx_act_scale_bytes(a.rows_cap, a.E, a.d) / 256, 256, 2,
+                   false) ||
+      !make_map_u8(&tsb, wb + L.w2tsf, 256, E * NT_f * KB_d * 4, 256, 4, false))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_mx_any(GEMM_DGRAD2_SWIGLU, pair, ta, tb, tsa, tsb, kp, st);
+  if (e != cudaSuccess) return e;
+  // DGRAD1: dxp = dabq W1^T-quantised (K = 2f, N = d)
+  const uint64_t NT_d = (d + 255) / 256, KB_2f = 2 * f / 128;
+  kp.num_n_tiles = static_cast<int>(NT_d);
+  kp.num_kb = 2 * a.f / MX_BK;
+  kp.n_out = a.d;
+  kp.n_blocks_mn = static_cast<int>(NT_d);
+  kp.b_rows = a.d;
+  kp.aux = nullptr;
+  kp.out0 = static_cast<__nv_bfloat16*>(a.dxp);
+  kp.out_q = nullptr;
+  kp.out_sf = nullptr;
+  if (!make_map_u8(&ta, a.dabq, 2 * f, rows, 128, 128, true) ||
+      !make_map_u8(&tb, wb + L.w1tq, 2 * f, E * d, 128, 128, true) ||
+      !make_map_u8(&tsa, a.dab_sf, 256, mx_act_scale_bytes(a.rows_cap, a.E, 2 * a.f) / 256, 256,
+                   2, false) ||
+      !make_map_u8(&tsb, wb + L.w1tsf, 256, E * NT_d * KB_2f * 4, 256, 4, false))
+    return cudaErrorInvalidValue;
+  return launch_mx_any(GEMM_DGRAD1, pair, ta, tb, tsa, tsb, kp, st);
 }
 
 }  // namespace moe
