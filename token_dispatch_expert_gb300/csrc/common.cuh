@@ -42,6 +42,13 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+// sigma(a) for the SwiGLU epilogues through CUDA's fast exponential and division
+// intrinsics (a few ulp of fp32; the results are rounded to bf16 afterwards).  For
+// a < -88 the exponential overflows to +inf and the division returns 0.
+__device__ __forceinline__ float sigmoid_fast(float a) {
+  return __fdividef(1.0f, 1.0f + __expf(-a));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

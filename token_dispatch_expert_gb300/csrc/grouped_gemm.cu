@@ -156,7 +156,7 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+__device__ __forceinline__ float silu_f(float a) { return a * sigmoid_fast(a); }
 
 // Every lane of the warp waits; the result is made warp-uniform so that a timeout seen by
 // one lane sends the whole warp down the same path (later warp-collective ops stay legal).
@@ -616,7 +616,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float dh = __uint_as_float(ra[v * 8 + e]);
-                const float sg = 1.0f / (1.0f + expf(-a[e]));
+                const float sg = sigmoid_fast(a[e]);
                 const float silu = a[e] * sg;
                 const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
                 da[e] = dh * b[e] * dsilu;

@@ -382,7 +382,7 @@ __device__ __forceinline__ bool mx_warp_wait(uint32_t bar, uint32_t parity, vola
   return __all_sync(FULL_MASK, mbar_wait_bounded(bar, parity, abort, err, budget));
 }
 
-__device__ __forceinline__ float silu_mx(float a) { return a / (1.0f + expf(-a)); }
+__device__ __forceinline__ float silu_mx(float a) { return a * sigmoid_fast(a); }
 __device__ __forceinline__ float bf16r(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
@@ -710,7 +710,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float dh = __uint_as_float(acc[32 * c + 8 * v + e]);
-                const float sg = 1.0f / (1.0f + expf(-a[e]));
+                const float sg = sigmoid_fast(a[e]);
                 const float silu = a[e] * sg;
                 const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
                 da[e] = dh * b[e] * dsilu;
