@@ -3,7 +3,7 @@
 Small and mid shapes: every output compared in full (y, dx, dW1, dW2, dlogits, the
 shared expert's grads, and the saved routing bit-exact).  The five workload shapes at
 full size, in the configuration the benchmark times: routing bit-exact in full; y, dx
-and dlogits on sampled tokens; weight-gradient entries of three whole experts (the
+and dlogits on 256 sampled tokens; weight-gradient entries of three whole experts (the
 most loaded, the least loaded non-empty one and expert 0) on sampled rows/columns --
 each sampled value is the oracle's exact definition restricted to that output."""
 
@@ -89,15 +89,15 @@ def test_layer_full_size_sampled(name):
     for key in ROUTE_KEYS:
         np.testing.assert_array_equal(np_i(v[key]), o_r[key], err_msg=key)
     rng = np.random.default_rng(0)
-    toks = rng.choice(c.T, size=24, replace=False)
+    toks = rng.choice(c.T, size=256, replace=False)
     if c.capacity:   # make sure some sampled tokens have dropped slots
         dropped = np.nonzero(o_r["drop_mask"].any(1))[0]
         toks = np.unique(np.concatenate([toks, dropped[:8]]))
     kept = o_r["kept"]
     nz = np.nonzero(kept)[0]
     experts = sorted({int(np.argmax(kept)), int(nz[np.argmin(kept[nz])]), 0})
-    wcols = np.sort(rng.choice(min(c.f, c.fs) if c.fs else c.f, size=4, replace=False))
-    wrows = np.sort(rng.choice(c.d, size=16, replace=False))
+    wcols = np.sort(rng.choice(min(c.f, c.fs) if c.fs else c.f, size=16, replace=False))
+    wrows = np.sort(rng.choice(c.d, size=64, replace=False))
     s = oracle.layer_sampled(c, src, toks, experts, wcols, wrows)
     tk = s["tokens"]
     assert_close("y", f64(y[torch.as_tensor(tk).cuda()]), s["y"])

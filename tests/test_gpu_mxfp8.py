@@ -330,11 +330,12 @@ def test_layer_mx_full_size_sampled(name):
     assert layer.status() == (0, 0)
     src = oracle.TorchSource(g)
     rng = np.random.default_rng(1)
-    toks = rng.choice(c.T, size=16, replace=False)
+    toks = rng.choice(c.T, size=256, replace=False)
     kept = oracle.route(c, src.logits)["kept"]
-    experts = [int(np.argmax(kept))]
-    wcols = np.sort(rng.choice(c.f, size=4, replace=False))
-    wrows = np.sort(rng.choice(c.d, size=8, replace=False))
+    nz = np.nonzero(kept)[0]
+    experts = sorted({int(np.argmax(kept)), int(nz[np.argmin(kept[nz])]), 0} & set(nz.tolist()))
+    wcols = np.sort(rng.choice(c.f, size=16, replace=False))
+    wrows = np.sort(rng.choice(c.d, size=64, replace=False))
     s = oracle.layer_sampled(c, src, toks, experts, wcols, wrows, mx=True, mx_bwd=True)
     tk = torch.as_tensor(s["tokens"]).cuda()
     assert_close("y", f64(y[tk]), s["y"])
