@@ -173,7 +173,16 @@ class OracleTimer:
     """The CPU oracle's full forward + backward (routing, expert FFN with both weight
     gradients, combine, all in float64) on the first t tokens of the workload, with the
     workload's d, f, E, k, gate and capacity rule.  Inputs come from the host generators
-    and are built once."""
+    and are built once.
+
+    Workloads whose float64 weights and weight gradients for all E experts exceed
+    MEM_BUDGET (DeepSeek-V3: about 90 GB) run the sample on the experts its tokens route
+    to: the logits restricted to those experts' columns (kept in expert order) select the
+    same top-k with the same gate weights, because both gates (softmax renormalised over
+    the top-k, sigmoid normalised over the selected) depend only on the selected logits.
+    Their weights are drawn per expert from the same N(0, 0.02^2) bf16 distribution."""
+
+    MEM_BUDGET = 32 << 30
 
     def __init__(self, c):
         import oracle
@@ -189,29 +198,74 @@ class OracleTimer:
         self.logits = gen_logits(c)
         self.x = gen_bf16(c, "x", (c.T, c.d))
         self.dy = gen_bf16(c, "dy", (c.T, c.d))
-        self.W = {n: oracle.layer._f64(gen_bf16(c, n, shape, WEIGHT_STD))
-                  for n, shape in weight_shapes(c).items()}
+        per_expert = 2 * 3 * c.d * c.f * 8          # weights + weight gradients, float64
+        self.restrict = c.cap_factor is None and c.E * per_expert > self.MEM_BUDGET
+        self.max_experts = max(c.k, self.MEM_BUDGET // per_expert)
+        self.W = {}
+        self._expert_w = {}
+        for n, shape in weight_shapes(c).items():
+            if self.restrict and n in ("W1", "W2"):
+                continue
+            self.W[n] = oracle.layer._f64(gen_bf16(c, n, shape, WEIGHT_STD))
+
+    def _experts(self, t: int):
+        import numpy as np
+        import oracle
+        r = oracle.route(self.c.replace(T=t), self.logits[:t])
+        return np.unique(r["topk_idx"])
+
+    def _inputs(self, t: int):
+        import numpy as np
+        import oracle
+        from workloads import WEIGHT_STD, gen_bf16
+        c = self.c
+        inp = {"logits": self.logits[:t], "x": self.x[:t], "dy": self.dy[:t]}
+        inp.update(self.W)
+        if not self.restrict:
+            return c.replace(T=t), inp
+        used = self._experts(t)
+        for e in used:
+            if e not in self._expert_w:
+                self._expert_w[e] = tuple(
+                    oracle.layer._f64(gen_bf16(c, f"{n}[{e}]", shape, WEIGHT_STD))
+                    for n, shape in (("W1", (2 * c.f, c.d)), ("W2", (c.d, c.f))))
+        inp["logits"] = np.ascontiguousarray(self.logits[:t][:, used])
+        inp["W1"] = np.stack([self._expert_w[e][0] for e in used])
+        inp["W2"] = np.stack([self._expert_w[e][1] for e in used])
+        sub = c.replace(T=t, E=len(used))
+        if getattr(c, "select_bias", None) is not None:
+            sub = sub.replace(select_bias=np.ascontiguousarray(c.select_bias[used]))
+        return sub, inp
 
     def run(self, t: int) -> float:
         import oracle
-        c = self.c
-        sub = c.replace(T=t)
-        inp = {"logits": self.logits[:t], "x": self.x[:t], "dy": self.dy[:t]}
-        inp.update(self.W)
+        sub, inp = self._inputs(t)
         t0 = time.perf_counter()
         fo = oracle.layer_fwd(sub, inp)
         oracle.layer_bwd(sub, inp, fo)
         return time.perf_counter() - t0
 
+    def max_tokens(self) -> int:
+        """The largest sample whose experts fit MEM_BUDGET (all T when unrestricted)."""
+        if not self.restrict:
+            return self.c.T
+        t = 1
+        while t < self.c.T and len(self._experts(t + 1)) <= self.max_experts:
+            t += 1
+        return t
+
     def calibrate(self, budget_s: float) -> int:
         """Token count whose run takes about budget_s seconds: fit time = a + b*t from two
         probes (the weight-gradient buffers give the oracle a cost independent of t)."""
-        t1, t2 = 2, 6
+        t_max = self.max_tokens()
+        t1, t2 = min(2, t_max), min(6, t_max)
+        if t2 <= t1:
+            return t_max
         d1, d2 = self.run(t1), self.run(t2)
         b = max((d2 - d1) / (t2 - t1), 1e-6)
         a = max(d1 - b * t1, 0.0)
         t = int((budget_s - a) / b) if budget_s > a else t2
-        return int(min(self.c.T, max(t2, t)))
+        return int(min(t_max, max(t2, t)))
 
 
 # --------------------------------------------------------------------------- ours
@@ -612,7 +666,9 @@ def bench_ours(args, world, rank, local):
         line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": ot.threads,
                                 "kind": "oracle",
                                 "sample": f"full fwd+bwd of the first {t} tokens of the "
-                                          f"workload ({dt:.1f} s, float64 C oracle, OpenMP)"}
+                                          f"workload ({dt:.1f} s, float64 C oracle, OpenMP)"
+                                          + (", on the experts they route to"
+                                             if ot.restrict else "")}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -647,7 +703,8 @@ def bench_reference(args, world, rank, local):
                    "tokens_per_step": c.T},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": thr,
                          "kind": "oracle",
-                         "sample": f"each step: full fwd+bwd of the first {t} tokens"},
+                         "sample": f"each step: full fwd+bwd of the first {t} tokens"
+                                   + (", on the experts they route to" if ot.restrict else "")},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -110,14 +110,26 @@ def test_grouped_ffn_bwd(name):
     assert tde.moe_status(ws) == (0, 0)
 
 
-def test_grouped_ffn_segment_edges():
-    """Segment sizes chosen to hit the tile cases of the CTA-pair path: an empty segment,
-    one row, segment ends 1, 64, 127, 128, 129 and 255 rows into a 256-row tile, segments
-    of several tiles, and an N tail (f = 192)."""
-    sizes = [1, 64, 127, 128, 129, 255, 300, 600, 0, 385]
+EDGE_CASES = {
+    # an empty segment, one row, segment ends 1, 64, 127, 128, 129 and 255 rows into a
+    # 256-row tile, segments of several tiles, and an N tail (f = 192)
+    "edges": ([1, 64, 127, 128, 129, 255, 300, 600, 0, 385], 256, 192),
+    # the swap-AB tail tiles (a segment's last tile with at most 160 rows): N = rows rounded
+    # up to 32 at 31 / 32 / 33 rows, the largest tail (160), the smallest ordinary last tile
+    # (161), a full last tile (256), tails after full tiles (416 = 256 + 160, 417), and N
+    # tails in FC1 (f = 320: the last FC1 tile holds 64 valid columns, all in the first CTA)
+    # and in FC2 / FC1 data-gradient (d = 384)
+    "tail_edges": ([31, 32, 33, 160, 161, 256, 416, 417, 2, 700], 384, 320),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE_CASES))
+def test_grouped_ffn_segment_edges(name):
+    """Segment sizes chosen to hit the tile cases of the CTA-pair path."""
+    sizes, d, f = EDGE_CASES[name]
     E = len(sizes)
     n = sum(sizes)
-    c = MoEConfig("edges", T=n, d=256, E=E, k=1, f=192)
+    c = MoEConfig(name, T=n, d=d, E=E, k=1, f=f)
     assert n / E >= 192          # average rows per group: the pair path is taken
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     inp = gen_inputs_host(c)

@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -55,7 +56,12 @@ struct Geo {
   // the weight-gradient epilogue stores through shared memory with TMA: each epilogue
   // warp double-buffers a 32-row x 64-column bf16 box (4 KB)
   static constexpr bool TMA_STORE = MODE == GEMM_WGRAD;
-  static constexpr int STAGING_BYTES = TMA_STORE ? 4 * 2 * 4096 : 0;
+  // swap-AB tail tiles (CTA pairs, fixed-K modes): see tail_tokens()
+  static constexpr bool TAIL = PAIR == 2 && MODE != GEMM_WGRAD;
+  // the tail tiles' epilogue transposes through shared memory: one 32 x 32 fp32 block per
+  // epilogue warp, rows padded to 144 bytes
+  static constexpr int XCH_BYTES = TAIL ? 4 * 32 * 144 : 0;
+  static constexpr int STAGING_BYTES = (TMA_STORE ? 4 * 2 * 4096 : 0) + XCH_BYTES;
   static constexpr int STAGES = PAIR == 2 ? (TMA_STORE ? 5 : 6) : 4;
 };
 
@@ -67,12 +73,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_G = 256;
 constexpr int MAX_STAGES = 6;
 constexpr long long WAIT_BUDGET = 4000000000LL;   // clock cycles (about 2 s)
+// a segment's last M tile with at most this many rows runs as a swap-AB tail tile
+constexpr int TAIL_ROWS_MAX = 160;
 
 struct Ctl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t xfull[2][2];    // FC1 tail tiles: [warp pair][0] (one block per warp)
+  uint64_t xempty[2][2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -109,6 +119,8 @@ struct KParams {
   // gathered operand rows (FC1's A, WGRAD's B): source row of each row-buffer row
   const int32_t* gidx;
   int gather_rows;
+  // a segment's last M tile with at most this many rows runs swapped (0: never)
+  int tail_rows_max;
 };
 
 template <int MODE>
@@ -150,10 +162,6 @@ __device__ __forceinline__ void map_tile(const Ctl* ctl, const KParams& p, int t
     nt = local / mtg;
     mt = local - nt * mtg;
   }
-}
-
-__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
 __device__ __forceinline__ float silu_f(float a) { return a * sigmoid_fast(a); }
@@ -220,11 +228,174 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
   }
 }
 
+// The tail tiles' segment-row maps: entry i has a box of 16 (i + 1) rows, the rows one
+// CTA of a pair holds for N = 32 (i + 1), so each K block takes a single copy.
+struct TailMaps {
+  CUtensorMap m[8];
+};
+
+// Swap-AB tail tiles.  A segment's rows fill its M tiles of 256 except the last, which
+// holds rem = rows - 256 (mtg - 1) rows.  When rem <= tail_rows_max that tile computes the
+// transposed product, D^T = W_tile . X^T: the tile's 256 weight rows (output columns) are
+// the MMA's M (128 per CTA) and its rows the MMA's N, rounded up to a multiple of 32, so
+// the tensor-core time follows the rows present instead of a full 256.  Returns that N, or
+// 0 for an ordinary tile.
+template <int MODE, int PAIR>
+__device__ __forceinline__ int tail_tokens(const Ctl* ctl, const KParams& p, int g, int mt) {
+  if (!Geo<MODE, PAIR>::TAIL) return 0;
+  const int rows = ctl->gstart[g + 1] - ctl->gstart[g];
+  const int rem = rows - mt * 256;
+  if (rem > 256 || rem <= 0 || rem > p.tail_rows_max) return 0;   // not the last tile
+  return (rem + 31) & ~31;
+}
+
+// The copies of one K block of a tail tile: the weight rows into sb (as an ordinary tile's
+// B operand, except FC1: 64 gate rows then the matching 64 up rows per CTA, through tmW)
+// and this CTA's ntok / 2 rows of the segment into sa in one copy (tmT->m[ntok / 32 - 1]).
+// With GATHER the segment rows are left to the caller's gather4 copies.
+template <int MODE, bool GATHER>
+__device__ __forceinline__ void issue_loads_tail(const CUtensorMap* tmB, const TailMaps* tmT,
+                                                 const CUtensorMap* tmW, const KParams& p,
+                                                 uint32_t sa, uint32_t sb, uint32_t bar,
+                                                 int rank, int g, int mt, int nt, int seg0,
+                                                 int kb, int ntok) {
+  const int k0 = kb * BK;
+  if (MODE == GEMM_FC1_SWIGLU) {
+    const int wrow = g * 2 * p.f + nt * (BN / 2) + 64 * rank;
+    tma_load_2d_pair(sb, tmW, bar, k0, wrow);                 // gate -> TMEM lanes 0..63
+    tma_load_2d_pair(sb + 64 * BK * 2, tmW, bar, k0, wrow + p.f);   // up -> lanes 64..127
+  } else if (MODE == GEMM_FC2) {
+    tma_load_2d_pair(sb, tmB, bar, k0, g * p.d + nt * BN + rank * (BN / 2));
+  } else {   // DGRAD2, DGRAD1: the weight operand is MN-major
+    const int krow = (MODE == GEMM_DGRAD2_SWIGLU ? g * p.d : g * 2 * p.f) + k0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      tma_load_2d_pair(sb + j * CHUNK_BYTES, tmB, bar, nt * BN + rank * (BN / 2) + 64 * j, krow);
+  }
+  if (GATHER) return;
+  const int trow = seg0 + mt * 256 + rank * (ntok / 2);
+  tma_load_2d_pair(sa, &tmT->m[ntok / 32 - 1], bar, k0, trow);
+}
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Epilogue of a tail tile.  TMEM lane l of this CTA holds the tile's weight row (output
+// column) rank * 128 + l, and TMEM column j the tile's row row0 + j, for j < ntok.  Each
+// warp takes its 32 lanes x 32 rows per step, transposes them through its own block of
+// shared memory (fp32, rows padded to 144 bytes so both the column writes and the 32-byte
+// row reads are free of bank conflicts) and stores 16-byte pieces of 8 columns of a row.
+// FC1: lanes 0..63 hold gate columns, 64..127 the matching up columns; the up warp
+// (quarter 2 + i) only fills its block, and the gate warp (quarter i) reads both blocks and
+// stores a, b and h.  Returns false if a wait gave up.
+constexpr int XPOSE_PITCH = 144;                 // bytes per row of a transpose block
+constexpr int XPOSE_BYTES = 32 * XPOSE_PITCH;    // one warp's block
+
+__device__ __forceinline__ void ld_shared_f32x8(uint32_t addr, float* v) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr) : "memory");
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]) : "r"(addr + 16) : "memory");
+}
+
+template <int MODE>
+__device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32_t taddr,
+                                              uint32_t xch_base, int q, int lane, int rank,
+                                              int nt, long long row0, int nrows, int ntok,
+                                              int& xc, volatile int* abort_flag) {
+  const uint32_t blk = xch_base + static_cast<uint32_t>(q * XPOSE_BYTES);
+  const int pi = q & 1;                      // FC1: warp pair (gate quarter pi, up pi + 2)
+  const bool up = MODE == GEMM_FC1_SWIGLU && q >= 2;
+  // the warp's first output column
+  const int n0 = MODE == GEMM_FC1_SWIGLU ? nt * (BN / 2) + rank * 64 + pi * 32
+                                         : nt * BN + rank * 128 + q * 32;
+  const int n_lim = (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) ? p.n_out : p.f;
+  const bool cols_ok = n0 < n_lim;           // d, f are multiples of 64: all 32 or none
+#pragma unroll 1
+  for (int c = 0; c < ntok / 32; ++c, ++xc) {
+    uint32_t ra[32];
+    tmem_ld32(taddr + c * 32, ra);
+    tmem_ld_wait();
+    const uint32_t xph = static_cast<uint32_t>(xc) & 1u;
+    if (up && !warp_wait(smem_u32(&ctl->xempty[pi][0]), xph ^ 1u, abort_flag, p.err,
+                         WAIT_BUDGET))
+      return false;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(blk + j * XPOSE_PITCH + lane * 4),
+                   "f"(__uint_as_float(ra[j]))
+                   : "memory");
+    __syncwarp();
+    if (up) {
+      mbar_arrive(smem_u32(&ctl->xfull[pi][0]));
+      continue;
+    }
+    if (MODE == GEMM_FC1_SWIGLU &&
+        !warp_wait(smem_u32(&ctl->xfull[pi][0]), xph, abort_flag, p.err, WAIT_BUDGET))
+      return false;
+    // piece i of this lane: row j = lane / 4 + 8 i, columns n0 + 8 (lane % 4) + 0..7
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = lane / 4 + 8 * i;
+      const int cc = 8 * (lane & 3);
+      const bool ok = cols_ok && c * 32 + j < nrows;
+      float v[8];
+      ld_shared_f32x8(blk + j * XPOSE_PITCH + cc * 4, v);
+      const long long row = row0 + c * 32 + j;
+      if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
+        if (ok) *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + cc) = pack8(v);
+      } else if (MODE == GEMM_DGRAD2_SWIGLU) {
+        if (ok) {
+          const int f = p.f;
+          const long long base = row * 2 * f + n0 + cc;
+          float a[8], b[8], da[8], db[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base)), a);
+          unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base + f)), b);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float sg = sigmoid_fast(a[e]);
+            const float silu = a[e] * sg;
+            const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
+            da[e] = v[e] * b[e] * dsilu;
+            db[e] = v[e] * silu;
+          }
+          *reinterpret_cast<uint4*>(p.out0 + base) = pack8(da);
+          *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(db);
+        }
+      } else {   // FC1, gate warp: the matching up values sit in the up warp's block
+        float u[8];
+        ld_shared_f32x8(blk + 2 * XPOSE_BYTES + j * XPOSE_PITCH + cc * 4, u);
+        if (ok) {
+          const int f = p.f;
+          float a[8], b[8], h[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            // round a, b to bf16 first: h is computed from the stored values
+            a[e] = bf16_round(v[e]);
+            b[e] = bf16_round(u[e]);
+            h[e] = silu_f(a[e]) * b[e];
+          }
+          const long long base = row * 2 * f + n0 + cc;
+          *reinterpret_cast<uint4*>(p.out0 + base) = pack8(a);
+          *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(b);
+          *reinterpret_cast<uint4*>(p.out1 + row * f + n0 + cc) = pack8(h);
+        }
+      }
+    }
+    __syncwarp();                            // the block is read before the next step
+    if (MODE == GEMM_FC1_SWIGLU) mbar_arrive(smem_u32(&ctl->xempty[pi][0]));
+  }
+  return true;
+}
+
 template <int MODE, int PAIR, bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const KParams p) {
+                    const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ TailMaps tmT,
+                    const __grid_constant__ CUtensorMap tmW, const KParams p) {
   using GE = Geo<MODE, PAIR>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -232,6 +403,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES);
   const uint32_t staging_base = smem_u32(smem + STAGES * GE::STAGE_BYTES);
+  // the tail tiles' transpose blocks sit after the TMA-store staging (which only the
+  // weight-gradient mode, without tail tiles, uses)
+  const uint32_t xch_base = staging_base + (GE::STAGING_BYTES - GE::XCH_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   volatile int* abort_flag = &ctl->abort;
@@ -249,6 +423,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
       mbar_init(smem_u32(&ctl->tempty[b]), 4 * PAIR);
+      for (int w = 0; w < 2; ++w) {
+        mbar_init(smem_u32(&ctl->xfull[w][b]), 32);   // every lane of the writing warp
+        mbar_init(smem_u32(&ctl->xempty[w][b]), 32);  // every lane of the reading warp
+      }
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     fence_mbar_init();
@@ -259,6 +437,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (GE::TMA_STORE) tma_prefetch_desc(&tmC);
+    if (GE::TAIL && p.tail_rows_max > 0) {
+      if (!GATHER)
+        for (int i = 0; i < 8; ++i) tma_prefetch_desc(&tmT.m[i]);
+      if (MODE == GEMM_FC1_SWIGLU) tma_prefetch_desc(&tmW);
+    }
   }
   if (p.uniform_rows > 0) {
     if (threadIdx.x == 0) {
@@ -336,6 +519,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int seg0 = ctl->gstart[g];
       const int seg_rows = ctl->gstart[g + 1] - seg0;
       const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
+      const int ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
+      // a tail tile copies the weight rows and ntok / 2 segment rows per CTA
+      const uint32_t stage_tx =
+          ntok > 0 ? static_cast<uint32_t>(PAIR * (GE::B_BYTES + ntok * BK))
+                   : static_cast<uint32_t>(PAIR * GE::STAGE_BYTES);
       if (MODE == GEMM_WGRAD && p.gmaps != nullptr && g != map_g && nkb > 0) {
         // this segment's maps end at its last row: a K block that crosses the end loads
         // the rows past it as zeros (they belong to the next expert, or are unwritten).
@@ -360,7 +548,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int gi[4] = {0, 0, 0, 0};
       if (GATHER && nkb > 0) {
         if (MODE == GEMM_FC1_SWIGLU) {
-          const int r0 = seg0 + mt * GE::TILE_M + 128 * rank + 4 * lane;
+          // a tail tile's CTA takes ntok / 2 rows: lanes below ntok / 8 copy them
+          const int r0 = seg0 + mt * GE::TILE_M + (ntok > 0 ? ntok / 2 : 128) * rank + 4 * lane;
 #pragma unroll
           for (int q = 0; q < 4; ++q) gi[q] = gather_row(p, min(r0 + q, seg_last));
         } else if (MODE == GEMM_WGRAD && lane < 16) {
@@ -387,9 +576,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // down the leader's barrier directly (its stage is free, so the leader's barrier
         // for this stage has already completed its previous phase)
         if (lane == 0) {
-          if (leader) mbar_arrive_expect_tx(full_local, PAIR * GE::STAGE_BYTES);
-          issue_loads<MODE, PAIR, GATHER>(mA, mB, p, sa, sb, full_leader, PAIR == 2, rank, g,
-                                          mt, nt, seg0, kb);
+          if (leader) mbar_arrive_expect_tx(full_local, stage_tx);
+          if (GE::TAIL && ntok > 0)
+            issue_loads_tail<MODE, GATHER>(mB, &tmT, &tmW, p, sa, sb, full_leader, rank, g, mt,
+                                           nt, seg0, kb, ntok);
+          else
+            issue_loads<MODE, PAIR, GATHER>(mA, mB, p, sa, sb, full_leader, PAIR == 2, rank, g,
+                                            mt, nt, seg0, kb);
         }
         if (GATHER) {
           __syncwarp();
@@ -399,7 +592,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             else tma_gather4(dst, m, full_leader, x, gc[0], gc[1], gc[2], gc[3]);
           };
           if (MODE == GEMM_FC1_SWIGLU) {
-            g4(sa + lane * 512, mA, k0);              // rows 4*lane .. 4*lane+3 of the tile
+            if (ntok == 0 || lane < ntok / 8)
+              g4(sa + lane * 512, mA, k0);            // rows 4*lane .. 4*lane+3 of the tile
           } else if (MODE == GEMM_WGRAD && lane < 16) {
             // K rows 4*lane.. of each 64-column chunk; a chunk past the last column (an N
             // tail) re-reads the last chunk instead: its output columns are never stored
@@ -446,24 +640,38 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        // Operand descriptors for the whole tile, so the K loop below is the same
+        // instruction stream for both tile forms.  An ordinary tile reads A (the segment's
+        // rows) at sa and B (weights) at sb; a tail tile reads the weights at sb as its A
+        // and the segment's rows at sa as its B, with N = ntok.  K-major operands step
+        // 32 bytes per K16, MN-major ones one 64 x 16 core block (2 KB); descriptor start
+        // addresses count 16-byte units, so stage and K offsets add to the low field.
+        const int ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
+        const bool tail = GE::TAIL && ntok > 0;
+        const bool a_mn = tail ? ModeTraits<MODE>::B_MN : ModeTraits<MODE>::A_MN;
+        const bool b_mn = tail ? false : ModeTraits<MODE>::B_MN;
+        const uint32_t idesc =
+            tail ? make_idesc_bf16(256, ntok, ModeTraits<MODE>::B_MN ? 1 : 0, 0) : IDESC;
+        const uint64_t adesc0 = make_smem_desc(smem_base + (tail ? GE::A_BYTES : 0u),
+                                               a_mn ? CHUNK_BYTES : 16u, 1024);
+        const uint64_t bdesc0 = make_smem_desc(smem_base + (tail ? 0u : GE::A_BYTES),
+                                               b_mn ? CHUNK_BYTES : 16u, 1024);
+        const uint32_t astep = a_mn ? 2048 >> 4 : 32 >> 4;
+        const uint32_t bstep = b_mn ? 2048 >> 4 : 32 >> 4;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, p.err, WAIT_BUDGET)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_base + s * GE::STAGE_BYTES;
-          const uint32_t sb = sa + GE::A_BYTES;
           if (lane == 0) {
+            const uint64_t so = static_cast<uint64_t>((s * GE::STAGE_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              uint64_t adesc, bdesc;
-              if (ModeTraits<MODE>::A_MN) adesc = make_smem_desc(sa + kk * 2048, CHUNK_BYTES, 1024);
-              else adesc = make_smem_desc(sa + kk * 32, 16, 1024);
-              if (ModeTraits<MODE>::B_MN) bdesc = make_smem_desc(sb + kk * 2048, CHUNK_BYTES, 1024);
-              else bdesc = make_smem_desc(sb + kk * 32, 16, 1024);
-              if (PAIR == 2) tc_mma_bf16_pair(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
-              else tc_mma_bf16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              const uint64_t adesc = adesc0 + so + kk * astep;
+              const uint64_t bdesc = bdesc0 + so + kk * bstep;
+              if (PAIR == 2) tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
+              else tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
             }
             // the stage is free (in both CTAs) once these MMAs have read it
             if (PAIR == 2) tc_commit_pair_mc(smem_u32(&ctl->empty[s]), 0x3);
@@ -505,6 +713,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int store_buf = 0;                      // staging buffer of the TMA-store epilogue
     const int r_in_tile = rank * 128 + q * 32 + lane;
     int it = 0;
+    int xc = 0;                             // FC1 tail tiles: exchange blocks used so far
     for (int tile = unit; tile < total; tile += num_units, ++it) {
       int g, mt, nt;
       map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
@@ -516,7 +725,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      if (MODE == GEMM_FC1_SWIGLU) {
+      const int ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
+      if (GE::TAIL && ntok > 0) {
+        const long long row0 = static_cast<long long>(seg0) + mt * GE::TILE_M;
+        if (!tail_epilogue<MODE>(p, ctl, taddr, xch_base, q, lane, rank, nt, row0,
+                                 static_cast<int>(seg_end - row0), ntok, xc, abort_flag))
+          break;
+      } else if (MODE == GEMM_FC1_SWIGLU) {
         const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
         const bool valid = prow < seg_end;
         const int f = p.f;
@@ -771,7 +986,8 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 
 template <int MODE, int PAIR, bool GATHER = false>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                        const KParams& kp, cudaStream_t st) {
+                        const TailMaps& tt, const CUtensorMap& tw, const KParams& kp,
+                        cudaStream_t st) {
   auto kern = grouped_gemm_kernel<MODE, PAIR, GATHER>;
   constexpr size_t SMEM = smem_bytes<MODE, PAIR>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -801,15 +1017,18 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   } else {
     cfg.gridDim = dim3(static_cast<unsigned>(sms));
   }
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tt, tw, kp);
 }
 
+// tt, tw: the tail tiles' segment-row maps and, for FC1, weight map (64-row boxes); unused
+// (tt zeroed, tw = tb) when the tail tiles are off
 template <int MODE, bool GATHER = false>
 cudaError_t launch_pick(bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
-                        const KParams& kp, cudaStream_t st) {
+                        const TailMaps& tt, const CUtensorMap& tw, const KParams& kp,
+                        cudaStream_t st) {
   // the output map is used by the weight-gradient mode only; the others pass tb through
-  return pair ? launch_mode<MODE, 2, GATHER>(ta, tb, tb, kp, st)
-              : launch_mode<MODE, 1, GATHER>(ta, tb, tb, kp, st);
+  return pair ? launch_mode<MODE, 2, GATHER>(ta, tb, tb, tt, tw, kp, st)
+              : launch_mode<MODE, 1, GATHER>(ta, tb, tb, tt, tw, kp, st);
 }
 
 }  // namespace
@@ -847,7 +1066,18 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
   const bool pair_rows = rows_per_group >= 192.0;
   const bool pair = a.mode == GEMM_WGRAD ? true : pair_rows;
   const uint32_t b_rows = pair ? BN / 2 : BN;   // B rows (N) held by one CTA
-  CUtensorMap ta, tb;
+  // swap-AB tail tiles: CTA pairs, fixed-K modes
+  const bool tail = pair && a.mode != GEMM_WGRAD;
+  kp.tail_rows_max = tail ? TAIL_ROWS_MAX : 0;
+  CUtensorMap ta, tb, tw;
+  TailMaps tt;
+  memset(&tt, 0, sizeof(tt));
+  // the segment rows of a tail tile, one map per N = 32 (i + 1): boxes of 16 (i + 1) rows
+  auto tail_maps = [&](const void* base, uint64_t cols) {
+    for (int i = 0; i < 8; ++i)
+      if (!make_map(&tt.m[i], base, cols, rows, static_cast<uint32_t>(16 * (i + 1)))) return false;
+    return true;
+  };
   bool ok = true;
   switch (a.mode) {
     case GEMM_FC1_SWIGLU:
@@ -857,30 +1087,37 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
       ok = (gather ? make_map(&ta, a.gather_src, d, static_cast<uint64_t>(a.gather_rows), 1)
                    : make_map(&ta, a.A, d, rows, 128)) &&
            make_map(&tb, a.B, d, G * 2 * f, BN / 2);
+      // the tail tiles' segment rows come through the gather copies when gathering
+      tw = tb;
+      if (ok && tail)
+        ok = (gather || tail_maps(a.A, d)) && make_map(&tw, a.B, d, G * 2 * f, 64);
       if (!ok) return cudaErrorInvalidValue;
-      return gather ? launch_pick<GEMM_FC1_SWIGLU, true>(pair, ta, tb, kp, st)
-                    : launch_pick<GEMM_FC1_SWIGLU>(pair, ta, tb, kp, st);
+      return gather ? launch_pick<GEMM_FC1_SWIGLU, true>(pair, ta, tb, tt, tw, kp, st)
+                    : launch_pick<GEMM_FC1_SWIGLU>(pair, ta, tb, tt, tw, kp, st);
     case GEMM_FC2:
       kp.num_n_tiles = (a.d + BN - 1) / BN;
       kp.num_kb = a.f / BK;
       kp.n_out = a.d;
-      ok = make_map(&ta, a.A, f, rows, 128) && make_map(&tb, a.B, f, G * d, b_rows);
+      ok = make_map(&ta, a.A, f, rows, 128) && make_map(&tb, a.B, f, G * d, b_rows) &&
+           (!tail || tail_maps(a.A, f));
       if (!ok) return cudaErrorInvalidValue;
-      return launch_pick<GEMM_FC2>(pair, ta, tb, kp, st);
+      return launch_pick<GEMM_FC2>(pair, ta, tb, tt, tb, kp, st);
     case GEMM_DGRAD2_SWIGLU:
       kp.num_n_tiles = (a.f + BN - 1) / BN;
       kp.num_kb = a.d / BK;
       kp.n_out = a.f;
-      ok = make_map(&ta, a.A, d, rows, 128) && make_map(&tb, a.B, f, G * d, 64);
+      ok = make_map(&ta, a.A, d, rows, 128) && make_map(&tb, a.B, f, G * d, 64) &&
+           (!tail || tail_maps(a.A, d));
       if (!ok) return cudaErrorInvalidValue;
-      return launch_pick<GEMM_DGRAD2_SWIGLU>(pair, ta, tb, kp, st);
+      return launch_pick<GEMM_DGRAD2_SWIGLU>(pair, ta, tb, tt, tb, kp, st);
     case GEMM_DGRAD1:
       kp.num_n_tiles = (a.d + BN - 1) / BN;
       kp.num_kb = 2 * a.f / BK;
       kp.n_out = a.d;
-      ok = make_map(&ta, a.A, 2 * f, rows, 128) && make_map(&tb, a.B, d, G * 2 * f, 64);
+      ok = make_map(&ta, a.A, 2 * f, rows, 128) && make_map(&tb, a.B, d, G * 2 * f, 64) &&
+           (!tail || tail_maps(a.A, 2 * f));
       if (!ok) return cudaErrorInvalidValue;
-      return launch_pick<GEMM_DGRAD1>(pair, ta, tb, kp, st);
+      return launch_pick<GEMM_DGRAD1>(pair, ta, tb, tt, tb, kp, st);
     case GEMM_WGRAD:
       kp.num_n_tiles = (a.wg_N + BN - 1) / BN;
       kp.wg_m_tiles = (a.wg_M + 256 - 1) / 256;
@@ -906,8 +1143,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
           if (e != cudaSuccess) return e;
           kp.gmaps = maps;
         }
-        return gather ? launch_mode<GEMM_WGRAD, 2, true>(ta, tb, tc, kp, st)
-                      : launch_mode<GEMM_WGRAD, 2>(ta, tb, tc, kp, st);
+        return gather ? launch_mode<GEMM_WGRAD, 2, true>(ta, tb, tc, tt, tb, kp, st)
+                      : launch_mode<GEMM_WGRAD, 2>(ta, tb, tc, tt, tb, kp, st);
       }
     default:
       return cudaErrorInvalidValue;
