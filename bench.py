@@ -47,8 +47,8 @@ def load_peaks():
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the `mixtral_e2` profiling
 # shape -- the same per-expert GEMMs with 1/4 of the experts and 1/4 of the rows, every
 # operand and result scaling with those -- times 4.  Valid for the grouped-GEMM kernel as of
-# the per-segment-map / WGRAD-tile-order version; set to None when the kernel changes.
-GEMM_TRAFFIC_PER_LAUNCH = {"mixtral": 4 * (657 + 340 + 485 + 253 + 671 + 544) / 6 * 1e6}
+# the swap-AB tail-tile version; set to None when the kernel changes.
+GEMM_TRAFFIC_PER_LAUNCH = {"mixtral": 4 * (654 + 341 + 484 + 252 + 671 + 545) / 6 * 1e6}
 
 
 def gemm_algorithmic_bytes(c, rows_kept: int) -> float:
