@@ -633,6 +633,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int lrow = mt * GE::TILE_M + r_in_tile;
       const long long prow = static_cast<long long>(seg0) + lrow;
       const bool valid = prow < ctl->gstart[g + 1];
+      // DGRAD2: the saved a, b of this row do not depend on the MMAs, so the first 32
+      // columns are loaded before the accumulator is ready and each later chunk one chunk
+      // ahead of its use (the epilogue was bound by these loads' latency)
+      const int dg_n0 = nt * 256 + 128 * hh;
+      const bool dg_ok = MODE == GEMM_DGRAD2_SWIGLU && valid && dg_n0 < p.f;
+      const uint4* dg_a = reinterpret_cast<const uint4*>(p.aux + prow * 2 * p.f + dg_n0);
+      const uint4* dg_b = dg_a + p.f / 8;
+      uint4 na[4], nb[4];
+      if (dg_ok) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          na[v] = __ldg(dg_a + v);
+          nb[v] = __ldg(dg_b + v);
+        }
+      }
       if (!mx_warp_wait(smem_u32(&ctl->tfull), it & 1, abort_flag, p.err, MX_WAIT_BUDGET)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -693,20 +708,31 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // dh of columns [n0, n0 + 128) of f; the SwiGLU backward from the saved a, b gives
         // da, db (bf16, for the bf16 weight gradient) and their MXFP8 form (for DGRAD1)
         const int f = p.f;
-        const int n0 = nt * 256 + 128 * hh;
-        if (n0 < f) {                          // f is a multiple of 128: all or nothing
-          const uint4* arow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + n0);
-          const uint4* brow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + f + n0);
+        const int n0 = dg_n0;
+        if (dg_ok) {                           // f is a multiple of 128: all or nothing
           uint4* da_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
           uint4* db_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {        // 32 columns = one MX block per chunk
+            uint4 ca[4], cb[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              ca[v] = na[v];
+              cb[v] = nb[v];
+            }
+            if (c + 1 < 4) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                na[v] = __ldg(dg_a + 4 * (c + 1) + v);
+                nb[v] = __ldg(dg_b + 4 * (c + 1) + v);
+              }
+            }
             uint4 pda[4], pdb[4];              // da, db as bf16 (what is stored)
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float a[8], b[8], da[8], db[8];
-              unpack8(__ldg(arow + 4 * c + v), a);
-              unpack8(__ldg(brow + 4 * c + v), b);
+              unpack8(ca[v], a);
+              unpack8(cb[v], b);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float dh = __uint_as_float(acc[32 * c + 8 * v + e]);
