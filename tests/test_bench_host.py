@@ -1,0 +1,38 @@
+"""Host-side arithmetic of bench.py: the per-launch GEMM flops and bytes, and the exactness
+of the CPU baseline's expert restriction (routing a token sample over only the experts it
+selects gives the same choices and gate weights)."""
+
+import numpy as np
+import pytest
+
+import bench
+import oracle
+from workloads import CONFIGS, MoEConfig, gen_logits
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3", "capacity"])
+def test_gemm_phases_sum_to_the_step_totals(name):
+    c = CONFIGS[name]
+    rows = c.T * c.k
+    ph = bench.gemm_phases(c, rows)
+    assert len(ph) == 6
+    assert sum(f for f, _ in ph) == pytest.approx(bench.gemm_flops(c, rows), rel=1e-12)
+    if not c.fs:
+        assert sum(b for _, b in ph) == pytest.approx(bench.gemm_algorithmic_bytes(c, rows),
+                                                      rel=1e-12)
+    # FC1 and the FC1 data-gradient and weight-gradient carry 4 d f per row, the rest 2 d f
+    F = rows * c.d * c.f + (c.T * c.d * c.fs if c.fs else 0)
+    assert [round(f / F) for f, _ in ph] == [4, 2, 2, 2, 4, 4]
+
+
+@pytest.mark.parametrize("gate,scale", [("softmax", 1.0), ("sigmoid", 2.5)])
+def test_expert_restriction_keeps_choices_and_weights(gate, scale):
+    c = MoEConfig("restrict", T=48, d=64, E=40, k=6, f=64, gate=gate, route_scale=scale,
+                  zipf_s=1.2)
+    lg = gen_logits(c)
+    full = oracle.route(c, lg)
+    used = np.unique(full["topk_idx"])
+    assert len(used) < c.E
+    sub = oracle.route(c.replace(E=len(used)), np.ascontiguousarray(lg[:, used]))
+    np.testing.assert_array_equal(used[sub["topk_idx"]], full["topk_idx"])
+    np.testing.assert_array_equal(sub["topk_w"], full["topk_w"])
