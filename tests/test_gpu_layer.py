@@ -24,6 +24,9 @@ SMALL = {
     "mid": MoEConfig("mid", T=1024, d=512, E=8, k=2, f=512, zipf_s=1.1),
     "mid_sig_shared": MoEConfig("mid_sig_shared", T=768, d=384, E=16, k=4, f=256, fs=256,
                                 gate="sigmoid", route_scale=2.5, cap_factor=1.0, zipf_s=1.2),
+    # 600 = 2 x 256 + 88 rows: the shared expert's last M tile is a swap-AB tail tile
+    "shared_tail": MoEConfig("shared_tail", T=600, d=256, E=4, k=2, f=320, fs=192,
+                             gate="sigmoid", route_scale=2.5, zipf_s=1.0),
 }
 
 ROUTE_KEYS = ["topk_idx", "counts", "kept", "offsets", "dest_row", "src_tok", "src_slot",

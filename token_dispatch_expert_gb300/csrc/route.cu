@@ -68,23 +68,36 @@ route_topk_chunk_kernel(const float* __restrict__ logits, const float* __restric
   const int64_t t0 = chunk * CHUNK;
   for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) s_bits[e] = 0u;
 
+  // each warp takes CHUNK / 8 tokens in turn; the next token's logits are loaded while the
+  // current one is selected, so the loads' latency is paid once per warp, not per token
+  auto load_row = [&](int i, float* dst) {
+    const int64_t t = t0 + warp * (CHUNK / 8) + i;
+#pragma unroll
+    for (int s = 0; s < VPL; ++s) {
+      const int e = lane + 32 * s;
+      dst[s] = (t < T && e < E) ? logits[t * E + e] : 0.0f;
+    }
+  };
+  float vn[VPL];
+  load_row(0, vn);
 #pragma unroll 1
   for (int i = 0; i < CHUNK / 8; ++i) {
     const int tl = warp * (CHUNK / 8) + i;
     const int64_t t = t0 + tl;
+    float v[VPL];
+#pragma unroll
+    for (int s = 0; s < VPL; ++s) v[s] = vn[s];
+    if (i + 1 < CHUNK / 8) load_row(i + 1, vn);
     if (t >= T) {
       if (lane < 8) s_idx[tl][lane] = -1;
       continue;
     }
-    const float* row = logits + t * E;
-    float v[VPL];
     unsigned long long key[VPL];
     bool nan_here = false;
 #pragma unroll
     for (int s = 0; s < VPL; ++s) {
       const int e = lane + 32 * s;
       if (e < E) {
-        v[s] = row[e];
         // the selection key: the logit, or (fp32) logit + bias; the weights use the logit
         const float kv = select_bias ? v[s] + __ldg(select_bias + e) : v[s];
         const uint32_t kf = order_key(kv, nan_here);
@@ -194,12 +207,22 @@ route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
   for (int e = warp; e < E; e += 32) {
     int32_t* col = chunk_cnt + static_cast<int64_t>(e) * nch;
     int running = 0;
-    for (int64_t base = 0; base < nch; base += 32) {
-      const int64_t c = base + lane;
-      const int v = c < nch ? col[c] : 0;
-      const int incl = warp_incl_scan(v);
-      if (c < nch) col[c] = running + incl - v;   // chunk's base rank for expert e
-      running += __shfl_sync(FULL_MASK, incl, 31);
+    // 256 chunks at a time: the eight loads are issued before any store (the stores go to
+    // the same array, so loads interleaved with them would each wait a full round trip)
+    for (int64_t base = 0; base < nch; base += 256) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t c = base + 32 * i + lane;
+        v[i] = c < nch ? col[c] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t c = base + 32 * i + lane;
+        const int incl = warp_incl_scan(v[i]);
+        if (c < nch) col[c] = running + incl - v[i];   // chunk's base rank for expert e
+        running += __shfl_sync(FULL_MASK, incl, 31);
+      }
     }
     if (lane == 0) {
       const int kp = (cap > 0 && running > cap) ? cap : running;
