@@ -25,8 +25,10 @@ from .layer import (  # noqa: F401
     e4m3,
     e4m3_code,
     mx_quantize_rows,
+    mx_quantize_cols,
     ffn_fwd_rows_mx,
     ffn_bwd_rows_mx,
+    ffn_wgrad_rows_mx,
     HostSource,
     TorchSource,
 )

@@ -160,6 +160,31 @@ def mx_quantize_rows(v):
     return codes, scales, deq
 
 
+def mx_quantize_cols(v):
+    """MXFP8 of each column of v [rows, cols] in blocks of 32 consecutive rows from row 0;
+    a short last block is quantised as if zero-padded to 32 rows (zeros never raise the
+    block maximum).  Returns the dequantised float64 [rows, cols]: the weight-gradient
+    operands quantised along the tokens of one expert segment."""
+    v = _f64(v)
+    rows, cols = v.shape
+    if rows == 0:
+        return np.zeros((0, cols))
+    rp = -(-rows // 32) * 32
+    t = np.zeros((cols, rp))
+    t[:, :rows] = v.T
+    return np.ascontiguousarray(mx_quantize_rows(t)[2][:, :rows].T)
+
+
+def ffn_wgrad_rows_mx(xr, h, dyp, dab, d, f):
+    """The expert's weight gradients on MXFP8 operands quantised along its tokens:
+    dW1 = Q(dab)^T Q(xr), dW2 = Q(dyp)^T Q(h), each Q in 32-row blocks from the segment's
+    first row (mx_quantize_cols); float64 accumulation."""
+    if xr is None or xr.shape[0] == 0:
+        return np.zeros((2 * f, d)), np.zeros((d, f))
+    return ffn_wgrad_rows(mx_quantize_cols(xr), mx_quantize_cols(h), mx_quantize_cols(dyp),
+                          mx_quantize_cols(dab), d, f)
+
+
 def ffn_fwd_rows_mx(xr, W1e, W2e):
     """The expert FFN forward on MXFP8 operands: (ab, h, yp, h codes, h scales)."""
     lib = _load()
@@ -289,10 +314,12 @@ def layer_fwd(cfg, inp: dict, rnd: bool = True, r: dict | None = None, mx: bool 
     return out
 
 
-def layer_bwd(cfg, inp: dict, fwd: dict, rnd: bool = True, mx: bool = False) -> dict:
+def layer_bwd(cfg, inp: dict, fwd: dict, rnd: bool = True, mx: bool = False,
+              mx_wgrad: bool = False) -> dict:
     """Whole backward on the host given the forward's saved tensors and inp['dy'].
-    mx: the routed experts' data-gradient GEMMs on MXFP8 operands (ffn_bwd_rows_mx); the
-    weight gradients and the shared expert stay bf16."""
+    mx: the routed experts' data-gradient GEMMs on MXFP8 operands (ffn_bwd_rows_mx);
+    mx_wgrad: their weight gradients too, on operands quantised along each segment's tokens
+    (ffn_wgrad_rows_mx).  The shared expert stays bf16."""
     r = fwd["route"]
     off = r["offsets"]
     x = _f64(inp["x"]); dy = _f64(inp["dy"])
@@ -307,8 +334,8 @@ def layer_bwd(cfg, inp: dict, fwd: dict, rnd: bool = True, mx: bool = False) -> 
             dab[s:t], dxp[s:t], _, _ = ffn_bwd_rows_mx(dyp[s:t], fwd["ab"][s:t], W1[e], W2[e])
         else:
             dab[s:t], dxp[s:t] = ffn_bwd_rows(dyp[s:t], fwd["ab"][s:t], W1[e], W2[e], rnd)
-        dW1[e], dW2[e] = ffn_wgrad_rows(fwd["xp"][s:t], fwd["h"][s:t], dyp[s:t], dab[s:t],
-                                        cfg.d, cfg.f)
+        wg = ffn_wgrad_rows_mx if mx_wgrad else ffn_wgrad_rows
+        dW1[e], dW2[e] = wg(fwd["xp"][s:t], fwd["h"][s:t], dyp[s:t], dab[s:t], cfg.d, cfg.f)
     out = dict(dyp=dyp, dlogits=dlogits, dab=dab, dxp=dxp)
     dxs = None
     if cfg.fs:
@@ -370,7 +397,7 @@ class TorchSource:
 
 
 def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True,
-                  mx: bool = False, mx_bwd: bool = False) -> dict:
+                  mx: bool = False, mx_bwd: bool = False, mx_wgrad: bool = False) -> dict:
     """The exact layer restricted to a subset of outputs (for configurations too big
     to evaluate in full on the host):
 
@@ -383,9 +410,10 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     Every value is computed from the inputs alone through the same steps as the full
     layer; only the rows/columns that the requested outputs depend on are evaluated.
     mx: the routed experts' forward on MXFP8 operands (as layer_fwd(mx=True)); mx_bwd:
-    their data-gradient GEMMs too (as layer_bwd(mx=True)).  The restriction stays exact
-    because every MX block lies inside one token row or one row of a weight (or of its
-    transpose)."""
+    their data-gradient GEMMs too (as layer_bwd(mx=True)); mx_wgrad: their weight
+    gradients too (as layer_bwd(mx_wgrad=True)).  The restriction stays exact because
+    every MX block lies inside one token row, one row of a weight (or of its transpose), or
+    one column of an expert segment's rows."""
     r = route(cfg, src.logits)
     k, d, f = cfg.k, cfg.d, cfg.f
     toks = np.unique(np.asarray(tokens, np.int64))
@@ -446,7 +474,8 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
             dyp_e = src.rows("dy", tk) * w[:, None]
             if rnd:
                 dyp_e = bf16(dyp_e)
-            g1, g2 = _wgrad_cols(xr, dyp_e, W1e, W2e, wcols, wrows, rnd, mx=mx, mx_bwd=mx_bwd)
+            g1, g2 = _wgrad_cols(xr, dyp_e, W1e, W2e, wcols, wrows, rnd, mx=mx, mx_bwd=mx_bwd,
+                                 mx_wgrad=mx_wgrad)
             dW1[e] = g1; dW2[e] = g2
         out["dW1"] = dW1; out["dW2"] = dW2
         out["wcols"] = wcols; out["wrows"] = wrows
@@ -457,7 +486,7 @@ def layer_sampled(cfg, src, tokens, experts=(), wcols=None, wrows=None, rnd=True
     return out
 
 
-def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False, mx_bwd=False):
+def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False, mx_bwd=False, mx_wgrad=False):
     """dW2[drows][:, cols] and dW1[[cols, f+cols]][:, drows] of one expert from all its rows,
     evaluating only the FFN columns `cols` (exact: a, b, h, dh, da, db of column c depend
     on column c alone).  Uses the oracle's row steps on the column-restricted weights.
@@ -483,8 +512,12 @@ def _wgrad_cols(xr, dyp, W1e, W2e, cols, drows, rnd, mx=False, mx_bwd=False):
     else:
         dab, _ = ffn_bwd_rows(dyp, ab, W1c, W2c, rnd)       # [da_cols | db_cols]
     m = len(cols)
-    dW2 = (dyp[:, drows].T @ h)                              # [len(drows), m]
-    dW1 = (dab.T @ xr[:, drows])                             # [2m, len(drows)]
+    if mx_wgrad:   # operands quantised per column along the segment's rows
+        dW2 = mx_quantize_cols(dyp[:, drows]).T @ mx_quantize_cols(h)
+        dW1 = mx_quantize_cols(dab).T @ mx_quantize_cols(xr[:, drows])
+    else:
+        dW2 = (dyp[:, drows].T @ h)                          # [len(drows), m]
+        dW1 = (dab.T @ xr[:, drows])                         # [2m, len(drows)]
     if rnd:
         dW2 = bf16(dW2); dW1 = bf16(dW1)
     return dW1.reshape(2, m, len(drows)), dW2

@@ -8,6 +8,10 @@
   (multiplying a block by 2^j shifts its scale code by j and keeps its element codes).
 * The MXFP8 FFN forward: equal to the plain FFN when every operand is exactly
   representable; otherwise equal to a torch float64 composition of the pinned quantiser.
+* The MXFP8 weight gradients: the column quantiser (32-row blocks from a segment's first
+  row) on the hand-worked blocks laid down a column, by brute force on a segment with a
+  short tail, block locality, exactness on representable operands, and the composition
+  Q(dab)^T Q(xp), Q(dyp)^T Q(h).
 CPU only."""
 
 import json
@@ -216,3 +220,109 @@ def test_mx_bwd_matches_torch_composition():
     np.testing.assert_allclose(dab, dab_t.numpy(), rtol=2 ** -7, atol=1e-12)
     dx_t = bf(q(dab) @ q(W1.T).T)                          # contraction over 2f
     np.testing.assert_allclose(dx, dx_t.numpy(), rtol=2 ** -7, atol=1e-10)
+
+
+# --------------------------------------------------------------- weight gradients (along tokens)
+def test_hand_worked_blocks_down_a_column():
+    """The column quantiser on the hand-worked blocks laid down a column: the same scale
+    codes and element values as the blocks worked along a row."""
+    g = json.load(open(os.path.join(HERE, "golden", "mxfp8_blocks_hand_worked.json")))
+    nb = len(g["blocks"])
+    col = np.zeros((32 * nb, 3))
+    for i, b in enumerate(g["blocks"]):
+        for k, x in b["values"].items():
+            col[32 * i + int(k), 1] = x
+    deq = oracle.mx_quantize_cols(col)
+    for i, b in enumerate(g["blocks"]):
+        X = b["scale"] - 127
+        want = np.zeros(32)
+        for k, c in b["codes"].items():
+            s, e, m = c >> 7, (c >> 3) & 15, c & 7
+            mag = (1 + m / 8) * 2.0 ** (e - 7) if e else m / 8 * 2.0 ** -6
+            want[int(k)] = (-mag if s else mag) * 2.0 ** X
+        np.testing.assert_array_equal(deq[32 * i:32 * i + 32, 1], want)
+    assert (deq[:, 0] == 0).all() and (deq[:, 2] == 0).all()
+
+
+def test_column_blocks_start_at_row_zero_and_short_tail_ignores_padding():
+    """Blocks are rows [32j, 32j + 32) of the segment; the short last block is quantised
+    from its own values only (as if zero-padded); a change in one block leaves every other
+    block alone."""
+    rng = np.random.default_rng(21)
+    n = 70                                     # 32 + 32 + 6
+    v = rng.standard_normal((n, 5)) * np.exp(rng.uniform(-4, 4, (1, 5)))
+    deq = oracle.mx_quantize_cols(v)
+    # each block by brute force: the scale rule and E4M3 rounding element by element
+    for c in range(5):
+        for r0 in (0, 32, 64):
+            blk = v[r0:min(r0 + 32, n), c]
+            amax = np.abs(blk).max()
+            X = max(-127, min(127, int(np.frexp(amax)[1]) - 1 - 8))
+            want = np.array([oracle.e4m3(x / 2.0 ** X) for x in blk]) * 2.0 ** X
+            np.testing.assert_array_equal(deq[r0:r0 + len(blk), c], want)
+    v2 = v.copy()
+    v2[40, 2] *= 1000.0                        # only rows 32..63 of column 2 may change
+    d2 = oracle.mx_quantize_cols(v2)
+    changed = d2 != deq
+    assert changed[32:64, 2].any()
+    changed[32:64, 2] = False
+    assert not changed.any()
+
+
+def test_mx_wgrad_equals_plain_on_representable_operands():
+    """With each operand exactly representable in 32-row column blocks, the MXFP8 weight
+    gradients equal the plain ones exactly."""
+    rng = np.random.default_rng(31)
+    n, d, f = 64, 64, 32
+    def col_repr(shape):
+        return np.ascontiguousarray(exactly_representable(shape[::-1], rng).T)
+    xr, h, dyp, dab = col_repr((n, d)), col_repr((n, f)), col_repr((n, d)), col_repr((n, 2 * f))
+    for m in (xr, h, dyp, dab):
+        np.testing.assert_array_equal(oracle.mx_quantize_cols(m), m)
+    w1, w2 = oracle.ffn_wgrad_rows_mx(xr, h, dyp, dab, d, f)
+    p1, p2 = oracle.layer.ffn_wgrad_rows(xr, h, dyp, dab, d, f)
+    np.testing.assert_array_equal(w1, p1)
+    np.testing.assert_array_equal(w2, p2)
+
+
+def test_mx_wgrad_matches_numpy_composition():
+    """dW1 = Q(dab)^T Q(xp) and dW2 = Q(dyp)^T Q(h), Q the column quantiser, summed over an
+    uneven segment (45 rows: one full block and a 13-row tail)."""
+    n, d, f = 45, 64, 32
+    xr = bf16_bits_to_f64(gen_rows_bf16("mxw_x", n, d))
+    h = bf16_bits_to_f64(gen_rows_bf16("mxw_h", n, f))
+    dyp = bf16_bits_to_f64(gen_rows_bf16("mxw_dy", n, d))
+    dab = bf16_bits_to_f64(gen_rows_bf16("mxw_dab", n, 2 * f))
+    w1, w2 = oracle.ffn_wgrad_rows_mx(xr, h, dyp, dab, d, f)
+    Q = oracle.mx_quantize_cols
+    np.testing.assert_allclose(w1, Q(dab).T @ Q(xr), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(w2, Q(dyp).T @ Q(h), rtol=1e-12, atol=1e-14)
+    # the quantisation is applied: differs from the plain gradients
+    p1, _ = oracle.layer.ffn_wgrad_rows(xr, h, dyp, dab, d, f)
+    assert (w1 != p1).any()
+    # an empty segment gives zero gradients
+    z1, z2 = oracle.ffn_wgrad_rows_mx(xr[:0], h[:0], dyp[:0], dab[:0], d, f)
+    assert not z1.any() and not z2.any()
+
+
+def test_sampled_mx_wgrad_matches_full():
+    from workloads import MoEConfig, gen_inputs_host
+    cfg = MoEConfig("mxw_sample", T=96, d=128, E=4, k=2, f=128, cap_factor=0.8, zipf_s=1.1)
+    inp = gen_inputs_host(cfg)
+    f = oracle.layer_fwd(cfg, inp, mx=True)
+    b = oracle.layer_bwd(cfg, inp, f, mx=True, mx_wgrad=True)
+    wcols = np.array([0, 7, 63, 100])
+    wrows = np.array([1, 2, 63, 127])
+    experts = [0, 3]
+    s = oracle.layer_sampled(cfg, oracle.HostSource(inp), [0, 5], experts, wcols, wrows,
+                             mx=True, mx_bwd=True, mx_wgrad=True)
+    one_ulp = 2.0 ** -7
+    for e in experts:
+        np.testing.assert_allclose(s["dW1"][e][0], b["dW1"][e][np.ix_(wcols, wrows)],
+                                   rtol=one_ulp, atol=1e-30)
+        np.testing.assert_allclose(s["dW1"][e][1], b["dW1"][e][np.ix_(wcols + cfg.f, wrows)],
+                                   rtol=one_ulp, atol=1e-30)
+        np.testing.assert_allclose(s["dW2"][e], b["dW2"][e][np.ix_(wrows, wcols)],
+                                   rtol=one_ulp, atol=1e-30)
+    b0 = oracle.layer_bwd(cfg, inp, f, mx=True)
+    assert (b0["dW2"] != b["dW2"]).any()
