@@ -311,7 +311,7 @@ def bench_ours(args, world, rank, local):
     cfg = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity,
                           select_bias=bias_t, drop_negative=c.drop_negative,
                           recompute=c.recompute, drop_by_score=c.drop_by_score,
-                          mxfp8=args.mxfp8)
+                          mxfp8=(2 if args.mx_wgrad else 1) if args.mxfp8 else 0)
     g = gen_inputs_device(c, dev, seed=rank)
     R = c.T * c.k
     ws_b, ctx_b = tde.moe_workspace_size(cfg)
@@ -423,7 +423,8 @@ def bench_ours(args, world, rank, local):
         tde.moe_combine_bwd(cfg, g["dy"], v["yp"], g["logits"], v["topk_idx"], v["topk_w"],
                             v["dest_row"], dyp, dl, ws)
         mark()
-        if args.mxfp8:   # the data-gradient GEMMs on MXFP8 operands, weight gradients bf16
+        if args.mxfp8:   # the data-gradient GEMMs on MXFP8 operands (with --mx-wgrad the
+            #              weight gradients too, else bf16)
             tde.moe_grouped_ffn_bwd_mx(cfg, dyp, v["xp"], v["offsets"], wq, v["ab"], v["h"], dab,
                                        dxp, dW1, dW2, ws)
         elif args.fuse_gather:
@@ -452,6 +453,9 @@ def bench_ours(args, world, rank, local):
         launches_per_step += 2                          # score scatter + select
     if args.mxfp8:
         launches_per_step += 1                          # dyp quantised for the data gradients
+    if args.mxfp8 and args.mx_wgrad:
+        launches_per_step += 2                          # 4 along-token quantisations replace
+        #                                                 the 2 per-segment map preparations
     if args.mxfp8 and not args.mx_cache_weights:
         launches_per_step += 4                          # the four weight-quantisation kernels
     for _ in range(args.warmup):
@@ -584,13 +588,15 @@ def bench_ours(args, world, rank, local):
         # the forward (at that rate) and everything else (bf16); the peak reported is the
         # flop rate that ideal time stands for.
         # routed FC1 + FC2 (6 d f per row) and the two data gradients (6 d f per row) run at
-        # the E4M3 rate; the weight gradients and the shared expert at the bf16 rate
-        fwd_mx = 12.0 * c.d * c.f * rows_kept
+        # the E4M3 rate, with --mx-wgrad the two weight gradients (6 d f per row) too; the
+        # rest (bf16 weight gradients, the shared expert) at the bf16 rate
+        fwd_mx = (18.0 if args.mx_wgrad else 12.0) * c.d * c.f * rows_kept
         ideal_s = fwd_mx / (2 * peak * 1e12) + (flops - fwd_mx) / (peak * 1e12)
         ideal_b = fwd_mx / (2 * burst * 1e12) + (flops - fwd_mx) / (burst * 1e12)
         # (the ffn_fwd phase also holds the bf16 shared expert when there is one)
         mx_line = {"ffn_fwd_tflops": None if c.fs else
-                   round(fwd_mx / 2 / (phase_ms["ffn_fwd"] * 1e-3) / 1e12, 1),
+                   round(6.0 * c.d * c.f * rows_kept / (phase_ms["ffn_fwd"] * 1e-3) / 1e12,
+                         1),
                    "fp8_peak_sustained": 2 * peak, "fp8_peak_burst": 2 * burst,
                    "weight_quant_ms": round(phase_ms["mx_weight_quant"], 4),
                    "note": ("weights quantised once before timing (cached)"
@@ -643,7 +649,8 @@ def bench_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "mxfp8 (routed fwd + dgrad) + bf16" if args.mxfp8 else "bf16",
+        "dtype": (("mxfp8 (routed fwd + dgrad + wgrad) + bf16 shared" if args.mx_wgrad else
+                   "mxfp8 (routed fwd + dgrad) + bf16") if args.mxfp8 else "bf16"),
         "data": "synthetic (seeded N(0,1) tokens/logits, N(0,0.02) bf16 weights)",
         "config": {"workload": f"{c.name}: T={c.T} d={c.d} E={c.E} top-{c.k} "
                                f"{c.gate} f={c.f}" + (f" shared fs={c.fs}" if c.fs else "")
@@ -654,6 +661,7 @@ def bench_ours(args, world, rank, local):
                                + (" drop-by-score" if c.drop_by_score else "")
                                + (" recompute-FC1" if c.recompute else "")
                                + (" MXFP8-forward" if args.mxfp8 else "")
+                               + (" MXFP8-wgrad" if args.mxfp8 and args.mx_wgrad else "")
                                + (" cached-weight-quant" if args.mxfp8 and args.mx_cache_weights
                                   else ""),
                    "tokens_per_step": c.T, "rows_kept": rows_kept,
@@ -681,7 +689,8 @@ def bench_ours(args, world, rank, local):
                      "peak_source": (f"bf16_tflops_sustained of {peak_src} (kernel timed "
                                      f"inside a continuous step loop); burst {burst}"
                                      if not args.mxfp8 else
-                                     f"flop-weighted: routed FC1, FC2 and data gradients at "
+                                     f"flop-weighted: routed FC1, FC2, data gradients"
+                                     f"{' and weight gradients' if args.mx_wgrad else ''} at "
                                      f"2x, the rest at 1x bf16_tflops_sustained of "
                                      f"{peak_src}; burst {burst}"),
                      "traffic": GEMM_TRAFFIC_PER_LAUNCH.get(c.name),
@@ -779,6 +788,9 @@ def main():
     ap.add_argument("--mxfp8", action="store_true",
                     help="routed experts' forward and data-gradient GEMMs on MXFP8 operands "
                          "(weight gradients bf16)")
+    ap.add_argument("--mx-wgrad", action="store_true",
+                    help="with --mxfp8: the weight gradients on MXFP8 operands too, quantised "
+                         "along each expert segment's tokens")
     ap.add_argument("--mx-cache-weights", action="store_true",
                     help="with --mxfp8: quantise the weights once, outside the timed steps")
     ap.add_argument("--drop-by-score", action="store_true",

@@ -110,7 +110,14 @@ typedef struct {
                                  (moe_layer_fwd_mx), and with moe_layer_bwd_mx the data-
                                  gradient GEMMs of the backward too; needs d and ffn
                                  multiples of 128 and more ws for the quantised
-                                 activations.  The weight gradients stay bf16.            */
+                                 activations.  The weight gradients stay bf16.
+                                 2: as 1, and the weight gradients too: their operands
+                                 (dyp, h, dab, xp) are quantised along each segment's
+                                 tokens, in 32-row blocks from the segment's first row
+                                 (the Primus MoE blog, FP8 section: permuted tokens padded
+                                 to the quantisation block boundary); needs about
+                                 (2d + 3ffn) * (T*k + 128*E) * 33/32 more bytes of ws.
+                                 0, 1, 2 only.                                            */
 } moe_config_t;
 
 /* Index of each saved tensor inside the forward context `ctx` (see moe_ctx_offsets). */
@@ -365,19 +372,22 @@ moe_status_t moe_layer_fwd_mx(const moe_config_t *cfg, const float *logits, cons
                               const void *wq, const void *W1s, const void *W2s, void *y,
                               void *ctx, void *ws, void *stream);
 
-/* B2..B5 with the data-gradient GEMMs on MXFP8 operands (cfg->mxfp8 = 1): dyp is
+/* B2..B5 with the data-gradient GEMMs on MXFP8 operands (cfg->mxfp8 = 1 or 2): dyp is
  * quantised along d; dh = deq(MX(dyp)) deq(W2^T codes), the SwiGLU backward gives dab
- * (bf16 out) which is quantised along 2f; dxp = bf16(deq(MX(dab)) deq(W1^T codes)).  The
- * weight gradients dW1, dW2 are computed from the bf16 xp, h, dyp and dab as in
- * moe_grouped_ffn_bwd.  wq: the blob of moe_mx_quantize_weights.  The quantised dyp and
- * dab live in ws. */
+ * (bf16 out) which is quantised along 2f; dxp = bf16(deq(MX(dab)) deq(W1^T codes)).  With
+ * cfg->mxfp8 = 1 the weight gradients dW1, dW2 are computed from the bf16 xp, h, dyp and
+ * dab as in moe_grouped_ffn_bwd; with 2, dW2[e] = bf16(deq(Q(dyp_e))^T deq(Q(h_e))) and
+ * dW1[e] = bf16(deq(Q(dab_e))^T deq(Q(xp_e))), Q quantising each column of the segment's
+ * rows in 32-row blocks from its first row (an expert without rows gets zeros).
+ * wq: the blob of moe_mx_quantize_weights.  The quantised operands live in ws. */
 moe_status_t moe_grouped_ffn_bwd_mx(const moe_config_t *cfg, const void *dyp, const void *xp,
                                     const int32_t *offsets, const void *wq, const void *ab,
                                     const void *h, void *dab, void *dxp, void *dW1, void *dW2,
                                     void *ws, void *stream);
 
-/* Whole backward with the routed experts' data gradients in MXFP8 (cfg->mxfp8 = 1); as
- * moe_layer_bwd otherwise (the shared expert and the weight gradients stay bf16). */
+/* Whole backward with the routed experts' data gradients in MXFP8 (cfg->mxfp8 = 1; with 2
+ * their weight gradients too, as in moe_grouped_ffn_bwd_mx); as moe_layer_bwd otherwise
+ * (the shared expert stays bf16). */
 moe_status_t moe_layer_bwd_mx(const moe_config_t *cfg, const void *ctx, const float *logits,
                               const void *x, const void *dy, const void *wq, const void *W1s,
                               const void *W2s, void *dx, void *dW1, void *dW2, void *dW1s,

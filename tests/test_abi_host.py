@@ -77,6 +77,14 @@ def test_workspace_and_ctx_layout(L):
         plain = tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale,
                                 c.capacity or 1)
         assert tde.moe_workspace_size(bs)[0] - tde.moe_workspace_size(plain)[0] >= R * 4
+        # MXFP8 weight gradients: the four along-token quantised operands (codes + scales)
+        if c.d % 128 == 0 and c.f % 128 == 0:
+            mx = [tde.moe_workspace_size(tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs,
+                                                         c.gate, c.route_scale, c.capacity,
+                                                         mxfp8=m))[0] for m in (0, 1, 2)]
+            kcap = 128 * ((R + 127) // 128 + c.E)
+            assert mx[1] > mx[0]
+            assert mx[2] - mx[1] >= (2 * c.d + 3 * c.f) * kcap
 
 
 @pytest.mark.parametrize("bad,status", [
@@ -92,6 +100,9 @@ def test_workspace_and_ctx_layout(L):
     (dict(recompute=-1), 1),
     (dict(select_bias=2), 1),      # not 4-byte aligned
     (dict(drop_by_score=3), 1),
+    (dict(mxfp8=3), 1),
+    (dict(mxfp8=-1), 1),
+    (dict(mxfp8=2, d=192), 2),     # MXFP8 needs d, ffn multiples of 128
 ])
 def test_invalid_configs_rejected_before_launch(L, bad, status):
     base = dict(T=64, d=128, E=8, k=2, ffn=128, ffn_shared=0, gate=0, route_scale=1.0,

@@ -102,11 +102,13 @@ def lib() -> ctypes.CDLL:
 def make_config(T, d, E, k, ffn, ffn_shared=0, gate="softmax", route_scale=1.0,
                 capacity=0, select_bias=None, drop_negative=False,
                 recompute=False, drop_by_score=False, mxfp8=False) -> MoEConfigC:
-    """select_bias: a float32 device tensor [E] (kept alive by the returned config) or None."""
+    """select_bias: a float32 device tensor [E] (kept alive by the returned config) or None.
+    mxfp8: 0 / False (bf16), 1 / True (routed forward and data gradients in MXFP8) or 2 (and
+    the weight gradients)."""
     cfg = MoEConfigC(int(T), int(d), int(E), int(k), int(ffn), int(ffn_shared),
                      GATES[gate] if isinstance(gate, str) else int(gate), float(route_scale),
                      int(capacity), _p(select_bias), int(bool(drop_negative)),
-                     int(bool(recompute)), int(bool(drop_by_score)), int(bool(mxfp8)))
+                     int(bool(recompute)), int(bool(drop_by_score)), int(mxfp8))
     cfg._keep = select_bias
     return cfg
 

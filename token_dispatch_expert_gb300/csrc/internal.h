@@ -167,4 +167,36 @@ struct MxDgradArgs {
 };
 cudaError_t launch_mx_ffn_dgrad(const MxDgradArgs& a, cudaStream_t st);
 
+// MXFP8 weight gradients.  Their contraction runs over an expert segment's rows, so each
+// operand is quantised along the rows: the segment is cut into K blocks of 128 rows (the
+// last zero-padded) and expert e's blocks follow e-1's (block kb0_e + i, kb0_e the sum of
+// ceil(n_e' / 128) over e' < e).  Codes go transposed, [C][128 * kb_cap] (K-major along
+// the rows); scales as atoms for the GEMM role: the M operand [C/128][kb_cap][512], the N
+// operand [ceil(C/256)][kb_cap][2][512].  kb_cap = ceil(rows_cap / 128) + E.
+inline int64_t mx_tok_kb_cap(int64_t rows_cap, int E) { return (rows_cap + 127) / 128 + E; }
+inline size_t mx_tok_codes_bytes(int64_t rows_cap, int E, int C) {
+  return static_cast<size_t>(C) * 128 * static_cast<size_t>(mx_tok_kb_cap(rows_cap, E));
+}
+inline size_t mx_tok_scale_bytes(int64_t rows_cap, int E, int C, bool role_n) {
+  const size_t kb = static_cast<size_t>(mx_tok_kb_cap(rows_cap, E));
+  return role_n ? static_cast<size_t>((C + 255) / 256) * kb * 1024
+                : static_cast<size_t>(C / 128) * kb * 512;
+}
+cudaError_t launch_mx_quant_tok(const void* X, const int32_t* offsets, int E, int64_t rows_cap,
+                                int C, bool role_n, uint8_t* codes, uint8_t* scales, int* err,
+                                cudaStream_t st);
+struct MxWgradArgs {
+  int E;
+  int64_t rows_cap;
+  const int32_t* offsets;
+  int M, N;              // dW [E][M][N] = A^T B over each segment's rows
+  const uint8_t* aq;     // [M][128 kb_cap] codes, role M
+  const uint8_t* a_sf;
+  const uint8_t* bq;     // [N][128 kb_cap] codes, role N
+  const uint8_t* b_sf;
+  void* dW;              // [E][M][N] bf16 out
+  int* err;
+};
+cudaError_t launch_mx_wgrad(const MxWgradArgs& a, cudaStream_t st);
+
 }  // namespace moe

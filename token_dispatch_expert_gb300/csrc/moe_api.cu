@@ -26,7 +26,7 @@ moe_status_t validate(const moe_config_t* c) {
   if (!std::isfinite(c->route_scale)) return MOE_ERR_INVALID_ARG;
   if ((c->drop_negative != 0 && c->drop_negative != 1) ||
       (c->recompute != 0 && c->recompute != 1) ||
-      (c->drop_by_score != 0 && c->drop_by_score != 1) || (c->mxfp8 != 0 && c->mxfp8 != 1))
+      (c->drop_by_score != 0 && c->drop_by_score != 1) || (c->mxfp8 < 0 || c->mxfp8 > 2))
     return MOE_ERR_INVALID_ARG;
   if (c->select_bias && (reinterpret_cast<uintptr_t>(c->select_bias) & 3u))
     return MOE_ERR_INVALID_ARG;
@@ -92,7 +92,7 @@ CtxLayout ctx_layout(const moe_config_t* c) {
 
 struct WsLayout {
   size_t route, maps, dyp, dab, dxp, dab_s, dx_s, ab, h, ab_s, h_s, xq, x_sf, hq, h_sf, dyq,
-      dy_sf, dabq, dab_sf, total;
+      dy_sf, dabq, dab_sf, dyT, dyT_sf, hT, hT_sf, dabT, dabT_sf, xpT, xpT_sf, total;
 };
 
 WsLayout ws_layout(const moe_config_t* c) {
@@ -125,6 +125,19 @@ WsLayout ws_layout(const moe_config_t* c) {
   L.dy_sf = o; o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, c->d) : 0);
   L.dabq = o;  o += align_up(mx ? R * 2 * f : 0);
   L.dab_sf = o; o += align_up(mx ? mx_act_scale_bytes(c->T * c->k, c->E, 2 * c->ffn) : 0);
+  // ... and with mxfp8 = 2 the weight gradients' operands, quantised along the tokens:
+  // dW2 = dyp^T h (dyp the M operand, h the N operand), dW1 = dab^T xp
+  const bool mw = c->mxfp8 == 2;
+  const int64_t Rc = c->T * c->k;
+  const int E = c->E, D = c->d, F = c->ffn;
+  L.dyT = o;     o += align_up(mw ? mx_tok_codes_bytes(Rc, E, D) : 0);
+  L.dyT_sf = o;  o += align_up(mw ? mx_tok_scale_bytes(Rc, E, D, false) : 0);
+  L.hT = o;      o += align_up(mw ? mx_tok_codes_bytes(Rc, E, F) : 0);
+  L.hT_sf = o;   o += align_up(mw ? mx_tok_scale_bytes(Rc, E, F, true) : 0);
+  L.dabT = o;    o += align_up(mw ? mx_tok_codes_bytes(Rc, E, 2 * F) : 0);
+  L.dabT_sf = o; o += align_up(mw ? mx_tok_scale_bytes(Rc, E, 2 * F, false) : 0);
+  L.xpT = o;     o += align_up(mw ? mx_tok_codes_bytes(Rc, E, D) : 0);
+  L.xpT_sf = o;  o += align_up(mw ? mx_tok_scale_bytes(Rc, E, D, true) : 0);
   L.total = o;
   return L;
 }
@@ -570,7 +583,8 @@ moe_status_t moe_layer_fwd_mx(const moe_config_t* cfg, const float* logits, cons
 
 namespace {
 // The MXFP8 backward of the routed experts' FFN: quantise dyp, DGRAD2 and DGRAD1 on MXFP8
-// operands, then the two bf16 weight gradients.
+// operands, then the two weight gradients: bf16 (mxfp8 = 1), or (mxfp8 = 2) on operands
+// quantised along each segment's tokens.
 moe_status_t ffn_bwd_mx(const moe_config_t* c, const void* dyp, const void* xp,
                         const int32_t* offsets, const void* wq, const void* ab, const void* h,
                         void* dab, void* dxp, void* dW1, void* dW2, void* ws, cudaStream_t st) {
@@ -595,6 +609,40 @@ moe_status_t ffn_bwd_mx(const moe_config_t* c, const void* dyp, const void* xp,
   a.dxp = dxp;
   a.err = err;
   MOE_TRY(launch_mx_ffn_dgrad(a, st));
+  if (c->mxfp8 == 2) {
+    auto quant = [&](const void* X, int C, bool role_n, size_t q, size_t sf) {
+      return launch_mx_quant_tok(X, offsets, c->E, R, C, role_n, at<uint8_t>(ws, q),
+                                 at<uint8_t>(ws, sf), err, st);
+    };
+    MxWgradArgs g{};
+    g.E = c->E;
+    g.rows_cap = R;
+    g.offsets = offsets;
+    g.err = err;
+    // dW2 [E][d][f] = dyp^T h
+    MOE_TRY(quant(dyp, c->d, false, W.dyT, W.dyT_sf));
+    MOE_TRY(quant(h, c->ffn, true, W.hT, W.hT_sf));
+    g.M = c->d;
+    g.N = c->ffn;
+    g.aq = at<uint8_t>(ws, W.dyT);
+    g.a_sf = at<uint8_t>(ws, W.dyT_sf);
+    g.bq = at<uint8_t>(ws, W.hT);
+    g.b_sf = at<uint8_t>(ws, W.hT_sf);
+    g.dW = dW2;
+    MOE_TRY(launch_mx_wgrad(g, st));
+    // dW1 [E][2f][d] = dab^T xp
+    MOE_TRY(quant(dab, 2 * c->ffn, false, W.dabT, W.dabT_sf));
+    MOE_TRY(quant(xp, c->d, true, W.xpT, W.xpT_sf));
+    g.M = 2 * c->ffn;
+    g.N = c->d;
+    g.aq = at<uint8_t>(ws, W.dabT);
+    g.a_sf = at<uint8_t>(ws, W.dabT_sf);
+    g.bq = at<uint8_t>(ws, W.xpT);
+    g.b_sf = at<uint8_t>(ws, W.xpT_sf);
+    g.dW = dW1;
+    MOE_TRY(launch_mx_wgrad(g, st));
+    return MOE_OK;
+  }
   void* maps = at<uint8_t>(ws, W.maps);
   GroupedGemmArgs w2 = gemm_args(GEMM_WGRAD, c, offsets, 0, c->d, c->ffn, dyp, h, dW2, nullptr,
                                  nullptr, err);

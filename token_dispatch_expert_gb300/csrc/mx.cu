@@ -270,6 +270,86 @@ mx_weight_quant_t_kernel(const __nv_bfloat16* __restrict__ W, int Rk, int C,
   atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
 }
 
+// Along-token quantisation for the weight gradients: X [rows_cap][C] bf16 holds the expert
+// segments; expert e's rows form K blocks kb0_e .. kb0_e + ceil(n_e / 128) - 1 of 128 rows
+// (the last zero-padded).  For each column and each 32-row block: E4M3 codes into
+// xtq[c][128 kb + 32 j ..] and the E8M0 scale into the atom of the column's GEMM role (M
+// operand: atom (c / 128) kb_cap + kb; N operand: ((c / 256) kb_cap + kb) 2 + (c / 128) % 2).
+// One CTA per (64 columns, K block): the 128 x 64 tile goes through shared memory.
+constexpr int KQ_COLS = 64;
+
+__global__ void __launch_bounds__(256)
+mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ offsets,
+                    int E, long long rows_cap, int C, int kb_cap, int role_n,
+                    uint8_t* __restrict__ xtq, uint8_t* __restrict__ atoms, int* err) {
+  __shared__ __nv_bfloat16 tile[128][KQ_COLS + 2];   // +2: stagger the banks
+  __shared__ int s_kb0[MX_MAX_G + 1];
+  __shared__ int s_wsum[8];
+  __shared__ int s_bad;
+  const int kb = blockIdx.y, c0 = blockIdx.x * KQ_COLS;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  // K blocks per expert and their exclusive prefix (E <= 256: one expert per thread)
+  int nkb = 0;
+  if (tid < E) {
+    const int a = offsets[tid], b = offsets[tid + 1];
+    if (a < 0 || b < a || b > rows_cap) s_bad = 1;
+    nkb = b > a ? (b - a + 127) / 128 : 0;
+  }
+  const int incl = warp_incl_scan(nkb);
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += s_wsum[w];
+  if (tid < E) s_kb0[tid] = before + incl - nkb;
+  if (tid == E - 1) s_kb0[E] = before + incl;
+  __syncthreads();
+  if (s_bad) {
+    if (kb == 0 && blockIdx.x == 0 && tid == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
+    return;
+  }
+  if (kb >= s_kb0[E]) return;                      // past the last expert's blocks
+  int lo = 0, hi = E;                              // s_kb0[lo] <= kb < s_kb0[lo + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_kb0[mid] <= kb) lo = mid;
+    else hi = mid;
+  }
+  const int e = lo;
+  const long long r0 = static_cast<long long>(offsets[e]) + 128LL * (kb - s_kb0[e]);
+  const long long r_end = offsets[e + 1];
+  for (int i = tid; i < 128 * (KQ_COLS / 8); i += 256) {
+    const int r = i / (KQ_COLS / 8), c8 = (i % (KQ_COLS / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < r_end)
+      v = __ldg(reinterpret_cast<const uint4*>(X + (r0 + r) * C + c0 + c8));
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      tile[r][c8 + 2 * q] = h2[q].x;
+      tile[r][c8 + 2 * q + 1] = h2[q].y;
+    }
+  }
+  __syncthreads();
+  const int c = tid % KQ_COLS, j = tid / KQ_COLS;   // 4 blocks of 32 rows
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[32 * j + i][c]);
+  uint32_t code[8];
+  const uint32_t sc = mx_block(v, code);
+  const int col = c0 + c;
+  const long long kcap = 128LL * kb_cap;
+  uint4* dq = reinterpret_cast<uint4*>(xtq + static_cast<long long>(col) * kcap + 128LL * kb +
+                                       32 * j);
+  dq[0] = make_uint4(code[0], code[1], code[2], code[3]);
+  dq[1] = make_uint4(code[4], code[5], code[6], code[7]);
+  const long long atom =
+      role_n ? ((static_cast<long long>(col / 256) * kb_cap + kb) * 2 + ((col >> 7) & 1))
+             : (static_cast<long long>(col / 128) * kb_cap + kb);
+  atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
+}
+
 // ------------------------------------------------------------------ block-scaled GEMM
 // Per CTA and stage: A 128 rows x 128 B, B 128 rows (pair: this CTA's half of N) or 256
 // rows (one CTA) x 128 B, the A scale atom (512 B) and the B scale pair (1 KB).
@@ -299,6 +379,7 @@ struct MxCtl {
   int pad;
   int gstart[MX_MAX_G + 2];
   int tprefix[MX_MAX_G + 2];
+  int kbpre[MX_MAX_G + 2];    // WGRAD: each expert's first K block (exclusive prefix)
 };
 
 template <int PAIR>
@@ -323,6 +404,8 @@ struct MxParams {
   uint8_t* out_q;             // FC1: hq [rows_cap][f]   DGRAD2: dab codes [rows_cap][2f]
   uint8_t* out_sf;            // FC1: h's scales (K blocks f/128)  DGRAD2: dab's (2f/128)
   int* err;
+  // WGRAD: dW [G][wg_M][wg_N]; both operands along-token quantised (kb_cap K blocks)
+  int wg_M, wg_N, wg_m_tiles, kb_cap;
 };
 
 __device__ __forceinline__ int mx_ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -430,27 +513,42 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   for (int g = threadIdx.x; g <= p.G; g += MX_THREADS) ctl->gstart[g] = p.offsets[g];
   __syncthreads();
   if (warp == 0) {
+    // tiles per group: the segment's M tiles x the N tiles; WGRAD: the fixed weight-shaped
+    // grid of every expert (an empty one still writes its zero gradient), and its K blocks
+    auto tiles_of = [&](int a, int b) {
+      if (MODE == GEMM_WGRAD) return p.wg_m_tiles * p.num_n_tiles;
+      return b < a ? 0 : mx_ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
+    };
+    auto kblocks_of = [&](int a, int b) { return b > a ? mx_ceil_div(b - a, 128) : 0; };
     const int per = mx_ceil_div(p.G, 32);
-    int local = 0, bad = 0;
+    int local = 0, local_kb = 0, bad = 0;
     for (int i = 0; i < per; ++i) {
       const int g = lane * per + i;
       if (g < p.G) {
         const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
         if (b < a || a < 0 || b > p.rows_cap) bad = 1;
-        local += b < a ? 0 : mx_ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
+        local += tiles_of(a, b);
+        local_kb += kblocks_of(a, b);
       }
     }
     const int incl = warp_incl_scan(local);
-    int run = incl - local;
+    const int incl_kb = warp_incl_scan(local_kb);
+    int run = incl - local, run_kb = incl_kb - local_kb;
     for (int i = 0; i < per; ++i) {
       const int g = lane * per + i;
       if (g < p.G) {
         ctl->tprefix[g] = run;
+        ctl->kbpre[g] = run_kb;
         const int a = ctl->gstart[g], b = ctl->gstart[g + 1];
-        run += b < a ? 0 : mx_ceil_div(b - a, GE::TILE_M) * p.num_n_tiles;
+        run += tiles_of(a, b);
+        run_kb += kblocks_of(a, b);
       }
     }
-    if (lane == 31) ctl->tprefix[p.G] = incl;
+    if (lane == 31) {
+      ctl->tprefix[p.G] = incl;
+      ctl->kbpre[p.G] = incl_kb;
+    }
+    if (MODE == GEMM_WGRAD && incl_kb > p.kb_cap) bad = 1;
     if (ctl->gstart[0] != 0) bad = 1;
     bad = __any_sync(FULL_MASK, bad);
     if (lane == 0 && bad) {
@@ -483,7 +581,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     g = lo;
     const int local = tile - ctl->tprefix[g];
-    const int mtg = mx_ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], GE::TILE_M);
+    const int mtg = MODE == GEMM_WGRAD
+                        ? p.wg_m_tiles
+                        : mx_ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], GE::TILE_M);
     nt = local / mtg;
     mt = local - nt * mtg;
   };
@@ -493,10 +593,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    const int nkb = p.num_kb;
     for (int tile = unit; tile < total && ok; tile += num_units) {
       int g, mt, nt;
       map_tile(tile, g, mt, nt);
+      const int nkb = MODE == GEMM_WGRAD ? ctl->kbpre[g + 1] - ctl->kbpre[g] : p.num_kb;
       const int seg0 = ctl->gstart[g];
       const int lrow = mt * GE::TILE_M + 128 * rank;            // this CTA's first local row
       const int row0 = seg0 + lrow;
@@ -519,6 +619,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             else tma_load_2d(dst, m, full, x, y);
           };
           const int k0 = kb * MX_BK;
+          if (MODE == GEMM_WGRAD) {
+            // K runs along the expert's rows: its K blocks sit at kbpre[g] .. in both
+            // operands' along-token codes and scale atoms
+            const int kbg = ctl->kbpre[g] + kb;
+            const int arow = mt * GE::TILE_M + 128 * rank;
+            load(sa, &tmA, kbg * MX_BK, arow);
+            if (PAIR == 2) {
+              load(sb, &tmB, kbg * MX_BK, nt * 256 + rank * 128);
+            } else {
+              load(sb, &tmB, kbg * MX_BK, nt * 256);
+              load(sb + 128 * MX_BK, &tmB, kbg * MX_BK, nt * 256 + 128);
+            }
+            load(sa + GE::SFA_OFF, &tmSA, 0, ((arow >> 7) * p.kb_cap + kbg) * 2);
+            load(sa + GE::SFB_OFF, &tmSB, 0, (nt * p.kb_cap + kbg) * 4);
+          } else {
           load(sa, &tmA, k0, row0);
           if (MODE == GEMM_FC1_SWIGLU) {
             const int wrow = g * 2 * p.f + nt * 128;
@@ -539,6 +654,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           load(sa + GE::SFA_OFF, &tmSA, 0, (a_atom_blk * nkb + kb) * 2);
           load(sa + GE::SFB_OFF, &tmSB, 0, (b_atom + kb) * 4);
+          }
         }
         __syncwarp();
         if (++s == STAGES) {
@@ -562,8 +678,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t ph = 0;
       int it = 0;
       bool ok = true, issued_any = false;
-      const int nkb = p.num_kb;
       for (int tile = unit; tile < total && ok; tile += num_units, ++it) {
+        int nkb = p.num_kb;
+        if (MODE == GEMM_WGRAD) {
+          int g, mt, nt;
+          map_tile(tile, g, mt, nt);
+          nkb = ctl->kbpre[g + 1] - ctl->kbpre[g];
+        }
         if (!mx_warp_wait(smem_u32(&ctl->tempty), (it & 1) ^ 1u, abort_flag, p.err,
                           MX_WAIT_BUDGET)) {
           ok = false;
@@ -604,8 +725,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (!ok) break;
         if (lane == 0) {
-          if (PAIR == 2) tc_commit_pair_mc(smem_u32(&ctl->tfull), 0x3);
-          else tc_commit(smem_u32(&ctl->tfull));
+          const uint32_t tf = smem_u32(&ctl->tfull);
+          if (nkb > 0) {
+            if (PAIR == 2) tc_commit_pair_mc(tf, 0x3);
+            else tc_commit(tf);
+          } else {   // an expert without rows (WGRAD): nothing to wait for
+            mbar_arrive(tf);
+            if (PAIR == 2) mbar_arrive_remote(mapa_shared(tf, 1));
+          }
         }
         __syncwarp();
       }
@@ -631,8 +758,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       map_tile(tile, g, mt, nt);
       const int seg0 = ctl->gstart[g];
       const int lrow = mt * GE::TILE_M + r_in_tile;
-      const long long prow = static_cast<long long>(seg0) + lrow;
-      const bool valid = prow < ctl->gstart[g + 1];
+      // the output row: the segment's row, or WGRAD's row lrow of expert g's dW
+      const long long prow = MODE == GEMM_WGRAD
+                                 ? static_cast<long long>(g) * p.wg_M + lrow
+                                 : static_cast<long long>(seg0) + lrow;
+      const bool valid =
+          MODE == GEMM_WGRAD ? lrow < p.wg_M : prow < ctl->gstart[g + 1];
+      // WGRAD: an expert without rows has no accumulator to read, its gradient is zero
+      const bool acc_zero = MODE == GEMM_WGRAD && ctl->kbpre[g + 1] == ctl->kbpre[g];
       // DGRAD2: the saved a, b of this row do not depend on the MMAs, so the first 32
       // columns are loaded before the accumulator is ready and each later chunk one chunk
       // ahead of its use (the epilogue was bound by these loads' latency)
@@ -658,11 +791,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tmem_ld32(taddr + 64 * hh + 32, acc + 32);
         tmem_ld32(taddr + 128 + 64 * hh, acc + 64);
         tmem_ld32(taddr + 128 + 64 * hh + 32, acc + 96);
-      } else {
+      } else if (!acc_zero) {
         tmem_ld32(taddr + 128 * hh, acc);
         tmem_ld32(taddr + 128 * hh + 32, acc + 32);
         tmem_ld32(taddr + 128 * hh + 64, acc + 64);
         tmem_ld32(taddr + 128 * hh + 96, acc + 96);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0u;
       }
       tmem_ld_wait();
       tc_fence_before();
@@ -766,9 +902,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 static_cast<uint8_t>(sc);
           }
         }
-      } else {   // FC2, DGRAD1: plain bf16 rows
+      } else {   // FC2, DGRAD1, WGRAD: plain bf16 rows
         const int n0 = nt * 256 + 128 * hh;
-        if (n0 < p.n_out) {                    // d is a multiple of 128: all or nothing
+        if (n0 < p.n_out) {                    // n_out is a multiple of 128: all or nothing
           uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * p.n_out + n0);
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
@@ -938,6 +1074,8 @@ cudaError_t launch_mx_any(int mode, bool pair, const CUtensorMap& ta, const CUte
     MOE_MX_CASE(GEMM_FC2)
     MOE_MX_CASE(GEMM_DGRAD2_SWIGLU)
     MOE_MX_CASE(GEMM_DGRAD1)
+    case GEMM_WGRAD:
+      return launch_mx_mode<GEMM_WGRAD, 2>(ta, tb, tsa, tsb, kp, st);
     default:
       return cudaErrorInvalidValue;
   }
@@ -1056,6 +1194,44 @@ cudaError_t launch_mx_ffn_dgrad(const MxDgradArgs& a, cudaStream_t st) {
       !make_map_u8(&tsb, wb + L.w1tsf, 256, E * NT_d * KB_2f * 4, 256, 4, false))
     return cudaErrorInvalidValue;
   return launch_mx_any(GEMM_DGRAD1, pair, ta, tb, tsa, tsb, kp, st);
+}
+
+cudaError_t launch_mx_quant_tok(const void* X, const int32_t* offsets, int E, int64_t rows_cap,
+                                int C, bool role_n, uint8_t* codes, uint8_t* scales, int* err,
+                                cudaStream_t st) {
+  if (E < 1 || E > MX_MAX_G || C % 128) return cudaErrorInvalidValue;
+  const int64_t kb_cap = mx_tok_kb_cap(rows_cap, E);
+  mx_quant_tok_kernel<<<dim3(C / KQ_COLS, static_cast<unsigned>(kb_cap)), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(X), offsets, E, rows_cap, C, static_cast<int>(kb_cap),
+      role_n ? 1 : 0, codes, scales, err);
+  return cudaGetLastError();
+}
+
+// dW [E][M][N]: CTA pairs over 256 x 256 tiles of every expert's gradient, K = its rows
+cudaError_t launch_mx_wgrad(const MxWgradArgs& a, cudaStream_t st) {
+  if (a.E < 1 || a.E > MX_MAX_G || a.M % 128 || a.N % 128) return cudaErrorInvalidValue;
+  const int64_t kb_cap = mx_tok_kb_cap(a.rows_cap, a.E);
+  const uint64_t kcap = 128 * static_cast<uint64_t>(kb_cap);
+  const uint64_t M = static_cast<uint64_t>(a.M), N = static_cast<uint64_t>(a.N);
+  MxParams kp{};
+  kp.G = a.E;
+  kp.rows_cap = a.rows_cap;
+  kp.offsets = a.offsets;
+  kp.err = a.err;
+  kp.wg_M = a.M;
+  kp.wg_N = a.N;
+  kp.wg_m_tiles = (a.M + 255) / 256;
+  kp.kb_cap = static_cast<int>(kb_cap);
+  kp.num_n_tiles = (a.N + 255) / 256;
+  kp.n_out = a.N;
+  kp.out0 = static_cast<__nv_bfloat16*>(a.dW);
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!make_map_u8(&ta, a.aq, kcap, M, 128, 128, true) ||
+      !make_map_u8(&tb, a.bq, kcap, N, 128, 128, true) ||
+      !make_map_u8(&tsa, a.a_sf, 256, (M / 128) * kb_cap * 2, 256, 2, false) ||
+      !make_map_u8(&tsb, a.b_sf, 256, ((N + 255) / 256) * kb_cap * 4, 256, 4, false))
+    return cudaErrorInvalidValue;
+  return launch_mx_any(GEMM_WGRAD, true, ta, tb, tsa, tsb, kp, st);
 }
 
 }  // namespace moe
