@@ -286,7 +286,7 @@ mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restri
   __shared__ int s_kb0[MX_MAX_G + 1];
   __shared__ int s_wsum[8];
   __shared__ int s_bad;
-  const int kb = blockIdx.y, c0 = blockIdx.x * KQ_COLS;
+  const int c0 = blockIdx.x * KQ_COLS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_bad = 0;
   __syncthreads();
@@ -306,54 +306,77 @@ mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restri
   if (tid == E - 1) s_kb0[E] = before + incl;
   __syncthreads();
   if (s_bad) {
-    if (kb == 0 && blockIdx.x == 0 && tid == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
+    if (blockIdx.y == 0 && blockIdx.x == 0 && tid == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
     return;
   }
-  if (kb >= s_kb0[E]) return;                      // past the last expert's blocks
-  int lo = 0, hi = E;                              // s_kb0[lo] <= kb < s_kb0[lo + 1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_kb0[mid] <= kb) lo = mid;
-    else hi = mid;
-  }
-  const int e = lo;
-  const long long r0 = static_cast<long long>(offsets[e]) + 128LL * (kb - s_kb0[e]);
-  const long long r_end = offsets[e + 1];
-  for (int i = tid; i < 128 * (KQ_COLS / 8); i += 256) {
-    const int r = i / (KQ_COLS / 8), c8 = (i % (KQ_COLS / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r0 + r < r_end)
-      v = __ldg(reinterpret_cast<const uint4*>(X + (r0 + r) * C + c0 + c8));
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      tile[r][c8 + 2 * q] = h2[q].x;
-      tile[r][c8 + 2 * q + 1] = h2[q].y;
+  // this CTA's K blocks: kb, kb + gridDim.y, ... below the experts' total.  The next
+  // block's rows are loaded into registers while the current one is quantised.
+  const int total = s_kb0[E];
+  auto block_rows = [&](int kb, long long& r0, long long& r_end) {
+    int lo = 0, hi = E;                            // s_kb0[lo] <= kb < s_kb0[lo + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_kb0[mid] <= kb) lo = mid;
+      else hi = mid;
     }
-  }
-  __syncthreads();
-  const int c = tid % KQ_COLS, j = tid / KQ_COLS;   // 4 blocks of 32 rows
-  float v[32];
+    r0 = static_cast<long long>(offsets[lo]) + 128LL * (kb - s_kb0[lo]);
+    r_end = offsets[lo + 1];
+  };
+  constexpr int PER = 128 * (KQ_COLS / 8) / 256;   // 16-byte pieces per thread (4)
+  auto load_block = [&](int kb, uint4* reg) {
+    long long r0, r_end;
+    block_rows(kb, r0, r_end);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[32 * j + i][c]);
-  uint32_t code[8];
-  const uint32_t sc = mx_block(v, code);
-  const int col = c0 + c;
-  const long long kcap = 128LL * kb_cap;
-  uint4* dq = reinterpret_cast<uint4*>(xtq + static_cast<long long>(col) * kcap + 128LL * kb +
-                                       32 * j);
-  dq[0] = make_uint4(code[0], code[1], code[2], code[3]);
-  dq[1] = make_uint4(code[4], code[5], code[6], code[7]);
-  const long long atom =
-      role_n ? ((static_cast<long long>(col / 256) * kb_cap + kb) * 2 + ((col >> 7) & 1))
-             : (static_cast<long long>(col / 128) * kb_cap + kb);
-  atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
+    for (int u = 0; u < PER; ++u) {
+      const int i = tid + 256 * u;
+      const int r = i / (KQ_COLS / 8), c8 = (i % (KQ_COLS / 8)) * 8;
+      reg[u] = r0 + r < r_end
+                   ? __ldg(reinterpret_cast<const uint4*>(X + (r0 + r) * C + c0 + c8))
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  uint4 cur[PER];
+  if (static_cast<int>(blockIdx.y) < total) load_block(blockIdx.y, cur);
+  for (int kb = blockIdx.y; kb < total; kb += gridDim.y) {
+    __syncthreads();                               // the previous block's tile is consumed
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int i = tid + 256 * u;
+      const int r = i / (KQ_COLS / 8), c8 = (i % (KQ_COLS / 8)) * 8;
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&cur[u]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        tile[r][c8 + 2 * q] = h2[q].x;
+        tile[r][c8 + 2 * q + 1] = h2[q].y;
+      }
+    }
+    __syncthreads();
+    if (kb + static_cast<int>(gridDim.y) < total) load_block(kb + gridDim.y, cur);
+    const int c = tid % KQ_COLS, j = tid / KQ_COLS;   // 4 blocks of 32 rows
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[32 * j + i][c]);
+    uint32_t code[8];
+    const uint32_t sc = mx_block(v, code);
+    const int col = c0 + c;
+    const long long kcap = 128LL * kb_cap;
+    uint4* dq = reinterpret_cast<uint4*>(xtq + static_cast<long long>(col) * kcap + 128LL * kb +
+                                         32 * j);
+    dq[0] = make_uint4(code[0], code[1], code[2], code[3]);
+    dq[1] = make_uint4(code[4], code[5], code[6], code[7]);
+    const long long atom =
+        role_n ? ((static_cast<long long>(col / 256) * kb_cap + kb) * 2 + ((col >> 7) & 1))
+               : (static_cast<long long>(col / 128) * kb_cap + kb);
+    atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
+  }
 }
 
 // ------------------------------------------------------------------ block-scaled GEMM
 // Per CTA and stage: A 128 rows x 128 B, B 128 rows (pair: this CTA's half of N) or 256
-// rows (one CTA) x 128 B, the A scale atom (512 B) and the B scale pair (1 KB).
-template <int PAIR>
+// rows (one CTA) x 128 B, the A scale atom (512 B) and the B scale pair (1 KB).  WG (the
+// weight-gradient mode): 4 stages (its K is one expert's rows, a few K blocks) and a
+// TMA-store staging area, two 32 x 64 bf16 boxes (4 KB each) per epilogue warp.
+template <int PAIR, bool WG = false>
 struct MxGeo {
   static constexpr int B_ROWS = 256 / PAIR;
   static constexpr int A_BYTES = 128 * MX_BK;
@@ -362,7 +385,8 @@ struct MxGeo {
   static constexpr int SFB_OFF = SFA_OFF + MX_SFA_BYTES;
   static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + MX_SFA_BYTES + MX_SFB_BYTES;
   static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
-  static constexpr int STAGES = PAIR == 2 ? 6 : 4;
+  static constexpr int STAGES = WG ? 4 : (PAIR == 2 ? 6 : 4);
+  static constexpr int STAGING_BYTES = WG ? MX_EPI_WARPS * 2 * 4096 : 0;
   static constexpr int TILE_M = 128 * PAIR;
 };
 static_assert(MX_SF_COL0 + 12 * 6 <= MX_TMEM_COLS, "scale slots");
@@ -382,9 +406,10 @@ struct MxCtl {
   int kbpre[MX_MAX_G + 2];    // WGRAD: each expert's first K block (exclusive prefix)
 };
 
-template <int PAIR>
+template <int PAIR, bool WG>
 constexpr size_t mx_smem_bytes() {
-  return 1024 + MxGeo<PAIR>::STAGES * MxGeo<PAIR>::STAGE_BYTES + sizeof(MxCtl);
+  using GE = MxGeo<PAIR, WG>;
+  return 1024 + GE::STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES + sizeof(MxCtl);
 }
 
 struct MxParams {
@@ -473,17 +498,21 @@ __device__ __forceinline__ float bf16r(float v) {
 // tmA: the activation codes [rows, K] (box 128 x 128); tmB: the weight codes (box 128 x
 // 128); tmSA: the activation scale atoms viewed as [*, 256] bytes (box 256 x 2 = one atom);
 // tmSB: the weight scale atoms viewed as [*, 256] bytes (box 256 x 4 = one atom pair).
-template <int MODE, int PAIR>   // MODE: GEMM_FC1_SWIGLU or GEMM_FC2
+// WGRAD: A and B are along-token codes and atoms; tmC the gradient [E][M][N] bf16 (box
+// 64 x 32 x 1), written with TMA stores (the other modes take a placeholder).
+template <int MODE, int PAIR>
 __global__ void __launch_bounds__(MX_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-               const MxParams p) {
-  using GE = MxGeo<PAIR>;
+               const __grid_constant__ CUtensorMap tmC, const MxParams p) {
+  using GE = MxGeo<PAIR, MODE == GEMM_WGRAD>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  MxCtl* ctl = reinterpret_cast<MxCtl*>(smem + STAGES * GE::STAGE_BYTES);
+  MxCtl* ctl =
+      reinterpret_cast<MxCtl*>(smem + STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES);
+  const uint32_t staging_base = smem_u32(smem + STAGES * GE::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
   volatile int* abort_flag = &ctl->abort;
@@ -509,6 +538,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmSA);
     tma_prefetch_desc(&tmSB);
+    if (MODE == GEMM_WGRAD) tma_prefetch_desc(&tmC);
   }
   for (int g = threadIdx.x; g <= p.G; g += MX_THREADS) ctl->gstart[g] = p.offsets[g];
   __syncthreads();
@@ -581,6 +611,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     g = lo;
     const int local = tile - ctl->tprefix[g];
+    if (MODE == GEMM_WGRAD && p.wg_m_tiles > p.num_n_tiles) {
+      // consecutive tiles share the M operand's (larger) tile and walk the N tiles, so the
+      // larger operand streams through once and the smaller one is re-read from L2
+      mt = local / p.num_n_tiles;
+      nt = local - mt * p.num_n_tiles;
+      return;
+    }
     const int mtg = MODE == GEMM_WGRAD
                         ? p.wg_m_tiles
                         : mx_ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], GE::TILE_M);
@@ -752,6 +789,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int r_in_tile = rank * 128 + q * 32 + lane;
     const uint32_t tempty_leader =
         PAIR == 2 ? mapa_shared(smem_u32(&ctl->tempty), 0) : smem_u32(&ctl->tempty);
+    int store_buf = 0;                       // WGRAD: this warp's staging buffer in turn
     int it = 0;
     for (int tile = unit; tile < total; tile += num_units, ++it) {
       int g, mt, nt;
@@ -806,6 +844,41 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (lane == 0) {   // the accumulator is free (the leader counts both CTAs' warps)
         if (PAIR == 2) mbar_arrive_remote(tempty_leader);
         else mbar_arrive(tempty_leader);
+      }
+      if (MODE == GEMM_WGRAD) {
+        // this warp's 32 rows of dW[g] and its 128 columns, as two 32 x 64 boxes written
+        // through 128-byte-swizzled shared memory with TMA stores (rows past M and columns
+        // past N: M and N are multiples of 128, so a box is wholly in or out)
+        const int m_base = mt * GE::TILE_M + rank * 128 + q * 32;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int n0 = nt * 256 + 128 * hh + 64 * b;
+          if (m_base >= p.wg_M || n0 >= p.wg_N) continue;
+          const uint32_t buf_addr = staging_base +
+                                    static_cast<uint32_t>(((warp - 2) * 2 + store_buf) * 4096);
+          if (lane == 0) bulk_wait_group_read<1>();   // the store two boxes ago has read it
+          __syncwarp();
+          const uint32_t row_addr = buf_addr + lane * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(acc[64 * b + 8 * c + e]);
+            const uint4 v = pack8(x);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             row_addr + ((c ^ (lane & 7)) << 4)),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmC, buf_addr, n0, m_base, g);
+            bulk_commit_group();
+          }
+          store_buf ^= 1;
+        }
+        continue;
       }
       if (!valid) continue;
       if (MODE == GEMM_FC1_SWIGLU) {
@@ -902,7 +975,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 static_cast<uint8_t>(sc);
           }
         }
-      } else {   // FC2, DGRAD1, WGRAD: plain bf16 rows
+      } else {   // FC2, DGRAD1: plain bf16 rows
         const int n0 = nt * 256 + 128 * hh;
         if (n0 < p.n_out) {                    // n_out is a multiple of 128: all or nothing
           uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * p.n_out + n0);
@@ -916,6 +989,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
     }
+    if (MODE == GEMM_WGRAD && lane == 0) bulk_wait_group_all();   // stores done before exit
   }
   tc_fence_before();
   if (PAIR == 2) cluster_sync_all();
@@ -959,6 +1033,23 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
          CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map over a weight gradient viewed as [groups][rows][cols], 128-byte
+// swizzle, box 64 columns x 32 rows x 1 group (a store never crosses into the next
+// group's rows)
+bool make_map_dw(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                 uint64_t groups) {
+  auto enc = mx_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {cols, rows, groups};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 int grid_rows(int64_t rows) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -970,9 +1061,10 @@ int grid_rows(int64_t rows) {
 
 template <int MODE, int PAIR>
 cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                           const CUtensorMap& tsb, const MxParams& kp, cudaStream_t st) {
+                           const CUtensorMap& tsb, const CUtensorMap& tc, const MxParams& kp,
+                           cudaStream_t st) {
   auto kern = mx_gemm_kernel<MODE, PAIR>;
-  constexpr size_t SMEM = mx_smem_bytes<PAIR>();
+  constexpr size_t SMEM = mx_smem_bytes<PAIR, MODE == GEMM_WGRAD>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
@@ -999,7 +1091,7 @@ cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const C
   } else {
     cfg.gridDim = dim3(static_cast<unsigned>(sms));
   }
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, kp);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tc, kp);
 }
 
 }  // namespace
@@ -1062,20 +1154,22 @@ cudaError_t launch_mx_permute_quant(const void* x, const int32_t* src_tok,
 }
 
 namespace {
+// tc: WGRAD's output map; the other modes pass ta in its place (never used)
 cudaError_t launch_mx_any(int mode, bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
                           const CUtensorMap& tsa, const CUtensorMap& tsb, const MxParams& kp,
-                          cudaStream_t st) {
+                          cudaStream_t st, const CUtensorMap* tc = nullptr) {
 #define MOE_MX_CASE(M)                                                   \
   case M:                                                                \
-    return pair ? launch_mx_mode<M, 2>(ta, tb, tsa, tsb, kp, st)         \
-                : launch_mx_mode<M, 1>(ta, tb, tsa, tsb, kp, st);
+    return pair ? launch_mx_mode<M, 2>(ta, tb, tsa, tsb, ta, kp, st)     \
+                : launch_mx_mode<M, 1>(ta, tb, tsa, tsb, ta, kp, st);
   switch (mode) {
     MOE_MX_CASE(GEMM_FC1_SWIGLU)
     MOE_MX_CASE(GEMM_FC2)
     MOE_MX_CASE(GEMM_DGRAD2_SWIGLU)
     MOE_MX_CASE(GEMM_DGRAD1)
     case GEMM_WGRAD:
-      return launch_mx_mode<GEMM_WGRAD, 2>(ta, tb, tsa, tsb, kp, st);
+      if (!tc) return cudaErrorInvalidValue;
+      return launch_mx_mode<GEMM_WGRAD, 2>(ta, tb, tsa, tsb, *tc, kp, st);
     default:
       return cudaErrorInvalidValue;
   }
@@ -1201,7 +1295,9 @@ cudaError_t launch_mx_quant_tok(const void* X, const int32_t* offsets, int E, in
                                 cudaStream_t st) {
   if (E < 1 || E > MX_MAX_G || C % 128) return cudaErrorInvalidValue;
   const int64_t kb_cap = mx_tok_kb_cap(rows_cap, E);
-  mx_quant_tok_kernel<<<dim3(C / KQ_COLS, static_cast<unsigned>(kb_cap)), 256, 0, st>>>(
+  // each CTA walks up to 8 K blocks of its 64 columns (its expert prefix is built once)
+  const unsigned gy = static_cast<unsigned>((kb_cap + 7) / 8);
+  mx_quant_tok_kernel<<<dim3(C / KQ_COLS, gy), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(X), offsets, E, rows_cap, C, static_cast<int>(kb_cap),
       role_n ? 1 : 0, codes, scales, err);
   return cudaGetLastError();
@@ -1225,13 +1321,14 @@ cudaError_t launch_mx_wgrad(const MxWgradArgs& a, cudaStream_t st) {
   kp.num_n_tiles = (a.N + 255) / 256;
   kp.n_out = a.N;
   kp.out0 = static_cast<__nv_bfloat16*>(a.dW);
-  CUtensorMap ta, tb, tsa, tsb;
+  CUtensorMap ta, tb, tsa, tsb, tc;
   if (!make_map_u8(&ta, a.aq, kcap, M, 128, 128, true) ||
       !make_map_u8(&tb, a.bq, kcap, N, 128, 128, true) ||
       !make_map_u8(&tsa, a.a_sf, 256, (M / 128) * kb_cap * 2, 256, 2, false) ||
-      !make_map_u8(&tsb, a.b_sf, 256, ((N + 255) / 256) * kb_cap * 4, 256, 4, false))
+      !make_map_u8(&tsb, a.b_sf, 256, ((N + 255) / 256) * kb_cap * 4, 256, 4, false) ||
+      !make_map_dw(&tc, a.dW, N, M, static_cast<uint64_t>(a.E)))
     return cudaErrorInvalidValue;
-  return launch_mx_any(GEMM_WGRAD, true, ta, tb, tsa, tsb, kp, st);
+  return launch_mx_any(GEMM_WGRAD, true, ta, tb, tsa, tsb, kp, st, &tc);
 }
 
 }  // namespace moe
