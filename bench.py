@@ -521,48 +521,75 @@ def bench_ours(args, world, rank, local):
     e2e_value = None
     h2d = d2h = 0
     if not args.no_e2e:
-        # end to end through the public whole-layer API, host buffers in pinned memory
+        # End to end through the public whole-layer API with host buffers in pinned memory,
+        # the way a training loop streams them: every step copies its inputs (logits, x,
+        # dy) host -> device and its results (y, dx, dlogits) device -> host, on a copy
+        # stream, double-buffered so that step i+1's inputs and step i's results move
+        # while the GPU computes.  All copies fall inside the timed region.
         layer = tde.MoELayer(cfg, device=dev)
         h_logits = g["logits"].cpu().pin_memory()
         h_x = g["x"].cpu().pin_memory()
         h_dy = g["dy"].cpu().pin_memory()
-        d_logits = torch.empty_like(g["logits"]); d_x = torch.empty_like(g["x"])
-        d_dy = torch.empty_like(g["dy"])
         h_y = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
         h_dx = torch.empty((c.T, c.d), dtype=torch.bfloat16).pin_memory()
         h_dl = torch.empty((c.T, c.E), dtype=torch.float32).pin_memory()
-        outs = {"dx": dx, "dW1": dW1, "dW2": dW2, "dlogits": dl}
-        if shared:
-            outs["dW1s"] = shared["dW1"]; outs["dW2s"] = shared["dW2"]
+        bufs = []
+        for b in range(2):
+            o = {"dx": torch.empty_like(dx), "dW1": dW1, "dW2": dW2,
+                 "dlogits": torch.empty_like(dl)}
+            if shared:
+                o["dW1s"] = shared["dW1"]; o["dW2s"] = shared["dW2"]
+            bufs.append({"logits": torch.empty_like(g["logits"]), "x": torch.empty_like(g["x"]),
+                         "dy": torch.empty_like(g["dy"]), "y": torch.empty_like(y), "out": o})
+        cstream = torch.cuda.Stream(device=dev)
+        ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "done", "copied")}
 
-        def e2e_step():
-            d_logits.copy_(h_logits, non_blocking=True)
-            d_x.copy_(h_x, non_blocking=True)
-            d_dy.copy_(h_dy, non_blocking=True)
-            if args.mxfp8:
-                if not args.mx_cache_weights:
-                    tde.moe_mx_quantize_weights(cfg, g["W1"], g["W2"], wq)
-                yy = layer.forward_mx(d_logits, d_x, wq, g.get("W1s"), g.get("W2s"), y=y)
-            else:
-                yy = layer.forward(d_logits, d_x, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
-                                   y=y)
-            if args.mxfp8:
-                layer.backward_mx(d_logits, d_x, d_dy, wq, g.get("W1s"), g.get("W2s"), out=outs)
-            else:
-                layer.backward(d_logits, d_x, d_dy, g["W1"], g["W2"], g.get("W1s"), g.get("W2s"),
-                               out=outs)
-            h_y.copy_(yy, non_blocking=True)
-            h_dx.copy_(outs["dx"], non_blocking=True)
-            h_dl.copy_(outs["dlogits"], non_blocking=True)
+        def copy_in(b):
+            with torch.cuda.stream(cstream):
+                bufs[b]["logits"].copy_(h_logits, non_blocking=True)
+                bufs[b]["x"].copy_(h_x, non_blocking=True)
+                bufs[b]["dy"].copy_(h_dy, non_blocking=True)
+                ev["in"][b].record(cstream)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        def e2e_run(n):
+            copy_in(0)
+            for i in range(n):
+                b = i & 1
+                B = bufs[b]
+                stream.wait_event(ev["in"][b])
+                if i >= 2:
+                    stream.wait_event(ev["copied"][b])   # step i-2's results are on the host
+                if args.mxfp8:
+                    if not args.mx_cache_weights:
+                        tde.moe_mx_quantize_weights(cfg, g["W1"], g["W2"], wq)
+                    layer.forward_mx(B["logits"], B["x"], wq, g.get("W1s"), g.get("W2s"),
+                                     y=B["y"])
+                    layer.backward_mx(B["logits"], B["x"], B["dy"], wq, g.get("W1s"),
+                                      g.get("W2s"), out=B["out"])
+                else:
+                    layer.forward(B["logits"], B["x"], g["W1"], g["W2"], g.get("W1s"),
+                                  g.get("W2s"), y=B["y"])
+                    layer.backward(B["logits"], B["x"], B["dy"], g["W1"], g["W2"],
+                                   g.get("W1s"), g.get("W2s"), out=B["out"])
+                ev["done"][b].record(stream)
+                if i + 1 < n:
+                    if i >= 1:   # buffer 1-b was last read by step i-1
+                        cstream.wait_event(ev["done"][1 - b])
+                    copy_in(1 - b)
+                with torch.cuda.stream(cstream):
+                    cstream.wait_event(ev["done"][b])
+                    h_y.copy_(B["y"], non_blocking=True)
+                    h_dx.copy_(B["out"]["dx"], non_blocking=True)
+                    h_dl.copy_(B["out"]["dlogits"], non_blocking=True)
+                    ev["copied"][b].record(cstream)
+            stream.wait_event(ev["copied"][(n - 1) & 1])
+
+        e2e_run(max(1, args.warmup))
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_run(args.steps)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
