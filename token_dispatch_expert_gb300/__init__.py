@@ -371,8 +371,8 @@ class MoELayer:
         return wq
 
     def forward_mx(self, logits, x, wq, W1s=None, W2s=None, y=None, stream=None):
-        """Forward with the routed experts in MXFP8 (config made with mxfp8=True); the
-        backward is the same bf16 call as after forward()."""
+        """Forward with the routed experts in MXFP8 (config made with mxfp8=1 or 2); the
+        bf16 backward() may follow it, or backward_mx()."""
         import torch
         if y is None:
             y = torch.empty_like(x)
@@ -380,8 +380,9 @@ class MoELayer:
         return y
 
     def backward_mx(self, logits, x, dy, wq, W1s=None, W2s=None, out=None, stream=None):
-        """Backward with the data-gradient GEMMs in MXFP8 (after forward_mx); `out` as in
-        backward(); the weight-gradient shapes come from the config."""
+        """Backward with the data-gradient GEMMs in MXFP8 (after forward_mx), and with
+        mxfp8=2 the routed weight gradients too; `out` as in backward(); the
+        weight-gradient shapes come from the config."""
         import torch
         c = self.cfg
         if out is None:
