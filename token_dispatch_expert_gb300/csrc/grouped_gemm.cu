@@ -24,9 +24,11 @@
 // the epilogue of one tile overlap the mainloop of the next.  The tile list is built on
 // the device from the segment offsets (no host synchronisation): tiles are ordered
 // expert-major, then N-tile, then M-tile, so CTAs running at the same time share one
-// weight tile (read from HBM once, the rest from L2).  Every wait on an mbarrier is
-// bounded; a wait that gives up sets MOE_DEVERR_TIMEOUT in the error word and the CTA
-// drains and exits.
+// weight tile (read from HBM once, the rest from L2).  On CTA pairs a segment's last,
+// partly filled M tile of at most TAIL_ROWS_MAX rows runs swapped (the weight rows as the
+// MMA's M, the segment's rows as its N; see tail_tokens()), so its tensor time follows the
+// rows present.  Every wait on an mbarrier is bounded; a wait that gives up sets
+// MOE_DEVERR_TIMEOUT in the error word and the CTA drains and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -1,5 +1,7 @@
-// mx.cu -- the MXFP8 forward of the routed experts: quantisation kernels and the
-// block-scaled grouped GEMMs (FC1 + SwiGLU + quantisation of h, FC2).
+// mx.cu -- the MXFP8 path of the routed experts: quantisation kernels and the block-scaled
+// grouped GEMMs (FC1 + SwiGLU + quantisation of h, FC2; the FC2 data-gradient with the
+// SwiGLU backward quantising dab, the FC1 data-gradient; and, at mxfp8 = 2, the weight
+// gradients on operands quantised along each expert segment's tokens).
 //
 // "MoE Training Optimization with Primus", FP8 section: the MXFP8 recipe (OCP E4M3
 // elements with per-block power-of-two scales) for the routed-expert grouped GEMMs, and
@@ -31,10 +33,17 @@
 // load the whole B scale pair; tcgen05.cp.cta_group::2 issued by the leader copies each
 // CTA's own shared-memory atoms into its own TMEM (measured with a second probe).
 //
-// TMEM holds one 256-column accumulator and 4 stages x 12 scale columns.  There is no
-// room for a second accumulator, so eight epilogue warps (two per lane quarter, each
+// TMEM holds one 256-column accumulator and up to 6 stages x 12 scale columns.  There is
+// no room for a second accumulator, so eight epilogue warps (two per lane quarter, each
 // taking half the columns) copy the accumulator into registers and release it at once;
 // the next tile's MMAs then overlap the epilogue's arithmetic and stores.
+//
+// Weight gradients (GEMM_WGRAD): dW[e] = A_e^T B_e with the contraction over the expert's
+// rows.  mx_quant_tok_kernel writes each operand transposed ([C][128 kb_cap] codes, K-major
+// along the rows) with each expert's rows as whole 128-row K blocks (the last one
+// zero-padded), 32-row MX blocks starting at the segment's first row, and the scales in
+// the atom layout of the operand's GEMM role; the GEMM walks every expert's fixed
+// weight-shaped tile grid over its K blocks and writes dW through TMA stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
