@@ -27,6 +27,12 @@ SMALL = {
     # 600 = 2 x 256 + 88 rows: the shared expert's last M tile is a swap-AB tail tile
     "shared_tail": MoEConfig("shared_tail", T=600, d=256, E=4, k=2, f=320, fs=192,
                              gate="sigmoid", route_scale=2.5, zipf_s=1.0),
+    # degenerate routings: every token to every expert (k = E), a single token, and a
+    # capacity of 6 rows per expert (most assignments dropped)
+    "k_eq_E": MoEConfig("k_eq_E", T=200, d=128, E=4, k=4, f=128),
+    "T1": MoEConfig("T1_layer", T=1, d=128, E=4, k=2, f=128),
+    "cap_tiny": MoEConfig("cap_tiny", T=256, d=128, E=8, k=2, f=128, cap_factor=0.1,
+                          zipf_s=1.2),
 }
 
 ROUTE_KEYS = ["topk_idx", "counts", "kept", "offsets", "dest_row", "src_tok", "src_slot",

@@ -36,6 +36,8 @@ CASES = {
                           zipf_s=1.0),
     # 256 fine-grained experts: the largest expert count, many empty and one-row segments
     "fine": MoEConfig("mx_fine", T=512, d=256, E=256, k=8, f=256, zipf_s=1.2),
+    # every token to every expert
+    "k_eq_E": MoEConfig("mx_kE", T=200, d=256, E=4, k=4, f=256),
 }
 
 
@@ -361,7 +363,7 @@ def test_grouped_ffn_bwd_mx_against_oracle(name, level):
 
 
 @pytest.mark.parametrize("name,level", [("small", 1), ("many", 1), ("pair", 1), ("fine", 1),
-                                        ("pair", 2), ("fine", 2)])
+                                        ("k_eq_E", 1), ("pair", 2), ("fine", 2), ("k_eq_E", 2)])
 def test_layer_mx_forward_and_backward(name, level):
     c = CASES[name]
     inp = gen_inputs_host(c)
