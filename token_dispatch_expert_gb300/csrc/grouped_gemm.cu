@@ -15,7 +15,9 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 in, fp32 accumulate in
 //               TMEM); tcgen05.commit frees a stage / hands an accumulator to the epilogue
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp its 32-lane quarter),
-//               fused SwiGLU / SwiGLU-backward, bf16 rounding, masked 16-byte stores
+//               fused SwiGLU / SwiGLU-backward, bf16 rounding; each 32 x 32 block goes
+//               through the warp's shared-memory block so that rows leave as 16-byte
+//               pieces, four lanes per 64-byte row segment, not one row per lane
 // Long segments run on CTA pairs (a cluster of 2 SMs): a 256 x 256 output tile, each CTA
 // holding 128 rows of A and 128 rows of B in a 6-stage ring, the leader issuing
 // M256 x N256 x K16 pair MMAs -- half the shared-memory traffic per SM of a one-CTA
@@ -60,9 +62,10 @@ struct Geo {
   static constexpr bool TMA_STORE = MODE == GEMM_WGRAD;
   // swap-AB tail tiles (CTA pairs, fixed-K modes): see tail_tokens()
   static constexpr bool TAIL = PAIR == 2 && MODE != GEMM_WGRAD;
-  // the tail tiles' epilogue transposes through shared memory: one 32 x 32 fp32 block per
-  // epilogue warp, rows padded to 144 bytes
-  static constexpr int XCH_BYTES = TAIL ? 4 * 32 * 144 : 0;
+  // the fixed-K epilogues transpose through shared memory: one block per epilogue warp
+  // (a tail tile's 32 x 32 fp32 with rows padded to 144 bytes; an ordinary tile's 32
+  // rows of 128 bytes, 16-byte pieces XOR-swizzled by row)
+  static constexpr int XCH_BYTES = MODE != GEMM_WGRAD ? 4 * 32 * 144 : 0;
   static constexpr int STAGING_BYTES = (TMA_STORE ? 4 * 2 * 4096 : 0) + XCH_BYTES;
   static constexpr int STAGES = PAIR == 2 ? (TMA_STORE ? 5 : 6) : 4;
 };
@@ -294,6 +297,21 @@ __device__ __forceinline__ float bf16_round(float v) {
 constexpr int XPOSE_PITCH = 144;                 // bytes per row of a transpose block
 constexpr int XPOSE_BYTES = 32 * XPOSE_PITCH;    // one warp's block
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void ld_shared_f32x4(uint32_t addr, float* v) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr) : "memory");
+}
 __device__ __forceinline__ void ld_shared_f32x8(uint32_t addr, float* v) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr) : "memory");
@@ -405,8 +423,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES);
   const uint32_t staging_base = smem_u32(smem + STAGES * GE::STAGE_BYTES);
-  // the tail tiles' transpose blocks sit after the TMA-store staging (which only the
-  // weight-gradient mode, without tail tiles, uses)
+  // the epilogue warps' transpose blocks (one per warp, used by every fixed-K tile) sit
+  // after the TMA-store staging, which only the weight-gradient mode uses
   const uint32_t xch_base = staging_base + (GE::STAGING_BYTES - GE::XCH_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -713,7 +731,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     int store_buf = 0;                      // staging buffer of the TMA-store epilogue
-    const int r_in_tile = rank * 128 + q * 32 + lane;
     int it = 0;
     int xc = 0;                             // FC1 tail tiles: exchange blocks used so far
     for (int tile = unit; tile < total; tile += num_units, ++it) {
@@ -734,115 +751,165 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                  static_cast<int>(seg_end - row0), ntok, xc, abort_flag))
           break;
       } else if (MODE == GEMM_FC1_SWIGLU) {
-        const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
-        const bool valid = prow < seg_end;
+        // Transposed through the warp's block like the FC2 data-gradient below: per
+        // 32-column chunk each lane writes bf16(a) and bf16(b) of its row (a's 16-byte
+        // pieces at 2k, b's at 2k + 1, XOR-swizzled by row), then each lane takes four
+        // 8-column pieces of rows lane / 4 + 8 i and stores a, b and h = silu(a) b.
         const int f = p.f;
+        const long long wrow0 = static_cast<long long>(seg0) + mt * GE::TILE_M + rank * 128 +
+                                q * 32;
+        const uint32_t blk = xch_base + static_cast<uint32_t>(q * XPOSE_BYTES);
+        const int cc = 8 * (lane & 3);
 #pragma unroll 1
         for (int c = 0; c < (BN / 2) / 32; ++c) {
+          const int n0 = nt * (BN / 2) + c * 32;
+          if (n0 >= f) break;                   // f is a multiple of 64: warp-uniform
           uint32_t ra[32], rb[32];
           tmem_ld32(taddr + c * 32, ra);
           tmem_ld32(taddr + BN / 2 + c * 32, rb);
           tmem_ld_wait();
-          const int n0 = nt * (BN / 2) + c * 32;
-          if (valid && n0 < f) {
-            uint4* ab_a = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
-            uint4* ab_b = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
-            uint4* hp = reinterpret_cast<uint4*>(p.out1 + prow * f + n0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
+          for (int k = 0; k < 4; ++k) {
+            float x[8], y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              x[e] = __uint_as_float(ra[8 * k + e]);
+              y[e] = __uint_as_float(rb[8 * k + e]);
+            }
+            const uint4 va = pack8(x), vb = pack8(y);
+            st_shared_v4(blk + lane * 128 + (((2 * k) ^ (lane & 7)) << 4), va);
+            st_shared_v4(blk + lane * 128 + (((2 * k + 1) ^ (lane & 7)) << 4), vb);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i;
+            const int k = lane & 3;
+            const uint4 va = ld_shared_v4(blk + r * 128 + (((2 * k) ^ (r & 7)) << 4));
+            const uint4 vb = ld_shared_v4(blk + r * 128 + (((2 * k + 1) ^ (r & 7)) << 4));
+            const long long prow = wrow0 + r;
+            if (prow < seg_end) {
               float a[8], b[8], h[8];
+              unpack8(va, a);                   // a, b as stored: h comes from them
+              unpack8(vb, b);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                // round a, b to bf16 first: h is computed from the stored values
-                a[e] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(ra[v * 8 + e])));
-                b[e] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(rb[v * 8 + e])));
-                h[e] = silu_f(a[e]) * b[e];
-              }
-              ab_a[v] = pack8(a);
-              ab_b[v] = pack8(b);
-              hp[v] = pack8(h);
+              for (int e = 0; e < 8; ++e) h[e] = silu_f(a[e]) * b[e];
+              *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0 + cc) = va;
+              *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0 + cc) = vb;
+              *reinterpret_cast<uint4*>(p.out1 + prow * f + n0 + cc) = pack8(h);
             }
           }
+          __syncwarp();                         // the block is read before the next chunk
         }
       } else if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
-        const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
-        const bool valid = prow < seg_end;
+        // Transposed through the warp's block: bf16 rows of 64 bytes (piece k at 2k,
+        // XOR-swizzled by row), stored as 16-byte row pieces, four lanes per row segment.
         const int n_out = p.n_out;
+        const long long wrow0 = static_cast<long long>(seg0) + mt * GE::TILE_M + rank * 128 +
+                                q * 32;
+        const uint32_t blk = xch_base + static_cast<uint32_t>(q * XPOSE_BYTES);
+        const int cc = 8 * (lane & 3);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          const int n0 = nt * BN + c * 32;
+          if (n0 >= n_out) break;               // n_out is a multiple of 64: warp-uniform
           uint32_t ra[32];
           tmem_ld32(taddr + c * 32, ra);
           tmem_ld_wait();
-          const int n0 = nt * BN + c * 32;
-          if (valid && n0 < n_out) {
-            uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * n_out + n0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float x[8];
+          for (int k = 0; k < 4; ++k) {
+            float x[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ra[v * 8 + e]);
-              o[v] = pack8(x);
-            }
+            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(ra[8 * k + e]);
+            st_shared_v4(blk + lane * 128 + (((2 * k) ^ (lane & 7)) << 4), pack8(x));
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i;
+            const uint4 v = ld_shared_v4(blk + r * 128 + (((2 * (lane & 3)) ^ (r & 7)) << 4));
+            const long long prow = wrow0 + r;
+            if (prow < seg_end)
+              *reinterpret_cast<uint4*>(p.out0 + prow * n_out + n0 + cc) = v;
+          }
+          __syncwarp();                         // the block is read before the next chunk
         }
       } else if (MODE == GEMM_DGRAD2_SWIGLU) {
-        const long long prow = static_cast<long long>(seg0) + mt * GE::TILE_M + r_in_tile;
-        const bool valid = prow < seg_end;
+        // The warp's 32 rows (TMEM lanes) x 32 columns of each chunk go through its 4 KB
+        // block of shared memory (128-byte rows, 16-byte pieces XOR-swizzled by row, free of
+        // bank conflicts both ways); each lane then takes four 8-column pieces, of rows
+        // lane / 4 + 8 i, so the saved a, b are read and da, db written as 16-byte pieces,
+        // four lanes per 64-byte row segment, instead of one row per lane.  The next chunk's
+        // a, b are loaded while the current one is computed.
         const int f = p.f;
-        // the saved pre-activations a, b of this row: 32 columns per chunk, fetched one
-        // chunk ahead into registers so their latency overlaps the previous chunk's work
-        const uint4* arow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f);
-        const uint4* brow = reinterpret_cast<const uint4*>(p.aux + prow * 2 * f + f);
-        auto chunk_ok = [&](int c) { return valid && nt * BN + c * 32 < f; };
-        uint4 na[4], nb[4];
-        if (chunk_ok(0)) {
+        const long long wrow0 = static_cast<long long>(seg0) + mt * GE::TILE_M + rank * 128 +
+                                q * 32;
+        // (the same region of the staging area as this warp's tail-tile block: the warps
+        // are not in step, so each keeps to its own)
+        const uint32_t blk = xch_base + static_cast<uint32_t>(q * XPOSE_BYTES);
+        const int cc = 8 * (lane & 3);
+        auto load_ab = [&](int c, uint4* xa, uint4* xb) {
+          const int n0 = nt * BN + c * 32;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            na[v] = __ldg(arow + (nt * BN) / 8 + v);
-            nb[v] = __ldg(brow + (nt * BN) / 8 + v);
-          }
-        }
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint4 ca[4], cb[4];
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            ca[v] = na[v];
-            cb[v] = nb[v];
-          }
-          if (c + 1 < BN / 32 && chunk_ok(c + 1)) {
-            const int nn = (nt * BN + (c + 1) * 32) / 8;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              na[v] = __ldg(arow + nn + v);
-              nb[v] = __ldg(brow + nn + v);
+          for (int i = 0; i < 4; ++i) {
+            const long long prow = wrow0 + (lane >> 2) + 8 * i;
+            if (prow < seg_end && n0 < f) {
+              const long long base = prow * 2 * f + n0 + cc;
+              xa[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base));
+              xb[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base + f));
             }
           }
+        };
+        uint4 na[4], nb[4];
+        load_ab(0, na, nb);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int n0 = nt * BN + c * 32;
+          if (n0 >= f) break;                   // f is a multiple of 64: warp-uniform
+          uint4 ca[4], cb[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ca[i] = na[i];
+            cb[i] = nb[i];
+          }
+          if (c + 1 < BN / 32) load_ab(c + 1, na, nb);
           uint32_t ra[32];
           tmem_ld32(taddr + c * 32, ra);
           tmem_ld_wait();
-          const int n0 = nt * BN + c * 32;
-          if (chunk_ok(c)) {
-            uint4* da_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
-            uint4* db_ = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
+          for (int k = 0; k < 8; ++k)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             blk + lane * 128 + ((k ^ (lane & 7)) << 4)),
+                         "r"(ra[4 * k]), "r"(ra[4 * k + 1]), "r"(ra[4 * k + 2]),
+                         "r"(ra[4 * k + 3])
+                         : "memory");
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = (lane >> 2) + 8 * i;
+            const int k0 = 2 * (lane & 3);
+            float dh[8];
+            ld_shared_f32x4(blk + r * 128 + ((k0 ^ (r & 7)) << 4), dh);
+            ld_shared_f32x4(blk + r * 128 + (((k0 + 1) ^ (r & 7)) << 4), dh + 4);
+            const long long prow = wrow0 + r;
+            if (prow < seg_end) {
               float a[8], b[8], da[8], db[8];
-              unpack8(ca[v], a);
-              unpack8(cb[v], b);
+              unpack8(ca[i], a);
+              unpack8(cb[i], b);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float dh = __uint_as_float(ra[v * 8 + e]);
                 const float sg = sigmoid_fast(a[e]);
                 const float silu = a[e] * sg;
                 const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
-                da[e] = dh * b[e] * dsilu;
-                db[e] = dh * silu;
+                da[e] = dh[e] * b[e] * dsilu;
+                db[e] = dh[e] * silu;
               }
-              da_[v] = pack8(da);
-              db_[v] = pack8(db);
+              const long long base = prow * 2 * f + n0 + cc;
+              *reinterpret_cast<uint4*>(p.out0 + base) = pack8(da);
+              *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(db);
             }
           }
+          __syncwarp();                         // the block is read before the next chunk
         }
       } else {   // WGRAD: dW[g][m][n], written as 32 x 64 boxes through shared memory
         const int m_base = mt * GE::TILE_M + rank * 128 + q * 32;   // this warp's 32 rows
