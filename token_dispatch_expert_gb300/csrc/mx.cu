@@ -395,7 +395,9 @@ struct MxGeo {
   static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + MX_SFA_BYTES + MX_SFB_BYTES;
   static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGES = WG ? 4 : (PAIR == 2 ? 6 : 4);
-  static constexpr int STAGING_BYTES = WG ? MX_EPI_WARPS * 2 * 4096 : 0;
+  // WG: TMA-store staging; otherwise each epilogue warp's 2 KB transpose block (32 rows of
+  // 64 bytes) through which its rows leave as 16-byte pieces
+  static constexpr int STAGING_BYTES = WG ? MX_EPI_WARPS * 2 * 4096 : MX_EPI_WARPS * 2048;
   static constexpr int TILE_M = 128 * PAIR;
 };
 static_assert(MX_SF_COL0 + 12 * 6 <= MX_TMEM_COLS, "scale slots");
@@ -500,6 +502,17 @@ __device__ __forceinline__ bool mx_warp_wait(uint32_t bar, uint32_t parity, vola
 }
 
 __device__ __forceinline__ float silu_mx(float a) { return a * sigmoid_fast(a); }
+__device__ __forceinline__ void mx_st_shared_v4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 mx_ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ float bf16r(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
@@ -889,16 +902,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         continue;
       }
-      if (!valid) continue;
       if (MODE == GEMM_FC1_SWIGLU) {
+        // gate columns [n0, n0 + 64) of f and their up columns; per 32-column block the
+        // SwiGLU and the quantisation of h run on this lane's row, then a, b and h leave
+        // through the warp's 2 KB block (64-byte rows, 16-byte pieces XOR-swizzled by row
+        // pair: conflict-free both ways) as 16-byte row pieces of rows lane / 4 + 8 i,
+        // four lanes per 64-byte row segment
         const int f = p.f;
         const int n0 = nt * 128 + 64 * hh;     // f is a multiple of 128: always in range
-        uint4* ab_a = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0);
-        uint4* ab_b = reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0);
-        uint4* hp = reinterpret_cast<uint4*>(p.out1 + prow * f + n0);
+        const long long wrow0 = prow - lane;   // this warp's first row
+        const uint32_t xb = staging_base + static_cast<uint32_t>((warp - 2) * 2048);
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
           float h[32];
+          uint4 pa[4], pb[4], phv[4];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             float a[8], b[8];
@@ -908,21 +925,77 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               b[e] = bf16r(__uint_as_float(acc[64 + 32 * blk + 8 * v + e]));
               h[8 * v + e] = bf16r(silu_mx(a[e]) * b[e]);
             }
-            ab_a[4 * blk + v] = pack8(a);
-            ab_b[4 * blk + v] = pack8(b);
-            hp[4 * blk + v] = pack8(h + 8 * v);
+            pa[v] = pack8(a);
+            pb[v] = pack8(b);
+            phv[v] = pack8(h + 8 * v);
           }
-          // the SwiGLU step quantises its own (bf16) output for FC2
-          uint32_t c[8];
-          const uint32_t sc = mx_block(h, c);
-          uint4* dq = reinterpret_cast<uint4*>(p.out_q + prow * f + n0 + 32 * blk);
-          dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
-          dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
-          const int sub = n0 / 32 + blk;        // 32-element block of h's row
-          p.out_sf[act_atom_byte(seg0, g, lrow, f / 128, sub >> 2, sub & 3)] =
-              static_cast<uint8_t>(sc);
+          if (valid) {
+            // the SwiGLU step quantises its own (bf16) output for FC2
+            uint32_t c[8];
+            const uint32_t sc = mx_block(h, c);
+            uint4* dq = reinterpret_cast<uint4*>(p.out_q + prow * f + n0 + 32 * blk);
+            dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
+            dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
+            const int sub = n0 / 32 + blk;      // 32-element block of h's row
+            p.out_sf[act_atom_byte(seg0, g, lrow, f / 128, sub >> 2, sub & 3)] =
+                static_cast<uint8_t>(sc);
+          }
+#pragma unroll
+          for (int o = 0; o < 3; ++o) {
+            const uint4* src = o == 0 ? pa : (o == 1 ? pb : phv);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mx_st_shared_v4(xb + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), src[k]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, k = lane & 3;
+              const uint4 v = mx_ld_shared_v4(xb + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
+              const long long row = wrow0 + r;
+              if (row < ctl->gstart[g + 1]) {
+                const int col = n0 + 32 * blk + 8 * k;
+                __nv_bfloat16* dst = o == 2 ? p.out1 + row * f + col
+                                            : p.out0 + row * 2 * f + (o == 1 ? f : 0) + col;
+                *reinterpret_cast<uint4*>(dst) = v;
+              }
+            }
+            __syncwarp();                       // the block is read before it is refilled
+          }
         }
-      } else if (MODE == GEMM_DGRAD2_SWIGLU) {
+        continue;
+      }
+      if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
+        // bf16 rows through the warp's 2 KB block as in FC1: 32 columns at a time, out as
+        // 16-byte row pieces of rows lane / 4 + 8 i
+        const int n0 = nt * 256 + 128 * hh;
+        if (n0 < p.n_out) {                    // n_out is a multiple of 128: warp-uniform
+          const long long wrow0 = prow - lane;
+          const uint32_t xb = staging_base + static_cast<uint32_t>((warp - 2) * 2048);
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(acc[32 * blk + 8 * k + e]);
+              mx_st_shared_v4(xb + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), pack8(x));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, k = lane & 3;
+              const uint4 v = mx_ld_shared_v4(xb + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
+              const long long row = wrow0 + r;
+              if (row < ctl->gstart[g + 1])
+                *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + 32 * blk + 8 * k) = v;
+            }
+            __syncwarp();
+          }
+        }
+        continue;
+      }
+      if (!valid) continue;
+      if (MODE == GEMM_DGRAD2_SWIGLU) {
         // dh of columns [n0, n0 + 128) of f; the SwiGLU backward from the saved a, b gives
         // da, db (bf16, for the bf16 weight gradient) and their MXFP8 form (for DGRAD1)
         const int f = p.f;
@@ -982,18 +1055,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             sub = (f + n0 + 32 * c) / 32;
             p.out_sf[act_atom_byte(seg0, g, lrow, 2 * f / 128, sub >> 2, sub & 3)] =
                 static_cast<uint8_t>(sc);
-          }
-        }
-      } else {   // FC2, DGRAD1: plain bf16 rows
-        const int n0 = nt * 256 + 128 * hh;
-        if (n0 < p.n_out) {                    // n_out is a multiple of 128: all or nothing
-          uint4* o = reinterpret_cast<uint4*>(p.out0 + prow * p.n_out + n0);
-#pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(acc[8 * v + e]);
-            o[v] = pack8(x);
           }
         }
       }
