@@ -385,8 +385,11 @@ mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restri
 // rows (one CTA) x 128 B, the A scale atom (512 B) and the B scale pair (1 KB).  WG (the
 // weight-gradient mode): 4 stages (its K is one expert's rows, a few K blocks) and a
 // TMA-store staging area, two 32 x 64 bf16 boxes (4 KB each) per epilogue warp.
-template <int PAIR, bool WG = false>
+template <int PAIR, int MODE>
 struct MxGeo {
+  static constexpr bool WG = MODE == GEMM_WGRAD;
+  // the CTA-pair FC2 data-gradient transposes fp32 dh through 4 KB per warp
+  static constexpr bool XD2 = MODE == GEMM_DGRAD2_SWIGLU && PAIR == 2;
   static constexpr int B_ROWS = 256 / PAIR;
   static constexpr int A_BYTES = 128 * MX_BK;
   static constexpr int B_BYTES = B_ROWS * MX_BK;
@@ -394,10 +397,11 @@ struct MxGeo {
   static constexpr int SFB_OFF = SFA_OFF + MX_SFA_BYTES;
   static constexpr int LOAD_BYTES = A_BYTES + B_BYTES + MX_SFA_BYTES + MX_SFB_BYTES;
   static constexpr int STAGE_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
-  static constexpr int STAGES = WG ? 4 : (PAIR == 2 ? 6 : 4);
-  // WG: TMA-store staging; otherwise each epilogue warp's 2 KB transpose block (32 rows of
-  // 64 bytes) through which its rows leave as 16-byte pieces
-  static constexpr int STAGING_BYTES = WG ? MX_EPI_WARPS * 2 * 4096 : MX_EPI_WARPS * 2048;
+  static constexpr int STAGES = (WG || PAIR == 1) ? 4 : (XD2 ? 5 : 6);
+  // WG: TMA-store staging; otherwise each epilogue warp's transpose block through which
+  // its rows leave as 16-byte pieces: 2 KB (32 rows of 64 bytes), 4 KB for XD2
+  static constexpr int STAGING_BYTES =
+      WG ? MX_EPI_WARPS * 2 * 4096 : MX_EPI_WARPS * (XD2 ? 4096 : 2048);
   static constexpr int TILE_M = 128 * PAIR;
 };
 static_assert(MX_SF_COL0 + 12 * 6 <= MX_TMEM_COLS, "scale slots");
@@ -417,9 +421,9 @@ struct MxCtl {
   int kbpre[MX_MAX_G + 2];    // WGRAD: each expert's first K block (exclusive prefix)
 };
 
-template <int PAIR, bool WG>
+template <int PAIR, int MODE>
 constexpr size_t mx_smem_bytes() {
-  using GE = MxGeo<PAIR, WG>;
+  using GE = MxGeo<PAIR, MODE>;
   return 1024 + GE::STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES + sizeof(MxCtl);
 }
 
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                const __grid_constant__ CUtensorMap tmC, const MxParams p) {
-  using GE = MxGeo<PAIR, MODE == GEMM_WGRAD>;
+  using GE = MxGeo<PAIR, MODE>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -830,7 +834,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // columns are loaded before the accumulator is ready and each later chunk one chunk
       // ahead of its use (the epilogue was bound by these loads' latency)
       const int dg_n0 = nt * 256 + 128 * hh;
-      const bool dg_ok = MODE == GEMM_DGRAD2_SWIGLU && valid && dg_n0 < p.f;
+      const bool dg_ok = MODE == GEMM_DGRAD2_SWIGLU && !GE::XD2 && valid && dg_n0 < p.f;
       const uint4* dg_a = reinterpret_cast<const uint4*>(p.aux + prow * 2 * p.f + dg_n0);
       const uint4* dg_b = dg_a + p.f / 8;
       uint4 na[4], nb[4];
@@ -994,6 +998,100 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         continue;
       }
+      if (GE::XD2) {
+        // CTA pairs: dh goes through the warp's 4 KB block (128-byte fp32 rows, 16-byte
+        // pieces XOR-swizzled by row) 32 columns at a time; each lane then takes the
+        // 8-column piece lane % 4 of rows lane / 4 + 8 i, reads a, b and writes da, db as
+        // 16-byte pieces, and the four lanes of a row share the 32-column MX block of dab:
+        // its maximum by two shuffles, then 8 codes (8 bytes) per lane
+        const int f = p.f;
+        const int n0 = nt * 256 + 128 * hh;
+        if (n0 < f) {                          // f is a multiple of 128: warp-uniform
+          const long long wrow0 = prow - lane;
+          const long long seg_end = ctl->gstart[g + 1];
+          const uint32_t xb = staging_base + static_cast<uint32_t>((warp - 2) * 4096);
+          const int kq = lane & 3;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx_st_shared_v4(xb + lane * 128 + ((k ^ (lane & 7)) << 4),
+                              make_uint4(acc[32 * blk + 4 * k], acc[32 * blk + 4 * k + 1],
+                                         acc[32 * blk + 4 * k + 2], acc[32 * blk + 4 * k + 3]));
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i;
+              const uint4 d0 = mx_ld_shared_v4(xb + r * 128 + (((2 * kq) ^ (r & 7)) << 4));
+              const uint4 d1 = mx_ld_shared_v4(xb + r * 128 + (((2 * kq + 1) ^ (r & 7)) << 4));
+              const float dh[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y),
+                                   __uint_as_float(d0.z), __uint_as_float(d0.w),
+                                   __uint_as_float(d1.x), __uint_as_float(d1.y),
+                                   __uint_as_float(d1.z), __uint_as_float(d1.w)};
+              const long long row = wrow0 + r;
+              const bool ok = row < seg_end;
+              const int col = n0 + 32 * blk + 8 * kq;
+              const long long base = row * 2 * f + col;
+              float a[8], b[8], da[8], db[8];
+              if (ok) {
+                unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base)), a);
+                unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base + f)), b);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] = b[e] = 0.0f;
+              }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float sg = sigmoid_fast(a[e]);
+                const float silu = a[e] * sg;
+                const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
+                da[e] = dh[e] * b[e] * dsilu;
+                db[e] = dh[e] * silu;
+              }
+              const uint4 pda = pack8(da), pdb = pack8(db);
+              if (ok) {
+                *reinterpret_cast<uint4*>(p.out0 + base) = pda;
+                *reinterpret_cast<uint4*>(p.out0 + base + f) = pdb;
+              }
+              // dab quantised along 2f from its bf16 value, one 32-column block per four
+              // lanes (a block never straddles the da | db boundary)
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint4 pv = half == 0 ? pda : pdb;
+                const uint32_t w[4] = {pv.x, pv.y, pv.z, pv.w};
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  x[2 * e] = __uint_as_float(w[e] << 16);
+                  x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+                amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, 2));
+                const int X = mx_exponent(amax);
+                const float inv = exp2_int(-X);
+                const uint32_t c0 = e4m3x2(x[0] * inv, x[1] * inv) |
+                                    (e4m3x2(x[2] * inv, x[3] * inv) << 16);
+                const uint32_t c1 = e4m3x2(x[4] * inv, x[5] * inv) |
+                                    (e4m3x2(x[6] * inv, x[7] * inv) << 16);
+                if (ok) {
+                  const long long qo = base + half * f;
+                  *reinterpret_cast<uint2*>(p.out_q + qo) = make_uint2(c0, c1);
+                  if (kq == 0) {
+                    const int sub = (half * f + n0 + 32 * blk) / 32;
+                    p.out_sf[act_atom_byte(seg0, g, static_cast<int>(row - seg0), 2 * f / 128,
+                                           sub >> 2, sub & 3)] = static_cast<uint8_t>(X + 127);
+                  }
+                }
+              }
+            }
+            __syncwarp();                       // the block is read before it is refilled
+          }
+        }
+        continue;
+      }
       if (!valid) continue;
       if (MODE == GEMM_DGRAD2_SWIGLU) {
         // dh of columns [n0, n0 + 128) of f; the SwiGLU backward from the saved a, b gives
@@ -1134,7 +1232,7 @@ cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const C
                            const CUtensorMap& tsb, const CUtensorMap& tc, const MxParams& kp,
                            cudaStream_t st) {
   auto kern = mx_gemm_kernel<MODE, PAIR>;
-  constexpr size_t SMEM = mx_smem_bytes<PAIR, MODE == GEMM_WGRAD>();
+  constexpr size_t SMEM = mx_smem_bytes<PAIR, MODE>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
