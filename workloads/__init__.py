@@ -90,9 +90,12 @@ CONFIGS = {
 
 # Smaller shapes with the same per-expert GEMM shapes, for profiler captures that must
 # stay within a few GB of device memory: Mixtral's expert (d=4096, f=14336, ~1024 rows
-# per expert) with 2 experts and top-1.
+# per expert) with 2 experts and top-1; Qwen3's (d=2048, f=768, ~512 rows per expert,
+# the same Zipf skew) with a quarter of the tokens and experts.
 PROFILE_CONFIGS = {
     "mixtral_e2": MoEConfig("mixtral_e2", T=2048, d=4096, E=2, k=1, f=14336),
+    "qwen3_e32": MoEConfig("qwen3_e32", T=2048, d=2048, E=32, k=8, f=768, zipf_s=1.1,
+                           zipf_alpha=0.5),
 }
 
 
