@@ -43,12 +43,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# DRAM bytes per grouped-GEMM launch (average over the six launches of a step), from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the `mixtral_e2` profiling
-# shape -- the same per-expert GEMMs with 1/4 of the experts and 1/4 of the rows, every
-# operand and result scaling with those -- times 4.  Valid for the grouped-GEMM kernel as of
-# the swap-AB tail-tile version; set to None when the kernel changes.
-GEMM_TRAFFIC_PER_LAUNCH = {"mixtral": 4 * (654 + 341 + 484 + 252 + 671 + 545) / 6 * 1e6}
+# DRAM bytes per bf16 grouped-GEMM launch (average over the six launches of a step), from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of a profiling shape with
+# the same per-expert GEMMs and 1/4 of the experts and of the rows -- every operand and
+# result scales with those -- times 4: `mixtral_e2` for the Mixtral layer, `qwen3_e32` for
+# the Qwen3 layer.  Valid for the grouped-GEMM kernel as of the transposed-epilogue version;
+# set to None when the kernel changes.
+GEMM_TRAFFIC_PER_LAUNCH = {
+    "mixtral": (4 * (658.7 + 340.1 + 490.5 + 252.5 + 671.2 + 544.8) / 6 * 1e6, "mixtral_e2"),
+    "qwen3": (4 * (325.9 + 163.5 + 242.9 + 143.4 + 300.6 + 261.7) / 6 * 1e6, "qwen3_e32"),
+}
 
 
 def gemm_algorithmic_bytes(c, rows_kept: int) -> float:
@@ -647,6 +651,10 @@ def bench_ours(args, world, rank, local):
                 "tensor_ms": round(t_tensor * 1e3, 4), "hbm_ms": round(t_hbm * 1e3, 4),
                 "hbm_bound": t_hbm > t_tensor, "gemm_bytes": gbytes,
                 "gemm_gbs": round(gbytes / gemm_s_per_step / 1e9, 1)}
+    # measured DRAM traffic of the bf16 grouped GEMMs (the MXFP8 and recompute runs launch
+    # other kernels, which have no capture here)
+    traffic = (GEMM_TRAFFIC_PER_LAUNCH.get(c.name) if not args.mxfp8 and not c.recompute
+               else None)
     # algorithmic bytes of the HBM-bound steps (each source row read once, each
     # destination row written once, index arrays counted)
     T_, d_, k_, E_ = c.T, c.d, c.k, c.E
@@ -720,9 +728,10 @@ def bench_ours(args, world, rank, local):
                                      f"{' and weight gradients' if args.mx_wgrad else ''} at "
                                      f"2x, the rest at 1x bf16_tflops_sustained of "
                                      f"{peak_src}; burst {burst}"),
-                     "traffic": GEMM_TRAFFIC_PER_LAUNCH.get(c.name),
-                     "traffic_note": "DRAM bytes per launch, average of the 6 GEMM launches "
-                                     "(ncu on the mixtral_e2 shape x4)",
+                     "traffic": traffic[0] if traffic else None,
+                     "traffic_note": (f"DRAM bytes per launch, average of the 6 GEMM launches "
+                                      f"(ncu on the {traffic[1]} shape x4)" if traffic else
+                                      "no ncu capture of this configuration's GEMMs"),
                      "algorithmic_bytes_per_launch": round(
                          gemm_algorithmic_bytes(c, rows_kept) / 6),
                      "gemm_ms_per_step": round(gemm_ms / args.steps, 4),

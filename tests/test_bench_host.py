@@ -36,3 +36,17 @@ def test_expert_restriction_keeps_choices_and_weights(gate, scale):
     sub = oracle.route(c.replace(E=len(used)), np.ascontiguousarray(lg[:, used]))
     np.testing.assert_array_equal(used[sub["topk_idx"]], full["topk_idx"])
     np.testing.assert_array_equal(sub["topk_w"], full["topk_w"])
+
+
+@pytest.mark.parametrize("name", sorted(bench.GEMM_TRAFFIC_PER_LAUNCH))
+def test_measured_traffic_is_near_the_algorithmic_bytes(name):
+    """Each stored DRAM figure names a profiling shape with the same per-expert GEMMs at a
+    quarter of the rows and experts, and lies near the workload's algorithmic bytes per
+    launch (ncu counts writes still held in L2 at the launch's end as not yet written)."""
+    from workloads import PROFILE_CONFIGS
+    traffic, shape = bench.GEMM_TRAFFIC_PER_LAUNCH[name]
+    c, p = CONFIGS[name], PROFILE_CONFIGS[shape]
+    assert (p.d, p.f) == (c.d, c.f)
+    assert p.T * p.k * 4 == c.T * c.k and p.E * 4 == c.E
+    alg = bench.gemm_algorithmic_bytes(c, c.T * c.k) / 6
+    assert 0.8 * alg < traffic < 1.1 * alg
