@@ -250,14 +250,8 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA),
-// ordering this thread's earlier shared-memory writes before the arrive at cluster scope
-__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// the same without the cluster-scope release (no fence on this thread's earlier memory
-// operations): for hand-offs whose data is ordered by other means (tcgen05 fences)
+// with no cluster-scope release (no fence on this thread's earlier memory operations): for
+// hand-offs whose data is ordered by other means (tcgen05 fences)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
