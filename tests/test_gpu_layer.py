@@ -33,6 +33,13 @@ SMALL = {
     "T1": MoEConfig("T1_layer", T=1, d=128, E=4, k=2, f=128),
     "cap_tiny": MoEConfig("cap_tiny", T=256, d=128, E=8, k=2, f=128, cap_factor=0.1,
                           zipf_s=1.2),
+    # extreme skew: every token to the same expert (1100 rows = 4 whole M tiles and a
+    # 76-row tail tile; the seven other experts empty), and every token to the same two
+    # experts of sixteen, with a shared expert
+    "one_hot": MoEConfig("one_hot", T=1100, d=256, E=8, k=1, f=256, zipf_s=1.0,
+                         zipf_alpha=20.0),
+    "two_hot_shared": MoEConfig("two_hot", T=700, d=256, E=16, k=2, f=192, fs=128,
+                                gate="sigmoid", route_scale=2.5, zipf_s=1.0, zipf_alpha=20.0),
 }
 
 ROUTE_KEYS = ["topk_idx", "counts", "kept", "offsets", "dest_row", "src_tok", "src_slot",

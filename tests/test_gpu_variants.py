@@ -128,3 +128,62 @@ def test_recompute_is_bit_identical(base):
     R = c.T * c.k
     saved = R * 3 * c.f * 2 + (c.T * 3 * c.fs * 2 if c.fs else 0)
     assert l0.ctx.numel() - l1.ctx.numel() >= saved
+
+
+ALL_DROPPED = {
+    "plain": MoEConfig("alldrop", T=300, d=128, E=8, k=2, f=128, drop_negative=True),
+    "sig_shared": MoEConfig("alldrop_s", T=300, d=128, E=8, k=3, f=128, fs=192,
+                            gate="sigmoid", route_scale=2.5, drop_negative=True),
+}
+
+
+def all_negative(inp):
+    inp = dict(inp)
+    inp["logits"] = -(np.abs(inp["logits"]) + np.float32(0.5))
+    return inp
+
+
+@pytest.mark.parametrize("name", list(ALL_DROPPED))
+def test_every_assignment_dropped(name):
+    """Every router logit negative with negative-score dropping: no row is kept, so the
+    grouped GEMMs run with zero rows.  y and dx are the shared expert's alone (zero without
+    one), every routed weight gradient and dlogits are zero, and the status stays clean."""
+    c = ALL_DROPPED[name]
+    inp = all_negative(gen_inputs_host(c))
+    layer, y, gr = run_layer(c, {k: dev(v) for k, v in inp.items()})
+    assert layer.status() == (0, 0)
+    fo = oracle.layer_fwd(c, inp)
+    bo = oracle.layer_bwd(c, inp, fo)
+    assert fo["route"]["offsets"][-1] == 0
+    v = layer.views()
+    for key in ROUTE_KEYS:
+        np.testing.assert_array_equal(np_i(v[key]), fo["route"][key], err_msg=key)
+    assert (f64(gr["dW1"]) == 0).all() and (f64(gr["dW2"]) == 0).all()
+    assert (f64(gr["dlogits"]) == 0).all()
+    if c.fs:
+        assert_close("y", f64(y), fo["y"])
+        assert_close("dx", f64(gr["dx"]), bo["dx"])
+        assert_close("dW1s", f64(gr["dW1s"]), bo["dW1s"])
+        assert_close("dW2s", f64(gr["dW2s"]), bo["dW2s"])
+    else:
+        assert (f64(y) == 0).all() and (f64(gr["dx"]) == 0).all()
+
+
+@pytest.mark.parametrize("level", [1, 2])
+def test_every_assignment_dropped_mx(level):
+    """The same degenerate routing through the MXFP8 layer calls (level 2: the MXFP8
+    weight-gradient path with zero rows per expert)."""
+    c = ALL_DROPPED["plain"]
+    inp = all_negative(gen_inputs_host(c))
+    g = {k: dev(v) for k, v in inp.items()}
+    cfg = tde.make_config(c.T, c.d, c.E, c.k, c.f, drop_negative=True, mxfp8=level)
+    layer = tde.MoELayer(cfg)
+    wq = layer.quantize_weights(g["W1"], g["W2"])
+    y = layer.forward_mx(g["logits"], g["x"], wq)
+    gr = layer.backward_mx(g["logits"], g["x"], g["dy"], wq)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    assert int(layer.views()["offsets"][-1]) == 0
+    for name, t in [("y", y), ("dx", gr["dx"]), ("dW1", gr["dW1"]), ("dW2", gr["dW2"]),
+                    ("dlogits", gr["dlogits"])]:
+        assert (f64(t) == 0).all(), name

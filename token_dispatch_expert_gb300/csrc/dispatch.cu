@@ -217,29 +217,46 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
     }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) dot[j] = warp_sum(dot[j]);
+    // Both gates normalise over the k selected experts, so the gradient of slot j is
+    // proportional to dot_j - sum_i u_i dot_i with sum_i u_i = 1 (u: the normalised
+    // scores).  It is summed pairwise, sum_i u_i (dot_j - dot_i): when one score carries
+    // almost all the weight the direct form subtracts two nearly equal fp32 numbers and
+    // keeps only a few bits of a tiny result, the pairwise form keeps them all.
     float dl[KMAX];
     if (gate == MOE_GATE_SOFTMAX_TOPK) {
-      float sw = 0.0f;
+      // dl_j = w_j (dot_j - sum_i w_i dot_i)
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (j < k) sw += wt[j] * dot[j];
+      for (int j = 0; j < KMAX; ++j) {
+        float acc = 0.0f;
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) dl[j] = wt[j] * (dot[j] - sw);
+        for (int i = 0; i < KMAX; ++i)
+          if (i < k && i != j) acc = fmaf(wt[i], dot[j] - dot[i], acc);
+        dl[j] = wt[j] * acc;
+      }
     } else {
-      float sg[KMAX], S = 0.0f, sd = 0.0f;
+      // w_j = scale s_j / S with s = sigma(logit), S = sum_i s_i:
+      // dl_j = scale / S^2 (sum_i s_i (dot_j - dot_i)) s_j (1 - s_j), with 1 - s_j taken
+      // as sigma(-logit) so that it does not round to 0 for large logits
+      float sg[KMAX], sm[KMAX], S = 0.0f;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         sg[j] = 0.0f;
+        sm[j] = 0.0f;
         if (j < k && se[j] >= 0) {
-          sg[j] = 1.0f / (1.0f + expf(-__ldg(logits + t * E + se[j])));
+          const float l = __ldg(logits + t * E + se[j]);
+          sg[j] = 1.0f / (1.0f + expf(-l));
+          sm[j] = 1.0f / (1.0f + expf(l));
           S += sg[j];
-          sd += sg[j] * dot[j];
         }
       }
+      const float c = scale / (S * S);
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
-        const float ds = scale * (dot[j] / S - sd / (S * S));
-        dl[j] = ds * sg[j] * (1.0f - sg[j]);
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i)
+          if (i < k && i != j) acc = fmaf(sg[i], dot[j] - dot[i], acc);
+        dl[j] = c * acc * sg[j] * sm[j];
       }
     }
     for (int e = lane; e < E; e += 32) {
