@@ -545,15 +545,18 @@ def bench_ours(args, world, rank, local):
                 o["dW1s"] = shared["dW1"]; o["dW2s"] = shared["dW2"]
             bufs.append({"logits": torch.empty_like(g["logits"]), "x": torch.empty_like(g["x"]),
                          "dy": torch.empty_like(g["dy"]), "y": torch.empty_like(y), "out": o})
-        cstream = torch.cuda.Stream(device=dev)
+        # one copy stream per direction: a step's inputs come in while the previous step's
+        # results go out (the two directions have their own copy engines)
+        in_stream = torch.cuda.Stream(device=dev)
+        out_stream = torch.cuda.Stream(device=dev)
         ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "done", "copied")}
 
         def copy_in(b):
-            with torch.cuda.stream(cstream):
+            with torch.cuda.stream(in_stream):
                 bufs[b]["logits"].copy_(h_logits, non_blocking=True)
                 bufs[b]["x"].copy_(h_x, non_blocking=True)
                 bufs[b]["dy"].copy_(h_dy, non_blocking=True)
-                ev["in"][b].record(cstream)
+                ev["in"][b].record(in_stream)
 
         def e2e_run(n):
             copy_in(0)
@@ -578,14 +581,14 @@ def bench_ours(args, world, rank, local):
                 ev["done"][b].record(stream)
                 if i + 1 < n:
                     if i >= 1:   # buffer 1-b was last read by step i-1
-                        cstream.wait_event(ev["done"][1 - b])
+                        in_stream.wait_event(ev["done"][1 - b])
                     copy_in(1 - b)
-                with torch.cuda.stream(cstream):
-                    cstream.wait_event(ev["done"][b])
+                with torch.cuda.stream(out_stream):
+                    out_stream.wait_event(ev["done"][b])
                     h_y.copy_(B["y"], non_blocking=True)
                     h_dx.copy_(B["out"]["dx"], non_blocking=True)
                     h_dl.copy_(B["out"]["dlogits"], non_blocking=True)
-                    ev["copied"][b].record(cstream)
+                    ev["copied"][b].record(out_stream)
             stream.wait_event(ev["copied"][(n - 1) & 1])
 
         e2e_run(max(1, args.warmup))
