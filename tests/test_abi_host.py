@@ -36,6 +36,7 @@ def test_every_declared_symbol_is_exported(L):
 def test_binding_names_match_the_header():
     for n in declared_symbols():
         assert hasattr(tde, n), n
+        assert n in tde.__all__, n
 
 
 def cfg_of(c):

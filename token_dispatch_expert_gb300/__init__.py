@@ -21,6 +21,10 @@ __all__ = [
     "moe_capacity_from_factor", "moe_workspace_size", "moe_ctx_offsets", "moe_ws_init",
     "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_combine_bwd",
     "moe_grouped_ffn_bwd", "moe_unpermute_reduce", "moe_layer_fwd", "moe_layer_bwd",
+    "moe_grouped_ffn_gather", "moe_grouped_ffn_bwd_gather",
+    "moe_mx_weights_size", "moe_mx_quantize_weights", "moe_mx_act_scales_size",
+    "moe_mx_permute_quant", "moe_grouped_ffn_mx", "moe_grouped_ffn_bwd_mx", "moe_layer_fwd_mx",
+    "moe_layer_bwd_mx",
     "moe_status", "moe_status_string", "moe_selftest_wait_timeout", "ctx_views", "MoELayer", "CTX_FIELDS",
 ]
 
