@@ -133,3 +133,12 @@ def test_status_strings(L):
     for s, name in tde.STATUS.items():
         assert tde.moe_status_string(s) == name
     assert tde.moe_status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The binding hands kernels raw pointers: a host tensor or a non-contiguous view is
+    refused before any call."""
+    import torch
+    with pytest.raises(ValueError, match="CUDA"):
+        tde._p(torch.zeros(4))
+    assert tde._p(None) is None and tde._p(1234) == 1234

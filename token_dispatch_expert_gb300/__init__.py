@@ -118,11 +118,17 @@ def make_config(T, d, E, k, ffn, ffn_shared=0, gate="softmax", route_scale=1.0,
 
 
 def _p(t):
-    """Device pointer of a tensor (or an int address); None -> NULL."""
+    """Device pointer of a tensor (or an int address); None -> NULL.  The C calls take
+    dense row-major device buffers: a host tensor or a strided view is refused here rather
+    than handed to a kernel as a pointer."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got strides {tuple(t.stride())}")
     return t.data_ptr()
 
 
