@@ -213,11 +213,7 @@ class OracleTimer:
 
         oracle.build()
         self.c = c
-        self.threads = os.cpu_count() or 1
-        try:
-            self.threads = len(os.sched_getaffinity(0))
-        except AttributeError:
-            pass
+        self.threads = oracle.threads()     # what its OpenMP loops run on
         self.logits = gen_logits(c)
         self.x = gen_bf16(c, "x", (c.T, c.d))
         self.dy = gen_bf16(c, "dy", (c.T, c.d))

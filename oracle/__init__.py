@@ -31,4 +31,5 @@ from .layer import (  # noqa: F401
     ffn_wgrad_rows_mx,
     HostSource,
     TorchSource,
+    threads,
 )

@@ -47,6 +47,8 @@ def _load():
         lib = ctypes.CDLL(_LIB)
         P = ctypes.c_void_p
         i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.orc_threads.argtypes = []
+        lib.orc_threads.restype = i32
         lib.orc_bf16.argtypes = [f64]
         lib.orc_bf16.restype = f64
         lib.orc_round_bf16_array.argtypes = [P, i64]
@@ -70,6 +72,11 @@ def _load():
         lib.orc_unpermute_reduce.argtypes = [i64, P, i32, i32, P, P, P, P, i32, P]
         _lib = lib
     return _lib
+
+
+def threads() -> int:
+    """Threads the C oracle's parallel loops run on (OpenMP's current maximum)."""
+    return int(_load().orc_threads())
 
 
 def _p(a):

@@ -73,6 +73,20 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads an OpenMP loop of this library runs on (1 without OpenMP): what a timing of the
+ * oracle reports as its core count. */
+int orc_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 #define GATE_SOFTMAX 0
 #define GATE_SIGMOID 1

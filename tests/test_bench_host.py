@@ -50,3 +50,48 @@ def test_measured_traffic_is_near_the_algorithmic_bytes(name):
     assert p.T * p.k * 4 == c.T * c.k and p.E * 4 == c.E
     alg = bench.gemm_algorithmic_bytes(c, c.T * c.k) / 6
     assert 0.8 * alg < traffic < 1.1 * alg
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _reference_lines(cmd, env_threads):
+    import json, os, subprocess, sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {**os.environ, "OMP_NUM_THREADS": str(env_threads)}
+    out = subprocess.run([sys.executable, *cmd], cwd=root, capture_output=True, text=True,
+                         timeout=900, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    return [json.loads(l) for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def _check_reference_line(d, n_gpus, threads):
+    assert d["impl"] == "reference" and d["n_gpus"] == n_gpus
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] == threads
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_one_line():
+    """`bench.py --impl reference` times the oracle on the host (no GPU needed) and prints
+    one JSON line whose core count is the threads the oracle actually ran on."""
+    lines = _reference_lines(["bench.py", "--impl", "reference", "--config", "tiny",
+                              "--steps", "1", "--warmup", "3"], 2)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 1, 2)
+
+
+def test_reference_arm_under_two_ranks():
+    """Launched as two ranks, rank 0 alone runs and prints; the other rank exits 0."""
+    lines = _reference_lines(["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node",
+                              "2", "--master-addr", "127.0.0.1", "--master-port",
+                              str(_free_port()), "bench.py", "--impl", "reference", "--gpus",
+                              "2", "--config", "tiny", "--steps", "1", "--warmup", "3"], 1)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 2, 1)
