@@ -22,6 +22,12 @@ CFGS = {
     "softmax_cap": MoEConfig("g_cap", T=48, d=64, E=4, k=2, f=64, cap_factor=0.5, zipf_s=1.5),
     "sigmoid_shared": MoEConfig("g_sig", T=36, d=64, E=5, k=3, f=64, fs=64, gate="sigmoid",
                                 route_scale=2.5, cap_factor=0.8, zipf_s=1.2),
+    # one score carries almost all the weight (a 14-logit gap between the two selected
+    # experts): the gate gradient is a tiny difference of nearly equal terms
+    "sigmoid_dominant": MoEConfig("g_dom", T=32, d=64, E=6, k=2, f=64, gate="sigmoid",
+                                  route_scale=2.5, zipf_s=1.0, zipf_alpha=20.0),
+    "softmax_dominant": MoEConfig("g_sdom", T=32, d=64, E=6, k=2, f=64, zipf_s=1.0,
+                                  zipf_alpha=20.0),
 }
 
 
