@@ -263,7 +263,9 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *yp, const int32_t 
  *   softmax gate: dlogits[t,e_j] = w_j (dw_j - sum_i w_i dw_i)
  *   sigmoid gate: S = sum_i s_i, s_i = sigma(l_i):
  *                 dlogits[t,e_j] = scale (dw_j / S - sum_i s_i dw_i / S^2) s_j (1 - s_j)
- *   dlogits [T,E] fp32 out, zero for unselected experts.
+ *   dlogits [T,E] fp32 out, zero for unselected experts.  Both are evaluated in the
+ *   equal pairwise form sum_i u_i (dw_j - dw_i) (u_i the normalised scores, summing to 1),
+ *   which keeps its precision when one score carries almost all the weight.
  */
 moe_status_t moe_combine_bwd(const moe_config_t *cfg, const void *dy, const void *yp,
                              const float *logits, const int32_t *topk_idx, const float *topk_w,
