@@ -700,7 +700,9 @@ def bench_ours(args, world, rank, local):
                                   else ""),
                    "tokens_per_step": c.T, "rows_kept": rows_kept,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "no flush: each step streams >10 GB of weights/grads (> 129 MB L2)"},
+                   "l2": (f"no flush: each step's GEMMs alone stream "
+                          f"{sum(b for _, b in gemm_phases(c, rows_kept)) / 1e9:.1f} GB of "
+                          f"weights, gradients and activations (L2 is 129 MB)")},
         "roofline": {"kernel": ("whole step, GEMM flops incl. the recomputed FC1 over the "
                                 "step time" if c.recompute else
                                 "grouped_gemm (tcgen05; FC1, FC2, 2 dgrad, 2 wgrad per step)"),
