@@ -10,6 +10,8 @@ Tokens whose k-th and (k+1)-th logits are closer than 10 eps are skipped for the
 logit derivatives, because the selection would flip inside the difference stencil.
 """
 
+import math
+
 import numpy as np
 import pytest
 
@@ -103,3 +105,35 @@ def test_backward_equals_finite_differences(name):
             fd = (lp - lm) / (2 * eps)
             tol = 1e-6 * max(1.0, abs(fd))
         assert abs(fd - b[grad][idx]) <= tol, (leaf, idx, fd, b[grad][idx])
+
+
+@pytest.mark.parametrize("gate", ["softmax", "sigmoid"])
+def test_two_expert_gate_gradient_closed_form(gate):
+    """k = 2 closed forms, derived by hand, with g_j = <dy, yp_j>:
+    softmax, w_0 = 1 / (1 + exp(l_1 - l_0)):  dl_0 = -dl_1 = w_0 w_1 (g_0 - g_1);
+    sigmoid, w_j = s sigma_j / S, S = sigma_0 + sigma_1:
+        dl_0 = s sigma_0 (1 - sigma_0) sigma_1 (g_0 - g_1) / S^2, and symmetrically."""
+    scale = 2.5 if gate == "sigmoid" else 1.0
+    cfg = MoEConfig("cf_" + gate, T=24, d=8, E=4, k=2, f=8, gate=gate, route_scale=scale)
+    lg = np.random.default_rng(3).standard_normal((cfg.T, cfg.E)).astype(np.float32) * 3
+    r = oracle.route(cfg, lg)
+    rng = np.random.default_rng(4)
+    yp = rng.standard_normal((cfg.T * cfg.k, cfg.d))
+    dy = rng.standard_normal((cfg.T, cfg.d))
+    _, dl = oracle.combine_bwd(cfg, lg, r, dy, yp, rnd=False)
+    for t in range(cfg.T):
+        e0, e1 = r["topk_idx"][t]
+        g0, g1 = (float(dy[t] @ yp[r["dest_row"][t, j]]) for j in range(2))
+        l0, l1 = float(lg[t, e0]), float(lg[t, e1])
+        if gate == "softmax":
+            w0 = 1.0 / (1.0 + math.exp(l1 - l0))
+            d0 = w0 * (1.0 - w0) * (g0 - g1)
+            d1 = -d0
+        else:
+            s0, s1 = 1.0 / (1.0 + math.exp(-l0)), 1.0 / (1.0 + math.exp(-l1))
+            S = s0 + s1
+            d0 = scale * s0 * (1.0 - s0) * s1 * (g0 - g1) / S ** 2
+            d1 = scale * s1 * (1.0 - s1) * s0 * (g1 - g0) / S ** 2
+        others = [e for e in range(cfg.E) if e not in (e0, e1)]
+        np.testing.assert_allclose([dl[t, e0], dl[t, e1]], [d0, d1], rtol=1e-12, atol=1e-15)
+        assert (dl[t, others] == 0).all()
