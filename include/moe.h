@@ -196,12 +196,19 @@ moe_status_t moe_route(const moe_config_t *cfg, const float *logits, int32_t *to
  *   Arguments as for moe_route, except that `ws` is replaced by dev_flags_or_null: an
  *   optional device int32 that receives the MOE_DEVERR_* bits (NaN logits); with NULL
  *   those flags are dropped.
- *   Limit: ceil(T/32) * E * 4 bytes must fit in MOE_NOALLOC_ROUTE_SCRATCH_BYTES (for
- *   example T = 32768 with E = 256); larger shapes return MOE_ERR_UNSUPPORTED with
- *   nothing enqueued.
+ *   Limit: the routing scratch must fit in MOE_NOALLOC_ROUTE_SCRATCH_BYTES.  With
+ *   up(n) = n rounded up to a multiple of 256, it takes
+ *       up(ceil(T/32) * E * 4)                                  bytes, plus, only when
+ *       drop_by_score is set with a capacity,  up((E+1) * 4) + up(T * k * 4)  bytes
+ *   (each expert's base and one 32-bit word per assignment for the score ranking).
+ *   Examples that fit: plain or token-order capacity routing up to T = 32768 with
+ *   E = 256 (exactly 1 MiB); drop-by-score routing with T = 16384, E = 64, k = 6
+ *   (128 KiB + 512 B + 384 KiB).  T = 32768, E = 256 with drop_by_score does not fit.
+ *   Larger shapes return MOE_ERR_UNSUPPORTED with nothing enqueued.
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any
- *   stream capture.
+ *   stream capture.  Only a successful lookup is remembered: if it fails (the call
+ *   returns MOE_ERR_CUDA, nothing enqueued), the next call on that device tries again.
  *   Sharing: every call on a device uses the same array and leaves its contents behind
  *   (the kernels overwrite every entry they read, so nothing has to be cleared between
  *   calls); calls whose execution overlaps on the GPU -- e.g. on two streams without an

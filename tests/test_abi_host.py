@@ -142,3 +142,29 @@ def test_binding_refuses_host_and_strided_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         tde._p(torch.zeros(4))
     assert tde._p(None) is None and tde._p(1234) == 1234
+
+
+def test_noalloc_route_refusals_before_any_device_call(L):
+    """moe_route_noalloc validates its arguments and the size of its fixed scratch on the
+    host: null or misaligned pointers and shapes whose routing scratch exceeds the array
+    are refused before anything touches a device."""
+    def cfg(T, E, k, cap=0, by_score=False):
+        return tde.make_config(T, 64, E, k, 64, capacity=cap, drop_by_score=by_score)
+
+    ok = [16] * 10
+    c = cfg(64, 8, 2)
+    assert L.moe_route_noalloc(ctypes.byref(c), *([None] * 10), None, None) == 1
+    assert L.moe_route_noalloc(ctypes.byref(c), 8, *ok[1:], None, None) == 1    # misaligned
+    assert L.moe_route_noalloc(ctypes.byref(c), *ok, 18, None) == 1             # flags word
+    # plain routing: ceil(T/32) * E * 4 bytes; T = 32768 more than E = 256 allows
+    assert L.moe_route_noalloc(ctypes.byref(cfg(32769, 256, 8)), *ok, None, None) == 2
+    # drop by score adds (E+1)*4 and T*k*4 bytes (each rounded up to 256): with E = 64 and
+    # k = 8 the 1 MiB array holds T = 26200 and not one token more
+    assert L.moe_route_noalloc(ctypes.byref(cfg(26201, 64, 8, 1, True)), *ok, None, None) == 2
+    # the same shape routed by token order needs only the histogram: not refused for size
+    # (with a device present this would launch, so it is only called where there is none)
+    import torch
+    if not torch.cuda.is_available():
+        for c2 in (cfg(26201, 64, 8, 1, False), cfg(26200, 64, 8, 1, True),
+                   cfg(32768, 256, 8)):
+            assert L.moe_route_noalloc(ctypes.byref(c2), *ok, None, None) == 3   # no device

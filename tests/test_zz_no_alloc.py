@@ -25,7 +25,7 @@ KEYS = ["topk_idx", "topk_w", "counts", "kept", "offsets", "dest_row", "src_tok"
         "drop_mask"]
 
 
-def route_both(c, logits):
+def route_both(c, logits, with_flags=True):
     cfg = cfg_c(c)
     ws = new_ws(cfg)
     ref = alloc_route(c)
@@ -34,7 +34,7 @@ def route_both(c, logits):
     for t in got.values():
         t.fill_(-7) if t.dtype != torch.float32 else t.fill_(float("nan"))
     flags = torch.zeros(4, dtype=torch.int32, device="cuda")
-    tde.moe_route_noalloc(cfg, logits, *[got[k] for k in KEYS], flags)
+    tde.moe_route_noalloc(cfg, logits, *[got[k] for k in KEYS], flags if with_flags else None)
     torch.cuda.synchronize()
     return ref, got, flags
 
@@ -64,4 +64,24 @@ def test_noalloc_route_reports_nan_and_rejects_oversize():
     out = alloc_route(big.replace(T=1))   # never touched: the call is refused up front
     with pytest.raises(tde.MoEError) as ei:
         tde.moe_route_noalloc(cfg_c(big), out["topk_w"], *[out[k] for k in KEYS])
+    assert ei.value.status == 2
+
+
+def test_noalloc_route_at_the_size_limit_and_without_flags():
+    """Drop-by-score routing with E = 64, k = 8 needs ceil(T/32)*E*4 + (E+1)*4 + T*k*4 bytes
+    (each part rounded up to 256): T = 26200 fills the 1 MiB array exactly and runs; one
+    token more is refused.  Both calls here pass no flags word (dev_flags = NULL), which
+    must leave the outputs unchanged."""
+    c = MoEConfig("nal_edge", T=26200, d=64, E=64, k=8, f=64, cap_factor=1.0, zipf_s=1.5,
+                  drop_by_score=True)
+    logits = dev(gen_logits(c))
+    for _ in range(2):
+        ref, got, _ = route_both(c, logits, with_flags=False)
+        for k in KEYS:
+            assert torch.equal(ref[k], got[k]), k
+        assert int((got["drop_mask"] != 0).sum()) > 0     # the capacity really cuts
+    over = c.replace(T=26201)
+    out = alloc_route(over)
+    with pytest.raises(tde.MoEError) as ei:
+        tde.moe_route_noalloc(cfg_c(over), dev(gen_logits(over)), *[out[k] for k in KEYS])
     assert ei.value.status == 2

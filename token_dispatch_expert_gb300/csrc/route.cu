@@ -444,7 +444,9 @@ cudaError_t launch_route(const moe_config_t* c, const float* logits, int32_t* to
 // the caller's `ws`.  The caller still passes every input and output.
 //
 // The array below is MOE_NOALLOC_ROUTE_SCRATCH_BYTES (1 MiB) per GPU; every GPU that loads
-// the library holds it until the process exits.  All calls share it and it keeps the last
+// the library holds it until the process exits.  A shape fits when route_scratch_bytes()
+// does: the chunk histogram, plus (drop by score with a capacity) the experts' bases and
+// one word per assignment.  All calls share it and it keeps the last
 // call's contents (the kernels overwrite every entry they read, so nothing needs
 // clearing); calls whose execution overlaps on the GPU therefore race on it.
 namespace {
@@ -453,21 +455,27 @@ __device__ __align__(256) int32_t g_noalloc_route_scratch[MOE_NOALLOC_ROUTE_SCRA
                                                           sizeof(int32_t)];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_noalloc_once[kMaxDevices];
-int32_t* g_noalloc_ptr[kMaxDevices];
-cudaError_t g_noalloc_err[kMaxDevices];
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[kMaxDevices];   // guarded by g_noalloc_mu; null until looked up
 
 // The host-side name of a __device__ array is only a stand-in, not a device address:
-// look the real address up once per device, with that device current.
+// look the real address up with that device current.  Only a successful lookup is kept;
+// a failed one (e.g. made while a stream capture forbids it) is retried by the next call,
+// and the error it leaves pending is cleared so that no later launch check reports it.
 cudaError_t noalloc_scratch(int dev, int32_t** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_noalloc_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
-    g_noalloc_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_route_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_route_scratch);
+    if (e != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    }
     g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
-  });
+  }
   *out = g_noalloc_ptr[dev];
-  return g_noalloc_err[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
