@@ -8,13 +8,13 @@
  * backward.
  *
  * Where each operation is defined (page title, then section / figure / field):
- *   - "MoE Training Optimization with Primus" (AMD blog), Figure 7 dataflow: the router
- *     picks each token's top-k experts; a permutation gathers tokens into expert
- *     order; FC1 (gate/up) and FC2 (down) grouped GEMMs with SwiGLU between them;
- *     a final unpermute-and-scale reduces the top-k contributions onto each token.
+ *   - "MoE Training Optimization with Primus" (AMD blog), Figure 7 dataflow: router
+ *     top-k per token; a permutation into expert order; FC1 (gate/up) and FC2 (down)
+ *     grouped GEMMs with SwiGLU between them; a last step that un-permutes the rows,
+ *     scales them by the gate weights and sums each token's k of them.
  *     MegaMoE section: the backward by dispatch/combine duality plus two
  *     variable-K weight-gradient GEMMs.  JAX section: one grouped-GEMM launch over
- *     ragged variable-M expert groups; "sync-free" token counts kept on the GPU.
+ *     ragged variable-M expert groups; token counts stay on the GPU (no host sync).
  *   - X-MoE verdict page (pith.science, arXiv 2508.13337), "key machinery": the
  *     padding-free token buffer -- only the routed tokens, stored contiguously per
  *     expert, with token ids, expert ids, per-expert counts and combine weights;
@@ -220,8 +220,8 @@ moe_status_t moe_route_noalloc(const moe_config_t *cfg, const float *logits, int
                                uint8_t *drop_mask, int32_t *dev_flags_or_null, void *stream);
 
 /*
- * F3: permute-gather into expert order (Primus MoE blog, Figure 7: "a permutation
- * gathers tokens into expert order"; X-MoE padding-free buffer).
+ * F3: permute-gather into expert order (Primus MoE blog, Figure 7, the permutation step
+ * before FC1; X-MoE padding-free buffer).
  *   xp[p] = x[src_tok[p]] for p < offsets[E]; rows past offsets[E] are not written.
  *   x [T,d] bf16 in, xp [T*k,d] bf16 out.  A pure bit copy.
  */
@@ -264,8 +264,8 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *yp, const int32_t 
                          void *stream);
 
 /*
- * B1: backward of combine and of the gate (Primus MoE blog, MegaMoE section:
- * "dispatch(dy)").  For each kept slot (t,j) with row p = dest_row[t,j]:
+ * B1: backward of combine and of the gate (Primus MoE blog, MegaMoE section: the
+ * dispatch of the upstream gradient dy).  For each kept slot (t,j) with row p = dest_row[t,j]:
  *   dyp[p] = bf16(topk_w[t,j] * dy[t]);  dw[t,j] = <dy[t], yp[p]> (0 if dropped)
  *   softmax gate: dlogits[t,e_j] = w_j (dw_j - sum_i w_i dw_i)
  *   sigmoid gate: S = sum_i s_i, s_i = sigma(l_i):
@@ -306,8 +306,8 @@ moe_status_t moe_grouped_ffn_bwd_gather(const moe_config_t *cfg, const void *dyp
                                         void *dW2, void *ws, void *stream);
 
 /*
- * B6: un-permute reduce (Primus MoE blog, MegaMoE section: "the FC1 data-gradient
- * fuses with the combine and reduction").
+ * B6: un-permute reduce (Primus MoE blog, MegaMoE section: the reduction of each
+ * token's rows after the FC1 data gradient).
  *   dx[t] = sum_{j kept} dxp[dest_row[t,j]] (+ dxs[t] if dxs_or_null), fp32 accumulation,
  *   gathered per token (deterministic, no atomics); bf16 [T,d] out.
  */

@@ -10,7 +10,7 @@
  * in double precision:
  *
  *   route       top-k selection on the fp32 router logits, the gate weights, the
- *               per-expert histogram, capacity dropping "only on overflow" in token
+ *               per-expert histogram, capacity dropping only on overflow, in token
  *               order, the exclusive scan of kept counts into segment offsets, and
  *               the padding-free token buffer's side arrays (token ids, slot ids,
  *               destination rows).  X-MoE verdict page (arXiv 2508.13337):
@@ -18,14 +18,13 @@
  *               ids, per-expert counts and combine weights), referee minor comment
  *               on section 4.1.1 Listing 1 (max_token_count = floor(c*S*K/E)) and
  *               major comment on section 5.6 (drops only on capacity).
- *               Primus MoE blog, Figure 7 dataflow: "the router scores each token
- *               and picks its top-k experts", "a permutation gathers tokens into
- *               expert order".
+ *               Primus MoE blog, Figure 7 dataflow: the router step and the
+ *               permutation into expert order.
  *   ffn         SwiGLU expert FFN with three matrices (gate, up: d x f; down: f x d).
  *               Primus MoE blog, Figure 7 dataflow (FC1 gate/up, SwiGLU, FC2 down);
  *               DeepSeek-V3 memory-model page, "key machinery" (three matrices per
  *               expert).
- *   combine     unpermute-and-scale: y[t] = sum over kept slots of w * yp[row].
+ *   combine     un-permute and scale: y[t] = sum over kept slots of w * yp[row].
  *               Primus MoE blog, Figure 7 dataflow, last step.
  *   mxfp8       MX block quantisation (OCP Microscaling formats v1.0: one E8M0 power-of-two
  *               scale per block of 32 consecutive elements along the contraction axis,
@@ -35,10 +34,10 @@
  *               contraction axis; the weight gradients stay bf16).  Primus MoE blog, FP8
  *               section (MXFP8 recipe, OCP E4M3 expert GEMMs) and MegaMoE section (the
  *               SwiGLU step quantises its own output).
- *   backward    dispatch(dy) -> FC2 data-grad, FC1 data-grad -> combine/reduce,
- *               plus the two variable-K weight gradients.  Primus MoE blog,
- *               MegaMoE section ("dispatch/combine duality") and the JAX grouped
- *               GEMM paragraph (two backward grouped GEMMs incl. variable-K).
+ *   backward    dy dispatched to the rows -> FC2 data-grad, FC1 data-grad -> per-token
+ *               reduce, plus the two variable-K weight gradients.  Primus MoE blog,
+ *               MegaMoE section (the dispatch/combine duality) and the JAX grouped
+ *               GEMM paragraph (the backward's grouped GEMMs, variable K included).
  *
  * Rounding points: when `rnd` is non-zero every tensor that the GPU path stores in
  * bf16 (a, b, h, yp, y, dyp, da, db, dxp, dx) is rounded to bf16 (round to nearest,

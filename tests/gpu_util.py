@@ -9,6 +9,11 @@ The second form is the max-abs bound of 2e-2 taken on the tensor's own scale; di
 by rms(o) + |o_i| keeps a one-ulp bf16 rounding difference on a large element (which
 any correct bf16 kernel may show) inside the bound while still bounding the error of
 every small element by 2e-2 * rms.
+
+Every comparison also records, for the report printed at the end of the run
+(tests/conftest.py): the raw max |g - o|, max |g - o| / rms(o) (the max-abs bound read on
+the tensor's RMS alone), and how many elements differ from the oracle by more than one
+bf16 ulp of the oracle's value (ulp(o) = 2^(floor(log2 |o|) - 7), 2^-133 at zero).
 """
 
 import numpy as np
@@ -54,18 +59,42 @@ def np_i(t) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
+def bf16_ulp(o) -> np.ndarray:
+    """One bf16 unit in the last place at each value of o (8 significant bits): 2^(e - 7)
+    for 2^e <= |o| < 2^(e+1), floored at the smallest bf16 subnormal 2^-133."""
+    o = np.abs(np.asarray(o, np.float64))
+    _, ex = np.frexp(o)                      # o = m * 2^ex, m in [0.5, 1)
+    return np.where(o < 2.0 ** -126, 2.0 ** -133, np.ldexp(1.0, ex - 8))
+
+
 def stats(g, o):
     g = np.asarray(g, np.float64); o = np.asarray(o, np.float64)
+    if not o.size:
+        return {"rel_l2": 0.0, "max_scaled": 0.0, "max_abs": 0.0, "max_over_rms": 0.0,
+                "n_gt_1ulp": 0, "n": 0}
     diff = np.abs(g - o)
     nrm = np.linalg.norm(o)
     rel = float(np.linalg.norm(g - o) / nrm) if nrm > 0 else float(np.linalg.norm(g - o))
-    rms = float(np.sqrt(np.mean(o * o))) if o.size else 0.0
-    mx = float((diff / (rms + np.abs(o) + 1e-30)).max()) if o.size else 0.0
-    return {"rel_l2": rel, "max_scaled": mx, "max_abs": float(diff.max()) if o.size else 0.0}
+    rms = float(np.sqrt(np.mean(o * o)))
+    mx = float((diff / (rms + np.abs(o) + 1e-30)).max())
+    return {"rel_l2": rel, "max_scaled": mx, "max_abs": float(diff.max()),
+            "max_over_rms": float(diff.max() / rms) if rms > 0 else float(diff.max()),
+            "n_gt_1ulp": int((diff > bf16_ulp(o)).sum()), "n": int(o.size)}
+
+
+# (test id, tensor name, stats) of every comparison in this process, for the end-of-run
+# report; the test id is set by an autouse fixture in conftest.py
+RECORDS = []
+CURRENT_TEST = ["?"]
+
+
+def record(name, s):
+    RECORDS.append((CURRENT_TEST[0], name, s))
 
 
 def assert_close(name, g, o, rel_tol=REL_L2_TOL, max_tol=MAX_TOL):
     s = stats(g, o)
+    record(name, s)
     assert np.isfinite(np.asarray(g, np.float64)).all(), f"{name}: non-finite values"
     assert s["rel_l2"] <= rel_tol and s["max_scaled"] <= max_tol, f"{name}: {s}"
     return s

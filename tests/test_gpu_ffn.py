@@ -177,10 +177,11 @@ def test_grouped_ffn_segment_edges(name):
 
 
 @pytest.mark.parametrize("name", list(CASES) + ["edges"])
-def test_gather_fused_ffn_is_bit_identical(name):
+def test_gather_fused_ffn_against_oracle(name):
     """The permute folded into FC1's operand loads (and into the FC1 weight gradient's):
-    the gathered rows are the same bf16 values the permute would have written, so every
-    output must equal the unfused path bit for bit."""
+    every output is compared with the oracle's per-expert rows on the gathered tokens
+    (ab, h, yp; dab, dxp, dW1, dW2), and must also equal the unfused path bit for bit (the
+    gathered rows are the same bf16 values the permute would have written)."""
     if name == "edges":
         sizes = [1, 64, 127, 128, 129, 255, 300, 600, 0, 385]
         c = MoEConfig("edges_g", T=sum(sizes), d=320, E=len(sizes), k=1, f=192)
@@ -206,10 +207,23 @@ def test_gather_fused_ffn_is_bit_identical(name):
     tde.moe_grouped_ffn(cfg, xp, d_off, W1, W2, *out_u, ws)
     tde.moe_grouped_ffn_gather(cfg, x, d_src, d_off, W1, W2, *out_g, ws)
     torch.cuda.synchronize()
-    for a, b, nm in zip(out_u, out_g, ("ab", "h", "yp")):
+    # the oracle on the rows the gather reads: xp[p] = x[src_tok[p]], built on the host
+    xp_h = inp["x"][src_tok[:n]]
+    r_ab = np.empty((n, 2 * c.f)); r_h = np.empty((n, c.f)); r_yp = np.empty((n, c.d))
+    for e in range(c.E):
+        s0, t0 = int(off[e]), int(off[e + 1])
+        r_ab[s0:t0], r_h[s0:t0], r_yp[s0:t0] = oracle.ffn_fwd_rows(xp_h[s0:t0], inp["W1"][e],
+                                                                   inp["W2"][e])
+    for a, b, r, nm in zip(out_u, out_g, (r_ab, r_h, r_yp), ("ab", "h", "yp")):
+        assert_close(f"gather {nm}", f64(b)[:n], r)
         assert torch.equal(a[:n], b[:n]), nm
-    dyp = dev(gen_rows_bf16("dyp_g", R, c.d))
-    ab, h = out_u[0], out_u[1]
+    # backward from the oracle's saved ab, h (bf16 values), on both paths
+    dyp_h = gen_rows_bf16("dyp_g", R, c.d)
+    dyp = dev(dyp_h)
+    ab = torch.full((R, 2 * c.f), float("nan"), **bf)
+    h = torch.full((R, c.f), float("nan"), **bf)
+    ab[:n] = torch.from_numpy(r_ab).to(torch.bfloat16).cuda()
+    h[:n] = torch.from_numpy(r_h).to(torch.bfloat16).cuda()
 
     def bwd(fn, src):
         dab = torch.empty((R, 2 * c.f), **bf)
@@ -226,6 +240,22 @@ def test_gather_fused_ffn_is_bit_identical(name):
         if nm in ("dab", "dxp"):
             a, b = a[:n], b[:n]
         assert torch.equal(a, b), nm
+    r_dab = np.empty((n, 2 * c.f)); r_dxp = np.empty((n, c.d))
+    g1, g2 = f64(g[2]), f64(g[3])
+    for e in range(c.E):
+        s0, t0 = int(off[e]), int(off[e + 1])
+        r_dab[s0:t0], r_dxp[s0:t0] = oracle.ffn_bwd_rows(dyp_h[s0:t0], r_ab[s0:t0],
+                                                         inp["W1"][e], inp["W2"][e])
+        if t0 == s0:
+            assert (g1[e] == 0).all() and (g2[e] == 0).all(), "empty expert must get zero dW"
+            continue
+        w1, w2 = oracle.layer.ffn_wgrad_rows(oracle.layer._f64(xp_h[s0:t0]), r_h[s0:t0],
+                                             oracle.layer._f64(dyp_h[s0:t0]), r_dab[s0:t0],
+                                             c.d, c.f)
+        assert_close(f"gather dW1[{e}]", g1[e], oracle.bf16(w1))
+        assert_close(f"gather dW2[{e}]", g2[e], oracle.bf16(w2))
+    assert_close("gather dab", f64(g[0])[:n], r_dab)
+    assert_close("gather dxp", f64(g[1])[:n], r_dxp)
     assert tde.moe_status(ws) == (0, 0)
 
 

@@ -1,9 +1,9 @@
 // dispatch.cu -- the HBM-bound row movers of the layer: permute (F3), combine (F7),
 // combine backward + gate backward (B1) and the un-permute reduce (B6).
 //
-// "MoE Training Optimization with Primus", Figure 7 dataflow: "a permutation gathers
-// tokens into expert order" and "a final unpermute-and-scale reduces the top-k
-// contributions back onto each token"; MegaMoE section: the backward mirrors them by
+// "MoE Training Optimization with Primus", Figure 7 dataflow: the permutation into
+// expert order before FC1, and the last step that un-permutes the expert outputs, scales
+// them by the gate weights and sums them per token; MegaMoE section: the backward mirrors them by
 // dispatch/combine duality.  X-MoE verdict page, key machinery: the padding-free token
 // buffer these kernels fill and drain.
 //

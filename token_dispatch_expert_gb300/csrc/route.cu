@@ -1,8 +1,8 @@
 // route.cu -- F1/F2: top-k gating, per-expert histogram, capacity, exclusive scan and the
 // padding-free buffer's side arrays.
 //
-// "MoE Training Optimization with Primus", Figure 7 dataflow: the router scores each
-// token and picks its top-k experts.  X-MoE verdict page (arXiv 2508.13337), key
+// "MoE Training Optimization with Primus", Figure 7 dataflow: the router step (top-k
+// experts per token).  X-MoE verdict page (arXiv 2508.13337), key
 // machinery: the padding-free token buffer with token ids, expert ids, per-expert
 // token counts and combine weights; referee minor comment on section 4.1.1 Listing 1
 // (max_token_count from the capacity factor) and major comment on section 5.6 (drop
