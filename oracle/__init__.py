@@ -17,6 +17,7 @@ from .layer import (  # noqa: F401
     layer_fwd,
     layer_bwd,
     layer_sampled,
+    permute,
     combine,
     combine_bwd,
     unpermute_reduce,

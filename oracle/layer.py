@@ -242,6 +242,15 @@ def ffn_wgrad_rows(xr, h, dyp, dab, d, f):
     return dW1, dW2
 
 
+def permute(cfg, r, x) -> np.ndarray:
+    """xp[p] = x[src_tok[p]] for the rows the routing kept (a plain copy)."""
+    n_rows = int(r["offsets"][-1])
+    x = _f64(x)
+    xp = np.empty((n_rows, cfg.d))
+    _load().orc_permute(n_rows, cfg.d, _p(_c(r["src_tok"], np.int32)), _p(x), _p(xp))
+    return xp
+
+
 def combine(cfg, dest_row, topk_w, yp, ys=None, toks=None, yp_row_of=None, rnd=True):
     lib = _load()
     d, k = cfg.d, cfg.k

@@ -1,6 +1,6 @@
-"""Host-side arithmetic of bench.py: the per-launch GEMM flops and bytes, and the exactness
-of the CPU baseline's expert restriction (routing a token sample over only the experts it
-selects gives the same choices and gate weights)."""
+"""Host-side logic of bench.py: the per-launch GEMM flops and bytes, the choice of the
+tensor peak from the sampled clocks, the clock window summary, and the CPU baseline's
+oracle timing (in full where it fits, extrapolated from row samples otherwise)."""
 
 import numpy as np
 import pytest
@@ -25,17 +25,51 @@ def test_gemm_phases_sum_to_the_step_totals(name):
     assert [round(f / F) for f, _ in ph] == [4, 2, 2, 2, 4, 4]
 
 
-@pytest.mark.parametrize("gate,scale", [("softmax", 1.0), ("sigmoid", 2.5)])
-def test_expert_restriction_keeps_choices_and_weights(gate, scale):
-    c = MoEConfig("restrict", T=48, d=64, E=40, k=6, f=64, gate=gate, route_scale=scale,
-                  zipf_s=1.2)
-    lg = gen_logits(c)
-    full = oracle.route(c, lg)
-    used = np.unique(full["topk_idx"])
-    assert len(used) < c.E
-    sub = oracle.route(c.replace(E=len(used)), np.ascontiguousarray(lg[:, used]))
-    np.testing.assert_array_equal(used[sub["topk_idx"]], full["topk_idx"])
-    np.testing.assert_array_equal(sub["topk_w"], full["topk_w"])
+def test_peak_follows_the_sampled_clock():
+    peaks = {"bf16_tflops": 1928.4, "bf16_tflops_sustained": 1716.7, "sm_max_mhz": 2070.0}
+    assert bench.choose_peak(peaks, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[:2] == \
+        (1928.4, "burst")
+    assert bench.choose_peak(peaks, {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0})[1] == "burst"
+    assert bench.choose_peak(peaks, {"sm_mhz": 1600.0, "sm_max_mhz": 2070.0})[:2] == \
+        (1716.7, "sustained")
+    assert bench.choose_peak(peaks, {"sm_mhz": None, "sm_max_mhz": None})[1] == "sustained"
+
+
+def test_clock_window_summary():
+    cs = bench.ClockSampler(0)
+    cs.proc = object()           # as if nvidia-smi were running
+    cs.samples = [(10.0, 2070.0, 2070.0, 500.0, set()),
+                  (10.05, 1900.0, 2070.0, 900.0, {"sw_power_cap"}),
+                  (10.1, 2000.0, 2070.0, 800.0, set()),
+                  (20.0, 1000.0, 2070.0, 100.0, {"hw_slowdown"})]
+    w = cs.window(10.0, 10.1)
+    assert w["samples"] == 3 and w["sm_mhz"] == 2000.0 and w["reasons"] == ["sw_power_cap"]
+    assert w["power_w_max"] == 900.0
+    # no sample inside: the nearest one stands in
+    w = cs.window(19.0, 19.5)
+    assert w["samples"] == 1 and w["sm_mhz"] == 1000.0
+
+
+def test_oracle_timer_full_and_extrapolated():
+    """Where the estimate fits the budget every expert's FFN is timed (nothing
+    extrapolated); with no budget the FFN is extrapolated from the row samples as
+    sum_e (a + b * rows_e)."""
+    c = CONFIGS["tiny"]
+    ot = bench.OracleTimer(c)
+    m = ot.measure(60.0)
+    assert not m["extrapolated"]
+    assert m["rows_kept"] == c.T * c.k
+    assert set(m["parts_s"]) == {"route", "permute", "combine", "combine_bwd",
+                                 "unpermute_reduce"}
+    assert m["tokens_per_s"] == pytest.approx(c.T / m["seconds_per_step"])
+    m = ot.measure(0.0)
+    assert m["extrapolated"]
+    a, b = m["ffn_fit"]["a_s"], m["ffn_fit"]["b_s_per_row"]
+    assert m["ffn_s"] == pytest.approx(sum(a + b * n for n in ot.kept if n))
+    assert "extrapolated" in ot.describe(m)
+    # one sample with the fixed cost given
+    m2 = ot.measure(0.0, a_fixed=a)
+    assert m2["extrapolated"] and len(m2["ffn_fit"]["samples"]) == 1
 
 
 @pytest.mark.parametrize("name", sorted(bench.GEMM_TRAFFIC_PER_LAUNCH))

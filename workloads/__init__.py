@@ -109,10 +109,14 @@ def _rng(seed: int, cfg_name: str, tensor: str) -> np.random.Generator:
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (round to nearest, ties to even) and return the raw
-    uint16 bit patterns.  Inputs here are finite draws from a normal distribution."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    uint16 bit patterns.  Inputs here are finite draws from a normal distribution: the
+    largest finite pattern plus 0x8000 still fits in 32 bits, so the sum cannot wrap."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
