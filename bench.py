@@ -12,11 +12,12 @@ capacity-shaped layers measured the same way, and an `mxfp8` block with the Mixt
 on MXFP8 operands.  The metric is tokens/s of the whole step; the dominant kernel (the
 tcgen05 grouped GEMM, six launches per step) is reported against its roofline.
 
-Timing: the step is captured once as a CUDA graph and replayed `steps` times between CUDA
-events on the launching stream (`value`); the per-phase split comes from a second graph
-holding `steps` steps with an event-record node at every phase boundary, so the GEMM time
-and the row movers' times are device times inside a replay, and their sum cannot exceed
-the step.
+Timing: `steps` steps are captured into one CUDA graph with an event-record node at every
+phase boundary and replayed once after the warm-up; `value`, the per-phase split, the GEMM
+time and the clocks all come from that one replay, so the GEMM time is a part of the step
+it divides.  The event nodes cost a few microseconds each (included: `value` is slightly
+conservative); a replay of a one-step graph without them and an eager loop are reported
+beside it.
 
 With N > 1 (torchrun) every rank runs an independent replica of the layer (the path
 does not shard: replicas only); the reported value is the sum over ranks, the time
@@ -703,25 +704,15 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
 
     barrier(world)
     torch.cuda.synchronize()
+    # 1. the per-phase split inside a graph replay (timed first, while the clocks are where
+    #    the plain replay below finds them: the GEMM time is taken from this run)
     w0 = time.time()
-    # eager launches with events at the phase boundaries (reported beside the graph figure;
-    # their phase split is the fallback when graph event nodes are unavailable)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    eager_events = []
-    for _ in range(args.steps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(wl.phases) + 1)]
-        wl.step(ev)
-        eager_events.append(ev)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    eager_ms = t_start.elapsed_time(t_end)
+    pg = None if args.no_graph else graph_phase_times(wl, args.steps)
+    w_pg = time.time()
+    # 2. the step captured once as a CUDA graph and replayed: `value`
     graph_ms = None
     g0w = g1w = None
     if not args.no_graph:
-        # the same step captured once as a CUDA graph and replayed: the kernels and their
-        # order are identical, only the host launch gaps between them go away
         gph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gph):
             wl.step()
@@ -739,7 +730,19 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
         g1w = time.time()
         graph_ms = g0.elapsed_time(g1)
         del gph
-    pg = None if args.no_graph else graph_phase_times(wl, args.steps)
+    # 3. eager launches with events at the phase boundaries (reported beside the graph
+    #    figure; their phase split is the fallback when graph event nodes are unavailable)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    eager_events = []
+    for _ in range(args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(wl.phases) + 1)]
+        wl.step(ev)
+        eager_events.append(ev)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = t_start.elapsed_time(t_end)
     w1 = time.time()
     barrier(world)
     st, fl = tde.moe_status(wl.ws)
@@ -752,24 +755,30 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
         phase_ms, phase_total = pg
         phase_src = ("CUDA-graph replay of the timed steps with an event-record node at each "
                      "phase boundary")
+        total_ms = phase_total * args.steps
     else:
         phase_ms, phase_total = eager_phase, eager_ms / args.steps
         phase_src = "eager launches with CUDA events at the phase boundaries"
-    total_ms = graph_ms if graph_ms is not None else eager_ms
+        total_ms = graph_ms if graph_ms is not None else eager_ms
     tokens_total, total_ms_max, value = replica_throughput(world, float(c.T * args.steps),
                                                            total_ms)
     ms_per_step = total_ms_max / args.steps
-    # clocks of this workload's timed region (eager, graph and phase-graph loops)
-    clk = clocks.window(w0, w1)
-    clk_graph = clocks.window(g0w, g1w) if g0w is not None else clk
+    # clocks: of the run the GEMM time comes from (the phase graph, else the eager loop),
+    # of the plain replay (`value`), and of the whole timed region
+    clk_all = clocks.window(w0, w1)
+    clk = clocks.window(w0, w_pg) if pg is not None else clk_all
+    clk_graph = clk if pg is not None else (clocks.window(g0w, g1w) if g0w is not None
+                                             else clk_all)
 
     res = {"workload": describe(c, mxfp8, fuse_gather, mx_cache), "tokens_per_step": c.T,
            "tokens_per_s": round(value, 1), "ms_per_step": round(ms_per_step, 4),
            "eager_ms_per_step": round(eager_ms / args.steps, 4),
+           "graph_no_events_ms_per_step": (round(graph_ms / args.steps, 4)
+                                            if graph_ms is not None else None),
            "rows_kept": rows_kept, "dropped": c.T * c.k - rows_kept,
            "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
            "phase_ms_total": round(phase_total, 4), "phase_timing": phase_src,
-           "launches_per_step": wl.launches_per_step(), "clocks": clk,
+           "launches_per_step": wl.launches_per_step(), "clocks": clk_all,
            "_tokens_total": tokens_total, "_clk_graph": clk_graph}
     if c.capacity:
         res["capacity"] = c.capacity
@@ -959,11 +968,12 @@ def bench_ours(args, world, rank, local):
                           f"{sum(b for _, b in gemm_phases(c, head['rows_kept'])) / 1e9:.1f} "
                           f"GB of weights, gradients and activations (L2 is 129 MB)")},
         "roofline": head["roofline"],
-        "timing": ("one step captured as a CUDA graph, replayed `steps` times between CUDA "
-                   "events on the launching stream; phase split from a graph of `steps` "
-                   "steps with event-record nodes" if not args.no_graph else
+        "timing": ("`steps` steps captured as one CUDA graph with an event-record node at "
+                   "each phase boundary, replayed once on the launching stream: value, phase "
+                   "split, GEMM time and clocks from that replay" if not args.no_graph else
                    "eager launches between CUDA events on the launching stream"),
         "eager_ms_per_step": head["eager_ms_per_step"],
+        "graph_no_events_ms_per_step": head["graph_no_events_ms_per_step"],
         "e2e": head.get("e2e"),
         "permute_gbs": head["memory_kernels"].get("permute", {}).get("GB/s"),
         "memory_kernels": head["memory_kernels"],

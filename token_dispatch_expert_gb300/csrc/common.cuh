@@ -20,6 +20,55 @@ __device__ __forceinline__ void flag_error(int* err, int bits) {
   if (err) atomicOr(err, bits);
 }
 
+// ----------------------------------------------------------------- dependent launches
+// Every kernel of the library is launched with programmatic stream serialisation allowed
+// (launch_pdl below): the hardware may schedule it while the previous kernel on the stream
+// is still finishing, which hides the launch latency between the layer's kernels.  So every
+// kernel starts with griddep_wait(), which returns once the previous kernel has completed
+// and its memory operations are visible (at once when there is none), and touches global
+// memory only after it.  griddep_launch() then lets the next kernel be scheduled as soon as
+// every CTA of this one has issued it; that kernel waits in turn, so the order of the
+// kernels' memory effects is the stream order.  Built with MOE_NO_PDL, launches are plain.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_enter() {
+  griddep_wait();
+  griddep_launch();
+}
+
+// Launch `kern` on `st` with programmatic stream serialisation allowed (plus an optional
+// cluster shape).  The arguments are converted to the kernel's parameter types.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+#ifndef MOE_NO_PDL
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+#endif
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ----------------------------------------------------------------- bf16 helpers
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(THREADS)
 permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
                const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap, int nvec,
                uint4* __restrict__ xp, int* err) {
+  griddep_enter();   // see common.cuh: dependent launches
   constexpr int B = 16;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ dest_row,
                const float* __restrict__ w, const uint4* __restrict__ add, int64_t T, int k,
                int nvec, int64_t rows_cap, uint4* __restrict__ y, int* err) {
+  griddep_enter();   // see common.cuh: dependent launches
   constexpr int B = KMAX == 6 ? 3 : 16 / KMAX;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
@@ -160,6 +162,7 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ dest_row,
                    int64_t T, int E, int k, int nvec, int gate, float scale, int64_t rows_cap,
                    uint4* __restrict__ dyp, float* __restrict__ dlogits, int* err) {
+  griddep_enter();   // see common.cuh: dependent launches
   constexpr int B = KMAX >= 6 ? 2 : 16 / (KMAX + 2);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
@@ -274,10 +277,9 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
 cudaError_t launch_permute(const void* x, const int32_t* src_tok, const int32_t* offsets, int E,
                            int64_t T, int64_t rows_cap, int d, void* xp, int* err,
                            cudaStream_t st) {
-  permute_kernel<<<grid_warps(rows_cap), THREADS, 0, st>>>(
-      static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d / 8,
-      static_cast<uint4*>(xp), err);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3(grid_warps(rows_cap)), dim3(THREADS), 0, st, 1,
+                    static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d / 8,
+                    static_cast<uint4*>(xp), err);
 }
 
 cudaError_t launch_combine(const void* rows, const int32_t* dest_row, const float* w,
@@ -285,15 +287,14 @@ cudaError_t launch_combine(const void* rows, const int32_t* dest_row, const floa
                            int* err, cudaStream_t st) {
   const int grid = grid_warps(T);
 #define MOE_COMBINE(KM)                                                                       \
-  combine_kernel<KM><<<grid, THREADS, 0, st>>>(static_cast<const uint4*>(rows), dest_row, w,    \
-                                               static_cast<const uint4*>(add), T, k, d / 8,     \
-                                               rows_cap, static_cast<uint4*>(y), err)
-  if (k <= 2) MOE_COMBINE(2);
-  else if (k <= 4) MOE_COMBINE(4);
-  else if (k <= 6) MOE_COMBINE(6);
-  else MOE_COMBINE(8);
+  launch_pdl(combine_kernel<KM>, dim3(grid), dim3(THREADS), 0, st, 1,                         \
+             static_cast<const uint4*>(rows), dest_row, w, static_cast<const uint4*>(add), T,  \
+             k, d / 8, rows_cap, static_cast<uint4*>(y), err)
+  if (k <= 2) return MOE_COMBINE(2);
+  if (k <= 4) return MOE_COMBINE(4);
+  if (k <= 6) return MOE_COMBINE(6);
+  return MOE_COMBINE(8);
 #undef MOE_COMBINE
-  return cudaGetLastError();
 }
 
 cudaError_t launch_combine_bwd(const void* dy, const void* yp, const float* logits,
@@ -303,15 +304,15 @@ cudaError_t launch_combine_bwd(const void* dy, const void* yp, const float* logi
                                float* dlogits, int* err, cudaStream_t st) {
   const int grid = grid_warps(T);
 #define MOE_COMBINE_BWD(KM)                                                                   \
-  combine_bwd_kernel<KM><<<grid, THREADS, 0, st>>>(                                            \
-      static_cast<const uint4*>(dy), static_cast<const uint4*>(yp), logits, topk_idx, topk_w,  \
-      dest_row, T, E, k, d / 8, gate, scale, rows_cap, static_cast<uint4*>(dyp), dlogits, err)
-  if (k <= 2) MOE_COMBINE_BWD(2);
-  else if (k <= 4) MOE_COMBINE_BWD(4);
-  else if (k <= 6) MOE_COMBINE_BWD(6);
-  else MOE_COMBINE_BWD(8);
+  launch_pdl(combine_bwd_kernel<KM>, dim3(grid), dim3(THREADS), 0, st, 1,                     \
+             static_cast<const uint4*>(dy), static_cast<const uint4*>(yp), logits, topk_idx,   \
+             topk_w, dest_row, T, E, k, d / 8, gate, scale, rows_cap,                          \
+             static_cast<uint4*>(dyp), dlogits, err)
+  if (k <= 2) return MOE_COMBINE_BWD(2);
+  if (k <= 4) return MOE_COMBINE_BWD(4);
+  if (k <= 6) return MOE_COMBINE_BWD(6);
+  return MOE_COMBINE_BWD(8);
 #undef MOE_COMBINE_BWD
-  return cudaGetLastError();
 }
 
 }  // namespace moe

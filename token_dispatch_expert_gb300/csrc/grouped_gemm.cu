@@ -416,6 +416,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ TailMaps tmT,
                     const __grid_constant__ CUtensorMap tmW, const KParams p) {
+  griddep_enter();   // see common.cuh: dependent launches
   using GE = Geo<MODE, PAIR>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -985,6 +986,7 @@ __global__ void prep_segment_maps(const __grid_constant__ CUtensorMap tmA,
                                   const __grid_constant__ CUtensorMap tmB,
                                   const int32_t* __restrict__ offsets, int G, long long rows_cap,
                                   CUtensorMap* out) {
+  griddep_enter();   // see common.cuh: dependent launches
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= G) return;
   long long end = offsets[g + 1];
@@ -1065,28 +1067,27 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM;
-  cfg.stream = st;
+  unsigned grid = static_cast<unsigned>(sms);
   if (PAIR == 2) {
+    // persistent: as many CTA pairs as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // persistent: as many CTA pairs as can be resident at once
     int clusters = 0;
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
       clusters = sms / 2;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  } else {
-    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+    grid = static_cast<unsigned>(2 * clusters);
   }
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tt, tw, kp);
+  return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM, st, PAIR, ta, tb, tc, tt, tw, kp);
 }
 
 // tt, tw: the tail tiles' segment-row maps and, for FC1, weight map (64-row boxes); unused
@@ -1206,9 +1207,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
           if (!a.seg_maps || (reinterpret_cast<uintptr_t>(a.seg_maps) & 127u))
             return cudaErrorInvalidValue;
           CUtensorMap* maps = static_cast<CUtensorMap*>(a.seg_maps);
-          prep_segment_maps<<<(kp.G + 63) / 64, 64, 0, st>>>(ta, tb, a.offsets, kp.G, a.rows_cap,
-                                                             maps);
-          const cudaError_t e = cudaGetLastError();
+          const cudaError_t e =
+              launch_pdl(prep_segment_maps, dim3((kp.G + 63) / 64), dim3(64), 0, st, 1, ta, tb,
+                         a.offsets, kp.G, a.rows_cap, maps);
           if (e != cudaSuccess) return e;
           kp.gmaps = maps;
         }

@@ -156,6 +156,7 @@ mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
                         const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap,
                         int d, uint4* __restrict__ xp, uint4* __restrict__ xq,
                         uint8_t* __restrict__ x_sf, int* err) {
+  griddep_enter();   // see common.cuh: dependent launches
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * QTHREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * QTHREADS) >> 5;
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(QTHREADS)
 mx_weight_quant_kernel(const uint4* __restrict__ W, int64_t n_rows, int rows_per_expert,
                        int K, int which, int f, int n_blocks_mn, uint4* __restrict__ wq,
                        uint8_t* __restrict__ atoms) {
+  griddep_enter();   // see common.cuh: dependent launches
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * QTHREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * QTHREADS) >> 5;
@@ -250,6 +252,7 @@ constexpr int TQ_ROWS = 128, TQ_COLS = 64;
 __global__ void __launch_bounds__(256)
 mx_weight_quant_t_kernel(const __nv_bfloat16* __restrict__ W, int Rk, int C,
                          uint8_t* __restrict__ wtq, uint8_t* __restrict__ atoms) {
+  griddep_enter();   // see common.cuh: dependent launches
   __shared__ __nv_bfloat16 tile[TQ_ROWS][TQ_COLS + 2];   // +2: stagger the banks
   const int e = blockIdx.z;
   const int r0 = blockIdx.y * TQ_ROWS, c0 = blockIdx.x * TQ_COLS;
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(256)
 mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ offsets,
                     int E, long long rows_cap, int C, int kb_cap, int role_n,
                     uint8_t* __restrict__ xtq, uint8_t* __restrict__ atoms, int* err) {
+  griddep_enter();   // see common.cuh: dependent launches
   __shared__ __nv_bfloat16 tile[128][KQ_COLS + 2];   // +2: stagger the banks
   __shared__ int s_kb0[MX_MAX_G + 1];
   __shared__ int s_wsum[8];
@@ -531,6 +535,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                const __grid_constant__ CUtensorMap tmC, const MxParams p) {
+  griddep_enter();   // see common.cuh: dependent launches
   using GE = MxGeo<PAIR, MODE>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1239,12 +1244,14 @@ cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const C
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(MX_THREADS);
-  cfg.dynamicSmemBytes = SMEM;
-  cfg.stream = st;
+  unsigned grid = static_cast<unsigned>(sms);
   if (PAIR == 2) {
+    // persistent: as many CTA pairs as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(MX_THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -1255,11 +1262,10 @@ cudaError_t launch_mx_mode(const CUtensorMap& ta, const CUtensorMap& tb, const C
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
       clusters = sms / 2;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  } else {
-    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+    grid = static_cast<unsigned>(2 * clusters);
   }
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tc, kp);
+  return launch_pdl(kern, dim3(grid), dim3(MX_THREADS), SMEM, st, PAIR, ta, tb, tsa, tsb, tc,
+                    kp);
 }
 
 }  // namespace
@@ -1297,28 +1303,30 @@ cudaError_t launch_mx_quant_weights(const void* W1, const void* W2, int E, int d
   e = cudaMemsetAsync(b + L.w1tsf, 127, L.total - L.w1tsf, st);
   if (e != cudaSuccess) return e;
   const int64_t r1 = static_cast<int64_t>(E) * 2 * f, r2 = static_cast<int64_t>(E) * d;
-  mx_weight_quant_kernel<<<grid_rows(r1), QTHREADS, 0, st>>>(
-      static_cast<const uint4*>(W1), r1, 2 * f, d, 0, f, f / 128,
-      reinterpret_cast<uint4*>(b + L.w1q), b + L.w1sf);
-  mx_weight_quant_kernel<<<grid_rows(r2), QTHREADS, 0, st>>>(
-      static_cast<const uint4*>(W2), r2, d, f, 1, f, (d + 255) / 256,
-      reinterpret_cast<uint4*>(b + L.w2q), b + L.w2sf);
+  e = launch_pdl(mx_weight_quant_kernel, dim3(grid_rows(r1)), dim3(QTHREADS), 0, st, 1,
+                 static_cast<const uint4*>(W1), r1, 2 * f, d, 0, f, f / 128,
+                 reinterpret_cast<uint4*>(b + L.w1q), b + L.w1sf);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(mx_weight_quant_kernel, dim3(grid_rows(r2)), dim3(QTHREADS), 0, st, 1,
+                 static_cast<const uint4*>(W2), r2, d, f, 1, f, (d + 255) / 256,
+                 reinterpret_cast<uint4*>(b + L.w2q), b + L.w2sf);
+  if (e != cudaSuccess) return e;
   // W2 [E][d][f] -> W2^T along d;  W1 [E][2f][d] -> W1^T along 2f
-  mx_weight_quant_t_kernel<<<dim3(f / TQ_COLS, d / TQ_ROWS, E), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(W2), d, f, b + L.w2tq, b + L.w2tsf);
-  mx_weight_quant_t_kernel<<<dim3(d / TQ_COLS, 2 * f / TQ_ROWS, E), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(W1), 2 * f, d, b + L.w1tq, b + L.w1tsf);
-  return cudaGetLastError();
+  e = launch_pdl(mx_weight_quant_t_kernel, dim3(f / TQ_COLS, d / TQ_ROWS, E), dim3(256), 0, st,
+                 1, static_cast<const __nv_bfloat16*>(W2), d, f, b + L.w2tq, b + L.w2tsf);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(mx_weight_quant_t_kernel, dim3(d / TQ_COLS, 2 * f / TQ_ROWS, E), dim3(256),
+                    0, st, 1, static_cast<const __nv_bfloat16*>(W1), 2 * f, d, b + L.w1tq,
+                    b + L.w1tsf);
 }
 
 cudaError_t launch_mx_permute_quant(const void* x, const int32_t* src_tok,
                                     const int32_t* offsets, int E, int64_t T, int64_t rows_cap,
                                     int d, void* xp_or_null, void* xq, uint8_t* x_sf, int* err,
                                     cudaStream_t st) {
-  mx_permute_quant_kernel<<<grid_rows(rows_cap), QTHREADS, 0, st>>>(
-      static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d,
-      static_cast<uint4*>(xp_or_null), static_cast<uint4*>(xq), x_sf, err);
-  return cudaGetLastError();
+  return launch_pdl(mx_permute_quant_kernel, dim3(grid_rows(rows_cap)), dim3(QTHREADS), 0, st, 1,
+                    static_cast<const uint4*>(x), src_tok, offsets, E, T, rows_cap, d,
+                    static_cast<uint4*>(xp_or_null), static_cast<uint4*>(xq), x_sf, err);
 }
 
 namespace {
@@ -1465,10 +1473,9 @@ cudaError_t launch_mx_quant_tok(const void* X, const int32_t* offsets, int E, in
   const int64_t kb_cap = mx_tok_kb_cap(rows_cap, E);
   // each CTA walks up to 8 K blocks of its 64 columns (its expert prefix is built once)
   const unsigned gy = static_cast<unsigned>((kb_cap + 7) / 8);
-  mx_quant_tok_kernel<<<dim3(C / KQ_COLS, gy), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(X), offsets, E, rows_cap, C, static_cast<int>(kb_cap),
-      role_n ? 1 : 0, codes, scales, err);
-  return cudaGetLastError();
+  return launch_pdl(mx_quant_tok_kernel, dim3(C / KQ_COLS, gy), dim3(256), 0, st, 1,
+                    static_cast<const __nv_bfloat16*>(X), offsets, E, rows_cap, C,
+                    static_cast<int>(kb_cap), role_n ? 1 : 0, codes, scales, err);
 }
 
 // dW [E][M][N]: CTA pairs over 256 x 256 tiles of every expert's gradient, K = its rows

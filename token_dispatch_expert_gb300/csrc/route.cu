@@ -59,6 +59,7 @@ route_topk_chunk_kernel(const float* __restrict__ logits, const float* __restric
                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                         int32_t* __restrict__ rank_out, int32_t* __restrict__ chunk_cnt,
                         int64_t nch, int* err) {
+  griddep_enter();   // see common.cuh: dependent launches
   // s_idx: the selected expert, or -1 for an empty token slot or an assignment dropped for
   // its negative score (it takes no place in the histogram)
   __shared__ int s_idx[CHUNK][8];
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
                   int32_t* __restrict__ counts, int32_t* __restrict__ kept,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ cnt_base) {
+  griddep_enter();   // see common.cuh: dependent launches
   __shared__ int s_kept[256];
   __shared__ int s_cnt[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -266,6 +268,7 @@ route_score_scatter_kernel(const float* __restrict__ logits, const int32_t* __re
                            int cap, const int32_t* __restrict__ chunk_base, int64_t nch,
                            const int32_t* __restrict__ counts,
                            const int32_t* __restrict__ cnt_base, uint32_t* __restrict__ list) {
+  griddep_enter();   // see common.cuh: dependent launches
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= T * k) return;
   const int in_chunk = in_chunk_rank[i];
@@ -306,6 +309,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& excl) {
 __global__ void __launch_bounds__(SELECT_THREADS)
 route_score_select_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ cnt_base,
                           int cap, uint32_t* __restrict__ list) {
+  griddep_enter();   // see common.cuh: dependent launches
   __shared__ int s_hist[256];
   __shared__ int s_warp[33];
   __shared__ uint32_t s_prefix;
@@ -366,6 +370,7 @@ route_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int 
                     const int32_t* __restrict__ cnt_base, const int32_t* __restrict__ score_rank,
                     int32_t* __restrict__ dest_row, int32_t* __restrict__ src_tok,
                     int32_t* __restrict__ src_slot, uint8_t* __restrict__ drop_mask) {
+  griddep_enter();   // see common.cuh: dependent launches
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t R = T * k;
   if (i >= R) return;
@@ -409,28 +414,33 @@ cudaError_t launch_route(const moe_config_t* c, const float* logits, int32_t* to
   const int64_t nch = route_chunks(T);
   const dim3 g1(static_cast<unsigned>(nch));
 #define MOE_ROUTE_LAUNCH(V)                                                                   \
-  route_topk_chunk_kernel<V><<<g1, ROUTE_THREADS, 0, st>>>(                                   \
-      logits, c->select_bias, c->drop_negative, T, E, k, c->gate, c->route_scale, topk_idx,  \
-      topk_w, dest_row, chunk_scratch, nch, err)
-  if (E <= 32) MOE_ROUTE_LAUNCH(1);
-  else if (E <= 64) MOE_ROUTE_LAUNCH(2);
-  else if (E <= 128) MOE_ROUTE_LAUNCH(4);
-  else MOE_ROUTE_LAUNCH(8);
+  launch_pdl(route_topk_chunk_kernel<V>, g1, dim3(ROUTE_THREADS), 0, st, 1, logits,            \
+             c->select_bias, c->drop_negative, T, E, k, c->gate, c->route_scale, topk_idx,     \
+             topk_w, dest_row, chunk_scratch, nch, err)
+  cudaError_t e;
+  if (E <= 32) e = MOE_ROUTE_LAUNCH(1);
+  else if (E <= 64) e = MOE_ROUTE_LAUNCH(2);
+  else if (E <= 128) e = MOE_ROUTE_LAUNCH(4);
+  else e = MOE_ROUTE_LAUNCH(8);
 #undef MOE_ROUTE_LAUNCH
-  route_scan_kernel<<<1, 1024, 0, st>>>(chunk_scratch, nch, E, cap, counts, kept, offsets,
-                                        cnt_base);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, st, 1, chunk_scratch, nch, E, cap,
+                 counts, kept, offsets, cnt_base);
+  if (e != cudaSuccess) return e;
   const int64_t R = T * k;
   const unsigned g_slots = static_cast<unsigned>((R + 255) / 256);
   if (by_score) {
-    route_score_scatter_kernel<<<g_slots, 256, 0, st>>>(logits, topk_idx, dest_row, T, k, E, cap,
-                                                        chunk_scratch, nch, counts, cnt_base,
-                                                        list);
-    route_score_select_kernel<<<E, SELECT_THREADS, 0, st>>>(counts, cnt_base, cap, list);
+    e = launch_pdl(route_score_scatter_kernel, dim3(g_slots), dim3(256), 0, st, 1, logits,
+                   topk_idx, dest_row, T, k, E, cap, chunk_scratch, nch, counts, cnt_base, list);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(route_score_select_kernel, dim3(E), dim3(SELECT_THREADS), 0, st, 1, counts,
+                   cnt_base, cap, list);
+    if (e != cudaSuccess) return e;
   }
-  route_assign_kernel<<<g_slots, 256, 0, st>>>(
-      topk_idx, T, k, E, cap, chunk_scratch, nch, offsets, counts, cnt_base,
-      reinterpret_cast<const int32_t*>(list), dest_row, src_tok, src_slot, drop_mask);
-  return cudaGetLastError();
+  return launch_pdl(route_assign_kernel, dim3(g_slots), dim3(256), 0, st, 1, topk_idx, T, k, E,
+                    cap, chunk_scratch, nch, offsets, counts, cnt_base,
+                    reinterpret_cast<const int32_t*>(list), dest_row, src_tok, src_slot,
+                    drop_mask);
 }
 
 // ---------------------------------------------------------------------------------------
