@@ -399,7 +399,8 @@ class Workload:
     """Device buffers and the step of one workload: the layer's calls in order, with an
     optional event recorded at each phase boundary (on the current stream)."""
 
-    def __init__(self, c, dev, seed=0, mxfp8=0, fuse_gather=False, mx_cache_weights=True):
+    def __init__(self, c, dev, seed=0, mxfp8=0, fuse_gather=False, mx_cache_weights=True,
+                 fuse_dispatch_bwd=False):
         import torch
 
         import token_dispatch_expert_gb300 as tde
@@ -407,6 +408,7 @@ class Workload:
 
         self.c, self.dev, self.mxfp8 = c, dev, mxfp8
         self.fuse_gather, self.mx_cache = fuse_gather, mx_cache_weights
+        self.fuse_dispatch_bwd = fuse_dispatch_bwd
         self.tde = tde
         bias_t = (torch.tensor(c.select_bias, dtype=torch.float32, device=dev)
                   if c.select_bias is not None else None)
@@ -546,6 +548,11 @@ class Workload:
             tde.moe_grouped_ffn_bwd_mx(self.cfg, self.dyp, v["xp"], v["offsets"], self.wq,
                                        v["ab"], v["h"], self.dab, self.dxp, self.dW1, self.dW2,
                                        ws)
+        elif self.fuse_dispatch_bwd:   # the FC2 data-gradient reads dy through src_tok
+            tde.moe_grouped_ffn_bwd_dispatch(self.cfg, g["dy"], v["topk_w"], v["src_tok"],
+                                             v["src_slot"], self.dyp, v["xp"], v["offsets"],
+                                             g["W1"], g["W2"], v["ab"], v["h"], self.dab,
+                                             self.dxp, self.dW1, self.dW2, ws)
         elif self.fuse_gather:
             tde.moe_grouped_ffn_bwd_gather(self.cfg, self.dyp, g["x"], v["src_tok"],
                                            v["offsets"], g["W1"], g["W2"], v["ab"], v["h"],
@@ -662,11 +669,16 @@ def graph_phase_times(wl, steps: int):
     try:
         evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(P + 1)]
                for _ in range(steps)]
+        # two adjacent event nodes ahead of the steps: the cost of one event-node hop, which
+        # every phase interval below includes and the step without events does not
+        probe = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
     except TypeError:
         return None
     try:
         gph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gph):
+            probe[0].record()
+            probe[1].record()
             for i in range(steps):
                 wl.step(evs[i])
         gph.replay()
@@ -676,19 +688,20 @@ def graph_phase_times(wl, steps: int):
         phase = {ph: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
                  for j, ph in enumerate(wl.phases)}
         total = evs[0][0].elapsed_time(evs[-1][-1]) / steps
+        hop = probe[0].elapsed_time(probe[1])
     except RuntimeError:
         return None
     del gph
-    return phase, total
+    return phase, total, hop
 
 
 def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=True,
-            fuse_gather=False, mx_cache=True) -> dict:
+            fuse_gather=False, mx_cache=True, fuse_dispatch_bwd=False) -> dict:
     """Times one workload (see the module docstring) and returns its results."""
     import torch
 
     wl = Workload(c, dev, seed=rank, mxfp8=mxfp8, fuse_gather=fuse_gather,
-                  mx_cache_weights=mx_cache)
+                  mx_cache_weights=mx_cache, fuse_dispatch_bwd=fuse_dispatch_bwd)
     tde = wl.tde
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -751,8 +764,9 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
                            f"{tde.moe_status_string(st)} {fl:#x}")
     eager_phase = {ph: sum(ev[i].elapsed_time(ev[i + 1]) for ev in eager_events) / args.steps
                    for i, ph in enumerate(wl.phases)}
+    hop_ms = None
     if pg is not None:
-        phase_ms, phase_total = pg
+        phase_ms, phase_total, hop_ms = pg
         phase_src = ("CUDA-graph replay of the timed steps with an event-record node at each "
                      "phase boundary")
         total_ms = phase_total * args.steps
@@ -770,7 +784,9 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
     clk_graph = clk if pg is not None else (clocks.window(g0w, g1w) if g0w is not None
                                              else clk_all)
 
-    res = {"workload": describe(c, mxfp8, fuse_gather, mx_cache), "tokens_per_step": c.T,
+    res = {"workload": describe(c, mxfp8, fuse_gather, mx_cache)
+                       + (" dispatch(dy)-fused-FC2-dgrad" if fuse_dispatch_bwd else ""),
+           "tokens_per_step": c.T,
            "tokens_per_s": round(value, 1), "ms_per_step": round(ms_per_step, 4),
            "eager_ms_per_step": round(eager_ms / args.steps, 4),
            "graph_no_events_ms_per_step": (round(graph_ms / args.steps, 4)
@@ -805,7 +821,11 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
         mem[ph] = {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
                    "us": round(phase_ms[ph] * 1e3, 2), "bytes": b}
     mem["route_us"] = round(phase_ms.get("route", 0.0) * 1e3, 2)
-    mem["note"] = f"hbm_gbs {hbm} of {peak_src}; times from the {phase_src}"
+    if hop_ms is not None:
+        mem["event_node_us"] = round(hop_ms * 1e3, 2)
+    mem["note"] = (f"hbm_gbs {hbm} of {peak_src}; times from the {phase_src}; each interval "
+                   f"includes one event-node hop (event_node_us, measured between two adjacent "
+                   f"event nodes of the same replay) that the step without events does not run")
     res["memory_kernels"] = mem
     if e2e and not args.no_e2e and not c.recompute:
         e_ms, h2d, d2h = wl.e2e(args.steps, args.warmup, world)
@@ -910,7 +930,7 @@ def bench_ours(args, world, rank, local):
     c = c.replace(drop_negative=args.drop_negative, recompute=args.recompute,
                   drop_by_score=args.drop_by_score)
     variant = (args.select_bias or args.drop_negative or args.recompute or args.drop_by_score
-               or args.fuse_gather or args.mxfp8)
+               or args.fuse_gather or args.mxfp8 or args.fuse_dispatch_bwd)
     torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
@@ -923,7 +943,8 @@ def bench_ours(args, world, rank, local):
     try:
         mx_level = (2 if args.mx_wgrad else 1) if args.mxfp8 else 0
         head = measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=mx_level,
-                       fuse_gather=args.fuse_gather, mx_cache=args.mx_cache_weights)
+                       fuse_gather=args.fuse_gather, mx_cache=args.mx_cache_weights,
+                       fuse_dispatch_bwd=args.fuse_dispatch_bwd)
         extra = {}
         if args.workloads == "auto":
             names = [] if variant or args.config != "mixtral" else EXTRA_WORKLOADS
@@ -1062,6 +1083,9 @@ def main():
                     help="drop selections whose raw logit is negative")
     ap.add_argument("--fuse-gather", action="store_true",
                     help="fold the permute into the FC1 and dW1 operand loads")
+    ap.add_argument("--fuse-dispatch-bwd", action="store_true",
+                    help="the FC2 data-gradient reads dy through src_tok, scaled by the gate "
+                         "weight in its epilogue")
     ap.add_argument("--mxfp8", action="store_true",
                     help="routed experts' forward and data-gradient GEMMs on MXFP8 operands "
                          "(weight gradients bf16)")

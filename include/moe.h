@@ -306,6 +306,29 @@ moe_status_t moe_grouped_ffn_bwd_gather(const moe_config_t *cfg, const void *dyp
                                         void *dW2, void *ws, void *stream);
 
 /*
+ * B1's dispatch of dy fused into B2 (Primus MoE blog, MegaMoE section: the dispatch of the
+ * upstream gradient folded into the FC2 data-gradient grouped GEMM).  As
+ * moe_grouped_ffn_bwd, except that the FC2 data-gradient takes its rows straight from dy:
+ * for row p of expert e, t = src_tok[p], s = src_slot[p],
+ *   dh = topk_w[s] * (dy[t] W2[e])      (fp32: the gate weight is applied to the product
+ *                                         in the GEMM's epilogue, so w * dy is never rounded
+ *                                         to bf16 on this path)
+ *   da, db from dh as in moe_grouped_ffn_bwd -> dab [T*k,2f] bf16
+ * dy [T,d] bf16 and topk_w [T,k] fp32 as moe_combine_bwd takes them; src_tok / src_slot
+ * [T*k] int32 from moe_route (entries < offsets[E] must lie in [0,T) and [0,T*k); a bad
+ * one sets MOE_DEVERR_BAD_INDEX, row 0 of dy / a weight of 0 is used instead).
+ * The FC2 weight gradient still contracts the rows dyp = bf16(w dy) that moe_combine_bwd
+ * writes, so dyp is an input here; dxp, dW1 and dW2 are as in moe_grouped_ffn_bwd.
+ */
+moe_status_t moe_grouped_ffn_bwd_dispatch(const moe_config_t *cfg, const void *dy,
+                                          const float *topk_w, const int32_t *src_tok,
+                                          const int32_t *src_slot, const void *dyp,
+                                          const void *xp, const int32_t *offsets,
+                                          const void *W1, const void *W2, const void *ab,
+                                          const void *h, void *dab, void *dxp, void *dW1,
+                                          void *dW2, void *ws, void *stream);
+
+/*
  * B6: un-permute reduce (Primus MoE blog, MegaMoE section: the reduction of each
  * token's rows after the FC1 data gradient).
  *   dx[t] = sum_{j kept} dxp[dest_row[t,j]] (+ dxs[t] if dxs_or_null), fp32 accumulation,

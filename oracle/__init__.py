@@ -23,6 +23,7 @@ from .layer import (  # noqa: F401
     unpermute_reduce,
     ffn_fwd_rows,
     ffn_bwd_rows,
+    ffn_bwd_rows_dispatch,
     e4m3,
     e4m3_code,
     mx_quantize_rows,

@@ -232,6 +232,16 @@ def ffn_bwd_rows(dyp, ab, W1e, W2e, rnd=True):
     return dab, dxr
 
 
+def ffn_bwd_rows_dispatch(dy_rows, w, ab, W1e, W2e):
+    """The expert's data gradients when the dispatch of dy is fused into the FC2
+    data-gradient (Primus MoE blog, MegaMoE section): each row's upstream gradient is its
+    token's dy row times the slot's gate weight, taken exactly (w * dy in float64, with no
+    bf16 rounding of the product), so dh = w (dy W2e); da, db and dxp then follow as in
+    ffn_bwd_rows, rounded where the GPU path stores them."""
+    g = _f64(dy_rows) * np.asarray(w, np.float64)[:, None]
+    return ffn_bwd_rows(g, ab, W1e, W2e)
+
+
 def ffn_wgrad_rows(xr, h, dyp, dab, d, f):
     lib = _load()
     dW1 = np.zeros((2 * f, d)); dW2 = np.zeros((d, f))

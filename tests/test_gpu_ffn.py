@@ -259,6 +259,74 @@ def test_gather_fused_ffn_against_oracle(name):
     assert tde.moe_status(ws) == (0, 0)
 
 
+@pytest.mark.parametrize("name", list(CASES) + ["edges"])
+def test_dispatch_fused_fc2_dgrad_against_oracle(name):
+    """The dispatch of dy fused into the FC2 data-gradient: its rows are dy[src_tok[p]] and
+    dh is scaled by the slot's gate weight in the epilogue (w * dy is never rounded to bf16),
+    so dab and dxp are compared with the oracle's exact-product variant; dW2 still contracts
+    the stored bf16(w * dy) rows, dW1 the fused dab.  Covers ragged segments, an empty
+    expert, the swap-AB tail tiles and a scrambled token order."""
+    if name == "edges":
+        sizes = [1, 64, 127, 128, 129, 255, 300, 600, 0, 385]
+        c = MoEConfig("edges_d", T=sum(sizes), d=320, E=len(sizes), k=1, f=192)
+        off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        perm = np.random.default_rng(7).permutation(c.T).astype(np.int32)
+        inp = gen_inputs_host(c)
+        src_tok, src_slot, n = perm, perm.copy(), c.T      # k = 1: slot = token
+        topk_w = np.random.default_rng(8).uniform(0.05, 1.0, c.T).astype(np.float32)
+    else:
+        c = CASES[name]
+        inp, o, n, _ = setup(c)
+        off, src_tok, src_slot = o["offsets"], o["src_tok"], o["src_slot"]
+        topk_w = o["topk_w"].reshape(-1).astype(np.float32)
+    R = c.T * c.k
+    xp_h = inp["x"][src_tok[:n]]
+    w_rows = topk_w[src_slot[:n]].astype(np.float64)
+    dy64 = oracle.layer._f64(inp["dy"])
+    # the forward's saved tensors and the stored dyp rows, from the oracle
+    r_ab = np.empty((n, 2 * c.f)); r_h = np.empty((n, c.f))
+    for e in range(c.E):
+        s0, t0 = int(off[e]), int(off[e + 1])
+        r_ab[s0:t0], r_h[s0:t0], _ = oracle.ffn_fwd_rows(xp_h[s0:t0], inp["W1"][e], inp["W2"][e])
+    dyp_h = oracle.bf16(dy64[src_tok[:n]] * w_rows[:, None])
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+
+    def rows(a, cols):
+        t = torch.full((R, cols), float("nan"), **bf)
+        t[:n] = torch.from_numpy(a).to(torch.bfloat16).cuda()
+        return t
+
+    cfg = cfg_c(c)
+    ws = new_ws(cfg)
+    slots = np.full(R, -1, np.int32); slots[:n] = src_slot[:n]
+    toks = np.full(R, -1, np.int32); toks[:n] = src_tok[:n]
+    dab = torch.empty((R, 2 * c.f), **bf)
+    dxp = torch.empty((R, c.d), **bf)
+    dW1 = torch.full((c.E, 2 * c.f, c.d), 7.0, **bf)
+    dW2 = torch.full((c.E, c.d, c.f), 7.0, **bf)
+    tde.moe_grouped_ffn_bwd_dispatch(cfg, dev(inp["dy"]), dev(topk_w), dev(toks), dev(slots),
+                                     rows(dyp_h, c.d), rows(oracle.layer._f64(xp_h), c.d),
+                                     dev(off), dev(inp["W1"]), dev(inp["W2"]),
+                                     rows(r_ab, 2 * c.f), rows(r_h, c.f), dab, dxp, dW1, dW2, ws)
+    torch.cuda.synchronize()
+    r_dab = np.empty((n, 2 * c.f)); r_dxp = np.empty((n, c.d))
+    g1, g2 = f64(dW1), f64(dW2)
+    for e in range(c.E):
+        s0, t0 = int(off[e]), int(off[e + 1])
+        r_dab[s0:t0], r_dxp[s0:t0] = oracle.ffn_bwd_rows_dispatch(
+            inp["dy"][src_tok[s0:t0]], w_rows[s0:t0], r_ab[s0:t0], inp["W1"][e], inp["W2"][e])
+        if t0 == s0:
+            assert (g1[e] == 0).all() and (g2[e] == 0).all(), "empty expert must get zero dW"
+            continue
+        w1, w2 = oracle.layer.ffn_wgrad_rows(oracle.layer._f64(xp_h[s0:t0]), r_h[s0:t0],
+                                             dyp_h[s0:t0], r_dab[s0:t0], c.d, c.f)
+        assert_close(f"dispatch dW1[{e}]", g1[e], oracle.bf16(w1))
+        assert_close(f"dispatch dW2[{e}]", g2[e], oracle.bf16(w2))
+    assert_close("dispatch dab", f64(dab)[:n], r_dab)
+    assert_close("dispatch dxp", f64(dxp)[:n], r_dxp)
+    assert tde.moe_status(ws) == (0, 0)
+
+
 def test_gather_flags_bad_source_rows():
     """An out-of-range source row is flagged (MOE_DEVERR_BAD_INDEX) and row 0 read instead;
     nothing outside x is touched."""

@@ -153,3 +153,52 @@ def test_sampled_layer_matches_full_layer():
     np.testing.assert_allclose(s["dW1s"][1], b["dW1s"][np.ix_(wcols + cfg.fs, wrows)],
                                rtol=one_ulp)
     np.testing.assert_allclose(s["dW2s"], b["dW2s"][np.ix_(wrows, wcols)], rtol=one_ulp)
+
+
+# ------------------------------------------------- dispatch of dy fused into the FC2 dgrad
+def _dispatch_case(seed=3, n=40, d=128, f=192):
+    rng = np.random.default_rng(seed)
+    bf = lambda a: oracle.bf16(np.asarray(a, np.float64))
+    dy = bf(rng.standard_normal((n, d)))
+    ab = bf(rng.standard_normal((n, 2 * f)))
+    W1 = bf(rng.standard_normal((2 * f, d)) * 0.05)
+    W2 = bf(rng.standard_normal((d, f)) * 0.05)
+    w = rng.uniform(0.05, 1.0, n).astype(np.float32).astype(np.float64)
+    return dy, w, ab, W1, W2
+
+
+def test_dispatch_bwd_with_exact_weights_equals_the_unfused_rows():
+    """With power-of-two gate weights w * dy is exact in bf16, so the fused path (dh from
+    w * dy taken exactly) and the unfused one (dh from the stored bf16(w * dy)) agree bit
+    for bit."""
+    dy, _, ab, W1, W2 = _dispatch_case()
+    w = 2.0 ** -(np.arange(dy.shape[0]) % 4)
+    fused = oracle.ffn_bwd_rows_dispatch(dy, w, ab, W1, W2)
+    plain = oracle.ffn_bwd_rows(oracle.bf16(dy * w[:, None]), ab, W1, W2)
+    for a, b in zip(fused, plain):
+        np.testing.assert_array_equal(a, b)
+    # doubling every weight doubles every output exactly (rounding commutes with 2x)
+    fused2 = oracle.ffn_bwd_rows_dispatch(dy, 2.0 * w, ab, W1, W2)
+    for a, b in zip(fused2, fused):
+        np.testing.assert_array_equal(a, 2.0 * b)
+
+
+def test_dispatch_bwd_against_torch_autograd():
+    """dh = w (dy W2) and the SwiGLU backward by torch float64 autograd (not the closed
+    form), rounded to bf16 where the GPU path stores da, db and dxp."""
+    dy, w, ab, W1, W2 = _dispatch_case(seed=5)
+    f = W2.shape[1]
+    dab, dxr = oracle.ffn_bwd_rows_dispatch(dy, w, ab, W1, W2)
+    t = lambda a: torch.tensor(a, dtype=torch.float64)
+    a = t(ab[:, :f]).requires_grad_(True)
+    b = t(ab[:, f:]).requires_grad_(True)
+    dh = (t(w)[:, None] * t(dy)) @ t(W2)
+    hh = torch.nn.functional.silu(a) * b
+    ga, gb = torch.autograd.grad(hh, (a, b), grad_outputs=dh)
+    r_dab = oracle.bf16(torch.cat([ga, gb], 1).numpy())
+    assert rel_l2(dab, r_dab) < 1e-12
+    r_dx = oracle.bf16((torch.tensor(r_dab) @ t(W1)).numpy())
+    np.testing.assert_array_equal(dxr, r_dx)
+    # and it differs from the unfused rows (bf16-rounded w * dy) only by that rounding
+    plain, _ = oracle.ffn_bwd_rows(oracle.bf16(dy * w[:, None]), ab, W1, W2)
+    assert 0 < rel_l2(dab, plain) < 1e-2

@@ -21,7 +21,7 @@ __all__ = [
     "moe_capacity_from_factor", "moe_workspace_size", "moe_ctx_offsets", "moe_ws_init",
     "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_combine_bwd",
     "moe_grouped_ffn_bwd", "moe_unpermute_reduce", "moe_layer_fwd", "moe_layer_bwd",
-    "moe_grouped_ffn_gather", "moe_grouped_ffn_bwd_gather",
+    "moe_grouped_ffn_gather", "moe_grouped_ffn_bwd_gather", "moe_grouped_ffn_bwd_dispatch",
     "moe_mx_weights_size", "moe_mx_quantize_weights", "moe_mx_act_scales_size",
     "moe_mx_permute_quant", "moe_grouped_ffn_mx", "moe_grouped_ffn_bwd_mx", "moe_layer_fwd_mx",
     "moe_layer_bwd_mx",
@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "moe_grouped_ffn": ([cfgp] + [P] * 9, I32),
             "moe_grouped_ffn_gather": ([cfgp] + [P] * 10, I32),
             "moe_grouped_ffn_bwd_gather": ([cfgp] + [P] * 14, I32),
+            "moe_grouped_ffn_bwd_dispatch": ([cfgp] + [P] * 17, I32),
             "moe_combine": ([cfgp] + [P] * 7, I32),
             "moe_combine_bwd": ([cfgp] + [P] * 10, I32),
             "moe_grouped_ffn_bwd": ([cfgp] + [P] * 13, I32),
@@ -228,6 +229,17 @@ def moe_grouped_ffn_bwd_gather(cfg, dyp, x, src_tok, offsets, W1, W2, ab, h, dab
                                             _p(W1), _p(W2), _p(ab), _p(h), _p(dab), _p(dxp),
                                             _p(dW1), _p(dW2), _p(ws), _s(stream)),
            "moe_grouped_ffn_bwd_gather")
+
+
+def moe_grouped_ffn_bwd_dispatch(cfg, dy, topk_w, src_tok, src_slot, dyp, xp, offsets, W1, W2,
+                                 ab, h, dab, dxp, dW1, dW2, ws, stream=None):
+    """moe_grouped_ffn_bwd with the FC2 data-gradient reading dy through src_tok and scaling
+    by the slot's gate weight (see include/moe.h)."""
+    _check(lib().moe_grouped_ffn_bwd_dispatch(_cfg(cfg), _p(dy), _p(topk_w), _p(src_tok),
+                                              _p(src_slot), _p(dyp), _p(xp), _p(offsets),
+                                              _p(W1), _p(W2), _p(ab), _p(h), _p(dab), _p(dxp),
+                                              _p(dW1), _p(dW2), _p(ws), _s(stream)),
+           "moe_grouped_ffn_bwd_dispatch")
 
 
 def moe_mx_weights_size(cfg):

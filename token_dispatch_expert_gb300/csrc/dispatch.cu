@@ -50,8 +50,12 @@ permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
     if (gw == 0 && lane == 0) flag_error(err, MOE_DEVERR_BAD_OFFSETS);
     n_rows = n_rows < 0 ? 0 : rows_cap;
   }
+  // the next row's source index is loaded while the current row is copied, so a warp
+  // with several rows does not wait for an index load before each row's copies
+  int t_next = gw < n_rows ? __ldg(src_tok + gw) : 0;
   for (int64_t p = gw; p < n_rows; p += nw) {
-    const int t = __ldg(src_tok + p);
+    const int t = t_next;
+    if (p + nw < n_rows) t_next = __ldg(src_tok + p + nw);
     if (t < 0 || t >= T) {
       if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
       continue;

@@ -121,9 +121,15 @@ struct KParams {
   int* err;
   // WGRAD: per-segment copies of the two operand maps (row extent = segment end), or null
   const CUtensorMap* gmaps;
-  // gathered operand rows (FC1's A, WGRAD's B): source row of each row-buffer row
+  // gathered operand rows (FC1's A, the FC2 data-gradient's A, WGRAD's B): source row of
+  // each row-buffer row
   const int32_t* gidx;
   int gather_rows;
+  // the FC2 data-gradient on gathered dy rows: dh of row p is scaled by gw[gslot[p]] (the
+  // gate weight of the row's slot) in the epilogue; null otherwise
+  const float* gw;
+  const int32_t* gslot;
+  long long n_slots;
   // a segment's last M tile with at most this many rows runs swapped (0: never)
   int tail_rows_max;
 };
@@ -189,6 +195,18 @@ __device__ __forceinline__ int gather_row(const KParams& p, int r) {
   return v;
 }
 
+// Gate weight of row-buffer row r for the FC2 data-gradient on gathered dy rows (1 when
+// the rows are the already-scaled dyp); an out-of-range slot is flagged and weighs 0.
+__device__ __forceinline__ float row_gate_weight(const KParams& p, long long r) {
+  if (!p.gw) return 1.0f;
+  const int s = __ldg(p.gslot + r);
+  if (s < 0 || s >= p.n_slots) {
+    flag_error(p.err, MOE_DEVERR_BAD_INDEX);
+    return 0.0f;
+  }
+  return __ldg(p.gw + s);
+}
+
 // Issue this CTA's share of the copies of one K block into stage (sa, sb).  With GATHER,
 // the gathered operand (FC1's A, WGRAD's B) is left to the caller's gather4 copies.
 template <int MODE, int PAIR, bool GATHER>
@@ -216,7 +234,7 @@ __device__ __forceinline__ void issue_loads(const CUtensorMap* tmA, const CUtens
     load(sa, tmA, k0, arow);
     load(sb, tmB, k0, g * p.d + nt * BN + rank * GE::BN_CTA);
   } else if (MODE == GEMM_DGRAD2_SWIGLU || MODE == GEMM_DGRAD1) {
-    load(sa, tmA, k0, arow);
+    if (!GATHER) load(sa, tmA, k0, arow);
     const int krow = (MODE == GEMM_DGRAD2_SWIGLU ? g * p.d : g * 2 * p.f) + k0;
 #pragma unroll
     for (int j = 0; j < GE::BN_CTA / 64; ++j)
@@ -372,6 +390,9 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
           float a[8], b[8], da[8], db[8];
           unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base)), a);
           unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base + f)), b);
+          const float wr = row_gate_weight(p, row);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] *= wr;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float sg = sigmoid_fast(a[e]);
@@ -568,7 +589,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int seg_last = seg0 + seg_rows - 1;
       int gi[4] = {0, 0, 0, 0};
       if (GATHER && nkb > 0) {
-        if (MODE == GEMM_FC1_SWIGLU) {
+        if (MODE == GEMM_FC1_SWIGLU || MODE == GEMM_DGRAD2_SWIGLU) {
           // a tail tile's CTA takes ntok / 2 rows: lanes below ntok / 8 copy them
           const int r0 = seg0 + mt * GE::TILE_M + (ntok > 0 ? ntok / 2 : 128) * rank + 4 * lane;
 #pragma unroll
@@ -612,7 +633,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (PAIR == 2) tma_gather4_pair(dst, m, full_leader, x, gc[0], gc[1], gc[2], gc[3]);
             else tma_gather4(dst, m, full_leader, x, gc[0], gc[1], gc[2], gc[3]);
           };
-          if (MODE == GEMM_FC1_SWIGLU) {
+          if (MODE == GEMM_FC1_SWIGLU || MODE == GEMM_DGRAD2_SWIGLU) {
             if (ntok == 0 || lane < ntok / 8)
               g4(sa + lane * 512, mA, k0);            // rows 4*lane .. 4*lane+3 of the tile
           } else if (MODE == GEMM_WGRAD && lane < 16) {
@@ -897,6 +918,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               float a[8], b[8], da[8], db[8];
               unpack8(ca[i], a);
               unpack8(cb[i], b);
+              const float wr = row_gate_weight(p, prow);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) dh[e] *= wr;
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float sg = sigmoid_fast(a[e]);
@@ -1121,10 +1145,21 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
   kp.gmaps = nullptr;
   const bool gather = a.gather_idx != nullptr;
   if (gather && (!a.gather_src || a.gather_rows < 1 || a.gather_rows > INT32_MAX ||
-                 (a.mode != GEMM_FC1_SWIGLU && a.mode != GEMM_WGRAD)))
+                 (a.mode != GEMM_FC1_SWIGLU && a.mode != GEMM_DGRAD2_SWIGLU &&
+                  a.mode != GEMM_WGRAD)))
     return cudaErrorInvalidValue;
   kp.gidx = a.gather_idx;
   kp.gather_rows = static_cast<int>(a.gather_rows);
+  kp.gw = nullptr;
+  kp.gslot = nullptr;
+  kp.n_slots = 0;
+  if (gather && a.mode == GEMM_DGRAD2_SWIGLU) {
+    // the rows are dy's tokens: each needs the gate weight of its slot
+    if (!a.gate_w || !a.gate_slot || a.n_slots < 1) return cudaErrorInvalidValue;
+    kp.gw = a.gate_w;
+    kp.gslot = a.gate_slot;
+    kp.n_slots = a.n_slots;
+  }
   const uint64_t G = static_cast<uint64_t>(kp.G);
   const uint64_t rows = static_cast<uint64_t>(a.rows_cap);
   const uint64_t d = static_cast<uint64_t>(a.d), f = static_cast<uint64_t>(a.f);
@@ -1176,10 +1211,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
       kp.num_n_tiles = (a.f + BN - 1) / BN;
       kp.num_kb = a.d / BK;
       kp.n_out = a.f;
-      ok = make_map(&ta, a.A, d, rows, 128) && make_map(&tb, a.B, f, G * d, 64) &&
-           (!tail || tail_maps(a.A, d));
+      // gathered: the rows of dy [gather_rows, d] (one-row boxes for the gather4 copies,
+      // which also bring a tail tile's rows)
+      ok = (gather ? make_map(&ta, a.gather_src, d, static_cast<uint64_t>(a.gather_rows), 1)
+                   : make_map(&ta, a.A, d, rows, 128)) &&
+           make_map(&tb, a.B, f, G * d, 64) && (!tail || gather || tail_maps(a.A, d));
       if (!ok) return cudaErrorInvalidValue;
-      return launch_pick<GEMM_DGRAD2_SWIGLU>(pair, ta, tb, tt, tb, kp, st);
+      return gather ? launch_pick<GEMM_DGRAD2_SWIGLU, true>(pair, ta, tb, tt, tb, kp, st)
+                    : launch_pick<GEMM_DGRAD2_SWIGLU>(pair, ta, tb, tt, tb, kp, st);
     case GEMM_DGRAD1:
       kp.num_n_tiles = (a.d + BN - 1) / BN;
       kp.num_kb = 2 * a.f / BK;

@@ -94,12 +94,17 @@ struct GroupedGemmArgs {
   // WGRAD over segments: device scratch for 2 * G tensor maps (128-byte aligned) whose row
   // extent ends at each segment's end, so rows past it load as zeros
   void* seg_maps;
-  // Gathered operand (FC1's A, or the WGRAD's B): when gather_idx is set, row p of that
-  // operand is row gather_idx[p] of gather_src [gather_rows, cols] instead of row p of the
-  // row buffer -- the permute step fused into the GEMM's loads (TMA gather4).
+  // Gathered operand (FC1's A, DGRAD2's A, or the WGRAD's B): when gather_idx is set, row p
+  // of that operand is row gather_idx[p] of gather_src [gather_rows, cols] instead of row p
+  // of the row buffer -- a dispatch fused into the GEMM's loads (TMA gather4).
   const int32_t* gather_idx;
   const void* gather_src;
   int64_t gather_rows;
+  // DGRAD2 with gathered rows (the rows of dy): dh of row p is scaled by
+  // gate_w[gate_slot[p]], gate_slot entries in [0, n_slots)
+  const float* gate_w;
+  const int32_t* gate_slot;
+  int64_t n_slots;
 };
 
 constexpr size_t SEG_MAP_BYTES = 128;   // one CUtensorMap

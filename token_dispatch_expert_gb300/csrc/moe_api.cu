@@ -205,13 +205,28 @@ moe_status_t ffn_fwd(const moe_config_t* c, const void* xp, const int32_t* offse
   return MOE_OK;
 }
 
+// The FC2 data-gradient's rows taken from dy through src_tok, each scaled by its slot's
+// gate weight in the epilogue (the dispatch of dy fused into that GEMM), or none.
+struct DyDispatch {
+  Gather rows;
+  const float* topk_w = nullptr;
+  const int32_t* src_slot = nullptr;
+  int64_t n_slots = 0;
+};
+
 moe_status_t ffn_bwd(const moe_config_t* c, const void* dyp, const void* xp,
                      const int32_t* offsets, int64_t uniform_rows, int f, const void* W1,
                      const void* W2, const void* ab, const void* h, void* dab, void* dxp,
                      void* dW1, void* dW2, void* seg_maps, int* err, cudaStream_t st,
-                     Gather gx = {}) {
+                     Gather gx = {}, DyDispatch gd = {}) {
   GroupedGemmArgs g2 = gemm_args(GEMM_DGRAD2_SWIGLU, c, offsets, uniform_rows, c->d, f, dyp, W2,
                                  dab, nullptr, ab, err);
+  if (gd.rows.idx) {
+    set_gather(g2, gd.rows);
+    g2.gate_w = gd.topk_w;
+    g2.gate_slot = gd.src_slot;
+    g2.n_slots = gd.n_slots;
+  }
   MOE_TRY(launch_grouped_gemm(g2, st));
   GroupedGemmArgs w2 = gemm_args(GEMM_WGRAD, c, offsets, uniform_rows, c->d, f, dyp, h, dW2,
                                  nullptr, nullptr, err);
@@ -388,6 +403,30 @@ moe_status_t moe_grouped_ffn_bwd_gather(const moe_config_t* cfg, const void* dyp
   return ffn_bwd(cfg, dyp, nullptr, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
                  at<uint8_t>(ws, ws_layout(cfg).maps), static_cast<int*>(ws),
                  static_cast<cudaStream_t>(stream), gx);
+}
+
+moe_status_t moe_grouped_ffn_bwd_dispatch(const moe_config_t* cfg, const void* dy,
+                                          const float* topk_w, const int32_t* src_tok,
+                                          const int32_t* src_slot, const void* dyp,
+                                          const void* xp, const int32_t* offsets,
+                                          const void* W1, const void* W2, const void* ab,
+                                          const void* h, void* dab, void* dxp, void* dW1,
+                                          void* dW2, void* ws, void* stream) {
+  moe_status_t s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!ptrs_ok(dy, topk_w, src_tok, src_slot, dyp, xp, offsets, W1, W2, ab, h, dab, dxp, dW1,
+               dW2, ws))
+    return MOE_ERR_INVALID_ARG;
+  DyDispatch gd;
+  gd.rows.idx = src_tok;
+  gd.rows.src = dy;
+  gd.rows.rows = cfg->T;
+  gd.topk_w = topk_w;
+  gd.src_slot = src_slot;
+  gd.n_slots = cfg->T * cfg->k;
+  return ffn_bwd(cfg, dyp, xp, offsets, 0, cfg->ffn, W1, W2, ab, h, dab, dxp, dW1, dW2,
+                 at<uint8_t>(ws, ws_layout(cfg).maps), static_cast<int*>(ws),
+                 static_cast<cudaStream_t>(stream), Gather{}, gd);
 }
 
 moe_status_t moe_unpermute_reduce(const moe_config_t* cfg, const void* dxp,
