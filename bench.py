@@ -56,11 +56,12 @@ def load_peaks():
 # one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of a profiling shape with
 # the same per-expert GEMMs and 1/4 of the experts and of the rows -- every operand and
 # result scales with those -- times 4: `mixtral_e2` for the Mixtral layer, `qwen3_e32` for
-# the Qwen3 layer.  Valid for the grouped-GEMM kernel as of the transposed-epilogue version;
-# set to None when the kernel changes.
+# the Qwen3 layer.  Valid for the grouped-GEMM kernel as of its dependent-launch version
+# (the dispatch-fused FC2 data-gradient option included); set to None when the kernel
+# changes.
 GEMM_TRAFFIC_PER_LAUNCH = {
-    "mixtral": (4 * (658.7 + 340.1 + 490.5 + 252.5 + 671.2 + 544.8) / 6 * 1e6, "mixtral_e2"),
-    "qwen3": (4 * (325.9 + 163.5 + 242.9 + 143.4 + 300.6 + 261.7) / 6 * 1e6, "qwen3_e32"),
+    "mixtral": (4 * (661.2 + 340.2 + 488.7 + 252.2 + 671.0 + 544.8) / 6 * 1e6, "mixtral_e2"),
+    "qwen3": (4 * (326.5 + 163.9 + 241.8 + 144.1 + 301.0 + 261.4) / 6 * 1e6, "qwen3_e32"),
 }
 
 # the extra workloads measured beside the headline, each in its own block of the line
