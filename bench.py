@@ -960,11 +960,16 @@ def bench_ours(args, world, rank, local):
         mx_block = None
         if not args.no_mx and not variant and args.config == "mixtral" and \
                 args.workloads != "none":
+            # the headline layer and the capacity layer, each with MXFP8 forward and data
+            # gradients (level 1) and with MXFP8 weight gradients too (level 2)
             mx_block = {}
-            for lvl in (1, 2):
-                r = measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=lvl)
-                r.pop("_tokens_total"); r.pop("_clk_graph")
-                mx_block["fwd_dgrad" if lvl == 1 else "fwd_dgrad_wgrad"] = r
+            for mc_name, mc_cfg in (("mixtral", c), ("capacity", CONFIGS["capacity"])):
+                for lvl in (1, 2):
+                    r = measure(mc_cfg, args, dev, world, rank, clocks, peaks, peak_src,
+                                mxfp8=lvl)
+                    r.pop("_tokens_total"); r.pop("_clk_graph")
+                    key = "fwd_dgrad" if lvl == 1 else "fwd_dgrad_wgrad"
+                    mx_block[key if mc_name == "mixtral" else f"{mc_name}_{key}"] = r
     finally:
         clocks.stop()
 
