@@ -12,12 +12,12 @@ capacity-shaped layers measured the same way, and an `mxfp8` block with the Mixt
 on MXFP8 operands.  The metric is tokens/s of the whole step; the dominant kernel (the
 tcgen05 grouped GEMM, six launches per step) is reported against its roofline.
 
-Timing: `steps` steps are captured into one CUDA graph with an event-record node at every
-phase boundary and replayed once after the warm-up; `value`, the per-phase split, the GEMM
-time and the clocks all come from that one replay, so the GEMM time is a part of the step
-it divides.  The event nodes cost a few microseconds each (included: `value` is slightly
-conservative); a replay of a one-step graph without them and an eager loop are reported
-beside it.
+Timing: `steps` steps are captured into one CUDA graph and replayed once after the
+warm-up; each phase boundary is an event-record node on a side branch that waits for the
+kernels before it, so the kernels keep their own chain (and their dependent-launch overlap)
+while the events time them.  `value`, the per-phase split, the GEMM time and the clocks all
+come from that one replay, so the GEMM time is a part of the step it divides; a replay of a
+one-step graph without events and an eager loop are reported beside it.
 
 With N > 1 (torchrun) every rank runs an independent replica of the layer (the path
 does not shard: replicas only); the reported value is the sum over ranks, the time
@@ -418,6 +418,7 @@ class Workload:
                                    drop_negative=c.drop_negative, recompute=c.recompute,
                                    drop_by_score=c.drop_by_score, mxfp8=mxfp8)
         g = self.g = gen_inputs_device(c, dev, seed=seed)
+        self.side = torch.cuda.Stream(device=dev)   # where the phase events are recorded
         R = c.T * c.k
         ws_b, ctx_b = tde.moe_workspace_size(self.cfg)
         self.ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
@@ -467,6 +468,11 @@ class Workload:
             else:
                 self.phases = ["mx_weight_quant"] + self.phases
 
+    def join_marks(self):
+        """The current stream waits for the side stream the phase events are recorded on."""
+        import torch
+        torch.cuda.current_stream().wait_stream(self.side)
+
     # route 3, permute 1, FC1+FC2 2, combine 1, combine-bwd 1, backward GEMMs 4 plus the two
     # per-segment map preparations, reduce 1; the shared expert 2 + 4
     def launches_per_step(self) -> int:
@@ -488,15 +494,22 @@ class Workload:
         return n
 
     def step(self, ev=None):
-        """One forward + backward.  ev: len(phases) + 1 events recorded at the phase
-        boundaries on the current stream (or None)."""
+        """One forward + backward.  ev: len(phases) + 1 events marking the phase boundaries
+        (or None).  Each is recorded on a side stream that first waits for the work enqueued
+        so far: the event completes when the kernels before it have, while the next kernel
+        still depends on the previous kernel alone, so its dependent-launch overlap and the
+        step's kernel-to-kernel chain are what they are without the events.  The caller
+        joins the side stream (`join_marks`) before the work after the step needs it."""
+        import torch
         tde, c, g, v, ws = self.tde, self.c, self.g, self.v, self.ws
         shared = self.shared
         n_mark = [0]
 
         def mark():
             if ev is not None:
-                ev[n_mark[0]].record()
+                self.side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(self.side):
+                    ev[n_mark[0]].record()
             n_mark[0] += 1
 
         mark()
@@ -662,26 +675,23 @@ class Workload:
 
 def graph_phase_times(wl, steps: int):
     """Per-phase device times inside a CUDA-graph replay: `steps` steps captured into one
-    graph with an event-record node at every phase boundary, replayed once to warm up and
-    once timed.  Returns (phase ms per step, total ms per step) or None when event-record
-    nodes are not available."""
+    graph whose phase boundaries are event-record nodes on side branches (each waits for
+    the kernels before it; the kernels keep their own chain, see Workload.step), replayed
+    once to warm up and once timed.  Returns (phase ms per step, total ms per step) or None
+    when event-record nodes are not available."""
     import torch
     P = len(wl.phases)
     try:
         evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(P + 1)]
                for _ in range(steps)]
-        # two adjacent event nodes ahead of the steps: the cost of one event-node hop, which
-        # every phase interval below includes and the step without events does not
-        probe = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
     except TypeError:
         return None
     try:
         gph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gph):
-            probe[0].record()
-            probe[1].record()
             for i in range(steps):
                 wl.step(evs[i])
+            wl.join_marks()
         gph.replay()
         torch.cuda.synchronize()
         gph.replay()
@@ -689,11 +699,10 @@ def graph_phase_times(wl, steps: int):
         phase = {ph: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
                  for j, ph in enumerate(wl.phases)}
         total = evs[0][0].elapsed_time(evs[-1][-1]) / steps
-        hop = probe[0].elapsed_time(probe[1])
     except RuntimeError:
         return None
     del gph
-    return phase, total, hop
+    return phase, total
 
 
 def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=True,
@@ -754,6 +763,7 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(wl.phases) + 1)]
         wl.step(ev)
         eager_events.append(ev)
+    wl.join_marks()
     t_end.record(stream)
     torch.cuda.synchronize()
     eager_ms = t_start.elapsed_time(t_end)
@@ -765,11 +775,10 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
                            f"{tde.moe_status_string(st)} {fl:#x}")
     eager_phase = {ph: sum(ev[i].elapsed_time(ev[i + 1]) for ev in eager_events) / args.steps
                    for i, ph in enumerate(wl.phases)}
-    hop_ms = None
     if pg is not None:
-        phase_ms, phase_total, hop_ms = pg
-        phase_src = ("CUDA-graph replay of the timed steps with an event-record node at each "
-                     "phase boundary")
+        phase_ms, phase_total = pg
+        phase_src = ("CUDA-graph replay of the timed steps with an event-record node on a "
+                     "side branch at each phase boundary")
         total_ms = phase_total * args.steps
     else:
         phase_ms, phase_total = eager_phase, eager_ms / args.steps
@@ -822,11 +831,8 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
         mem[ph] = {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),
                    "us": round(phase_ms[ph] * 1e3, 2), "bytes": b}
     mem["route_us"] = round(phase_ms.get("route", 0.0) * 1e3, 2)
-    if hop_ms is not None:
-        mem["event_node_us"] = round(hop_ms * 1e3, 2)
-    mem["note"] = (f"hbm_gbs {hbm} of {peak_src}; times from the {phase_src}; each interval "
-                   f"includes one event-node hop (event_node_us, measured between two adjacent "
-                   f"event nodes of the same replay) that the step without events does not run")
+    mem["note"] = (f"hbm_gbs {hbm} of {peak_src}; times from the {phase_src}: an interval "
+                   f"runs from the completion of the phase before to this phase's completion")
     res["memory_kernels"] = mem
     if e2e and not args.no_e2e and not c.recompute:
         e_ms, h2d, d2h = wl.e2e(args.steps, args.warmup, world)
@@ -995,9 +1001,10 @@ def bench_ours(args, world, rank, local):
                           f"{sum(b for _, b in gemm_phases(c, head['rows_kept'])) / 1e9:.1f} "
                           f"GB of weights, gradients and activations (L2 is 129 MB)")},
         "roofline": head["roofline"],
-        "timing": ("`steps` steps captured as one CUDA graph with an event-record node at "
-                   "each phase boundary, replayed once on the launching stream: value, phase "
-                   "split, GEMM time and clocks from that replay" if not args.no_graph else
+        "timing": ("`steps` steps captured as one CUDA graph with an event-record node on a "
+                   "side branch at each phase boundary (the kernels keep their own chain), "
+                   "replayed once on the launching stream: value, phase split, GEMM time and "
+                   "clocks from that replay" if not args.no_graph else
                    "eager launches between CUDA events on the launching stream"),
         "eager_ms_per_step": head["eager_ms_per_step"],
         "graph_no_events_ms_per_step": head["graph_no_events_ms_per_step"],

@@ -22,22 +22,21 @@ __device__ __forceinline__ void flag_error(int* err, int bits) {
 
 // ----------------------------------------------------------------- dependent launches
 // Every kernel of the library is launched with programmatic stream serialisation allowed
-// (launch_pdl below): the hardware may schedule it while the previous kernel on the stream
-// is still finishing, which hides the launch latency between the layer's kernels.  So every
+// (launch_pdl below): the hardware may schedule it before the previous kernel on the stream
+// has finished, which hides the launch latency between the layer's kernels.  So every
 // kernel starts with griddep_wait(), which returns once the previous kernel has completed
 // and its memory operations are visible (at once when there is none), and touches global
-// memory only after it.  griddep_launch() then lets the next kernel be scheduled as soon as
-// every CTA of this one has issued it; that kernel waits in turn, so the order of the
-// kernels' memory effects is the stream order.  Built with MOE_NO_PDL, launches are plain.
+// memory only after it; the order of the kernels' memory effects is the stream order.
+// Each kernel calls griddep_launch() once its own work is issued -- the row movers after
+// their loop, the grouped GEMMs when their producer warp has issued its last copy -- so the
+// next kernel is scheduled during this one's tail rather than at its start (scheduled
+// early, its waiting CTAs measurably slowed the memory-bound kernels they sat beside).
+// Built with MOE_NO_PDL, launches are plain.
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_enter() {
-  griddep_wait();
-  griddep_launch();
 }
 
 // Launch `kern` on `st` with programmatic stream serialisation allowed (plus an optional

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(THREADS)
 permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
                const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap, int nvec,
                uint4* __restrict__ xp, int* err) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   constexpr int B = 16;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
@@ -72,6 +72,7 @@ permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_tok,
         if (c0 + 32 * b < nvec) dst[c0 + 32 * b] = v[b];
     }
   }
+  griddep_launch();
 }
 
 // Slot indices and weights of token t, one lane per slot, broadcast to the warp.
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(THREADS)
 combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ dest_row,
                const float* __restrict__ w, const uint4* __restrict__ add, int64_t T, int k,
                int nvec, int64_t rows_cap, uint4* __restrict__ y, int* err) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   constexpr int B = KMAX == 6 ? 3 : 16 / KMAX;
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
@@ -154,6 +155,7 @@ combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ dest_
       }
     }
   }
+  griddep_launch();
 }
 
 // One warp per token: dyp[p_j] = w_j dy[t]; dw_j = <dy[t], yp[p_j]> (warp reduction);
@@ -166,7 +168,7 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
                    const float* __restrict__ topk_w, const int32_t* __restrict__ dest_row,
                    int64_t T, int E, int k, int nvec, int gate, float scale, int64_t rows_cap,
                    uint4* __restrict__ dyp, float* __restrict__ dlogits, int* err) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   constexpr int B = KMAX >= 6 ? 2 : 16 / (KMAX + 2);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x) >> 5;
@@ -274,6 +276,7 @@ combine_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ yp,
       dlogits[t * E + e] = val;
     }
   }
+  griddep_launch();
 }
 
 }  // namespace

@@ -437,7 +437,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ TailMaps tmT,
                     const __grid_constant__ CUtensorMap tmW, const KParams p) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   using GE = Geo<MODE, PAIR>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -651,6 +651,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
     }
+    // every copy of this CTA is issued: the next kernel may be scheduled (it waits for
+    // this one to complete before it touches memory)
+    griddep_launch();
     // wait until every stage is free again: all commits aimed at this CTA have landed
     for (int i = 0; i < STAGES && ok; ++i) {
       if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, WAIT_BUDGET / 4))
@@ -1002,6 +1005,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (PAIR == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  griddep_launch();
 }
 
 // One thread per segment: copy the two operand maps of the weight-gradient GEMM into
@@ -1010,7 +1014,7 @@ __global__ void prep_segment_maps(const __grid_constant__ CUtensorMap tmA,
                                   const __grid_constant__ CUtensorMap tmB,
                                   const int32_t* __restrict__ offsets, int G, long long rows_cap,
                                   CUtensorMap* out) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= G) return;
   long long end = offsets[g + 1];
@@ -1032,6 +1036,7 @@ __global__ void prep_segment_maps(const __grid_constant__ CUtensorMap tmA,
                "r"(e32)
                : "memory");
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  griddep_launch();
 }
 
 // ------------------------------------------------------------------ host side

@@ -156,7 +156,7 @@ mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
                         const int32_t* __restrict__ offsets, int E, int64_t T, int64_t rows_cap,
                         int d, uint4* __restrict__ xp, uint4* __restrict__ xq,
                         uint8_t* __restrict__ x_sf, int* err) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * QTHREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * QTHREADS) >> 5;
@@ -197,6 +197,7 @@ mx_permute_quant_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
       x_sf[act_atom_byte(seg0, e, l, d / 128, b >> 2, b & 3)] = static_cast<uint8_t>(s);
     }
   }
+  griddep_launch();
 }
 
 // Weight quantisation, warp per weight row.  W1 [E][2f][d]: codes row-major into w1q,
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(QTHREADS)
 mx_weight_quant_kernel(const uint4* __restrict__ W, int64_t n_rows, int rows_per_expert,
                        int K, int which, int f, int n_blocks_mn, uint4* __restrict__ wq,
                        uint8_t* __restrict__ atoms) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * QTHREADS + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * QTHREADS) >> 5;
@@ -240,6 +241,7 @@ mx_weight_quant_kernel(const uint4* __restrict__ W, int64_t n_rows, int rows_per
       atoms[atom * 512 + atom_byte(m, k1)] = static_cast<uint8_t>(s);
     }
   }
+  griddep_launch();
 }
 
 // Transposed weight quantisation for the data-gradient GEMMs: for each expert, Wt = W^T
@@ -252,7 +254,7 @@ constexpr int TQ_ROWS = 128, TQ_COLS = 64;
 __global__ void __launch_bounds__(256)
 mx_weight_quant_t_kernel(const __nv_bfloat16* __restrict__ W, int Rk, int C,
                          uint8_t* __restrict__ wtq, uint8_t* __restrict__ atoms) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   __shared__ __nv_bfloat16 tile[TQ_ROWS][TQ_COLS + 2];   // +2: stagger the banks
   const int e = blockIdx.z;
   const int r0 = blockIdx.y * TQ_ROWS, c0 = blockIdx.x * TQ_COLS;
@@ -280,6 +282,7 @@ mx_weight_quant_t_kernel(const __nv_bfloat16* __restrict__ W, int Rk, int C,
   const int kb = r0 / 128, j = blk;                          // r0 is a multiple of 128
   const long long atom = ((static_cast<long long>(e) * NT + col / 256) * KB + kb) * 2 + ((col >> 7) & 1);
   atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
+  griddep_launch();
 }
 
 // Along-token quantisation for the weight gradients: X [rows_cap][C] bf16 holds the expert
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(256)
 mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ offsets,
                     int E, long long rows_cap, int C, int kb_cap, int role_n,
                     uint8_t* __restrict__ xtq, uint8_t* __restrict__ atoms, int* err) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   __shared__ __nv_bfloat16 tile[128][KQ_COLS + 2];   // +2: stagger the banks
   __shared__ int s_kb0[MX_MAX_G + 1];
   __shared__ int s_wsum[8];
@@ -382,6 +385,7 @@ mx_quant_tok_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restri
                : (static_cast<long long>(col / 128) * kb_cap + kb);
     atoms[atom * 512 + atom_byte(col & 127, j)] = static_cast<uint8_t>(sc);
   }
+  griddep_launch();
 }
 
 // ------------------------------------------------------------------ block-scaled GEMM
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                const __grid_constant__ CUtensorMap tmC, const MxParams p) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   using GE = MxGeo<PAIR, MODE>;
   constexpr int STAGES = GE::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -731,6 +735,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
     }
+    // every copy of this CTA is issued: the next kernel may be scheduled (it waits for
+    // this one to complete before it touches memory)
+    griddep_launch();
     for (int i = 0; i < STAGES && ok; ++i) {
       if (!mx_warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, p.err, MX_WAIT_BUDGET / 4))
         break;
@@ -1172,6 +1179,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (PAIR == 2) tmem_dealloc_pair(tmem_base, MX_TMEM_COLS);
     else tmem_dealloc(tmem_base, MX_TMEM_COLS);
   }
+  griddep_launch();
 }
 
 // ------------------------------------------------------------------ host side

@@ -59,7 +59,7 @@ route_topk_chunk_kernel(const float* __restrict__ logits, const float* __restric
                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                         int32_t* __restrict__ rank_out, int32_t* __restrict__ chunk_cnt,
                         int64_t nch, int* err) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   // s_idx: the selected expert, or -1 for an empty token slot or an assignment dropped for
   // its negative score (it takes no place in the histogram)
   __shared__ int s_idx[CHUNK][8];
@@ -196,13 +196,14 @@ route_topk_chunk_kernel(const float* __restrict__ logits, const float* __restric
   if (e >= 0) rank_out[(t0 + tok) * k + j] = __popc(s_bits[e] & ((1u << tok) - 1u));
   for (int x = threadIdx.x; x < E; x += ROUTE_THREADS)
     chunk_cnt[static_cast<int64_t>(x) * nch + chunk] = __popc(s_bits[x]);
+  griddep_launch();
 }
 
 __global__ void __launch_bounds__(1024)
 route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
                   int32_t* __restrict__ counts, int32_t* __restrict__ kept,
                   int32_t* __restrict__ offsets, int32_t* __restrict__ cnt_base) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   __shared__ int s_kept[256];
   __shared__ int s_cnt[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,6 +258,7 @@ route_scan_kernel(int32_t* __restrict__ chunk_cnt, int64_t nch, int E, int cap,
     }
     if (lane == 31) dst[E] = incl;
   }
+  griddep_launch();
 }
 
 // Drop by score, step a: thread per slot.  An eligible assignment to an expert over
@@ -268,7 +270,7 @@ route_score_scatter_kernel(const float* __restrict__ logits, const int32_t* __re
                            int cap, const int32_t* __restrict__ chunk_base, int64_t nch,
                            const int32_t* __restrict__ counts,
                            const int32_t* __restrict__ cnt_base, uint32_t* __restrict__ list) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= T * k) return;
   const int in_chunk = in_chunk_rank[i];
@@ -278,6 +280,7 @@ route_score_scatter_kernel(const float* __restrict__ logits, const int32_t* __re
   const int r = chunk_base[static_cast<int64_t>(e) * nch + t / CHUNK] + in_chunk;
   bool nan_seen = false;
   list[cnt_base[e] + r] = order_key(logits[t * E + e], nan_seen);
+  griddep_launch();
 }
 
 constexpr int SELECT_THREADS = 1024;
@@ -309,7 +312,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& excl) {
 __global__ void __launch_bounds__(SELECT_THREADS)
 route_score_select_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ cnt_base,
                           int cap, uint32_t* __restrict__ list) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   __shared__ int s_hist[256];
   __shared__ int s_warp[33];
   __shared__ uint32_t s_prefix;
@@ -361,6 +364,7 @@ route_score_select_kernel(const int32_t* __restrict__ counts, const int32_t* __r
     ties_before += ties;
     kept_before += kept_n;
   }
+  griddep_launch();
 }
 
 __global__ void __launch_bounds__(256)
@@ -370,7 +374,7 @@ route_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int 
                     const int32_t* __restrict__ cnt_base, const int32_t* __restrict__ score_rank,
                     int32_t* __restrict__ dest_row, int32_t* __restrict__ src_tok,
                     int32_t* __restrict__ src_slot, uint8_t* __restrict__ drop_mask) {
-  griddep_enter();   // see common.cuh: dependent launches
+  griddep_wait();   // see common.cuh: dependent launches
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t R = T * k;
   if (i >= R) return;
@@ -395,6 +399,7 @@ route_assign_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k, int 
     src_tok[p] = static_cast<int32_t>(t);
     src_slot[p] = static_cast<int32_t>(i);
   }
+  griddep_launch();
 }
 
 }  // namespace
