@@ -727,12 +727,12 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
 
     barrier(world)
     torch.cuda.synchronize()
-    # 1. the per-phase split inside a graph replay (timed first, while the clocks are where
-    #    the plain replay below finds them: the GEMM time is taken from this run)
+    # 1. the timed replay: `value`, the per-phase split and the GEMM time (first after the
+    #    warm-up, so every workload is timed at the same point of its run)
     w0 = time.time()
     pg = None if args.no_graph else graph_phase_times(wl, args.steps)
     w_pg = time.time()
-    # 2. the step captured once as a CUDA graph and replayed: `value`
+    # 2. a one-step graph without phase events, replayed `steps` times (reported beside)
     graph_ms = None
     g0w = g1w = None
     if not args.no_graph:

@@ -168,3 +168,18 @@ def test_noalloc_route_refusals_before_any_device_call(L):
         for c2 in (cfg(26201, 64, 8, 1, False), cfg(26200, 64, 8, 1, True),
                    cfg(32768, 256, 8)):
             assert L.moe_route_noalloc(ctypes.byref(c2), *ok, None, None) == 3   # no device
+
+
+def test_dispatch_fused_backward_refusals(L):
+    """moe_grouped_ffn_bwd_dispatch checks its configuration and every pointer on the host
+    (null or not 16-byte aligned: MOE_ERR_INVALID_ARG) before anything is enqueued."""
+    cfg = cfg_of(CONFIGS["tiny"])
+    ok = [16] * 16
+    assert L.moe_grouped_ffn_bwd_dispatch(ctypes.byref(cfg), *([None] * 16), None) == 1
+    for i in range(16):
+        bad = list(ok)
+        bad[i] = None if i % 2 else 24          # null, or 8 bytes off a 16-byte boundary
+        assert L.moe_grouped_ffn_bwd_dispatch(ctypes.byref(cfg), *bad, None) == 1, i
+    big = tde.MoEConfigC(T=64, d=100, E=8, k=2, ffn=128, ffn_shared=0, gate=0,
+                         route_scale=1.0, capacity=0)
+    assert L.moe_grouped_ffn_bwd_dispatch(ctypes.byref(big), *ok, None) == 2   # d % 64
