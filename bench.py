@@ -60,8 +60,8 @@ def load_peaks():
 # (the dispatch-fused FC2 data-gradient option included); set to None when the kernel
 # changes.
 GEMM_TRAFFIC_PER_LAUNCH = {
-    "mixtral": (4 * (661.2 + 340.2 + 488.7 + 252.2 + 671.0 + 544.8) / 6 * 1e6, "mixtral_e2"),
-    "qwen3": (4 * (326.5 + 163.9 + 241.8 + 144.1 + 301.0 + 261.4) / 6 * 1e6, "qwen3_e32"),
+    "mixtral": (4 * (658.7 + 340.2 + 488.0 + 252.6 + 670.9 + 544.9) / 6 * 1e6, "mixtral_e2"),
+    "qwen3": (4 * (327.0 + 163.1 + 241.6 + 142.7 + 300.6 + 261.2) / 6 * 1e6, "qwen3_e32"),
 }
 
 # the extra workloads measured beside the headline, each in its own block of the line
