@@ -116,21 +116,36 @@ def memory_bytes(c, rows_kept: int) -> dict:
     }
 
 
-def choose_peak(peaks: dict, clk: dict):
+def choose_peak(peaks: dict, clk: dict, gemm_mhz=None):
     """The bf16 tensor peak that applies to a timed region: the burst figure (measured with
-    the SM clock at its maximum) when the region's median SM clock sat at the maximum, the
-    sustained figure (measured under the power cap) when it ran lower."""
+    the SM clock at its maximum) when the GEMMs ran at the maximum clock, the sustained
+    figure (measured under the power cap) when they ran lower.  The clock is the one the
+    GEMM kernels measured over their own tile loops (`gemm_mhz`, moe_gemm_clock_trace)
+    when given, else the median of the nvidia-smi samples in the region."""
     burst = float(peaks["bf16_tflops"])
     sus = float(peaks.get("bf16_tflops_sustained", burst))
-    med = clk.get("sm_mhz")
     mx = clk.get("sm_max_mhz") or peaks.get("sm_max_mhz")
+    if gemm_mhz is not None:
+        med, what = gemm_mhz, "SM clock of the GEMMs' tile loops (clock64 / %globaltimer)"
+    else:
+        med, what = clk.get("sm_mhz"), "median SM clock of the nvidia-smi samples"
     if med is None or not mx:
-        return sus, "sustained", "bf16_tflops_sustained (no SM clock samples in the region)"
+        return sus, "sustained", "bf16_tflops_sustained (no SM clock measured in the region)"
     if med >= 0.95 * mx:
-        return burst, "burst", (f"bf16_tflops (burst): median SM clock {med:.0f} MHz of "
+        return burst, "burst", (f"bf16_tflops (burst): {what} {med:.0f} MHz of "
                                 f"{mx:.0f} max in the timed region")
-    return sus, "sustained", (f"bf16_tflops_sustained: median SM clock {med:.0f} MHz, below "
+    return sus, "sustained", (f"bf16_tflops_sustained: {what} {med:.0f} MHz, below "
                               f"0.95 x {mx:.0f} max, in the timed region")
+
+
+def gemm_clock_summary(sums):
+    """moe_gemm_clock_read()'s (cycles, ns, loops) as the SM clock of the GEMM tile loops."""
+    cycles, ns, loops = sums
+    if not loops or not ns:
+        return None
+    return {"sm_mhz": round(cycles / ns * 1e3, 1), "loops": loops,
+            "source": "clock64 cycles over %globaltimer nanoseconds of every grouped-GEMM "
+                      "CTA's tile loop in the timed run (moe_gemm_clock_trace)"}
 
 
 # --------------------------------------------------------------------------- clocks
@@ -728,10 +743,17 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
     barrier(world)
     torch.cuda.synchronize()
     # 1. the timed replay: `value`, the per-phase split and the GEMM time (first after the
-    #    warm-up, so every workload is timed at the same point of its run)
+    #    warm-up, so every workload is timed at the same point of its run), with the GEMMs'
+    #    clock traced over it
+    tde.moe_gemm_clock_trace(True)
     w0 = time.time()
     pg = None if args.no_graph else graph_phase_times(wl, args.steps)
     w_pg = time.time()
+    gemm_clock = None
+    if pg is not None:
+        torch.cuda.synchronize()
+        tde.moe_gemm_clock_trace(False)
+        gemm_clock = gemm_clock_summary(tde.moe_gemm_clock_read())
     # 2. a one-step graph without phase events, replayed `steps` times (reported beside)
     graph_ms = None
     g0w = g1w = None
@@ -768,6 +790,9 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
     torch.cuda.synchronize()
     eager_ms = t_start.elapsed_time(t_end)
     w1 = time.time()
+    if pg is None:   # the eager loop is the timed run: its GEMMs' clock
+        tde.moe_gemm_clock_trace(False)
+        gemm_clock = gemm_clock_summary(tde.moe_gemm_clock_read())
     barrier(world)
     st, fl = tde.moe_status(wl.ws)
     if st != 0:
@@ -820,7 +845,8 @@ def measure(c, args, dev, world, rank, clocks, peaks, peak_src, mxfp8=0, e2e=Tru
         gemm_ms = phase_total      # the GEMMs are not separable from the two layer calls
     else:
         gemm_ms = phase_ms["ffn_fwd"] + phase_ms["ffn_bwd"]
-    res["roofline"] = gemm_roofline(c, rows_kept, gemm_ms, peaks, peak_src, clk, mxfp8)
+    res["roofline"] = gemm_roofline(c, rows_kept, gemm_ms, peaks, peak_src, clk, mxfp8,
+                                    gemm_clock)
     # ---- row movers against HBM (device times inside the replay)
     hbm = float(peaks["hbm_gbs"])
     mem = {}
@@ -859,7 +885,7 @@ def describe(c, mxfp8=0, fuse_gather=False, mx_cache=True) -> str:
             + (" cached-weight-quant" if mxfp8 and mx_cache else ""))
 
 
-def gemm_roofline(c, rows_kept, gemm_ms, peaks, peak_src, clk, mxfp8) -> dict:
+def gemm_roofline(c, rows_kept, gemm_ms, peaks, peak_src, clk, mxfp8, gemm_clock=None) -> dict:
     """The grouped GEMMs of one step against their roofline.  bf16: each of the six
     launches takes at least the larger of its tensor time and its HBM time; where the HBM
     terms dominate (weight streaming) the GEMMs are graded on HBM bandwidth."""
@@ -868,7 +894,8 @@ def gemm_roofline(c, rows_kept, gemm_ms, peaks, peak_src, clk, mxfp8) -> dict:
         flops += 4.0 * c.d * c.f * rows_kept + (4.0 * c.d * c.fs * c.T if c.fs else 0.0)
     gemm_s = gemm_ms / 1e3
     achieved = flops / gemm_s / 1e12
-    peak, which, why = choose_peak(peaks, clk)
+    peak, which, why = choose_peak(peaks, clk,
+                                   gemm_clock["sm_mhz"] if gemm_clock else None)
     burst = float(peaks["bf16_tflops"])
     sus = float(peaks.get("bf16_tflops_sustained", burst))
     hbm = float(peaks["hbm_gbs"])
@@ -878,7 +905,8 @@ def gemm_roofline(c, rows_kept, gemm_ms, peaks, peak_src, clk, mxfp8) -> dict:
                       if not mxfp8 else
                       "grouped GEMMs: block-scaled MXFP8 (routed fwd + dgrad"
                       + (" + wgrad" if mxfp8 == 2 else "") + ") and bf16 (the rest)"),
-           "gemm_flops_per_step": flops, "gemm_ms_per_step": round(gemm_ms, 4)}
+           "gemm_flops_per_step": flops, "gemm_ms_per_step": round(gemm_ms, 4),
+           "gemm_clock": gemm_clock}
     if mxfp8:
         # routed FC1 + FC2 and the two data gradients (12 d f per row), at level 2 the two
         # weight gradients (6 d f) too, run at the E4M3 rate; no E4M3 peak is measured here,

@@ -456,6 +456,26 @@ moe_status_t moe_layer_bwd(const moe_config_t *cfg, const void *ctx, const float
  */
 moe_status_t moe_selftest_wait_timeout(void *ws, int64_t budget_cycles, void *stream);
 
+/*
+ * Diagnostics: the SM clock the grouped GEMMs' mainloops ran at.  Under the power cap the
+ * clock that sampling tools report between samples can differ from the one the tensor-core
+ * loops see, which decides the peak their throughput is measured against.  While tracing
+ * is on, the MMA-issuing warp of every bf16 and MXFP8 grouped-GEMM CTA (the leader of a
+ * CTA pair) adds, once per launch, the SM cycles (clock64) and the nanoseconds
+ * (%globaltimer) of its tile loop to device-side sums; cycles / ns is that loop's clock.
+ * The cost is a flag load and two timer reads per CTA and launch, plus three atomics per
+ * CTA and launch while on.  (Not part of the layer; there is no counterpart on the pages.)
+ *
+ * moe_gemm_clock_trace(1) zeroes the sums and turns tracing on; moe_gemm_clock_trace(0)
+ * turns it off and keeps them.  moe_gemm_clock_read() returns the sums: *cycles and *ns
+ * over *loops loops (NULL pointers: MOE_ERR_INVALID_ARG).  Both are synchronous host
+ * calls on the current device, ordered with the legacy default stream only: call them
+ * with no grouped GEMM in flight (after a device or stream synchronisation).  Tracing
+ * state is per device and shared by every caller in the process.
+ */
+moe_status_t moe_gemm_clock_trace(int enable);
+moe_status_t moe_gemm_clock_read(uint64_t *cycles, uint64_t *ns, uint64_t *loops);
+
 /* Synchronise `stream`, then read and clear the device error word in `ws`.
  * Returns MOE_OK, MOE_ERR_DEVICE_FLAG or MOE_ERR_TIMEOUT (MOE_DEVERR_TIMEOUT set),
  * or MOE_ERR_CUDA; *flags (may be NULL) receives the MOE_DEVERR_* bits. */

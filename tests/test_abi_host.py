@@ -183,3 +183,11 @@ def test_dispatch_fused_backward_refusals(L):
     big = tde.MoEConfigC(T=64, d=100, E=8, k=2, ffn=128, ffn_shared=0, gate=0,
                          route_scale=1.0, capacity=0)
     assert L.moe_grouped_ffn_bwd_dispatch(ctypes.byref(big), *ok, None) == 2   # d % 64
+
+
+def test_gemm_clock_read_refuses_null_pointers(L):
+    """Refused before any device call, so it runs without a GPU."""
+    c = ctypes.c_uint64(0)
+    assert L.moe_gemm_clock_read(None, ctypes.byref(c), ctypes.byref(c)) == 1
+    assert L.moe_gemm_clock_read(ctypes.byref(c), None, ctypes.byref(c)) == 1
+    assert L.moe_gemm_clock_read(ctypes.byref(c), ctypes.byref(c), None) == 1

@@ -35,6 +35,23 @@ def test_peak_follows_the_sampled_clock():
     assert bench.choose_peak(peaks, {"sm_mhz": None, "sm_max_mhz": None})[1] == "sustained"
 
 
+def test_peak_follows_the_gemm_kernels_own_clock():
+    """The clock the GEMM tile loops measured overrides the nvidia-smi median."""
+    peaks = {"bf16_tflops": 1928.4, "bf16_tflops_sustained": 1716.7, "sm_max_mhz": 2070.0}
+    smi = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}
+    assert bench.choose_peak(peaks, smi, gemm_mhz=1709.0)[:2] == (1716.7, "sustained")
+    assert bench.choose_peak(peaks, smi, gemm_mhz=2050.0)[:2] == (1928.4, "burst")
+    assert "tile loops" in bench.choose_peak(peaks, smi, gemm_mhz=1709.0)[2]
+    assert bench.choose_peak(peaks, {"sm_mhz": 1600.0, "sm_max_mhz": 2070.0},
+                             gemm_mhz=2070.0)[1] == "burst"
+
+
+def test_gemm_clock_summary():
+    g = bench.gemm_clock_summary((3_400_000_000, 2_000_000_000, 152))
+    assert g["sm_mhz"] == 1700.0 and g["loops"] == 152
+    assert bench.gemm_clock_summary((0, 0, 0)) is None
+
+
 def test_clock_window_summary():
     cs = bench.ClockSampler(0)
     cs.proc = object()           # as if nvidia-smi were running

@@ -25,7 +25,8 @@ __all__ = [
     "moe_mx_weights_size", "moe_mx_quantize_weights", "moe_mx_act_scales_size",
     "moe_mx_permute_quant", "moe_grouped_ffn_mx", "moe_grouped_ffn_bwd_mx", "moe_layer_fwd_mx",
     "moe_layer_bwd_mx",
-    "moe_status", "moe_status_string", "moe_selftest_wait_timeout", "ctx_views", "MoELayer", "CTX_FIELDS",
+    "moe_status", "moe_status_string", "moe_selftest_wait_timeout", "moe_gemm_clock_trace",
+    "moe_gemm_clock_read", "ctx_views", "MoELayer", "CTX_FIELDS",
 ]
 
 GATES = {"softmax": 0, "sigmoid": 1}
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
             "moe_layer_bwd_mx": ([cfgp] + [P] * 15, I32),
             "moe_layer_bwd": ([cfgp] + [P] * 16, I32),
             "moe_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], I32),
+            "moe_gemm_clock_trace": ([I32], I32),
+            "moe_gemm_clock_read": ([ctypes.POINTER(ctypes.c_uint64)] * 3, I32),
             "moe_selftest_wait_timeout": ([P, I64, P], I32),
             "moe_status_string": ([I32], ctypes.c_char_p),
         }
@@ -322,6 +325,19 @@ def moe_selftest_wait_timeout(ws, budget_cycles, stream=None):
     """Enqueue a bounded wait that is never satisfied (see include/moe.h)."""
     _check(lib().moe_selftest_wait_timeout(_p(ws), int(budget_cycles), _s(stream)),
            "moe_selftest_wait_timeout")
+
+
+def moe_gemm_clock_trace(enable):
+    """Turn the grouped GEMMs' clock tracing on (zeroing its sums) or off (keeping them)."""
+    _check(lib().moe_gemm_clock_trace(1 if enable else 0), "moe_gemm_clock_trace")
+
+
+def moe_gemm_clock_read():
+    """The traced sums: (SM cycles, nanoseconds, loops) of the GEMM tile loops."""
+    c, n, k = ctypes.c_uint64(0), ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(lib().moe_gemm_clock_read(ctypes.byref(c), ctypes.byref(n), ctypes.byref(k)),
+           "moe_gemm_clock_read")
+    return c.value, n.value, k.value
 
 
 def moe_status(ws, stream=None):

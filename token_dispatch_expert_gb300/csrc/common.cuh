@@ -150,6 +150,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// ----------------------------------------------------------------- clock tracing
+// The SM clock a tensor-core mainloop actually ran at (moe_gemm_clock_trace).  Under the
+// power cap the clock the driver reports between samples can differ from the one the
+// GEMMs see, so each MMA issuer measures its own tile loop: SM cycles (clock64) over
+// nanoseconds (%globaltimer).  Every kernel file keeps one ClockTrace in device memory;
+// while `on` is set, each issuer adds its loop's cycles and nanoseconds once per launch.
+struct ClockTrace {
+  int on;
+  unsigned long long cycles, ns, loops;
+};
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void clock_trace_add(ClockTrace* t, long long cycles,
+                                                unsigned long long ns) {
+  atomicAdd(&t->cycles, static_cast<unsigned long long>(cycles));
+  atomicAdd(&t->ns, ns);
+  atomicAdd(&t->loops, 1ull);
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -42,6 +43,8 @@
 
 namespace moe {
 namespace {
+
+__device__ ClockTrace g_clock_trace;   // see ClockTrace (common.cuh)
 
 // One tile is TILE_M x 256 of the output.  PAIR = 1: one CTA, M128 x N256 MMAs, A 128 rows
 // and B 256 rows per CTA.  PAIR = 2: a CTA pair (cluster of 2) shares a 256 x 256 tile:
@@ -672,6 +675,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t ph = 0;
       int it = 0;
       bool ok = true, issued_any = false;
+      const bool trace = g_clock_trace.on != 0;
+      const long long trace_c0 = clock64();
+      const unsigned long long trace_n0 = globaltimer_ns();
       for (int tile = unit; tile < total && ok; tile += num_units, ++it) {
         int g, mt, nt;
         map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
@@ -742,6 +748,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         __syncwarp();
       }
+      if (trace && ok && issued_any && lane == 0)
+        clock_trace_add(&g_clock_trace, clock64() - trace_c0, globaltimer_ns() - trace_n0);
       if (!ok && issued_any && lane == 0) {
         // drain the MMAs in flight before TMEM is released
         if (PAIR == 2) tc_commit_pair(smem_u32(&ctl->drain));
@@ -1263,6 +1271,25 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t st) {
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t gemm_clock_trace_set(bool on) {
+  if (on) {
+    const ClockTrace t{1, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_clock_trace, &t, sizeof(t));
+  }
+  const int off = 0;
+  return cudaMemcpyToSymbol(g_clock_trace, &off, sizeof(off), offsetof(ClockTrace, on));
+}
+
+cudaError_t gemm_clock_trace_add(unsigned long long out[3]) {
+  ClockTrace t;
+  const cudaError_t e = cudaMemcpyFromSymbol(&t, g_clock_trace, sizeof(t));
+  if (e != cudaSuccess) return e;
+  out[0] += t.cycles;
+  out[1] += t.ns;
+  out[2] += t.loops;
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -204,4 +204,13 @@ struct MxWgradArgs {
 };
 cudaError_t launch_mx_wgrad(const MxWgradArgs& a, cudaStream_t st);
 
+// Clock tracing of the tensor-core mainloops (moe_gemm_clock_trace): the bf16 grouped GEMMs
+// and the MXFP8 GEMMs each keep their own device-side sums.  *_set(true) zeroes the sums
+// and turns tracing on, *_set(false) turns it off and keeps them; *_add adds the sums to
+// out[0..2] (SM cycles, nanoseconds, loops).  Synchronous; call with the device idle.
+cudaError_t gemm_clock_trace_set(bool on);
+cudaError_t gemm_clock_trace_add(unsigned long long out[3]);
+cudaError_t mx_clock_trace_set(bool on);
+cudaError_t mx_clock_trace_add(unsigned long long out[3]);
+
 }  // namespace moe

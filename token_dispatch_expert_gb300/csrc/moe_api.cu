@@ -809,6 +809,25 @@ moe_status_t moe_selftest_wait_timeout(void* ws, int64_t budget_cycles, void* st
   return cuda_status(cudaGetLastError());
 }
 
+moe_status_t moe_gemm_clock_trace(int enable) {
+  if (moe::gemm_clock_trace_set(enable != 0) != cudaSuccess ||
+      moe::mx_clock_trace_set(enable != 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_gemm_clock_read(uint64_t* cycles, uint64_t* ns, uint64_t* loops) {
+  if (!cycles || !ns || !loops) return MOE_ERR_INVALID_ARG;
+  unsigned long long sum[3] = {0, 0, 0};
+  if (moe::gemm_clock_trace_add(sum) != cudaSuccess ||
+      moe::mx_clock_trace_add(sum) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *cycles = sum[0];
+  *ns = sum[1];
+  *loops = sum[2];
+  return MOE_OK;
+}
+
 moe_status_t moe_status(void* ws, void* stream, int32_t* flags) {
   if (!ptrs_ok(ws)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

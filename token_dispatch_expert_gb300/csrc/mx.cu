@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "common.cuh"
@@ -55,6 +56,8 @@
 
 namespace moe {
 namespace {
+
+__device__ ClockTrace g_clock_trace;   // see ClockTrace (common.cuh)
 
 constexpr int MX_BK = 128;                 // E4M3 elements (bytes) per K block
 constexpr int MX_SFA_BYTES = 512;          // one scale atom
@@ -753,6 +756,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t ph = 0;
       int it = 0;
       bool ok = true, issued_any = false;
+      const bool trace = g_clock_trace.on != 0;
+      const long long trace_c0 = clock64();
+      const unsigned long long trace_n0 = globaltimer_ns();
       for (int tile = unit; tile < total && ok; tile += num_units, ++it) {
         int nkb = p.num_kb;
         if (MODE == GEMM_WGRAD) {
@@ -811,6 +817,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         __syncwarp();
       }
+      if (trace && ok && issued_any && lane == 0)
+        clock_trace_add(&g_clock_trace, clock64() - trace_c0, globaltimer_ns() - trace_n0);
       if (!ok && issued_any && lane == 0) {
         if (PAIR == 2) tc_commit_pair(smem_u32(&ctl->drain));
         else tc_commit(smem_u32(&ctl->drain));
@@ -1512,6 +1520,25 @@ cudaError_t launch_mx_wgrad(const MxWgradArgs& a, cudaStream_t st) {
       !make_map_dw(&tc, a.dW, N, M, static_cast<uint64_t>(a.E)))
     return cudaErrorInvalidValue;
   return launch_mx_any(GEMM_WGRAD, true, ta, tb, tsa, tsb, kp, st, &tc);
+}
+
+cudaError_t mx_clock_trace_set(bool on) {
+  if (on) {
+    const ClockTrace t{1, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_clock_trace, &t, sizeof(t));
+  }
+  const int off = 0;
+  return cudaMemcpyToSymbol(g_clock_trace, &off, sizeof(off), offsetof(ClockTrace, on));
+}
+
+cudaError_t mx_clock_trace_add(unsigned long long out[3]) {
+  ClockTrace t;
+  const cudaError_t e = cudaMemcpyFromSymbol(&t, g_clock_trace, sizeof(t));
+  if (e != cudaSuccess) return e;
+  out[0] += t.cycles;
+  out[1] += t.ns;
+  out[2] += t.loops;
+  return cudaSuccess;
 }
 
 }  // namespace moe
