@@ -14,8 +14,8 @@
  *               order, the exclusive scan of kept counts into segment offsets, and
  *               the padding-free token buffer's side arrays (token ids, slot ids,
  *               destination rows).  X-MoE verdict page (arXiv 2508.13337):
- *               "key machinery" (padding-free token buffer with token ids, expert
- *               ids, per-expert counts and combine weights), referee minor comment
+ *               key machinery (the padding-free token buffer and its side arrays:
+ *               source token, expert, rows per expert, combine weight), referee minor comment
  *               on section 4.1.1 Listing 1 (max_token_count = floor(c*S*K/E)) and
  *               major comment on section 5.6 (drops only on capacity).
  *               Primus MoE blog, Figure 7 dataflow: the router step and the

@@ -2,8 +2,9 @@
 
 * a per-expert selection bias that steers the top-k choice only (DeepSeek-V3-style
   balancing bias; the gate weights stay those of the raw logits);
-* negative-score dropping (X-MoE verdict page, major comment on section 5.6:
-  DeepSpeed-MoE also drops tokens with negative routing scores), read as: an assignment
+* negative-score dropping (X-MoE verdict page, major comment on section 5.6, which
+  attributes to DeepSpeed-MoE the discarding of assignments scored below zero), read as:
+  an assignment
   whose raw router logit is negative is dropped before the capacity ranking;
 * capacity dropping by score: an overflowing expert keeps the assignments with the
   largest raw logit (ties: lower token) instead of the earliest tokens.

@@ -3,8 +3,8 @@
 // "MoE Training Optimization with Primus": Figure 7 (FC1 gate/up and FC2 down grouped
 // GEMMs with SwiGLU between them), the MegaMoE section (backward = FC2 data-gradient,
 // FC1 data-gradient, plus two variable-K weight-gradient GEMMs) and the JAX section
-// (one launch over the ragged, variable-M per-expert groups of a sorted-by-expert
-// layout).  X-MoE verdict page, key machinery: the groups are the padding-free
+// (a single launch covers every expert's group of rows, each of its own length, in a
+// layout sorted by expert).  X-MoE verdict page, key machinery: the groups are the padding-free
 // buffer's expert segments -- no segment is padded; a tile that crosses a segment's
 // end masks its stores, and in the weight-gradient GEMMs (K = the segment's rows) each
 // segment gets its own copy of the operand maps whose row extent ends at the segment's

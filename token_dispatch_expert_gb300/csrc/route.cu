@@ -3,10 +3,10 @@
 //
 // "MoE Training Optimization with Primus", Figure 7 dataflow: the router step (top-k
 // experts per token).  X-MoE verdict page (arXiv 2508.13337), key
-// machinery: the padding-free token buffer with token ids, expert ids, per-expert
-// token counts and combine weights; referee minor comment on section 4.1.1 Listing 1
-// (max_token_count from the capacity factor) and major comment on section 5.6 (drop
-// only on capacity overflow).
+// machinery: the padding-free token buffer and its side arrays (which token, which
+// expert, how many rows per expert, the combine weight); referee minor comment on section
+// 4.1.1 Listing 1 (max_token_count from the capacity factor) and major comment on section
+// 5.6 (drop only on capacity overflow).
 //
 // Three kernels, all deterministic:
 //   1. route_topk_chunk: one CTA per 32-token chunk.  Each warp selects the top-k of 4
