@@ -9,17 +9,19 @@
  *
  * Where each operation is defined (page title, then section / figure / field):
  *   - "MoE Training Optimization with Primus" (AMD blog), Figure 7 dataflow: router
- *     top-k per token; a permutation into expert order; FC1 (gate/up) and FC2 (down)
- *     grouped GEMMs with SwiGLU between them; a last step that un-permutes the rows,
- *     scales them by the gate weights and sums each token's k of them.
- *     MegaMoE section: the backward by dispatch/combine duality plus two
- *     variable-K weight-gradient GEMMs.  JAX section: one grouped-GEMM launch over
- *     ragged variable-M expert groups; token counts stay on the GPU (no host sync).
+ *     top-k per token; a permutation into expert order; the grouped gate/up projection
+ *     (FC1), SwiGLU and the grouped down projection (FC2); a last step that un-permutes
+ *     the rows, scales them by the gate weights and sums each token's k of them.
+ *     MegaMoE section: the backward mirrors dispatch and combine, and adds the two
+ *     weight-gradient GEMMs whose K is each expert's row count.  JAX section: a single
+ *     grouped-GEMM launch covers all expert groups, each of its own length; the token
+ *     counts never leave the GPU (no host synchronisation).
  *   - X-MoE verdict page (pith.science, arXiv 2508.13337), "key machinery": the
  *     padding-free token buffer -- only the routed tokens, stored contiguously per
- *     expert, with token ids, expert ids, per-expert counts and combine weights;
- *     referee minor comment on section 4.1.1 Listing 1: max_token_count and
- *     c = 1.25; major comment on section 5.6: drops only on capacity overflow.
+ *     expert, plus side arrays giving each row's source token, its expert, the rows per
+ *     expert and the combine weight; referee minor comment on section 4.1.1 Listing 1:
+ *     max_token_count and c = 1.25; major comment on section 5.6: an assignment is
+ *     dropped only when its expert is over capacity.
  *
  * Conventions shared by every call
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except the

@@ -17,7 +17,7 @@
  *               key machinery (the padding-free token buffer and its side arrays:
  *               source token, expert, rows per expert, combine weight), referee minor comment
  *               on section 4.1.1 Listing 1 (max_token_count = floor(c*S*K/E)) and
- *               major comment on section 5.6 (drops only on capacity).
+ *               major comment on section 5.6 (dropping only on capacity overflow).
  *               Primus MoE blog, Figure 7 dataflow: the router step and the
  *               permutation into expert order.
  *   ffn         SwiGLU expert FFN with three matrices (gate, up: d x f; down: f x d).

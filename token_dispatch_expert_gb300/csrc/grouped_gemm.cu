@@ -1,8 +1,9 @@
 // grouped_gemm.cu -- the expert FFN's grouped GEMMs on the 5th-generation tensor cores.
 //
-// "MoE Training Optimization with Primus": Figure 7 (FC1 gate/up and FC2 down grouped
-// GEMMs with SwiGLU between them), the MegaMoE section (backward = FC2 data-gradient,
-// FC1 data-gradient, plus two variable-K weight-gradient GEMMs) and the JAX section
+// "MoE Training Optimization with Primus": Figure 7 (the grouped gate/up projection FC1,
+// SwiGLU, the grouped down projection FC2), the MegaMoE section (the backward's FC2 and
+// FC1 data-gradient GEMMs and the two weight-gradient GEMMs whose K is each expert's row
+// count) and the JAX section
 // (a single launch covers every expert's group of rows, each of its own length, in a
 // layout sorted by expert).  X-MoE verdict page, key machinery: the groups are the padding-free
 // buffer's expert segments -- no segment is padded; a tile that crosses a segment's
