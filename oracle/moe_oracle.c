@@ -61,7 +61,7 @@
  *     (in fp32) for the top-k choice only (DeepSeek-V3-style balancing bias); with
  *     negative-score dropping, an assignment whose raw logit is negative is dropped
  *     before the capacity ranking and is not counted (X-MoE verdict page, major comment
- *     on section 5.6: DeepSpeed-MoE also drops negative-score tokens);
+ *     on section 5.6, which credits DeepSpeed-MoE with discarding negative scores);
  *   - drop by score: when an expert overflows its capacity, the `cap` assignments it keeps
  *     are those with the largest raw fp32 logit (ties: lower token index first) instead of
  *     the first `cap` in token order; the kept rows still sit in token order inside the
