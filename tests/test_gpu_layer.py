@@ -40,6 +40,15 @@ SMALL = {
                          zipf_alpha=20.0),
     "two_hot_shared": MoEConfig("two_hot", T=700, d=256, E=16, k=2, f=192, fs=128,
                                 gate="sigmoid", route_scale=2.5, zipf_s=1.0, zipf_alpha=20.0),
+    # the edges of the shape limits: a single expert (k = 1; 300 rows = one whole M tile and
+    # a 44-row tail tile), the smallest dims (d = f = 64: one K block, one 64-column N
+    # tile), the largest expert count (E = 256, the group limit, with k = 8: about 16 rows
+    # per expert, one-CTA tiles, some experts empty), and dims that are odd multiples of 64
+    # on CTA pairs (d = 192: three K blocks; f = 448: a half-filled last N tile)
+    "E1": MoEConfig("E1", T=300, d=128, E=1, k=1, f=128),
+    "min_dims": MoEConfig("min_dims", T=129, d=64, E=4, k=2, f=64),
+    "E256": MoEConfig("E256", T=512, d=128, E=256, k=8, f=64, zipf_s=1.1),
+    "odd64": MoEConfig("odd64", T=1024, d=192, E=4, k=2, f=448, zipf_s=1.0),
 }
 
 ROUTE_KEYS = ["topk_idx", "counts", "kept", "offsets", "dest_row", "src_tok", "src_slot",
