@@ -120,6 +120,11 @@ EDGE_CASES = {
     # tails in FC1 (f = 320: the last FC1 tile holds 64 valid columns, all in the first CTA)
     # and in FC2 / FC1 data-gradient (d = 384)
     "tail_edges": ([31, 32, 33, 160, 161, 256, 416, 417, 2, 700], 384, 320),
+    # a long segment whose last M tile is a 64-row swap-AB tail tile, taken by CTA pairs
+    # that go on to ordinary FC1 tiles right after it: the up warp hands its transposed
+    # block to the gate warp and must not restage an ordinary tile into it before the gate
+    # warp has read it (once seen as corrupted b, h on the tail rows)
+    "long_tail": ([40000, 1000], 256, 512),
 }
 
 

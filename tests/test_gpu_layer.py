@@ -101,9 +101,14 @@ def test_layer_twice_is_bitwise_deterministic():
         assert torch.equal(g1[k], g2[k]), k
 
 
-@pytest.mark.parametrize("name", ["mixtral", "qwen3", "dsv3", "capacity"])
+# a long token axis with narrow experts: 262144 kept rows, about a thousand M tiles per
+# launch and a few hundred tiles per CTA pair, and a row count past 2^17 in every offset
+LONG = MoEConfig("long_tokens", T=131072, d=256, E=16, k=2, f=512, zipf_s=1.1)
+
+
+@pytest.mark.parametrize("name", ["mixtral", "qwen3", "dsv3", "capacity", "long_tokens"])
 def test_layer_full_size_sampled(name):
-    c = CONFIGS[name]
+    c = LONG if name == "long_tokens" else CONFIGS[name]
     g = gen_inputs_device(c, "cuda")
     layer, y, gr = run_layer(c, g)
     assert layer.status() == (0, 0)

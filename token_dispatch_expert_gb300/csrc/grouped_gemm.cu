@@ -431,6 +431,12 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
     __syncwarp();                            // the block is read before the next step
     if (MODE == GEMM_FC1_SWIGLU) mbar_arrive(smem_u32(&ctl->xempty[pi][0]));
   }
+  // FC1: the up warp's block is also its staging block for ordinary tiles, so it leaves
+  // only once the gate warp has read the last step out of it
+  if (up && ntok > 0 &&
+      !warp_wait(smem_u32(&ctl->xempty[pi][0]), (static_cast<uint32_t>(xc) & 1u) ^ 1u,
+                 abort_flag, p.err, WAIT_BUDGET))
+    return false;
   return true;
 }
 
