@@ -447,7 +447,11 @@ void orc_combine(int64_t n_tok, const int64_t *toks, int k, int d, const int32_t
  *   dyp[row] = w[t,j] * dy[t]                      for kept slots
  *   dw[t,j]  = <dy[t], yp[row]>                    (0 for a dropped slot)
  *   softmax gate: dl_j = w_j (dw_j - sum_i w_i dw_i)
- *   sigmoid gate: S = sum_i s_i, ds_j = scale (dw_j / S - sum_i s_i dw_i / S^2),
+ *   sigmoid gate: S = sum_i s_i; the derivative of w_j = scale s_j / S gives
+ *                 ds_j = scale (dw_j / S - sum_i s_i dw_i / S^2)
+ *                      = scale / S^2 * sum_i s_i (dw_j - dw_i),
+ *                 summed in the second form, which has no cancellation where the exact
+ *                 value is 0 (k = 1: the weight is the constant `scale`);
  *                 dl_j = ds_j s_j (1 - s_j)
  *   dlogits[t, e] = dl_j for e = topk_idx[t,j], 0 for unselected experts.
  * dy is indexed by q (the position in toks), yp through yp_row_of as in orc_combine,
@@ -488,15 +492,17 @@ void orc_combine_bwd(int64_t n_tok, const int64_t *toks, int E, int k, int d, in
             for (int j = 0; j < k; ++j)
                 dl[topk_idx[t * k + j]] = topk_w[t * k + j] * (dw[j] - sw);
         } else {
-            double S = 0.0, sd = 0.0;
+            double S = 0.0;
             for (int j = 0; j < k; ++j) {
                 double l = (double)logits[t * E + topk_idx[t * k + j]];
                 s[j] = 1.0 / (1.0 + exp(-l));
                 S += s[j];
-                sd += s[j] * dw[j];
             }
             for (int j = 0; j < k; ++j) {
-                double ds = scale * (dw[j] / S - sd / (S * S));
+                double acc = 0.0;
+                for (int i = 0; i < k; ++i)
+                    acc += s[i] * (dw[j] - dw[i]);
+                double ds = scale * acc / (S * S);
                 dl[topk_idx[t * k + j]] = ds * s[j] * (1.0 - s[j]);
             }
         }

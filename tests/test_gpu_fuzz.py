@@ -1,0 +1,82 @@
+"""Seeded random layer configurations, compared with the oracle in full (every output).
+
+Each case draws the shape (T, d, f, E, k, a shared expert or none), the gate, a capacity
+or none, a Zipf skew or none and the routing variants (selection-only bias, negative-score
+dropping, dropping by score, FC1 recompute) from a fixed seed, within the library's limits
+and small enough for the float64 oracle to finish in seconds.  The fixed cases elsewhere
+pin the known edges; these look for combinations nobody listed."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, dev, f64, np_i
+from test_gpu_layer import ROUTE_KEYS, run_layer
+from workloads import MoEConfig, gen_inputs_host
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 24
+
+
+def draw_config(i: int) -> MoEConfig:
+    rng = np.random.default_rng(1000 + i)
+    E = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16, 32, 64, 100, 256]))
+    k = int(rng.integers(1, min(8, E) + 1))
+    d = int(rng.choice([64, 128, 192, 256, 384, 512]))
+    f = int(rng.choice([64, 128, 192, 256, 320, 448, 512, 640]))
+    fs = int(rng.choice([64, 128, 192])) if rng.random() < 0.3 else 0
+    # tokens: mostly a sizeable fraction of a cap that keeps the oracle's work around 1e9
+    # flops, sometimes a handful (log-uniform)
+    cap_t = max(2, min(3000, int(1.5e9 / (12 * k * d * f + (12 * d * fs if fs else 0)))))
+    if rng.random() < 0.2:
+        T = max(1, int(np.exp(rng.uniform(0, np.log(cap_t)))))
+    else:
+        T = max(1, int(rng.uniform(0.25, 1.0) * cap_t))
+    sigmoid = rng.random() < 0.35
+    cap = float(rng.uniform(0.3, 1.5)) if rng.random() < 0.4 else None
+    zipf = float(rng.uniform(0.8, 1.6)) if rng.random() < 0.7 else None
+    alpha = float(rng.uniform(0.5, 3.0))
+    bias = (tuple(float(v) for v in rng.normal(0, 0.7, E)) if rng.random() < 0.15 else None)
+    drop_neg = bool(rng.random() < 0.1)
+    by_score = bool(cap is not None and rng.random() < 0.4)
+    recompute = bool(rng.random() < 0.15)
+    return MoEConfig(f"fuzz{i}", T=T, d=d, E=E, k=k, f=f, fs=fs,
+                     gate="sigmoid" if sigmoid else "softmax",
+                     route_scale=2.5 if sigmoid else 1.0, cap_factor=cap, zipf_s=zipf,
+                     zipf_alpha=alpha, select_bias=bias, drop_negative=drop_neg,
+                     drop_by_score=by_score, recompute=recompute)
+
+
+def test_draws_are_within_the_limits():
+    for i in range(N_CASES):
+        c = draw_config(i)
+        assert 1 <= c.k <= min(8, c.E) and c.E <= 256 and c.d % 64 == 0 and c.f % 64 == 0
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_layer_random_config_full_compare(i):
+    c = draw_config(i)
+    inp = gen_inputs_host(c)
+    g = {k: dev(v) for k, v in inp.items()}
+    layer, y, gr = run_layer(c, g)
+    assert layer.status() == (0, 0), c
+    fo = oracle.layer_fwd(c, inp)
+    bo = oracle.layer_bwd(c, inp, fo)
+    v = layer.views()
+    for key in ROUTE_KEYS:
+        if key in v:
+            np.testing.assert_array_equal(np_i(v[key]), fo["route"][key], err_msg=f"{key} {c}")
+    assert_close("y", f64(y), fo["y"])
+    assert_close("dx", f64(gr["dx"]), bo["dx"])
+    assert_close("dlogits", f64(gr["dlogits"]), bo["dlogits"])
+    for e in range(c.E):
+        if fo["route"]["kept"][e] == 0:
+            assert (f64(gr["dW1"][e]) == 0).all() and (f64(gr["dW2"][e]) == 0).all()
+            continue
+        assert_close(f"dW1[{e}]", f64(gr["dW1"][e]), bo["dW1"][e])
+        assert_close(f"dW2[{e}]", f64(gr["dW2"][e]), bo["dW2"][e])
+    if c.fs:
+        assert_close("dW1s", f64(gr["dW1s"]), bo["dW1s"])
+        assert_close("dW2s", f64(gr["dW2s"]), bo["dW2s"])

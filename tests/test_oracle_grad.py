@@ -137,3 +137,20 @@ def test_two_expert_gate_gradient_closed_form(gate):
         others = [e for e in range(cfg.E) if e not in (e0, e1)]
         np.testing.assert_allclose([dl[t, e0], dl[t, e1]], [d0, d1], rtol=1e-12, atol=1e-15)
         assert (dl[t, others] == 0).all()
+
+
+@pytest.mark.parametrize("gate", ["softmax", "sigmoid"])
+def test_single_expert_gate_gradient_is_zero(gate):
+    """k = 1: both gates renormalise over the one selected expert, so its weight is the
+    constant 1 (softmax) or `scale` (sigmoid) and every logit's gradient is exactly 0."""
+    scale = 2.5 if gate == "sigmoid" else 1.0
+    cfg = MoEConfig("k1_" + gate, T=64, d=8, E=6, k=1, f=8, gate=gate, route_scale=scale)
+    lg = np.random.default_rng(5).standard_normal((cfg.T, cfg.E)).astype(np.float32) * 3
+    r = oracle.route(cfg, lg)
+    np.testing.assert_allclose(r["topk_w"], np.full((cfg.T, 1), scale), rtol=1e-15)
+    rng = np.random.default_rng(6)
+    yp = rng.standard_normal((cfg.T, cfg.d))
+    dy = rng.standard_normal((cfg.T, cfg.d))
+    _, dl = oracle.combine_bwd(cfg, lg, r, dy, yp, rnd=False)
+    assert (dl == 0).all()
+
