@@ -18,6 +18,7 @@ from workloads import MoEConfig, gen_inputs_host
 pytestmark = pytest.mark.gpu
 
 N_CASES = 24
+N_PAIR_CASES = 16
 
 
 def draw_config(i: int) -> MoEConfig:
@@ -49,15 +50,39 @@ def draw_config(i: int) -> MoEConfig:
                      drop_by_score=by_score, recompute=recompute)
 
 
+def draw_pair_config(i: int) -> MoEConfig:
+    """Few experts and many rows each, so the CTA-pair tiles, their swap-AB tail tiles and
+    long segments are exercised (at least 192 rows per expert on average)."""
+    rng = np.random.default_rng(2000 + i)
+    E = int(rng.choice([1, 2, 3, 4, 5, 6, 8]))
+    k = int(rng.integers(1, min(4, E) + 1))
+    d = int(rng.choice([64, 128, 192, 256]))
+    f = int(rng.choice([64, 128, 192, 256, 320, 384]))
+    fs = int(rng.choice([64, 128])) if rng.random() < 0.25 else 0
+    lo = (192 * E + k - 1) // k
+    hi = max(lo + 1, min(12000, int(2e9 / (12 * k * d * f + (12 * d * fs if fs else 0)))))
+    T = int(rng.integers(lo, hi + 1))
+    sigmoid = rng.random() < 0.3
+    cap = float(rng.uniform(0.8, 1.5)) if rng.random() < 0.3 else None
+    zipf = float(rng.uniform(0.5, 1.3)) if rng.random() < 0.5 else None
+    return MoEConfig(f"fuzzpair{i}", T=T, d=d, E=E, k=k, f=f, fs=fs,
+                     gate="sigmoid" if sigmoid else "softmax",
+                     route_scale=2.5 if sigmoid else 1.0, cap_factor=cap, zipf_s=zipf,
+                     zipf_alpha=float(rng.uniform(0.3, 1.0)),
+                     drop_by_score=bool(cap is not None and rng.random() < 0.4),
+                     recompute=bool(rng.random() < 0.15))
+
+
 def test_draws_are_within_the_limits():
-    for i in range(N_CASES):
-        c = draw_config(i)
+    for c in [draw_config(i) for i in range(N_CASES)] + [draw_pair_config(i)
+                                                         for i in range(N_PAIR_CASES)]:
         assert 1 <= c.k <= min(8, c.E) and c.E <= 256 and c.d % 64 == 0 and c.f % 64 == 0
 
 
-@pytest.mark.parametrize("i", range(N_CASES))
+@pytest.mark.parametrize("i", [f"any{i}" for i in range(N_CASES)] +
+                         [f"pair{i}" for i in range(N_PAIR_CASES)])
 def test_layer_random_config_full_compare(i):
-    c = draw_config(i)
+    c = draw_config(int(i[3:])) if i.startswith("any") else draw_pair_config(int(i[4:]))
     inp = gen_inputs_host(c)
     g = {k: dev(v) for k, v in inp.items()}
     layer, y, gr = run_layer(c, g)
