@@ -203,8 +203,9 @@ int64_t orc_route(int64_t T, int E, int k, int gate, double scale, int64_t cap,
             double z = 0.0;
             for (int j = 0; j < k; ++j)
                 z += 1.0 / (1.0 + exp(-sel[j]));
+            /* scale * (sigma / z): a lone selected expert's weight is exactly `scale` */
             for (int j = 0; j < k; ++j)
-                topk_w[t * k + j] = scale * (1.0 / (1.0 + exp(-sel[j]))) / z;
+                topk_w[t * k + j] = scale * ((1.0 / (1.0 + exp(-sel[j]))) / z);
         }
     }
 

@@ -11,8 +11,10 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, dev, f64, np_i
+import token_dispatch_expert_gb300 as tde
+from gpu_util import assert_close, dev, f64, np_i, record, stats
 from test_gpu_layer import ROUTE_KEYS, run_layer
+from test_gpu_mxfp8 import assert_layer_mx_wgrad, mx_cfg
 from workloads import MoEConfig, gen_inputs_host
 
 pytestmark = pytest.mark.gpu
@@ -105,3 +107,65 @@ def test_layer_random_config_full_compare(i):
     if c.fs:
         assert_close("dW1s", f64(gr["dW1s"]), bo["dW1s"])
         assert_close("dW2s", f64(gr["dW2s"]), bo["dW2s"])
+
+
+N_MX_CASES = 12
+
+
+def draw_mx_config(i: int):
+    """The MXFP8 layer (routed forward and data gradients, with level 2 the weight
+    gradients too): d, f multiples of 128, one-CTA and CTA-pair segment lengths."""
+    rng = np.random.default_rng(3000 + i)
+    E = int(rng.choice([1, 2, 3, 4, 8, 16, 64]))
+    k = int(rng.integers(1, min(4, E) + 1))
+    d = int(rng.choice([128, 256, 384]))
+    f = int(rng.choice([128, 256, 384, 512]))
+    fs = int(rng.choice([128, 256])) if rng.random() < 0.25 else 0
+    cap_t = max(2, min(6000, int(1.5e9 / (12 * k * d * f + (12 * d * fs if fs else 0)))))
+    T = max(1, int(rng.uniform(0.1, 1.0) * cap_t))
+    sigmoid = rng.random() < 0.3
+    cap = float(rng.uniform(0.6, 1.5)) if rng.random() < 0.3 else None
+    zipf = float(rng.uniform(0.6, 1.4)) if rng.random() < 0.5 else None
+    level = int(rng.choice([1, 2]))
+    c = MoEConfig(f"fuzzmx{i}", T=T, d=d, E=E, k=k, f=f, fs=fs,
+                  gate="sigmoid" if sigmoid else "softmax",
+                  route_scale=2.5 if sigmoid else 1.0, cap_factor=cap, zipf_s=zipf)
+    return c, level
+
+
+@pytest.mark.parametrize("i", range(N_MX_CASES))
+def test_mx_layer_random_config(i):
+    c, level = draw_mx_config(i)
+    inp = gen_inputs_host(c)
+    g = {k: dev(v) for k, v in inp.items()}
+    layer = tde.MoELayer(mx_cfg(c, level))
+    wq = layer.quantize_weights(g["W1"], g["W2"])
+    y = layer.forward_mx(g["logits"], g["x"], wq, g.get("W1s"), g.get("W2s"))
+    gr = layer.backward_mx(g["logits"], g["x"], g["dy"], wq, g.get("W1s"), g.get("W2s"))
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0), (c, level)
+    fo = oracle.layer_fwd(c, inp, mx=True)
+    bo = oracle.layer_bwd(c, inp, fo, mx=True, mx_wgrad=level == 2)
+    plain = oracle.layer_bwd(c, inp, fo, mx=True) if level == 2 else None
+    # y and dx pass through E4M3 codes that each side takes from its own bf16 h and dab;
+    # where those differ by one bf16 step at a block's largest element the whole block's
+    # scale can move, so these two take the layer-level MXFP8 bound (rel-L2 1e-2, every
+    # entry within 0.1 of rms + |o|); dlogits does not pass through a quantisation
+    for name, got, ref in (("y", y, fo["y"]), ("dx", gr["dx"], bo["dx"])):
+        st = stats(f64(got), ref)
+        record(name, st)
+        assert st["rel_l2"] <= 1e-2 and st["max_scaled"] <= 0.1, (name, st)
+    assert_close("dlogits", f64(gr["dlogits"]), bo["dlogits"])
+    for e in range(c.E):
+        if fo["route"]["kept"][e] == 0:
+            continue
+        if level == 2:
+            assert_layer_mx_wgrad(f"dW1[{e}]", f64(gr["dW1"][e]), bo["dW1"][e], plain["dW1"][e])
+            assert_layer_mx_wgrad(f"dW2[{e}]", f64(gr["dW2"][e]), bo["dW2"][e], plain["dW2"][e])
+        else:
+            assert_close(f"dW1[{e}]", f64(gr["dW1"][e]), bo["dW1"][e])
+            assert_close(f"dW2[{e}]", f64(gr["dW2"][e]), bo["dW2"][e])
+    if c.fs:
+        assert_close("dW1s", f64(gr["dW1s"]), bo["dW1s"])
+        assert_close("dW2s", f64(gr["dW2s"]), bo["dW2s"])
+

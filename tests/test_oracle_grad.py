@@ -147,7 +147,7 @@ def test_single_expert_gate_gradient_is_zero(gate):
     cfg = MoEConfig("k1_" + gate, T=64, d=8, E=6, k=1, f=8, gate=gate, route_scale=scale)
     lg = np.random.default_rng(5).standard_normal((cfg.T, cfg.E)).astype(np.float32) * 3
     r = oracle.route(cfg, lg)
-    np.testing.assert_allclose(r["topk_w"], np.full((cfg.T, 1), scale), rtol=1e-15)
+    np.testing.assert_array_equal(r["topk_w"], np.full((cfg.T, 1), scale))
     rng = np.random.default_rng(6)
     yp = rng.standard_normal((cfg.T, cfg.d))
     dy = rng.standard_normal((cfg.T, cfg.d))

@@ -160,9 +160,11 @@ route_topk_chunk_kernel(const float* __restrict__ logits, const float* __restric
           w[j] = 1.0f / (1.0f + expf(-sel_l[j]));
           z += w[j];
         }
+      // scale * (sigma / z): with one selected expert sigma / z is exactly 1, so its
+      // weight is exactly `scale`, as the definition gives
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (j < k) w[j] = scale * w[j] / z;
+        if (j < k) w[j] = scale * (w[j] / z);
     }
     int my_e = 0;
     float my_w = 0.0f;
