@@ -11,6 +11,7 @@ import torch
 import oracle
 import token_dispatch_expert_gb300 as tde
 from gpu_util import assert_close, cfg_c, dev, f64, new_ws
+from test_gpu_fuzz import draw_config, draw_pair_config
 from workloads import CONFIGS, MoEConfig, gen_bf16, gen_inputs_host, gen_logits, gen_rows_bf16
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +26,13 @@ CASES = {
     "single": MoEConfig("single", T=300, d=128, E=1, k=1, f=256),
     "deepK": MoEConfig("deepK", T=256, d=1024, E=3, k=1, f=640),
 }
+# seeded random shapes (the layer fuzz's drawers, routing variants off): three on the
+# one-CTA path, three on the CTA-pair path
+for _i in range(3):
+    CASES[f"rand{_i}"] = draw_config(100 + _i).replace(
+        select_bias=None, drop_negative=False, drop_by_score=False, recompute=False)
+    CASES[f"randpair{_i}"] = draw_pair_config(100 + _i).replace(drop_by_score=False,
+                                                               recompute=False)
 
 
 def setup(c):
