@@ -13,7 +13,7 @@ import torch
 import oracle
 import token_dispatch_expert_gb300 as tde
 from gpu_util import assert_close, dev, f64, np_i, record, stats
-from test_gpu_layer import ROUTE_KEYS, run_layer
+from test_gpu_layer import ROUTE_KEYS, check_layer_sampled, run_layer
 from test_gpu_mxfp8 import assert_layer_mx_wgrad, mx_cfg
 from workloads import MoEConfig, gen_inputs_host
 
@@ -168,4 +168,34 @@ def test_mx_layer_random_config(i):
     if c.fs:
         assert_close("dW1s", f64(gr["dW1s"]), bo["dW1s"])
         assert_close("dW2s", f64(gr["dW2s"]), bo["dW2s"])
+
+
+N_BIG_CASES = 8
+
+
+def draw_big_config(i: int) -> MoEConfig:
+    """Large shapes, checked on sampled outputs: tens of thousands of tokens, widths up to
+    4096, up to 256 experts, many tiles per CTA and long or very uneven segments."""
+    rng = np.random.default_rng(4000 + i)
+    E = int(rng.choice([2, 4, 8, 16, 32, 64, 128, 256]))
+    k = int(rng.integers(1, min(8, E) + 1))
+    d = int(rng.choice([512, 1024, 2048, 4096]))
+    f = int(rng.choice([256, 512, 768, 1024, 1408, 2048]))
+    fs = int(rng.choice([512, 1024])) if rng.random() < 0.25 else 0
+    T = int(rng.choice([4096, 8192, 16384, 32768, 65536]))
+    while T * k * max(d, f) * 6 > (40 << 30) or E * 3 * d * f * 2 > (8 << 30):
+        T //= 2                                  # keep the device footprint to a few GB
+    sigmoid = rng.random() < 0.3
+    cap = float(rng.uniform(0.7, 1.5)) if rng.random() < 0.35 else None
+    zipf = float(rng.uniform(0.6, 1.6)) if rng.random() < 0.7 else None
+    return MoEConfig(f"fuzzbig{i}", T=T, d=d, E=E, k=k, f=f, fs=fs,
+                     gate="sigmoid" if sigmoid else "softmax",
+                     route_scale=2.5 if sigmoid else 1.0, cap_factor=cap, zipf_s=zipf,
+                     zipf_alpha=float(rng.uniform(0.3, 2.0)),
+                     drop_by_score=bool(cap is not None and rng.random() < 0.4))
+
+
+@pytest.mark.parametrize("i", range(N_BIG_CASES))
+def test_layer_random_large_config_sampled(i):
+    check_layer_sampled(draw_big_config(i))
 

@@ -108,7 +108,14 @@ LONG = MoEConfig("long_tokens", T=131072, d=256, E=16, k=2, f=512, zipf_s=1.1)
 
 @pytest.mark.parametrize("name", ["mixtral", "qwen3", "dsv3", "capacity", "long_tokens"])
 def test_layer_full_size_sampled(name):
-    c = LONG if name == "long_tokens" else CONFIGS[name]
+    check_layer_sampled(LONG if name == "long_tokens" else CONFIGS[name])
+
+
+def check_layer_sampled(c):
+    """The layer at a size the oracle cannot evaluate in full: routing in full; y, dx and
+    dlogits on 256 sampled tokens (plus dropped ones under a capacity); 16 x 64 entries of
+    the weight gradients of three experts (the most loaded, the least loaded non-empty one,
+    expert 0) and of the shared expert."""
     g = gen_inputs_device(c, "cuda")
     layer, y, gr = run_layer(c, g)
     assert layer.status() == (0, 0)
