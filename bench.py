@@ -56,12 +56,12 @@ def load_peaks():
 # one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of a profiling shape with
 # the same per-expert GEMMs and 1/4 of the experts and of the rows -- every operand and
 # result scales with those -- times 4: `mixtral_e2` for the Mixtral layer, `qwen3_e32` for
-# the Qwen3 layer.  Valid for the grouped-GEMM kernel as of its dependent-launch version
-# (the dispatch-fused FC2 data-gradient option included); set to None when the kernel
+# the Qwen3 layer.  Valid for the grouped-GEMM kernel as it stands (late dependent-launch
+# release, clock trace, the FC1 tail-tile hand-off wait); set to None when the kernel
 # changes.
 GEMM_TRAFFIC_PER_LAUNCH = {
-    "mixtral": (4 * (658.7 + 340.2 + 488.0 + 252.6 + 670.9 + 544.9) / 6 * 1e6, "mixtral_e2"),
-    "qwen3": (4 * (327.0 + 163.1 + 241.6 + 142.7 + 300.6 + 261.2) / 6 * 1e6, "qwen3_e32"),
+    "mixtral": (4 * (659.4 + 340.3 + 486.9 + 252.3 + 670.9 + 545.0) / 6 * 1e6, "mixtral_e2"),
+    "qwen3": (4 * (327.0 + 163.4 + 241.4 + 142.6 + 300.6 + 261.5) / 6 * 1e6, "qwen3_e32"),
 }
 
 # the extra workloads measured beside the headline, each in its own block of the line
