@@ -199,3 +199,46 @@ def draw_big_config(i: int) -> MoEConfig:
 def test_layer_random_large_config_sampled(i):
     check_layer_sampled(draw_big_config(i))
 
+
+N_ROUTE_CASES = 40
+
+
+def draw_route_config(i: int):
+    """Routing alone (bit-exact): any token count up to 2^17, any expert count up to 256,
+    k up to 8, the gates, capacities, skews, ties and the routing variants.  Returns the
+    configuration and its logits; a third of the cases quantise the logits to a coarse grid
+    so that ties between experts and between tokens are common."""
+    rng = np.random.default_rng(5000 + i)
+    E = int(rng.integers(1, 257))
+    k = int(rng.integers(1, min(8, E) + 1))
+    T = int(np.exp(rng.uniform(0, np.log(1 << 17))))
+    sigmoid = rng.random() < 0.3
+    cap = float(rng.uniform(0.1, 2.0)) if rng.random() < 0.5 else None
+    c = MoEConfig(f"fuzzroute{i}", T=max(1, T), d=64, E=E, k=k, f=64,
+                  gate="sigmoid" if sigmoid else "softmax",
+                  route_scale=2.5 if sigmoid else 1.0, cap_factor=cap,
+                  zipf_s=float(rng.uniform(0.5, 2.0)) if rng.random() < 0.6 else None,
+                  zipf_alpha=float(rng.uniform(0.3, 3.0)),
+                  select_bias=(tuple(float(v) for v in np.round(rng.normal(0, 1, E), 2))
+                               if rng.random() < 0.25 else None),
+                  drop_negative=bool(rng.random() < 0.2),
+                  drop_by_score=bool(cap is not None and rng.random() < 0.5))
+    from workloads import gen_logits
+    logits = gen_logits(c)
+    if rng.random() < 0.33:
+        logits = np.round(logits * 2.0) / 2.0          # a half-unit grid: many exact ties
+    return c, logits.astype(np.float32)
+
+
+@pytest.mark.parametrize("i", range(N_ROUTE_CASES))
+def test_route_random_config_bit_exact(i):
+    from gpu_util import run_route
+    c, logits = draw_route_config(i)
+    r, ws = run_route(c, dev(logits))
+    o = oracle.route(c, logits)
+    for key in ROUTE_KEYS:
+        np.testing.assert_array_equal(np_i(r[key]), o[key], err_msg=f"{key} {c}")
+    w = np_i(r["topk_w"]).astype(np.float64)
+    np.testing.assert_allclose(w, o["topk_w"], rtol=2.0 ** -20, atol=1e-30)
+    assert tde.moe_status(ws) == (0, 0)
+
