@@ -41,6 +41,22 @@ CASES = {
 }
 
 
+def _random_mx_shape(i):
+    """A seeded random shape within the MXFP8 limits (d, f multiples of 128)."""
+    rng = np.random.default_rng(6000 + i)
+    E = int(rng.choice([2, 3, 4, 8, 32]))
+    k = int(rng.integers(1, min(4, E) + 1))
+    return MoEConfig(f"mx_rand{i}", T=int(rng.integers(64, 2500)),
+                     d=int(rng.choice([128, 256, 384, 512])), E=E, k=k,
+                     f=int(rng.choice([128, 256, 384, 640])),
+                     zipf_s=float(rng.uniform(0.5, 1.5)),
+                     cap_factor=float(rng.uniform(0.7, 1.3)) if rng.random() < 0.3 else None)
+
+
+for _i in range(3):
+    CASES[f"rand{_i}"] = _random_mx_shape(_i)
+
+
 def mx_cfg(c, level=1):
     return tde.make_config(c.T, c.d, c.E, c.k, c.f, c.fs, c.gate, c.route_scale, c.capacity,
                            mxfp8=level)
