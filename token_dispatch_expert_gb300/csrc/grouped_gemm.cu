@@ -72,6 +72,16 @@ struct Geo {
   static constexpr int XCH_BYTES = MODE != GEMM_WGRAD ? 4 * 32 * 144 : 0;
   static constexpr int STAGING_BYTES = (TMA_STORE ? 4 * 2 * 4096 : 0) + XCH_BYTES;
   static constexpr int STAGES = PAIR == 2 ? (TMA_STORE ? 5 : 6) : 4;
+  // The fixed-K modes look each CTA's tiles up once, at the start, into a table in shared
+  // memory (TileEnt); tiles past its end are looked up when they come.  The lookup (a
+  // search over the groups' tile prefix, a division, a few loads) costs the issuing warps
+  // 0.5-1.6k cycles per tile, and the tensor pipe, which runs barely ahead of the MMA warp,
+  // waits for every cycle the MMA warp spends between two MMAs.
+  static constexpr int TILE_TABLE = MODE == GEMM_WGRAD ? 0 : 1024;
+};
+
+struct TileEnt {
+  uint16_t g, mt, nt, ntok;
 };
 
 constexpr int BK = 64;
@@ -104,7 +114,8 @@ struct Ctl {
 template <int MODE, int PAIR>
 constexpr size_t smem_bytes() {
   using GE = Geo<MODE, PAIR>;
-  return 1024 + GE::STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES + sizeof(Ctl);
+  return 1024 + GE::STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES + sizeof(Ctl) +
+         GE::TILE_TABLE * sizeof(TileEnt);
 }
 
 struct KParams {
@@ -454,6 +465,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * GE::STAGE_BYTES + GE::STAGING_BYTES);
+  TileEnt* table = reinterpret_cast<TileEnt*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(Ctl));
   const uint32_t staging_base = smem_u32(smem + STAGES * GE::STAGE_BYTES);
   // the epilogue warps' transpose blocks (one per warp, used by every fixed-K tile) sit
   // after the TMA-store staging, which only the weight-gradient mode uses
@@ -556,6 +568,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int total = ctl->bad ? 0 : ctl->tprefix[p.G];
   const uint32_t tmem_base = ctl->tmem_base;
+  // this CTA's tiles are unit, unit + num_units, ...: their lookups, shared by all roles
+  // (entries hold 16-bit tile coordinates: segments of up to 2^24 rows, 2^16 N tiles)
+  const bool fits16 = p.rows_cap <= 65535LL * GE::TILE_M && p.num_n_tiles <= 65535;
+  const int n_mine = total > unit ? ceil_div(total - unit, num_units) : 0;
+  const int n_table = !fits16 ? 0 : (n_mine < GE::TILE_TABLE ? n_mine : GE::TILE_TABLE);
+  for (int i = threadIdx.x; i < n_table; i += NUM_THREADS) {
+    int g, mt, nt;
+    map_tile<MODE, PAIR>(ctl, p, unit + i * num_units, g, mt, nt);
+    table[i] = TileEnt{static_cast<uint16_t>(g), static_cast<uint16_t>(mt),
+                       static_cast<uint16_t>(nt),
+                       static_cast<uint16_t>(tail_tokens<MODE, PAIR>(ctl, p, g, mt))};
+  }
+  __syncthreads();
+  // the i-th tile of this CTA: from the table, or looked up now past its end
+  auto tile_of = [&](int i, int tile, int& g, int& mt, int& nt, int& ntok) {
+    if (i < n_table) {
+      const TileEnt e = table[i];
+      g = e.g;
+      mt = e.mt;
+      nt = e.nt;
+      ntok = e.ntok;
+    } else {
+      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
+      ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (whole warp)
@@ -565,13 +603,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const CUtensorMap* mA = &tmA;
     const CUtensorMap* mB = &tmB;
     int map_g = -1;
-    for (int tile = unit; tile < total && ok; tile += num_units) {
-      int g, mt, nt;
-      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
+    int pit = 0;
+    for (int tile = unit; tile < total && ok; tile += num_units, ++pit) {
+      int g, mt, nt, ntok;
+      tile_of(pit, tile, g, mt, nt, ntok);
       const int seg0 = ctl->gstart[g];
       const int seg_rows = ctl->gstart[g + 1] - seg0;
       const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
-      const int ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
       // a tail tile copies the weight rows and ntok / 2 segment rows per CTA
       const uint32_t stage_tx =
           ntok > 0 ? static_cast<uint32_t>(PAIR * (GE::B_BYTES + ntok * BK))
@@ -686,10 +724,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const long long trace_c0 = clock64();
       const unsigned long long trace_n0 = globaltimer_ns();
       for (int tile = unit; tile < total && ok; tile += num_units, ++it) {
-        int g, mt, nt;
-        map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
-        const int seg_rows = ctl->gstart[g + 1] - ctl->gstart[g];
-        const int nkb = (MODE == GEMM_WGRAD) ? ceil_div(seg_rows, BK) : p.num_kb;
+        int g, mt, nt, ntok;
+        tile_of(it, tile, g, mt, nt, ntok);
+        const int nkb = (MODE == GEMM_WGRAD)
+                            ? ceil_div(ctl->gstart[g + 1] - ctl->gstart[g], BK) : p.num_kb;
         const int buf = it & 1;
         const uint32_t tph = (it >> 1) & 1;
         if (!warp_wait(smem_u32(&ctl->tempty[buf]), tph ^ 1u, abort_flag, p.err, WAIT_BUDGET)) {
@@ -704,7 +742,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // and the segment's rows at sa as its B, with N = ntok.  K-major operands step
         // 32 bytes per K16, MN-major ones one 64 x 16 core block (2 KB); descriptor start
         // addresses count 16-byte units, so stage and K offsets add to the low field.
-        const int ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
         const bool tail = GE::TAIL && ntok > 0;
         const bool a_mn = tail ? ModeTraits<MODE>::B_MN : ModeTraits<MODE>::A_MN;
         const bool b_mn = tail ? false : ModeTraits<MODE>::B_MN;
@@ -774,8 +811,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int it = 0;
     int xc = 0;                             // FC1 tail tiles: exchange blocks used so far
     for (int tile = unit; tile < total; tile += num_units, ++it) {
-      int g, mt, nt;
-      map_tile<MODE, PAIR>(ctl, p, tile, g, mt, nt);
+      int g, mt, nt, ntok;
+      tile_of(it, tile, g, mt, nt, ntok);
       const int seg0 = ctl->gstart[g];
       const int seg_end = ctl->gstart[g + 1];
       const int buf = it & 1;
@@ -784,7 +821,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      const int ntok = tail_tokens<MODE, PAIR>(ctl, p, g, mt);
       if (GE::TAIL && ntok > 0) {
         const long long row0 = static_cast<long long>(seg0) + mt * GE::TILE_M;
         if (!tail_epilogue<MODE>(p, ctl, taddr, xch_base, q, lane, rank, nt, row0,
