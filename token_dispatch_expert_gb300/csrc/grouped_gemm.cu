@@ -857,25 +857,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             st_shared_v4(blk + lane * 128 + (((2 * k + 1) ^ (lane & 7)) << 4), vb);
           }
           __syncwarp();
+          // all four pieces are read out first and the block released, so that the
+          // arithmetic and stores of the four rows interleave
+          uint4 va[4], vb[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = (lane >> 2) + 8 * i;
             const int k = lane & 3;
-            const uint4 va = ld_shared_v4(blk + r * 128 + (((2 * k) ^ (r & 7)) << 4));
-            const uint4 vb = ld_shared_v4(blk + r * 128 + (((2 * k + 1) ^ (r & 7)) << 4));
-            const long long prow = wrow0 + r;
+            va[i] = ld_shared_v4(blk + r * 128 + (((2 * k) ^ (r & 7)) << 4));
+            vb[i] = ld_shared_v4(blk + r * 128 + (((2 * k + 1) ^ (r & 7)) << 4));
+          }
+          __syncwarp();                         // the block is read before the next chunk
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const long long prow = wrow0 + (lane >> 2) + 8 * i;
             if (prow < seg_end) {
               float a[8], b[8], h[8];
-              unpack8(va, a);                   // a, b as stored: h comes from them
-              unpack8(vb, b);
+              unpack8(va[i], a);                // a, b as stored: h comes from them
+              unpack8(vb[i], b);
 #pragma unroll
               for (int e = 0; e < 8; ++e) h[e] = silu_f(a[e]) * b[e];
-              *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0 + cc) = va;
-              *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0 + cc) = vb;
+              *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0 + cc) = va[i];
+              *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0 + cc) = vb[i];
               *reinterpret_cast<uint4*>(p.out1 + prow * f + n0 + cc) = pack8(h);
             }
           }
-          __syncwarp();                         // the block is read before the next chunk
         }
       } else if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
         // Transposed through the warp's block: bf16 rows of 64 bytes (piece k at 2k,
@@ -900,15 +906,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             st_shared_v4(blk + lane * 128 + (((2 * k) ^ (lane & 7)) << 4), pack8(x));
           }
           __syncwarp();
+          uint4 v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = (lane >> 2) + 8 * i;
-            const uint4 v = ld_shared_v4(blk + r * 128 + (((2 * (lane & 3)) ^ (r & 7)) << 4));
-            const long long prow = wrow0 + r;
-            if (prow < seg_end)
-              *reinterpret_cast<uint4*>(p.out0 + prow * n_out + n0 + cc) = v;
+            v[i] = ld_shared_v4(blk + r * 128 + (((2 * (lane & 3)) ^ (r & 7)) << 4));
           }
           __syncwarp();                         // the block is read before the next chunk
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const long long prow = wrow0 + (lane >> 2) + 8 * i;
+            if (prow < seg_end)
+              *reinterpret_cast<uint4*>(p.out0 + prow * n_out + n0 + cc) = v[i];
+          }
         }
       } else if (MODE == GEMM_DGRAD2_SWIGLU) {
         // The warp's 32 rows (TMEM lanes) x 32 columns of each chunk go through its 4 KB
@@ -960,14 +970,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                          "r"(ra[4 * k + 3])
                          : "memory");
           __syncwarp();
+          // all four pieces are read out first and the block released, so that the
+          // arithmetic and stores of the four rows interleave
+          float dhs[4][8];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = (lane >> 2) + 8 * i;
             const int k0 = 2 * (lane & 3);
-            float dh[8];
-            ld_shared_f32x4(blk + r * 128 + ((k0 ^ (r & 7)) << 4), dh);
-            ld_shared_f32x4(blk + r * 128 + (((k0 + 1) ^ (r & 7)) << 4), dh + 4);
-            const long long prow = wrow0 + r;
+            ld_shared_f32x4(blk + r * 128 + ((k0 ^ (r & 7)) << 4), dhs[i]);
+            ld_shared_f32x4(blk + r * 128 + (((k0 + 1) ^ (r & 7)) << 4), dhs[i] + 4);
+          }
+          __syncwarp();                         // the block is read before the next chunk
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float* dh = dhs[i];
+            const long long prow = wrow0 + (lane >> 2) + 8 * i;
             if (prow < seg_end) {
               float a[8], b[8], da[8], db[8];
               unpack8(ca[i], a);
@@ -988,7 +1005,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(db);
             }
           }
-          __syncwarp();                         // the block is read before the next chunk
         }
       } else {   // WGRAD: dW[g][m][n], written as 32 x 64 boxes through shared memory
         const int m_base = mt * GE::TILE_M + rank * 128 + q * 32;   // this warp's 32 rows
