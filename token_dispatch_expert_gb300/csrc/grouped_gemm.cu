@@ -367,6 +367,21 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
   const bool cols_ok = n0 < n_lim;           // d, f are multiples of 64: all 32 or none
 #pragma unroll 1
   for (int c = 0; c < ntok / 32; ++c, ++xc) {
+    // piece i of this lane: row j = lane / 4 + 8 i, columns n0 + 8 (lane % 4) + 0..7
+    const int cc = 8 * (lane & 3);
+    uint4 xa[4], xb[4];                      // FC2 data-gradient: the saved a, b
+    if (MODE == GEMM_DGRAD2_SWIGLU) {
+      // issued first, so that the four rows' loads are in flight together
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = lane / 4 + 8 * i;
+        const long long base = (row0 + c * 32 + j) * 2 * p.f + n0 + cc;
+        if (cols_ok && c * 32 + j < nrows) {
+          xa[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base));
+          xb[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base + p.f));
+        }
+      }
+    }
     uint32_t ra[32];
     tmem_ld32(taddr + c * 32, ra);
     tmem_ld_wait();
@@ -387,14 +402,23 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
     if (MODE == GEMM_FC1_SWIGLU &&
         !warp_wait(smem_u32(&ctl->xfull[pi][0]), xph, abort_flag, p.err, WAIT_BUDGET))
       return false;
-    // piece i of this lane: row j = lane / 4 + 8 i, columns n0 + 8 (lane % 4) + 0..7
+    // the four pieces (and FC1's up pieces) are read out first and the blocks released,
+    // then the four rows are computed and stored together
+    float vs[4][8], us[4][8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int j = lane / 4 + 8 * i;
-      const int cc = 8 * (lane & 3);
+      ld_shared_f32x8(blk + j * XPOSE_PITCH + cc * 4, vs[i]);
+      if (MODE == GEMM_FC1_SWIGLU)   // the matching up values sit in the up warp's block
+        ld_shared_f32x8(blk + 2 * XPOSE_BYTES + j * XPOSE_PITCH + cc * 4, us[i]);
+    }
+    __syncwarp();                            // the blocks are read before the next step
+    if (MODE == GEMM_FC1_SWIGLU) mbar_arrive(smem_u32(&ctl->xempty[pi][0]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = lane / 4 + 8 * i;
       const bool ok = cols_ok && c * 32 + j < nrows;
-      float v[8];
-      ld_shared_f32x8(blk + j * XPOSE_PITCH + cc * 4, v);
+      float* v = vs[i];
       const long long row = row0 + c * 32 + j;
       if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
         if (ok) *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + cc) = pack8(v);
@@ -403,8 +427,8 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
           const int f = p.f;
           const long long base = row * 2 * f + n0 + cc;
           float a[8], b[8], da[8], db[8];
-          unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base)), a);
-          unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base + f)), b);
+          unpack8(xa[i], a);
+          unpack8(xb[i], b);
           const float wr = row_gate_weight(p, row);
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] *= wr;
@@ -419,9 +443,8 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
           *reinterpret_cast<uint4*>(p.out0 + base) = pack8(da);
           *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(db);
         }
-      } else {   // FC1, gate warp: the matching up values sit in the up warp's block
-        float u[8];
-        ld_shared_f32x8(blk + 2 * XPOSE_BYTES + j * XPOSE_PITCH + cc * 4, u);
+      } else {   // FC1, gate warp
+        const float* u = us[i];
         if (ok) {
           const int f = p.f;
           float a[8], b[8], h[8];
@@ -439,8 +462,6 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
         }
       }
     }
-    __syncwarp();                            // the block is read before the next step
-    if (MODE == GEMM_FC1_SWIGLU) mbar_arrive(smem_u32(&ctl->xempty[pi][0]));
   }
   // FC1: the up warp's block is also its staging block for ordinary tiles, so it leaves
   // only once the gate warp has read the last step out of it

@@ -971,19 +971,24 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int k = 0; k < 4; ++k)
               mx_st_shared_v4(xb + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), src[k]);
             __syncwarp();
+            // the four pieces are read out first, then stored
+            uint4 v[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = (lane >> 2) + 8 * i, k = lane & 3;
-              const uint4 v = mx_ld_shared_v4(xb + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
-              const long long row = wrow0 + r;
-              if (row < ctl->gstart[g + 1]) {
-                const int col = n0 + 32 * blk + 8 * k;
-                __nv_bfloat16* dst = o == 2 ? p.out1 + row * f + col
-                                            : p.out0 + row * 2 * f + (o == 1 ? f : 0) + col;
-                *reinterpret_cast<uint4*>(dst) = v;
-              }
+              v[i] = mx_ld_shared_v4(xb + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
             }
             __syncwarp();                       // the block is read before it is refilled
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const long long row = wrow0 + (lane >> 2) + 8 * i;
+              if (row < ctl->gstart[g + 1]) {
+                const int col = n0 + 32 * blk + 8 * (lane & 3);
+                __nv_bfloat16* dst = o == 2 ? p.out1 + row * f + col
+                                            : p.out0 + row * 2 * f + (o == 1 ? f : 0) + col;
+                *reinterpret_cast<uint4*>(dst) = v[i];
+              }
+            }
           }
         }
         continue;
@@ -1005,15 +1010,20 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               mx_st_shared_v4(xb + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), pack8(x));
             }
             __syncwarp();
+            uint4 v[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = (lane >> 2) + 8 * i, k = lane & 3;
-              const uint4 v = mx_ld_shared_v4(xb + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
-              const long long row = wrow0 + r;
-              if (row < ctl->gstart[g + 1])
-                *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + 32 * blk + 8 * k) = v;
+              v[i] = mx_ld_shared_v4(xb + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
             }
-            __syncwarp();
+            __syncwarp();                       // the block is read before it is refilled
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const long long row = wrow0 + (lane >> 2) + 8 * i;
+              if (row < ctl->gstart[g + 1])
+                *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + 32 * blk +
+                                          8 * (lane & 3)) = v[i];
+            }
           }
         }
         continue;
