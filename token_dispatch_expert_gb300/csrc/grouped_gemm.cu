@@ -376,6 +376,7 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
       for (int i = 0; i < 4; ++i) {
         const int j = lane / 4 + 8 * i;
         const long long base = (row0 + c * 32 + j) * 2 * p.f + n0 + cc;
+        xa[i] = xb[i] = make_uint4(0u, 0u, 0u, 0u);
         if (cols_ok && c * 32 + j < nrows) {
           xa[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base));
           xb[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base + p.f));
@@ -414,52 +415,65 @@ __device__ __forceinline__ bool tail_epilogue(const KParams& p, Ctl* ctl, uint32
     }
     __syncwarp();                            // the blocks are read before the next step
     if (MODE == GEMM_FC1_SWIGLU) mbar_arrive(smem_u32(&ctl->xempty[pi][0]));
+    // the four rows are computed without branches (rows past the tile's end on zeros or
+    // unused accumulator columns, not stored), then stored
+    uint4 o0[4], o1[4], o2[4];
+    if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o0[i] = pack8(vs[i]);
+    } else if (MODE == GEMM_DGRAD2_SWIGLU) {
+      float wr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = lane / 4 + 8 * i;
+        wr[i] = cols_ok && c * 32 + j < nrows ? row_gate_weight(p, row0 + c * 32 + j) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a[8], b[8], da[8], db[8];
+        unpack8(xa[i], a);
+        unpack8(xb[i], b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float dh = vs[i][e] * wr[i];
+          const float sg = sigmoid_fast(a[e]);
+          const float silu = a[e] * sg;
+          const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
+          da[e] = dh * b[e] * dsilu;
+          db[e] = dh * silu;
+        }
+        o0[i] = pack8(da);
+        o1[i] = pack8(db);
+      }
+    } else {   // FC1, gate warp
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a[8], b[8], h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          // round a, b to bf16 first: h is computed from the stored values
+          a[e] = bf16_round(vs[i][e]);
+          b[e] = bf16_round(us[i][e]);
+          h[e] = silu_f(a[e]) * b[e];
+        }
+        o0[i] = pack8(a);
+        o1[i] = pack8(b);
+        o2[i] = pack8(h);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int j = lane / 4 + 8 * i;
-      const bool ok = cols_ok && c * 32 + j < nrows;
-      float* v = vs[i];
+      if (!(cols_ok && c * 32 + j < nrows)) continue;
       const long long row = row0 + c * 32 + j;
       if (MODE == GEMM_FC2 || MODE == GEMM_DGRAD1) {
-        if (ok) *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + cc) = pack8(v);
-      } else if (MODE == GEMM_DGRAD2_SWIGLU) {
-        if (ok) {
-          const int f = p.f;
-          const long long base = row * 2 * f + n0 + cc;
-          float a[8], b[8], da[8], db[8];
-          unpack8(xa[i], a);
-          unpack8(xb[i], b);
-          const float wr = row_gate_weight(p, row);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] *= wr;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float sg = sigmoid_fast(a[e]);
-            const float silu = a[e] * sg;
-            const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
-            da[e] = v[e] * b[e] * dsilu;
-            db[e] = v[e] * silu;
-          }
-          *reinterpret_cast<uint4*>(p.out0 + base) = pack8(da);
-          *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(db);
-        }
-      } else {   // FC1, gate warp
-        const float* u = us[i];
-        if (ok) {
-          const int f = p.f;
-          float a[8], b[8], h[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            // round a, b to bf16 first: h is computed from the stored values
-            a[e] = bf16_round(v[e]);
-            b[e] = bf16_round(u[e]);
-            h[e] = silu_f(a[e]) * b[e];
-          }
-          const long long base = row * 2 * f + n0 + cc;
-          *reinterpret_cast<uint4*>(p.out0 + base) = pack8(a);
-          *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(b);
-          *reinterpret_cast<uint4*>(p.out1 + row * f + n0 + cc) = pack8(h);
-        }
+        *reinterpret_cast<uint4*>(p.out0 + row * p.n_out + n0 + cc) = o0[i];
+      } else {
+        const long long base = row * 2 * p.f + n0 + cc;
+        *reinterpret_cast<uint4*>(p.out0 + base) = o0[i];
+        *reinterpret_cast<uint4*>(p.out0 + base + p.f) = o1[i];
+        if (MODE == GEMM_FC1_SWIGLU)
+          *reinterpret_cast<uint4*>(p.out1 + row * p.f + n0 + cc) = o2[i];
       }
     }
   }
@@ -889,18 +903,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             vb[i] = ld_shared_v4(blk + r * 128 + (((2 * k + 1) ^ (r & 7)) << 4));
           }
           __syncwarp();                         // the block is read before the next chunk
+          uint4 vh[4];                          // h of the four rows, without branches
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float a[8], b[8], h[8];
+            unpack8(va[i], a);                  // a, b as stored: h comes from them
+            unpack8(vb[i], b);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[e] = silu_f(a[e]) * b[e];
+            vh[i] = pack8(h);
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const long long prow = wrow0 + (lane >> 2) + 8 * i;
             if (prow < seg_end) {
-              float a[8], b[8], h[8];
-              unpack8(va[i], a);                // a, b as stored: h comes from them
-              unpack8(vb[i], b);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) h[e] = silu_f(a[e]) * b[e];
               *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + n0 + cc) = va[i];
               *reinterpret_cast<uint4*>(p.out0 + prow * 2 * f + f + n0 + cc) = vb[i];
-              *reinterpret_cast<uint4*>(p.out1 + prow * f + n0 + cc) = pack8(h);
+              *reinterpret_cast<uint4*>(p.out1 + prow * f + n0 + cc) = vh[i];
             }
           }
         }
@@ -960,6 +979,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const long long prow = wrow0 + (lane >> 2) + 8 * i;
+            xa[i] = xb[i] = make_uint4(0u, 0u, 0u, 0u);
             if (prow < seg_end && n0 < f) {
               const long long base = prow * 2 * f + n0 + cc;
               xa[i] = __ldg(reinterpret_cast<const uint4*>(p.aux + base));
@@ -969,6 +989,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         };
         uint4 na[4], nb[4];
         load_ab(0, na, nb);
+        // the gate weight of each of the lane's four rows, looked up once per tile (0 past
+        // the segment's end)
+        float wr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const long long prow = wrow0 + (lane >> 2) + 8 * i;
+          wr[i] = prow < seg_end ? row_gate_weight(p, prow) : 0.0f;
+        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           const int n0 = nt * BN + c * 32;
@@ -1002,28 +1030,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             ld_shared_f32x4(blk + r * 128 + (((k0 + 1) ^ (r & 7)) << 4), dhs[i] + 4);
           }
           __syncwarp();                         // the block is read before the next chunk
+          // the SwiGLU backward of the four rows without branches (rows past the segment's
+          // end compute on zeros and are not stored), so that their arithmetic interleaves
+          uint4 oda[4], odb[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            float* dh = dhs[i];
+            float a[8], b[8], da[8], db[8];
+            unpack8(ca[i], a);
+            unpack8(cb[i], b);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float dh = dhs[i][e] * wr[i];
+              const float sg = sigmoid_fast(a[e]);
+              const float silu = a[e] * sg;
+              const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
+              da[e] = dh * b[e] * dsilu;
+              db[e] = dh * silu;
+            }
+            oda[i] = pack8(da);
+            odb[i] = pack8(db);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
             const long long prow = wrow0 + (lane >> 2) + 8 * i;
             if (prow < seg_end) {
-              float a[8], b[8], da[8], db[8];
-              unpack8(ca[i], a);
-              unpack8(cb[i], b);
-              const float wr = row_gate_weight(p, prow);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) dh[e] *= wr;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float sg = sigmoid_fast(a[e]);
-                const float silu = a[e] * sg;
-                const float dsilu = sg * (1.0f + a[e] * (1.0f - sg));
-                da[e] = dh[e] * b[e] * dsilu;
-                db[e] = dh[e] * silu;
-              }
               const long long base = prow * 2 * f + n0 + cc;
-              *reinterpret_cast<uint4*>(p.out0 + base) = pack8(da);
-              *reinterpret_cast<uint4*>(p.out0 + base + f) = pack8(db);
+              *reinterpret_cast<uint4*>(p.out0 + base) = oda[i];
+              *reinterpret_cast<uint4*>(p.out0 + base + f) = odb[i];
             }
           }
         }
