@@ -56,9 +56,14 @@ def load_peaks():
 # one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of a profiling shape with
 # the same per-expert GEMMs and 1/4 of the experts and of the rows -- every operand and
 # result scales with those -- times 4: `mixtral_e2` for the Mixtral layer, `qwen3_e32` for
-# the Qwen3 layer.  Emptied whenever the kernel changes, until the capture is taken again
-# on the kernel as it stands.
-GEMM_TRAFFIC_PER_LAUNCH = {}
+# the Qwen3 layer.  Valid for the grouped-GEMM kernel as it stands (late dependent-launch
+# release, clock trace, the FC1 tail-tile hand-off wait, the per-CTA tile table, the
+# epilogues that read a chunk's row pieces first and compute its rows without branches);
+# emptied whenever the kernel changes, until the capture is taken again.
+GEMM_TRAFFIC_PER_LAUNCH = {
+    "mixtral": (4 * (658.3 + 340.3 + 488.8 + 252.4 + 670.9 + 544.8) / 6 * 1e6, "mixtral_e2"),
+    "qwen3": (4 * (326.2 + 163.0 + 242.9 + 142.8 + 300.6 + 261.2) / 6 * 1e6, "qwen3_e32"),
+}
 
 # the extra workloads measured beside the headline, each in its own block of the line
 EXTRA_WORKLOADS = ["tiny", "qwen3", "dsv3", "capacity"]
