@@ -1041,8 +1041,22 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const long long seg_end = ctl->gstart[g + 1];
           const uint32_t xb = staging_base + static_cast<uint32_t>((warp - 2) * 4096);
           const int kq = lane & 3;
+          // the saved a, b of the lane's piece of row (blk, i), loaded one row ahead of
+          // their use so that each load's latency overlaps the previous row's work (zero
+          // past the segment's end)
+          auto load_ab = [&](int blk, int i, uint4& xa, uint4& xv) {
+            const long long row = wrow0 + (lane >> 2) + 8 * i;
+            const long long base = row * 2 * f + n0 + 32 * blk + 8 * kq;
+            xa = xv = make_uint4(0u, 0u, 0u, 0u);
+            if (row < seg_end) {
+              xa = __ldg(reinterpret_cast<const uint4*>(p.aux + base));
+              xv = __ldg(reinterpret_cast<const uint4*>(p.aux + base + f));
+            }
+          };
 #pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
+            uint4 na, nb;
+            load_ab(blk, 0, na, nb);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mx_st_shared_v4(xb + lane * 128 + ((k ^ (lane & 7)) << 4),
@@ -1051,6 +1065,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
+              const uint4 ca = na, cb = nb;
+              if (i < 3) load_ab(blk, i + 1, na, nb);
               const int r = (lane >> 2) + 8 * i;
               const uint4 d0 = mx_ld_shared_v4(xb + r * 128 + (((2 * kq) ^ (r & 7)) << 4));
               const uint4 d1 = mx_ld_shared_v4(xb + r * 128 + (((2 * kq + 1) ^ (r & 7)) << 4));
@@ -1063,13 +1079,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const int col = n0 + 32 * blk + 8 * kq;
               const long long base = row * 2 * f + col;
               float a[8], b[8], da[8], db[8];
-              if (ok) {
-                unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base)), a);
-                unpack8(__ldg(reinterpret_cast<const uint4*>(p.aux + base + f)), b);
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) a[e] = b[e] = 0.0f;
-              }
+              unpack8(ca, a);                   // bf16 zero bits: 0.0f past the end
+              unpack8(cb, b);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float sg = sigmoid_fast(a[e]);
