@@ -60,10 +60,7 @@ def load_peaks():
 # release, clock trace, the FC1 tail-tile hand-off wait, the per-CTA tile table, the
 # epilogues that read a chunk's row pieces first and compute its rows without branches);
 # emptied whenever the kernel changes, until the capture is taken again.
-GEMM_TRAFFIC_PER_LAUNCH = {
-    "mixtral": (4 * (658.3 + 340.3 + 488.8 + 252.4 + 670.9 + 544.8) / 6 * 1e6, "mixtral_e2"),
-    "qwen3": (4 * (326.2 + 163.0 + 242.9 + 142.8 + 300.6 + 261.2) / 6 * 1e6, "qwen3_e32"),
-}
+GEMM_TRAFFIC_PER_LAUNCH = {}
 
 # the extra workloads measured beside the headline, each in its own block of the line
 EXTRA_WORKLOADS = ["tiny", "qwen3", "dsv3", "capacity"]

@@ -199,6 +199,22 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
       "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// An L2 policy that makes the lines it touches the first to be evicted (their dirty data
+// goes back to memory early instead of lingering in L2 past the kernel).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// tma_store_3d with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const void* tmap, uint32_t src, int x, int y,
+                                                  int z, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(x), "r"(y), "r"(z), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -1099,7 +1099,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&tmC, buf_addr, n0, m_base, g);
+              tma_store_3d_hint(&tmC, buf_addr, n0, m_base, g, l2_policy_evict_first());
               bulk_commit_group();
             }
             store_buf ^= 1;
