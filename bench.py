@@ -58,9 +58,13 @@ def load_peaks():
 # result scales with those -- times 4: `mixtral_e2` for the Mixtral layer, `qwen3_e32` for
 # the Qwen3 layer.  Valid for the grouped-GEMM kernel as it stands (late dependent-launch
 # release, clock trace, the FC1 tail-tile hand-off wait, the per-CTA tile table, the
-# epilogues that read a chunk's row pieces first and compute its rows without branches);
-# emptied whenever the kernel changes, until the capture is taken again.
-GEMM_TRAFFIC_PER_LAUNCH = {}
+# epilogues that read a chunk's row pieces first and compute its rows without branches,
+# the evict-first weight-gradient stores); emptied whenever the kernel changes, until the
+# capture is taken again.
+GEMM_TRAFFIC_PER_LAUNCH = {
+    "mixtral": (4 * (658.5 + 340.6 + 491.2 + 248.1 + 671.1 + 540.5) / 6 * 1e6, "mixtral_e2"),
+    "qwen3": (4 * (326.0 + 162.7 + 243.3 + 137.4 + 300.5 + 256.3) / 6 * 1e6, "qwen3_e32"),
+}
 
 # the extra workloads measured beside the headline, each in its own block of the line
 EXTRA_WORKLOADS = ["tiny", "qwen3", "dsv3", "capacity"]
