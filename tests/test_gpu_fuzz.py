@@ -19,8 +19,8 @@ from workloads import MoEConfig, gen_inputs_host
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 24
-N_PAIR_CASES = 16
+N_CASES = 64
+N_PAIR_CASES = 40
 
 
 def draw_config(i: int) -> MoEConfig:
@@ -109,7 +109,7 @@ def test_layer_random_config_full_compare(i):
         assert_close("dW2s", f64(gr["dW2s"]), bo["dW2s"])
 
 
-N_MX_CASES = 12
+N_MX_CASES = 40
 
 
 def draw_mx_config(i: int):
@@ -200,7 +200,7 @@ def test_layer_random_large_config_sampled(i):
     check_layer_sampled(draw_big_config(i))
 
 
-N_ROUTE_CASES = 40
+N_ROUTE_CASES = 200
 
 
 def draw_route_config(i: int):
