@@ -199,8 +199,8 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
       "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-// An L2 policy that makes the lines it touches the first to be evicted (their dirty data
-// goes back to memory early instead of lingering in L2 past the kernel).
+// An L2 policy under which the lines an access touches are the first candidates for
+// eviction (for outputs that nothing reads soon after they are written).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
